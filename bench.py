@@ -1,0 +1,656 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 W8A8 rollout linear path on GB300.
+
+One step = one pass of the hot path over one Qwen3-8B-shaped decoder layer:
+  1. weight sync: the layer's seven bf16 linears quantised to E4M3 with fp32
+     128x128 block scales (one batched launch);
+  2. rollout forward of the same layer on a batch of M tokens: 1x128 activation
+     quantisation of each linear's input, then the four block-scaled GEMMs
+     (fused qkv, o_proj, fused gate-up, down);
+  3. the MoE expert pair of a Qwen3-30B-A3B-shaped layer (grouped gate-up and
+     down GEMMs over replayed top-8 routing of T tokens, activations quantised
+     per 1x128 group).
+`value` is the step's weight-sync throughput in GB/s (algorithmic bytes of
+step 1 over the device time of step 1, summed over ranks), the first part of
+the headline metric; the GEMM TFLOPS and every phase's roofline fraction ride
+in the same JSON line.  Extra sections, timed in the same run outside the step:
+the full-model weight sync (36 layers), the MoE weight sync (48 layers x 128
+experts), the GEMM sweep over M in {16, 128, 1024, 8192}, and the UE8M0 variants.
+
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload (the reference arm of this build; there is no other implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "weight-sync quant GB/s; W8A8 block-scaled GEMM TFLOPS; % of roofline, 1 GB300"
+UNIT = "GB/s"
+WORKLOAD = "qwen3-8b-layer"
+STEP_M = 8192          # tokens in the step's forward batch
+MOE_T = 4096           # tokens of the MoE layer (x top-8 = 32768 grouped rows)
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sections", default="all",
+                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0 (or all/none)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- algorithmic work
+
+def wq_bytes(n, k, scale_bytes=4):
+    """Weight-sync bytes: bf16 in, E4M3 out, one scale per 128x128 block."""
+    return 3 * n * k + scale_bytes * ((n + 127) // 128) * ((k + 127) // 128)
+
+
+def aq_bytes(m, k, scale_bytes=4):
+    return 3 * m * k + scale_bytes * m * ((k + 127) // 128)
+
+
+def gemm_flops(m, n, k):
+    return 2 * m * n * k
+
+
+def gemm_bytes(m, n, k, scale_bytes=4):
+    return n * k + m * k + 2 * m * n + scale_bytes * (m * (k // 128) + (n // 128) * (k // 128))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str, enabled: bool = True):
+        self.index = index
+        self.proc = None
+        self.enabled = enabled
+
+    def __enter__(self):
+        if self.enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_smi_id(torch, local: int) -> str:
+    """nvidia-smi --id of this process's GPU (its UUID, so that a remapped
+    CUDA_VISIBLE_DEVICES still names the right physical device)."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        return ids[local] if local < len(ids) else str(local)
+
+
+# --------------------------------------------------------------------------- our arm
+
+class Timer:
+    """Per-phase CUDA-event timing on the launching stream."""
+
+    def __init__(self, torch, stream):
+        self.torch = torch
+        self.stream = stream
+        self.pending = []
+        self.totals = {}
+        self.counts = {}
+
+    def phase(self, name):
+        timer = self
+
+        class _P:
+            def __enter__(self_inner):
+                self_inner.a = timer.torch.cuda.Event(enable_timing=True)
+                self_inner.b = timer.torch.cuda.Event(enable_timing=True)
+                self_inner.a.record(timer.stream)
+
+            def __exit__(self_inner, *exc):
+                self_inner.b.record(timer.stream)
+                timer.pending.append((name, self_inner.a, self_inner.b))
+        return _P()
+
+    def collect(self):
+        self.torch.cuda.synchronize()
+        for name, a, b in self.pending:
+            self.totals[name] = self.totals.get(name, 0.0) + a.elapsed_time(b)
+            self.counts[name] = self.counts.get(name, 0) + 1
+        self.pending = []
+
+    def avg_ms(self, name):
+        return self.totals[name] / self.counts[name]
+
+
+def gemm_available(fp8rl, torch):
+    """True once the library's GEMM entry points run (not FP8RL_ERR_UNSUPPORTED)."""
+    dev = torch.device("cuda")
+    xq = torch.zeros((1, 128), dtype=torch.uint8, device=dev)
+    sx = torch.ones((1, 1), dtype=torch.float32, device=dev)
+    wq = torch.zeros((128, 128), dtype=torch.uint8, device=dev)
+    sw = torch.ones((1, 1), dtype=torch.float32, device=dev)
+    try:
+        fp8rl.gemm(xq, sx, wq, sw)
+        torch.cuda.synchronize()
+        return True
+    except fp8rl.Fp8rlError as e:
+        if e.status == 4:
+            return False
+        raise
+
+
+def build_step_inputs(torch, synth, fp8rl, dev, seed, have_gemm):
+    """Everything the step reads, resident in HBM before timing starts."""
+    layer = synth.qwen3_8b_layer(0, seed, device=dev)
+    weights = [w for _, w in layer]
+    wout = [(torch.empty(w.shape, dtype=torch.uint8, device=dev),
+             torch.empty(((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128),
+                         dtype=torch.float32, device=dev)) for w in weights]
+    descs = fp8rl.weight_descs([(w, q, s) for w, (q, s) in zip(weights, wout)])
+    inp = {"weights": weights, "wout": wout, "descs": descs, "gemms": [], "moe": None}
+    if not have_gemm:
+        return inp
+    # fused forward weights, pre-quantised once (the step re-quantises the
+    # per-matrix weights above; the GEMMs read these fused copies)
+    for name, n, k in synth.QWEN3_8B_GEMMS:
+        w = synth.weight_bf16(n, k, seed, "step-fused", name, device=dev)
+        wq, sw = fp8rl.quant_weight(w)
+        del w
+        x = synth.activation_bf16(STEP_M, k, seed, "step-x", name, device=dev)
+        xq = torch.empty((STEP_M, k), dtype=torch.uint8, device=dev)
+        sx = torch.empty((k // 128, STEP_M), dtype=torch.float32, device=dev)
+        y = torch.empty((STEP_M, n), dtype=torch.bfloat16, device=dev)
+        inp["gemms"].append((name, n, k, x, xq, sx, wq, sw, y))
+    # MoE expert pair, one layer
+    r = synth.moe_routing(MOE_T, synth.MOE_EXPERTS, synth.MOE_TOPK, seed, 0)
+    offsets = torch.from_numpy(r.offsets).to(dev)
+    rows = int(r.offsets[-1])
+    moe = {"offsets": offsets, "rows": rows, "pairs": []}
+    for which, n, k in (("gate_up", 2 * synth.MOE_INTER, synth.MOE_HIDDEN),
+                        ("down", synth.MOE_HIDDEN, synth.MOE_INTER)):
+        wb = synth.moe_expert_weights(n, k, synth.MOE_EXPERTS, seed, 0, which, device=dev)
+        wq, sw = fp8rl.quant_weight(wb.view(-1, k))
+        del wb
+        wq = wq.view(synth.MOE_EXPERTS, n, k)
+        sw = sw.view(synth.MOE_EXPERTS, n // 128, k // 128)
+        x = synth.normal_bf16((rows, k), 1.0, seed, "moe-x", which, device=dev)
+        xq = torch.empty((rows, k), dtype=torch.uint8, device=dev)
+        sx = torch.empty((k // 128, rows), dtype=torch.float32, device=dev)
+        y = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
+        moe["pairs"].append((which, n, k, x, xq, sx, wq, sw, y))
+    inp["moe"] = moe
+    return inp
+
+
+def run_step(fp8rl, inp, timer, stream):
+    """One pass of the hot path; returns the number of kernel launches."""
+    launches = 0
+    with timer.phase("weight_sync"):
+        fp8rl.fp8rl_quant_weight_blockwise_batched(inp["descs"], len(inp["weights"]), 0, stream)
+    launches += 1
+    for name, n, k, x, xq, sx, wq, sw, y in inp["gemms"]:
+        with timer.phase(f"act_quant_{name}"):
+            fp8rl.fp8rl_quant_act_group(x, STEP_M, k, k, xq, k, sx, 0, stream)
+        with timer.phase(f"gemm_{name}"):
+            fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, STEP_M, n, k, 0, stream)
+        launches += 2
+    if inp["moe"] is not None:
+        moe = inp["moe"]
+        for which, n, k, x, xq, sx, wq, sw, y in moe["pairs"]:
+            with timer.phase(f"moe_act_quant_{which}"):
+                fp8rl.fp8rl_quant_act_group(x, moe["rows"], k, k, xq, k, sx, 0, stream)
+            with timer.phase(f"moe_gemm_{which}"):
+                fp8rl.fp8rl_grouped_gemm_blockscaled(xq, sx, wq, sw, moe["offsets"], wq.shape[0],
+                                                     moe["rows"], n, k, y, 0, stream)
+            launches += 2
+    return launches
+
+
+def step_rooflines(inp, timer, peaks):
+    """Per-phase achieved rate against its bound (HBM for quantisers and
+    weight-streaming GEMMs, FP8 tensor peak for the others)."""
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # fp8 dense = 2x bf16 (nominal ratio)
+    out = {}
+    wbytes = sum(wq_bytes(*w.shape) for w in inp["weights"])
+    ms = timer.avg_ms("weight_sync")
+    out["weight_sync"] = {"bound": "hbm", "ms": ms, "achieved": wbytes / ms / 1e6, "peak": hbm,
+                          "unit": "GB/s", "frac": wbytes / ms / 1e6 / hbm, "bytes": wbytes}
+    for name, n, k, *_ in inp["gemms"]:
+        ms = timer.avg_ms(f"act_quant_{name}")
+        b = aq_bytes(STEP_M, k)
+        out[f"act_quant_{name}"] = {"bound": "hbm", "ms": ms, "achieved": b / ms / 1e6, "peak": hbm,
+                                    "unit": "GB/s", "frac": b / ms / 1e6 / hbm, "bytes": b}
+        ms = timer.avg_ms(f"gemm_{name}")
+        f = gemm_flops(STEP_M, n, k)
+        out[f"gemm_{name}"] = gemm_roof(f, gemm_bytes(STEP_M, n, k), ms, hbm, fp8_peak)
+    if inp["moe"] is not None:
+        rows = inp["moe"]["rows"]
+        for which, n, k, x, xq, sx, wq, sw, y in inp["moe"]["pairs"]:
+            ms = timer.avg_ms(f"moe_act_quant_{which}")
+            b = aq_bytes(rows, k)
+            out[f"moe_act_quant_{which}"] = {"bound": "hbm", "ms": ms, "achieved": b / ms / 1e6,
+                                             "peak": hbm, "unit": "GB/s",
+                                             "frac": b / ms / 1e6 / hbm, "bytes": b}
+            ms = timer.avg_ms(f"moe_gemm_{which}")
+            e = wq.shape[0]
+            bytes_ = e * n * k + rows * k + 2 * rows * n + 4 * (rows * k // 128 + e * (n // 128) * (k // 128))
+            out[f"moe_gemm_{which}"] = gemm_roof(gemm_flops(rows, n, k), bytes_, ms, hbm, fp8_peak)
+    return out
+
+
+def gemm_roof(flops, bytes_, ms, hbm_gbs, fp8_tflops):
+    """The lower of the two roofs decides the bound."""
+    t_tensor = flops / (fp8_tflops * 1e12)
+    t_hbm = bytes_ / (hbm_gbs * 1e9)
+    if t_hbm > t_tensor:
+        return {"bound": "hbm", "ms": ms, "achieved": bytes_ / ms / 1e6, "peak": hbm_gbs,
+                "unit": "GB/s", "frac": bytes_ / ms / 1e6 / hbm_gbs, "bytes": bytes_,
+                "tflops": flops / ms / 1e9}
+    return {"bound": "tensor", "ms": ms, "achieved": flops / ms / 1e9, "peak": fp8_tflops,
+            "unit": "TFLOP/s", "frac": flops / ms / 1e9 / fp8_tflops, "flops": flops,
+            "tflops": flops / ms / 1e9}
+
+
+def e2e_weight_sync(torch, fp8rl, inp, stream, steps):
+    """Weight sync through the C ABI from pinned HOST buffers: H2D of the bf16
+    weights, the quantiser, D2H of codes and scales, all inside the timed region."""
+    host_w = [w.cpu().pin_memory() for w in inp["weights"]]
+    host_q = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for q, _ in inp["wout"]]
+    host_s = [torch.empty(s.shape, dtype=s.dtype, pin_memory=True) for _, s in inp["wout"]]
+    h2d = sum(w.numel() * 2 for w in host_w)
+    d2h = sum(q.numel() + s.numel() * 4 for q, s in zip(host_q, host_s))
+
+    def one():
+        for hw, dw in zip(host_w, inp["weights"]):
+            dw.copy_(hw, non_blocking=True)
+        fp8rl.fp8rl_quant_weight_blockwise_batched(inp["descs"], len(inp["weights"]), 0, stream)
+        for (dq, ds), hq, hs in zip(inp["wout"], host_q, host_s):
+            hq.copy_(dq, non_blocking=True)
+            hs.copy_(ds, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    wbytes = sum(wq_bytes(*w.shape) for w in inp["weights"])
+    return {"value": wbytes / ms / 1e6, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def time_loop(torch, fn, iters, warmup, flush=None):
+    """Median per-call device time of fn (CUDA events), optional L2 flush between calls."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def section_model_sync(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
+    """Full-model weight sync: 36 layers x 7 linears (~6.95e9 params) in one pass."""
+    weights = []
+    for layer in range(synth.QWEN3_8B_LAYERS):
+        weights += [w for _, w in synth.qwen3_8b_layer(layer, seed, device=dev)]
+    sb = 4 if fmt == 0 else 1
+    outs = [(torch.empty(w.shape, dtype=torch.uint8, device=dev),
+             torch.empty(((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128),
+                         dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev))
+            for w in weights]
+    descs = fp8rl.weight_descs([(w, q, s) for w, (q, s) in zip(weights, outs)])
+    ms = time_loop(torch, lambda: fp8rl.fp8rl_quant_weight_blockwise_batched(descs, len(weights), fmt),
+                   5, 2)
+    b = sum(wq_bytes(*w.shape, sb) for w in weights)
+    res = {"matrices": len(weights), "params": sum(w.numel() for w in weights), "ms": ms,
+           "gbs": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"],
+           "launches": (len(weights) + 255) // 256}
+    del weights, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def section_moe_sync(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
+    """Weight sync of all MoE experts: 48 layers x 128 experts x (gate-up, down)."""
+    weights = []
+    for layer in range(synth.MOE_LAYERS):
+        for which, n, k in (("gate_up", 2 * synth.MOE_INTER, synth.MOE_HIDDEN),
+                            ("down", synth.MOE_HIDDEN, synth.MOE_INTER)):
+            w = synth.normal_bf16((synth.MOE_EXPERTS * n, k), synth.WEIGHT_STD, seed, "moe-sync",
+                                  layer, which, device=dev)
+            weights.append(w)
+    outs = [(torch.empty(w.shape, dtype=torch.uint8, device=dev),
+             torch.empty(((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128),
+                         dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev))
+            for w in weights]
+    descs = fp8rl.weight_descs([(w, q, s) for w, (q, s) in zip(weights, outs)])
+    ms = time_loop(torch, lambda: fp8rl.fp8rl_quant_weight_blockwise_batched(descs, len(weights), fmt),
+                   3, 1)
+    sb = 4 if fmt == 0 else 1
+    b = sum(wq_bytes(*w.shape, sb) for w in weights)
+    res = {"params": sum(w.numel() for w in weights), "ms": ms, "gbs": b / ms / 1e6,
+           "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"]}
+    del weights, outs
+    torch.cuda.empty_cache()
+    return res
+
+
+def section_sweep(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
+    """GEMM sweep at Qwen3-8B shapes; small working sets rotate copies > 4x L2."""
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    res = {}
+    sdt = torch.float32 if fmt == 0 else torch.uint8
+    for name, n, k in synth.QWEN3_8B_GEMMS:
+        w = synth.weight_bf16(n, k, seed, "sweep", name, device=dev)
+        wq, sw = fp8rl.quant_weight(w, fmt)
+        del w
+        for m in synth.GEMM_SWEEP_M:
+            x = synth.activation_bf16(m, k, seed, "sweep-x", name, m, device=dev)
+            xq, sx = fp8rl.quant_act(x, fmt)
+            ws = n * k + m * k + 2 * m * n
+            copies = max(1, min(16, (4 * L2_BYTES) // ws + 1))
+            sets = [(xq, sx, wq, sw, torch.empty((m, n), dtype=torch.bfloat16, device=dev))]
+            for _ in range(copies - 1):
+                sets.append((xq.clone(), sx.clone(), wq.clone(), sw.clone(),
+                             torch.empty((m, n), dtype=torch.bfloat16, device=dev)))
+            it = [0]
+
+            def call():
+                a = sets[it[0] % len(sets)]
+                it[0] += 1
+                fp8rl.fp8rl_gemm_blockscaled(a[0], a[1], a[2], a[3], a[4], m, n, k, fmt)
+            ms = time_loop(torch, call, 20, 5)
+            r = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k, 4 if fmt == 0 else 1), ms,
+                          peaks["hbm_gbs"], fp8_peak)
+            res[f"{name}_m{m}"] = {"m": m, "n": n, "k": k, "ms": ms, "tflops": r["tflops"],
+                                   "bound": r["bound"], "frac": r["frac"]}
+            del sets
+        del wq, sw
+    torch.cuda.empty_cache()
+    return res
+
+
+def section_ue8m0(torch, synth, fp8rl, dev, seed, peaks, have_gemm):
+    """UE8M0 (power-of-two) scale variants: layer weight sync and the gate-up GEMM."""
+    layer = [w for _, w in synth.qwen3_8b_layer(0, seed, device=dev)]
+    outs = [(torch.empty(w.shape, dtype=torch.uint8, device=dev),
+             torch.empty(((w.shape[0] + 127) // 128, (w.shape[1] + 127) // 128), dtype=torch.uint8,
+                         device=dev)) for w in layer]
+    descs = fp8rl.weight_descs([(w, q, s) for w, (q, s) in zip(layer, outs)])
+    ms = time_loop(torch, lambda: fp8rl.fp8rl_quant_weight_blockwise_batched(descs, len(layer), 1), 20, 5)
+    b = sum(wq_bytes(*w.shape, 1) for w in layer)
+    res = {"weight_sync_layer": {"ms": ms, "gbs": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"]}}
+    if have_gemm:
+        res["gemm"] = section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, "gate_up", 24576, 4096,
+                                        STEP_M, 1)
+    return res
+
+
+def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt):
+    w = synth.weight_bf16(n, k, seed, "ue8m0", name, device=dev)
+    wq, sw = fp8rl.quant_weight(w, fmt)
+    x = synth.activation_bf16(m, k, seed, "ue8m0-x", name, device=dev)
+    xq, sx = fp8rl.quant_act(x, fmt)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    ms = time_loop(torch, lambda: fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, m, n, k, fmt), 20, 5)
+    r = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k, 1), ms, peaks["hbm_gbs"],
+                  2.0 * peaks["bf16_tflops_sustained"])
+    return {"m": m, "n": n, "k": k, "ms": ms, "tflops": r["tflops"], "frac": r["frac"], "bound": r["bound"]}
+
+
+def cpu_baseline_sample(synth, seconds_cap=30.0):
+    """The oracle, as it stands, on a bounded sample of the step's weight sync:
+    the layer's matrices one after another until the time cap."""
+    import oracle
+    threads = oracle.default_threads()
+    layer = synth.qwen3_8b_layer(0, 0, device="cpu")
+    done_bytes, t0, names = 0, time.perf_counter(), []
+    for name, w in layer:
+        bits = synth.bf16_bits(w)
+        oracle.quant_weight_blockwise(bits, oracle.SCALE_FP32, threads)
+        done_bytes += wq_bytes(*w.shape)
+        names.append(name)
+        if time.perf_counter() - t0 > seconds_cap:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"oracle weight sync of {'+'.join(names)} of one Qwen3-8B-shaped layer "
+                      f"({done_bytes / 1e6:.0f} MB algorithmic), fp32 scales, {dt:.1f} s"}
+
+
+def main_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import fp8_w8a8_rollout_gb300 as fp8rl
+    from fp8_w8a8_rollout_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fp8rl.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    peaks = load_peaks()
+    seed = 1000 + rank  # each rank syncs and runs its own layer replica (weak scaling)
+    have_gemm = gemm_available(fp8rl, torch)
+
+    inp = build_step_inputs(torch, synth, fp8rl, dev, seed, have_gemm)
+    timer = Timer(torch, torch.cuda.current_stream())
+    for _ in range(args.warmup):
+        run_step(fp8rl, inp, timer, stream)
+    torch.cuda.synchronize()
+    timer = Timer(torch, torch.cuda.current_stream())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    launches = 0
+    with ClockSampler(gpu_smi_id(torch, local), not args.no_clocks) as clocks:
+        barrier()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            launches += run_step(fp8rl, inp, timer, stream)
+        end.record()
+        barrier()
+    total_ms = start.elapsed_time(end)
+    timer.collect()
+    status = fp8rl.fp8rl_sync_status()
+    if status != 0:
+        raise RuntimeError(f"device reported {fp8rl.STATUS.get(status, status)}")
+    sync_ms = timer.avg_ms("weight_sync")
+    wbytes = sum(wq_bytes(*w.shape) for w in inp["weights"])
+    t = torch.tensor([total_ms, sync_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, sync_ms = float(t[0]), float(t[1])
+    value = world * wbytes / sync_ms / 1e6
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    roofs = step_rooflines(inp, timer, peaks)
+    dominant = max(roofs, key=lambda k: roofs[k]["ms"])
+    d = roofs[dominant]
+    roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "peak_source": f"{peaks['source']} ({'hbm_gbs' if d['bound'] == 'hbm' else '2 x bf16_tflops_sustained'})"}
+    e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
+    sections = {}
+    wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
+        {"model", "moe_sync", "sweep", "ue8m0"} if args.sections == "all" else set())
+    del inp
+    torch.cuda.empty_cache()
+    if "model" in wanted:
+        sections["model_sync_qwen3_8b_36_layers"] = section_model_sync(torch, synth, fp8rl, dev, seed, peaks)
+    if "moe_sync" in wanted:
+        sections["moe_sync_qwen3_30b_a3b_48x128_experts"] = section_moe_sync(torch, synth, fp8rl, dev, seed, peaks)
+    if "sweep" in wanted and have_gemm:
+        sections["gemm_sweep_qwen3_8b"] = section_sweep(torch, synth, fp8rl, dev, seed, peaks)
+    if "ue8m0" in wanted:
+        sections["ue8m0"] = section_ue8m0(torch, synth, fp8rl, dev, seed, peaks, have_gemm)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline_sample(synth)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 acc -> bf16",
+        "data": "synthetic (seeded; N(0,0.02) weights with 0.1% x20 outliers, lognormal-channel activations)",
+        "config": {"workload": WORKLOAD, "weight_sync": "7 linears, 192,937,984 bf16 params, fp32 128x128 scales",
+                   "forward_tokens": STEP_M if have_gemm else 0, "moe_tokens": MOE_T if have_gemm else 0,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "step working set > 1 GB, larger than L2 (129 MB); no explicit flush"},
+        "weight_sync_ms": sync_ms,
+        "gemm_available": have_gemm,
+        "roofline": roofline,
+        "phases": roofs,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+        "sections": sections,
+        "peaks": peaks,
+    }
+    print(json.dumps(line))
+    sys.stdout.flush()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main_reference(args):
+    """The CPU oracle as the reference arm, on rank 0 only."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    from fp8_w8a8_rollout_gb300 import synth
+    threads = oracle.default_threads()
+    layer = synth.qwen3_8b_layer(0, 0, device="cpu")
+    mats = [(name, synth.bf16_bits(w)) for name, w in layer]
+    # each step quantises one matrix of the layer, rotating through them
+    for i in range(args.warmup):
+        oracle.quant_weight_blockwise(mats[i % len(mats)][1], oracle.SCALE_FP32, threads)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        bits = mats[i % len(mats)][1]
+        oracle.quant_weight_blockwise(bits, oracle.SCALE_FP32, threads)
+        done += wq_bytes(*bits.shape)
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 CPU",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "parallelism": "rank 0 only"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "one matrix of the Qwen3-8B-shaped layer per step, rotating"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        main_reference(a)
+    else:
+        main_ours(a)

@@ -1,1 +1,248 @@
-"""GB300-native FP8 W8A8 rollout linear path (binding filled in with the CUDA library)."""
+"""GB300-native FP8 W8A8 rollout linear path: Python binding of ``libfp8rl.so``.
+
+The functions named ``fp8rl_*`` mirror the C ABI in ``include/fp8rl.h`` one
+to one: they only marshal arguments (a torch tensor becomes its device
+pointer, ``stream=None`` becomes torch's current stream) and raise
+``Fp8rlError`` on a non-OK status.  Every step of the path runs in the CUDA
+kernels of the library; there is no CPU or PyTorch fallback, and loading fails
+loudly when the library has not been built.
+
+The convenience helpers below them (``quant_weight``, ``quant_act``,
+``gemm``, ``grouped_gemm``, ``quant_weights_batched``) allocate the outputs
+with torch and call the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "Fp8rlError", "SCALE_FP32", "SCALE_UE8M0", "load_library", "library_path",
+    "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
+    "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
+    "fp8rl_e4m3_encode", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
+    "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm",
+]
+
+SCALE_FP32 = 0
+SCALE_UE8M0 = 1
+
+STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_INVALID_ARG", 2: "FP8RL_ERR_SHAPE",
+          3: "FP8RL_ERR_ALIGNMENT", 4: "FP8RL_ERR_UNSUPPORTED", 5: "FP8RL_ERR_CUDA",
+          6: "FP8RL_ERR_TIMEOUT"}
+
+
+class Fp8rlError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+class WeightDesc(ctypes.Structure):
+    """fp8rl_weight_desc"""
+    _fields_ = [("w_bf16", ctypes.c_void_p), ("q_e4m3", ctypes.c_void_p),
+                ("w_scale", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("ldw", ctypes.c_int64), ("ldq", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False):
+    """Load ``libfp8rl.so`` (raises if it is missing and building is not asked for)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing:
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise FileNotFoundError(
+                f"{_build.LIB} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
+        lib = ctypes.CDLL(_build.LIB)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        st = ctypes.c_int
+        sig = {
+            "fp8rl_quant_weight_blockwise": [vp, i64, i64, i64, vp, i64, vp, st, vp],
+            "fp8rl_quant_weight_blockwise_batched": [ctypes.POINTER(WeightDesc), i32, st, vp],
+            "fp8rl_quant_act_group": [vp, i64, i64, i64, vp, i64, vp, st, vp],
+            "fp8rl_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
+            "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
+            "fp8rl_e4m3_encode": [vp, i64, vp, vp],
+            "fp8rl_sync_status": [vp],
+            "fp8rl_status_string": [st],
+            "fp8rl_version": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = st
+        lib.fp8rl_status_string.restype = ctypes.c_char_p
+        lib.fp8rl_version.restype = i32
+        _lib = lib
+        return lib
+
+
+# --------------------------------------------------------------------------- marshalling
+
+def _p(x) -> int | None:
+    """A device pointer from a tensor, an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ok(status: int, what: str) -> None:
+    if status != 0:
+        raise Fp8rlError(status, what)
+
+
+# --------------------------------------------------------------------------- C ABI, 1:1
+
+def fp8rl_quant_weight_blockwise(w_bf16, n, k, ldw, q_e4m3, ldq, w_scale, fmt=SCALE_FP32,
+                                 stream=None) -> None:
+    _ok(load_library().fp8rl_quant_weight_blockwise(_p(w_bf16), n, k, ldw, _p(q_e4m3), ldq,
+                                                    _p(w_scale), fmt, _stream(stream)),
+        "fp8rl_quant_weight_blockwise")
+
+
+def fp8rl_quant_weight_blockwise_batched(descs, count, fmt=SCALE_FP32, stream=None) -> None:
+    _ok(load_library().fp8rl_quant_weight_blockwise_batched(descs, count, fmt, _stream(stream)),
+        "fp8rl_quant_weight_blockwise_batched")
+
+
+def fp8rl_quant_act_group(x_bf16, m, k, ldx, q_e4m3, ldq, x_scale, fmt=SCALE_FP32,
+                          stream=None) -> None:
+    _ok(load_library().fp8rl_quant_act_group(_p(x_bf16), m, k, ldx, _p(q_e4m3), ldq, _p(x_scale),
+                                             fmt, _stream(stream)),
+        "fp8rl_quant_act_group")
+
+
+def fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt=SCALE_FP32,
+                           stream=None) -> None:
+    _ok(load_library().fp8rl_gemm_blockscaled(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
+                                              _p(y_bf16), m, n, k, fmt, _stream(stream)),
+        "fp8rl_gemm_blockscaled")
+
+
+def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k,
+                                   y_bf16, fmt=SCALE_FP32, stream=None) -> None:
+    _ok(load_library().fp8rl_grouped_gemm_blockscaled(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
+                                                      _p(d_offsets), num_experts, rows, n, k,
+                                                      _p(y_bf16), fmt, _stream(stream)),
+        "fp8rl_grouped_gemm_blockscaled")
+
+
+def fp8rl_e4m3_encode(d_in, n, d_out, stream=None) -> None:
+    _ok(load_library().fp8rl_e4m3_encode(_p(d_in), n, _p(d_out), _stream(stream)), "fp8rl_e4m3_encode")
+
+
+def fp8rl_sync_status(stream=None) -> int:
+    """Synchronise and return the status code (0 = OK, 6 = a device wait ran out)."""
+    return int(load_library().fp8rl_sync_status(_stream(stream)))
+
+
+def fp8rl_status_string(status: int) -> str:
+    return load_library().fp8rl_status_string(int(status)).decode()
+
+
+def fp8rl_version() -> int:
+    return int(load_library().fp8rl_version())
+
+
+# --------------------------------------------------------------------------- helpers
+
+def _scale_dtype(fmt):
+    return torch.float32 if fmt == SCALE_FP32 else torch.uint8
+
+
+def _check_bf16_2d(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D bf16 tensor with unit column stride")
+
+
+def quant_weight(w: torch.Tensor, fmt=SCALE_FP32, stream=None):
+    """E4M3 codes (uint8 [n,k]) and block scales ([ceil(n/128), ceil(k/128)]) of w."""
+    _check_bf16_2d(w, "w")
+    n, k = w.shape
+    q = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    s = torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=_scale_dtype(fmt), device=w.device)
+    fp8rl_quant_weight_blockwise(w, n, k, w.stride(0), q, k, s, fmt, stream)
+    return q, s
+
+
+def weight_descs(items):
+    """fp8rl_weight_desc array from (w, q, scale) tensor triples."""
+    arr = (WeightDesc * max(1, len(items)))()
+    for i, (w, q, s) in enumerate(items):
+        arr[i] = WeightDesc(w.data_ptr(), q.data_ptr(), s.data_ptr(), w.shape[0], w.shape[1],
+                            w.stride(0), q.stride(0))
+    return arr
+
+
+def quant_weights_batched(weights, fmt=SCALE_FP32, stream=None, outputs=None):
+    """Quantise a list of bf16 matrices in one pass; returns [(q, scale), ...]."""
+    if outputs is None:
+        outputs = []
+        for w in weights:
+            _check_bf16_2d(w, "w")
+            n, k = w.shape
+            outputs.append((torch.empty((n, k), dtype=torch.uint8, device=w.device),
+                            torch.empty(((n + 127) // 128, (k + 127) // 128),
+                                        dtype=_scale_dtype(fmt), device=w.device)))
+    descs = weight_descs([(w, q, s) for w, (q, s) in zip(weights, outputs)])
+    fp8rl_quant_weight_blockwise_batched(descs, len(weights), fmt, stream)
+    return outputs
+
+
+def quant_act(x: torch.Tensor, fmt=SCALE_FP32, stream=None):
+    """E4M3 codes (uint8 [m,k]) and group scales ([ceil(k/128), m]) of x."""
+    _check_bf16_2d(x, "x")
+    m, k = x.shape
+    q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    s = torch.empty(((k + 127) // 128, m), dtype=_scale_dtype(fmt), device=x.device)
+    fp8rl_quant_act_group(x, m, k, x.stride(0), q, k, s, fmt, stream)
+    return q, s
+
+
+def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None):
+    """bf16 Y [m, n] = block-scaled X W^T."""
+    m, k = xq.shape
+    n = wq.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device)
+    fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, out, m, n, k, fmt, stream)
+    return out
+
+
+def grouped_gemm(xq, x_scale, wq, w_scale, d_offsets, fmt=SCALE_FP32, out=None, stream=None):
+    """bf16 Y [rows, n]: expert e's weights applied to its row segment."""
+    rows, k = xq.shape
+    e, n, _ = wq.shape
+    if out is None:
+        out = torch.empty((rows, n), dtype=torch.bfloat16, device=xq.device)
+    fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, e, rows, n, k, out, fmt,
+                                   stream)
+    return out

@@ -1,0 +1,71 @@
+// common.cuh -- device-side numerics shared by the quantiser and GEMM kernels.
+//
+// E4M3 conversion uses the hardware convert (cvt.rn.satfinite.e4m3x2.f32:
+// round-to-nearest-even, saturating to +-448); the scale is the IEEE fp32
+// quotient amax / 448 and each element is rounded from the IEEE fp32 quotient
+// x / scale (FP8-RL page, "Prerequisites / FP8 quantisation format", read as
+// scale = amax / 448).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8rl.h"
+
+namespace fp8rl {
+
+constexpr int kBlock = 128;         // weight block edge and activation group width
+constexpr float kE4M3Max = 448.0f;  // largest finite E4M3 magnitude
+
+// ------------------------------------------------------------------ bf16 pairs
+
+// the two bf16 values packed in a 32-bit word, low half first
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// |a| and |b| of two packed bf16 values, then the per-half unsigned max; the
+// magnitude bit patterns of non-negative floats order like unsigned integers.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t acc, uint32_t u) {
+  return __vmaxu2(acc, u & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ float absmax_bf16x2_to_f32(uint32_t acc) {
+  uint32_t lo = acc & 0xFFFFu, hi = acc >> 16;
+  return __uint_as_float((lo > hi ? lo : hi) << 16);
+}
+
+// ------------------------------------------------------------------ E4M3
+
+// two fp32 values -> two E4M3 codes (a in the low byte, b in the high byte)
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// ------------------------------------------------------------------ scales
+
+// fp32 scale of a block with absolute maximum amax (zeros: 1.0)
+__device__ __forceinline__ float scale_fp32(float amax) {
+  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, kE4M3Max);
+}
+
+// UE8M0 exponent: smallest e with 448 * 2^e >= amax, in [-127, 127]; zeros: 0.
+// amax is a finite bf16 magnitude, so the fp64 comparison is exact.
+__device__ __forceinline__ int scale_ue8m0_exponent(float amax) {
+  if (amax == 0.0f) return 0;
+  // start from a bound one below the answer and step up with exact comparisons
+  int e = ilogbf(amax) - 9;
+  if (e < -127) e = -127;
+  while (e < 127 && ldexp(448.0, e) < (double)amax) ++e;
+  return e;
+}
+
+// 2^-e as an fp32 (e in [-126, 127] gives a normal number; -127 -> 2^127)
+__device__ __forceinline__ float exp2_neg(int e) { return __int_as_float((127 - e) << 23); }
+
+// ------------------------------------------------------------------ errors
+
+// bits recorded in a device error word
+constexpr uint32_t kErrTimeout = 1u;
+
+}  // namespace fp8rl

@@ -1,0 +1,412 @@
+// quant.cu -- weight-sync (128x128 block) and activation (1x128 group) E4M3
+// quantisers for sm_103a.
+//
+// FP8-RL page, "Prerequisites / FP8 quantisation format": one scale per
+// 128x128 weight block, W_hat = round(W / scale) in E4M3; "Method steps",
+// step 1: weights quantised once per sync, activations in every forward pass.
+//
+// Both kernels are HBM-bound streams (2 bytes in, 1 byte + a scale out per
+// element).  Each thread issues several independent 16-byte non-allocating
+// loads before it touches any of them, so that enough bytes are in flight per
+// SM; the block maximum is reduced in registers, across the warp with one
+// redux and across warps through shared memory; the codes leave as 16-byte
+// stores.  Grids are persistent: a multiple of the SM count, striding over the
+// blocks or groups.
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+
+namespace fp8rl {
+
+// ============================================================================
+// weight blocks
+// ============================================================================
+
+struct WDesc {
+  const uint16_t* w;
+  uint8_t* q;
+  void* scale;
+  int64_t n, k, ldw, ldq;
+  int64_t kbs;          // blocks along K
+  int64_t block_begin;  // first global block index of this matrix
+  int32_t vec;          // rows are 16-byte aligned: vector path allowed
+  int32_t pad;
+};
+
+template <int MAXD>
+struct WBatch {
+  int32_t count;
+  int32_t pad;
+  int64_t total_blocks;
+  WDesc d[MAXD];
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// 8 bf16 (one uint4) -> 8 E4M3 codes (two 32-bit words), fp32-scale variant
+__device__ __forceinline__ uint2 quant8_div(uint4 v, float s) {
+  uint2 r;
+  r.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
+        (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
+  r.y = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
+        (e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+  return r;
+}
+
+// the same with an exact power-of-two multiplier (UE8M0 variant)
+__device__ __forceinline__ uint2 quant8_mul(uint4 v, float f) {
+  uint2 r;
+  r.x = e4m3x2(bf16_lo(v.x) * f, bf16_hi(v.x) * f) | (e4m3x2(bf16_lo(v.y) * f, bf16_hi(v.y) * f) << 16);
+  r.y = e4m3x2(bf16_lo(v.z) * f, bf16_hi(v.z) * f) | (e4m3x2(bf16_lo(v.w) * f, bf16_hi(v.w) * f) << 16);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t absmax_u4(uint32_t acc, uint4 v) {
+  acc = absmax_bf16x2(acc, v.x);
+  acc = absmax_bf16x2(acc, v.y);
+  acc = absmax_bf16x2(acc, v.z);
+  return absmax_bf16x2(acc, v.w);
+}
+
+template <int MAXD>
+__device__ __forceinline__ int find_desc(const WBatch<MAXD>& b, int64_t blk) {
+  if (MAXD == 1) return 0;
+  int lo = 0, hi = b.count - 1;  // largest d with block_begin <= blk
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (b.d[mid].block_begin <= blk) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// One CTA of 256 threads quantises one 128x128 block per loop iteration.
+// Full, aligned blocks: thread t owns rows (t/8) + 32 i, i = 0..3, and the 16
+// columns starting at 16 (t%8): four rows x 32 bytes in, four 16-byte stores out.
+template <int MAXD, bool UE8M0>
+__global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant__ WBatch<MAXD> batch) {
+  __shared__ uint32_t red[2][8];
+  const int t = threadIdx.x, warp = t >> 5;
+  int parity = 0;
+  for (int64_t blk = blockIdx.x; blk < batch.total_blocks; blk += gridDim.x, parity ^= 1) {
+    const WDesc& D = batch.d[find_desc<MAXD>(batch, blk)];
+    const int64_t local = blk - D.block_begin;
+    const int64_t nb = local / D.kbs, kb = local - nb * D.kbs;
+    const int64_t r0 = nb * kBlock, c0 = kb * kBlock;
+    const bool full = D.vec && r0 + kBlock <= D.n && c0 + kBlock <= D.k;
+    if (full) {
+      const int rs = t >> 3, cc = (t & 7) * 16;
+      uint4 v[4][2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint16_t* p = D.w + (r0 + rs + 32 * i) * D.ldw + c0 + cc;
+        v[i][0] = ld_stream(p);
+        v[i][1] = ld_stream(p + 8);
+      }
+      uint32_t acc = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc = absmax_u4(absmax_u4(acc, v[i][0]), v[i][1]);
+      uint32_t am = __reduce_max_sync(0xffffffffu, (acc & 0xFFFFu) > (acc >> 16) ? (acc & 0xFFFFu) : (acc >> 16));
+      if ((t & 31) == 0) red[parity][warp] = am;
+      __syncthreads();
+      uint32_t m8 = red[parity][0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) m8 = max(m8, red[parity][w]);
+      const float amax = __uint_as_float(m8 << 16);
+      if (UE8M0) {
+        const int e = scale_ue8m0_exponent(amax);
+        const float f = exp2_neg(e);
+        if (t == 0) static_cast<uint8_t*>(D.scale)[local] = (uint8_t)(e + 127);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint2 a = quant8_mul(v[i][0], f), b = quant8_mul(v[i][1], f);
+          st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
+        }
+      } else {
+        const float s = scale_fp32(amax);
+        if (t == 0) static_cast<float*>(D.scale)[local] = s;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint2 a = quant8_div(v[i][0], s), b = quant8_div(v[i][1], s);
+          st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
+        }
+      }
+    } else {
+      // ragged or unaligned block: scalar loads with bounds, two passes
+      const int64_t rows = min((int64_t)kBlock, D.n - r0), cols = min((int64_t)kBlock, D.k - c0);
+      uint32_t acc = 0;
+      for (int idx = t; idx < kBlock * kBlock; idx += 256) {
+        const int r = idx >> 7, c = idx & 127;
+        if (r < rows && c < cols) acc = max(acc, (uint32_t)(D.w[(r0 + r) * D.ldw + c0 + c] & 0x7FFFu));
+      }
+      uint32_t am = __reduce_max_sync(0xffffffffu, acc);
+      if ((t & 31) == 0) red[parity][warp] = am;
+      __syncthreads();
+      uint32_t m8 = red[parity][0];
+      for (int w = 1; w < 8; ++w) m8 = max(m8, red[parity][w]);
+      const float amax = __uint_as_float(m8 << 16);
+      int e = 0;
+      float s = 1.0f, f = 1.0f;
+      if (UE8M0) {
+        e = scale_ue8m0_exponent(amax);
+        f = exp2_neg(e);
+        if (t == 0) static_cast<uint8_t*>(D.scale)[local] = (uint8_t)(e + 127);
+      } else {
+        s = scale_fp32(amax);
+        if (t == 0) static_cast<float*>(D.scale)[local] = s;
+      }
+      for (int idx = t; idx < kBlock * kBlock; idx += 256) {
+        const int r = idx >> 7, c = idx & 127;
+        if (r < rows && c < cols) {
+          const float x = __uint_as_float((uint32_t)D.w[(r0 + r) * D.ldw + c0 + c] << 16);
+          const float y = UE8M0 ? x * f : __fdiv_rn(x, s);
+          D.q[(r0 + r) * D.ldq + c0 + c] = (uint8_t)(e4m3x2(y, 0.0f) & 0xFFu);
+        }
+      }
+    }
+  }
+}
+
+// ============================================================================
+// activation groups
+// ============================================================================
+
+// A half-warp quantises one 1x128 group: each of its 16 lanes loads 8 bf16.
+// Groups are numbered g-major (task = g * m + row) so that the scale stores of
+// neighbouring half-warps are contiguous in the [K/128][m] scale layout.  A
+// warp takes 2 * kActUnroll consecutive tasks per iteration (half-warp h gets
+// tasks base + 2u + h), issuing all loads before any use.  The loop bound is
+// warp-uniform, so the full-mask shuffles always see all 32 lanes.
+constexpr int kActUnroll = 4;
+
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int64_t m,
+                                                        int64_t k, int64_t ldx, uint8_t* __restrict__ q,
+                                                        int64_t ldq, void* __restrict__ scale,
+                                                        int64_t groups, int vec) {
+  const int lane16 = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
+  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t warp_count = (int64_t)gridDim.x * 8;
+  const int64_t tasks = m * groups;
+  constexpr int kPerWarp = 2 * kActUnroll;
+  for (int64_t base = warp * kPerWarp; base < tasks; base += warp_count * kPerWarp) {
+    uint4 v[kActUnroll];
+    int64_t row[kActUnroll], g[kActUnroll];
+    bool fast[kActUnroll];
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+      const int64_t task = base + 2 * u + half;
+      g[u] = task / m;
+      row[u] = task - g[u] * m;
+      const int64_t c = g[u] * kBlock + lane16 * 8;
+      fast[u] = task < tasks && vec && (g[u] + 1) * kBlock <= k;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (fast[u]) {
+        v[u] = ld_stream(x + row[u] * ldx + c);
+      } else if (task < tasks) {
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = (c + j < k) ? (uint32_t)x[row[u] * ldx + c + j] : 0u;
+        v[u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                          h[6] | (h[7] << 16));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+      const int64_t task = base + 2 * u + half;
+      const uint32_t acc = absmax_u4(0u, v[u]);
+      uint32_t am = max(acc & 0xFFFFu, acc >> 16);
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
+      if (task >= tasks) continue;
+      const float amax = __uint_as_float(am << 16);
+      uint2 codes;
+      if (UE8M0) {
+        const int e = scale_ue8m0_exponent(amax);
+        codes = quant8_mul(v[u], exp2_neg(e));
+        if (lane16 == 0) static_cast<uint8_t*>(scale)[g[u] * m + row[u]] = (uint8_t)(e + 127);
+      } else {
+        const float s = scale_fp32(amax);
+        codes = quant8_div(v[u], s);
+        if (lane16 == 0) static_cast<float*>(scale)[g[u] * m + row[u]] = s;
+      }
+      const int64_t c = g[u] * kBlock + lane16 * 8;
+      uint8_t* dst = q + row[u] * ldq + c;
+      if (fast[u]) {
+        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(codes.x), "r"(codes.y) : "memory");
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (c + j < k) dst[j] = (uint8_t)(((j < 4 ? codes.x : codes.y) >> (8 * (j & 3))) & 0xFFu);
+      }
+    }
+  }
+}
+
+// ============================================================================
+// the device codec alone (fp32 -> E4M3), for whole-format checks
+// ============================================================================
+
+__global__ void __launch_bounds__(256) e4m3_encode_kernel(const float* __restrict__ in, int64_t n,
+                                                          uint8_t* __restrict__ out) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x * 2;
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2; i < n; i += stride) {
+    const float a = in[i], b = (i + 1 < n) ? in[i + 1] : 0.0f;
+    const uint32_t c = e4m3x2(a, b);
+    out[i] = (uint8_t)(c & 0xFFu);
+    if (i + 1 < n) out[i + 1] = (uint8_t)(c >> 8);
+  }
+}
+
+// ============================================================================
+// host side
+// ============================================================================
+
+namespace {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+fp8rl_status check_weight(const fp8rl_weight_desc& d, fp8rl_scale_fmt fmt) {
+  if (d.n < 0 || d.k < 0 || d.ldw < d.k || d.ldq < d.k) return FP8RL_ERR_INVALID_ARG;
+  if (d.n == 0 || d.k == 0) return FP8RL_OK;
+  if (!d.w_bf16 || !d.q_e4m3 || !d.w_scale) return FP8RL_ERR_INVALID_ARG;
+  if (!aligned(d.w_bf16, 16) || !aligned(d.q_e4m3, 16)) return FP8RL_ERR_ALIGNMENT;
+  if (fmt == FP8RL_SCALE_FP32 && !aligned(d.w_scale, 4)) return FP8RL_ERR_ALIGNMENT;
+  return FP8RL_OK;
+}
+
+constexpr int kMaxBatch = 256;
+constexpr int kWeightCtasPerSm = 4;  // 256 threads each, about 64 registers
+
+template <int MAXD>
+fp8rl_status launch_weight(const WBatch<MAXD>& b, fp8rl_scale_fmt fmt, cudaStream_t stream) {
+  if (b.total_blocks == 0) return FP8RL_OK;
+  const int64_t grid = std::min<int64_t>(b.total_blocks, (int64_t)sm_count() * kWeightCtasPerSm);
+  if (fmt == FP8RL_SCALE_UE8M0)
+    quant_weight_kernel<MAXD, true><<<(unsigned)grid, 256, 0, stream>>>(b);
+  else
+    quant_weight_kernel<MAXD, false><<<(unsigned)grid, 256, 0, stream>>>(b);
+  return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
+WDesc make_desc(const fp8rl_weight_desc& s, int64_t begin) {
+  WDesc d{};
+  d.w = static_cast<const uint16_t*>(s.w_bf16);
+  d.q = static_cast<uint8_t*>(s.q_e4m3);
+  d.scale = s.w_scale;
+  d.n = s.n;
+  d.k = s.k;
+  d.ldw = s.ldw;
+  d.ldq = s.ldq;
+  d.kbs = (s.k + kBlock - 1) / kBlock;
+  d.block_begin = begin;
+  d.vec = (s.ldw * 2) % 16 == 0 && s.ldq % 16 == 0;
+  return d;
+}
+
+}  // namespace
+}  // namespace fp8rl
+
+using namespace fp8rl;
+
+extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise(const void* w_bf16, int64_t n,
+                                                               int64_t k, int64_t ldw, void* q_e4m3,
+                                                               int64_t ldq, void* w_scale,
+                                                               fp8rl_scale_fmt fmt, void* stream) {
+  if (fmt != FP8RL_SCALE_FP32 && fmt != FP8RL_SCALE_UE8M0) return FP8RL_ERR_INVALID_ARG;
+  fp8rl_weight_desc s{w_bf16, q_e4m3, w_scale, n, k, ldw, ldq};
+  fp8rl_status st = check_weight(s, fmt);
+  if (st != FP8RL_OK || n == 0 || k == 0) return st;
+  WBatch<1> b{};
+  b.count = 1;
+  b.d[0] = make_desc(s, 0);
+  b.total_blocks = ((n + kBlock - 1) / kBlock) * b.d[0].kbs;
+  return launch_weight(b, fmt, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise_batched(const fp8rl_weight_desc* descs,
+                                                                       int32_t count,
+                                                                       fp8rl_scale_fmt fmt,
+                                                                       void* stream) {
+  if (fmt != FP8RL_SCALE_FP32 && fmt != FP8RL_SCALE_UE8M0) return FP8RL_ERR_INVALID_ARG;
+  if (count < 0 || (count > 0 && !descs)) return FP8RL_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < count; ++i) {
+    fp8rl_status st = check_weight(descs[i], fmt);
+    if (st != FP8RL_OK) return st;
+  }
+  // heap-allocated host staging: the parameter block is ~18 KB
+  std::vector<WBatch<kMaxBatch>> staged(1);
+  WBatch<kMaxBatch>& b = staged[0];
+  int32_t i = 0;
+  while (i < count) {
+    b.count = 0;
+    b.total_blocks = 0;
+    for (; i < count && b.count < kMaxBatch; ++i) {
+      const fp8rl_weight_desc& s = descs[i];
+      if (s.n == 0 || s.k == 0) continue;
+      b.d[b.count] = make_desc(s, b.total_blocks);
+      b.total_blocks += ((s.n + kBlock - 1) / kBlock) * b.d[b.count].kbs;
+      ++b.count;
+    }
+    if (b.count == 0) continue;
+    fp8rl_status st = launch_weight(b, fmt, static_cast<cudaStream_t>(stream));
+    if (st != FP8RL_OK) return st;
+  }
+  return FP8RL_OK;
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int64_t m, int64_t k,
+                                                        int64_t ldx, void* q_e4m3, int64_t ldq,
+                                                        void* x_scale, fp8rl_scale_fmt fmt,
+                                                        void* stream) {
+  if (fmt != FP8RL_SCALE_FP32 && fmt != FP8RL_SCALE_UE8M0) return FP8RL_ERR_INVALID_ARG;
+  fp8rl_weight_desc s{x_bf16, q_e4m3, x_scale, m, k, ldx, ldq};
+  fp8rl_status st = check_weight(s, fmt);
+  if (st != FP8RL_OK || m == 0 || k == 0) return st;
+  const int64_t groups = (k + kBlock - 1) / kBlock;
+  const int64_t tasks = m * groups;
+  const int64_t warps = (tasks + 2 * kActUnroll - 1) / (2 * kActUnroll);
+  const int64_t want = (warps + 7) / 8;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
+  const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (fmt == FP8RL_SCALE_UE8M0)
+    quant_act_kernel<true><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), m, k,
+                                                           ldx, static_cast<uint8_t*>(q_e4m3), ldq,
+                                                           x_scale, groups, vec);
+  else
+    quant_act_kernel<false><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), m, k,
+                                                            ldx, static_cast<uint8_t*>(q_e4m3), ldq,
+                                                            x_scale, groups, vec);
+  return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_e4m3_encode(const float* d_in, int64_t n, uint8_t* d_out,
+                                                   void* stream) {
+  if (n < 0 || (n > 0 && (!d_in || !d_out))) return FP8RL_ERR_INVALID_ARG;
+  if (n == 0) return FP8RL_OK;
+  if (!aligned(d_in, 4)) return FP8RL_ERR_ALIGNMENT;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((n + 511) / 512, (int64_t)sm_count() * 8));
+  e4m3_encode_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(d_in, n, d_out);
+  return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
+}

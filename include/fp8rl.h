@@ -1,0 +1,206 @@
+/*
+ * fp8rl.h -- C ABI of the GB300 (sm_103a) FP8 W8A8 rollout linear path.
+ *
+ * The path, as the FP8-RL pages describe it ("FP8-RL: A Practical and Stable
+ * Low-Precision Stack for LLM Reinforcement Learning"):
+ *   1. weight sync: bf16 weights are quantised to E4M3 with one scale per
+ *      128x128 block, once per RL step ("Method steps", steps 1 and 2;
+ *      format and block formula in "Prerequisites / FP8 quantisation format");
+ *   2. activations are quantised dynamically in every forward pass (step 1),
+ *      here in 1x128 groups along K;
+ *   3. the linears run as W8A8 FP8 GEMMs with fp32 accumulation and bf16
+ *      output ("Core method": compute-level W8A8; "Results": FP8 GEMM
+ *      kernels), including the MoE expert linears fc1/fc2 (step 1), whose
+ *      token-to-expert assignment is a fixed, replayed integer routing
+ *      ("MoE RL routing replay (R3)", section 4).
+ *   The scale is fp32 (the main variant) or UE8M0, a power of two stored as a
+ *   biased 8-bit exponent ("Results", scale-format ablation).
+ *
+ * Numerics (readings of the pages, fixed here so that results are bit-exact):
+ *   scale      = amax / 448 in IEEE fp32 (a block of zeros gets scale 1.0);
+ *   UE8M0      = 2^e, e the smallest integer with 448 * 2^e >= amax, clamped
+ *                to [-127, 127], stored as the byte e + 127 (zeros: 127);
+ *   code       = E4M3 round-to-nearest-even, saturating at +-448, of the fp32
+ *                quotient x / scale (UE8M0: the exact x * 2^-e); the sign bit
+ *                of x is kept, so -0 gives 0x80;
+ *   GEMM       = Y[m][n] = bf16_rne( sum_kb sx[kb][m] * sw[n/128][kb] * P_kb[m][n] )
+ *                with P_kb the fp32-accumulated E4M3 products over the 128-wide
+ *                K chunk kb, scales applied in fp32 and one rounding at the end
+ *                ("Where Rounding Happens Matters": round once, at the end of
+ *                the fused region).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented as device pointers are device memory;
+ *     the caller allocates and owns all of it.  The library allocates no
+ *     memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  Results are ready once the stream
+ *     is synchronised.
+ *   - Arguments are validated on the host before any launch; a call that
+ *     returns an error launched nothing.
+ *   - Matrices are row-major with an explicit leading dimension in elements.
+ *   - No call throws; every call returns an fp8rl_status.
+ *   - Non-finite inputs give unspecified codes.
+ */
+#ifndef FP8RL_H
+#define FP8RL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP8RL_API __attribute__((visibility("default")))
+#else
+#define FP8RL_API
+#endif
+
+typedef enum {
+    FP8RL_OK = 0,
+    FP8RL_ERR_INVALID_ARG = 1, /* null pointer, negative size, unknown enum  */
+    FP8RL_ERR_SHAPE = 2,       /* a size the operation does not support      */
+    FP8RL_ERR_ALIGNMENT = 3,   /* pointer or leading dimension misaligned    */
+    FP8RL_ERR_UNSUPPORTED = 4, /* device is not sm_103 / feature unavailable */
+    FP8RL_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed       */
+    FP8RL_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out         */
+} fp8rl_status;
+
+typedef enum {
+    FP8RL_SCALE_FP32 = 0,  /* one fp32 scale per block or group          */
+    FP8RL_SCALE_UE8M0 = 1  /* one byte per block or group: exponent + 127 */
+} fp8rl_scale_fmt;
+
+/*
+ * Weight-sync quantisation of one bf16 matrix W [n][k] to E4M3 with one scale
+ * per 128x128 block ("Prerequisites / FP8 quantisation format": per-block
+ * scale, W_hat = round(W / scale); "Method steps", step 2: done at every
+ * weight sync).
+ *   w_bf16   device, bf16 [n][k], row stride ldw elements (ldw >= k)
+ *   q_e4m3   device, E4M3 bytes [n][k], row stride ldq bytes (ldq >= k)
+ *   w_scale  device, [ceil(n/128)][ceil(k/128)] row-major; fp32 or uint8 (fmt)
+ * Partial edge blocks take amax over their valid elements only.
+ * n == 0 or k == 0 is a no-op.
+ * Errors: INVALID_ARG (null pointer, n/k < 0, ld < k, bad fmt),
+ *         ALIGNMENT (w_bf16, q_e4m3 not 16-byte aligned, or w_scale not
+ *         4-byte aligned for fp32), CUDA (launch failure).
+ * Rows whose byte stride is not a multiple of 16 take a slower scalar path.
+ */
+FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise(const void* w_bf16, int64_t n, int64_t k,
+                                                    int64_t ldw, void* q_e4m3, int64_t ldq,
+                                                    void* w_scale, fp8rl_scale_fmt fmt,
+                                                    void* stream);
+
+/* One matrix of a batched weight sync. */
+typedef struct {
+    const void* w_bf16; /* device, bf16 [n][k], row stride ldw       */
+    void* q_e4m3;       /* device, E4M3 [n][k], row stride ldq       */
+    void* w_scale;      /* device, [ceil(n/128)][ceil(k/128)]         */
+    int64_t n, k, ldw, ldq;
+} fp8rl_weight_desc;
+
+/*
+ * Weight sync of many matrices in one pass (a whole model: every linear of
+ * every layer).  Same numerics and layout per matrix as
+ * fp8rl_quant_weight_blockwise.  `descs` is HOST memory, read during the
+ * call only; the descriptors travel to the device inside the launch
+ * parameters, so no device-side table is needed.  Matrices are processed as
+ * one grid of 128x128 blocks; large counts are split into a few launches.
+ * Errors: as fp8rl_quant_weight_blockwise, for any descriptor; count < 0 or a
+ * null descs with count > 0 is INVALID_ARG.  count == 0 is a no-op.
+ */
+FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise_batched(const fp8rl_weight_desc* descs,
+                                                            int32_t count, fp8rl_scale_fmt fmt,
+                                                            void* stream);
+
+/*
+ * Dynamic activation quantisation in 1x128 groups along K (one scale per token
+ * and per 128 columns; "Method steps", step 1: activations quantised in every
+ * forward pass).
+ *   x_bf16   device, bf16 [m][k], row stride ldx elements
+ *   q_e4m3   device, E4M3 [m][k], row stride ldq bytes
+ *   x_scale  device, [ceil(k/128)][m] (group-major, so that a GEMM reads one
+ *            contiguous run of m scales per K chunk); fp32 or uint8 (fmt)
+ * A partial last group takes amax over its valid columns.
+ * Errors: as fp8rl_quant_weight_blockwise.
+ */
+FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int64_t m, int64_t k, int64_t ldx,
+                                             void* q_e4m3, int64_t ldq, void* x_scale,
+                                             fp8rl_scale_fmt fmt, void* stream);
+
+/*
+ * Block-scaled W8A8 GEMM: Y = X W^T with E4M3 operands, fp32 accumulation per
+ * 128-wide K chunk on the tensor cores, the two chunk scales applied in fp32,
+ * and one bf16 round-to-nearest-even at the end ("Core method": W8A8
+ * linears; "Where Rounding Happens Matters": round once).
+ *   xq       device, E4M3 [m][k] row-major (row stride k)
+ *   x_scale  device, [k/128][m] (layout of fp8rl_quant_act_group)
+ *   wq       device, E4M3 [n][k] row-major (row stride k)
+ *   w_scale  device, [n/128][k/128] (layout of fp8rl_quant_weight_blockwise)
+ *   y_bf16   device, bf16 [m][n] row-major (row stride n)
+ * n and k must be multiples of 128 (SHAPE otherwise); m >= 0 is free.
+ * xq, wq and y_bf16 must be 16-byte aligned, the scales 4-byte (fp32).
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, UNSUPPORTED (not an sm_103 device),
+ *         CUDA; a device-side wait that runs out is reported as TIMEOUT by
+ *         the next fp8rl_sync_status.
+ */
+FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const void* x_scale, const void* wq,
+                                              const void* w_scale, void* y_bf16, int64_t m,
+                                              int64_t n, int64_t k, fp8rl_scale_fmt fmt,
+                                              void* stream);
+
+/*
+ * Grouped (MoE expert) block-scaled GEMM over row segments: for every expert e,
+ * rows offsets[e] .. offsets[e+1]-1 of X are multiplied by expert e's weights
+ * ("Method steps", step 1: MoE fc1 / fc2 are quantised; "MoE RL routing
+ * replay (R3)": the routing is a fixed integer assignment, so the segments
+ * are known before the call).
+ *   xq        device, E4M3 [rows][k] (rows grouped by expert)
+ *   x_scale   device, [k/128][rows]
+ *   wq        device, E4M3 [num_experts][n][k]
+ *   w_scale   device, [num_experts][n/128][k/128]
+ *   d_offsets device, int32 [num_experts + 1], offsets[0] == 0, non-decreasing,
+ *             offsets[num_experts] == rows.  Not read on the host; values
+ *             outside that contract give unspecified output (rows outside every
+ *             segment are left unwritten), never an out-of-bounds access.
+ *   y_bf16    device, bf16 [rows][n]
+ * Errors: as fp8rl_gemm_blockscaled; num_experts < 1 is INVALID_ARG.
+ */
+FP8RL_API fp8rl_status fp8rl_grouped_gemm_blockscaled(const void* xq, const void* x_scale,
+                                                      const void* wq, const void* w_scale,
+                                                      const int32_t* d_offsets, int64_t num_experts,
+                                                      int64_t rows, int64_t n, int64_t k,
+                                                      void* y_bf16, fp8rl_scale_fmt fmt,
+                                                      void* stream);
+
+/*
+ * The device E4M3 codec alone: out[i] = E4M3 code of the fp32 in[i],
+ * round-to-nearest-even, saturating at +-448, sign bit kept (the conversion
+ * every quantiser above applies to its fp32 quotient; FP8-RL page,
+ * "Prerequisites / FP8 quantisation format").  Exposed so that the whole fp32
+ * input space can be checked against an independent encoder.
+ *   d_in   device, fp32 [n] (4-byte aligned)
+ *   d_out  device, uint8 [n]
+ * Errors: INVALID_ARG (n < 0, null pointer with n > 0), ALIGNMENT, CUDA.
+ */
+FP8RL_API fp8rl_status fp8rl_e4m3_encode(const float* d_in, int64_t n, uint8_t* d_out, void* stream);
+
+/*
+ * Synchronise `stream` and report the first error recorded since the last
+ * call: a failed launch (CUDA), or a device-side wait that ran out (TIMEOUT).
+ * Clears the recorded device error word of the current device.
+ */
+FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
+
+/* Static, NUL-terminated name of a status code. */
+FP8RL_API const char* fp8rl_status_string(fp8rl_status s);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+FP8RL_API int32_t fp8rl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8RL_H */

@@ -1,0 +1,133 @@
+"""The C ABI library builds, loads and exports every declared entry point, and
+rejects bad arguments on the host before touching the GPU.  CPU only: no call
+here reaches a kernel launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import fp8_w8a8_rollout_gb300 as fp8rl
+from fp8_w8a8_rollout_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"FP8RL_API\s+[\w\s\*]+?\b(fp8rl_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fp8rl.load_library()
+
+
+def test_header_declares_the_path_entry_points():
+    names = declared_entry_points()
+    for required in ("fp8rl_quant_weight_blockwise", "fp8rl_quant_act_group",
+                     "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
+                     "fp8rl_quant_weight_blockwise_batched", "fp8rl_sync_status",
+                     "fp8rl_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(fp8rl_\w+)", out))
+    declared = set(declared_entry_points())
+    assert declared <= exported, declared - exported
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_library_targets_sm103a_only():
+    # the build passes exactly one -gencode, for sm_103a
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code, name in fp8rl.STATUS.items():
+        assert fp8rl.fp8rl_status_string(code) == name
+    assert fp8rl.fp8rl_version() >= 100
+
+
+def _rc(fn, *args):
+    return getattr(fp8rl.load_library(), fn)(*args)
+
+
+def test_weight_quant_rejects_bad_arguments_on_host(lib):
+    a16 = 1 << 20  # an aligned fake address (never dereferenced: validation fails first)
+    # null pointers
+    assert _rc("fp8rl_quant_weight_blockwise", None, 128, 128, 128, a16, 128, a16, 0, None) == 1
+    # negative sizes, short leading dimensions, unknown format
+    assert _rc("fp8rl_quant_weight_blockwise", a16, -1, 128, 128, a16, 128, a16, 0, None) == 1
+    assert _rc("fp8rl_quant_weight_blockwise", a16, 128, 128, 64, a16, 128, a16, 0, None) == 1
+    assert _rc("fp8rl_quant_weight_blockwise", a16, 128, 128, 128, a16, 128, a16, 7, None) == 1
+    # misaligned pointers
+    assert _rc("fp8rl_quant_weight_blockwise", a16 + 2, 128, 128, 128, a16, 128, a16, 0, None) == 3
+    assert _rc("fp8rl_quant_weight_blockwise", a16, 128, 128, 128, a16 + 1, 128, a16, 0, None) == 3
+    assert _rc("fp8rl_quant_weight_blockwise", a16, 128, 128, 128, a16, 128, a16 + 2, 0, None) == 3
+    # empty work is fine and launches nothing
+    assert _rc("fp8rl_quant_weight_blockwise", None, 0, 128, 128, None, 128, None, 0, None) == 0
+
+
+def test_act_quant_rejects_bad_arguments_on_host(lib):
+    a16 = 1 << 20
+    assert _rc("fp8rl_quant_act_group", None, 16, 256, 256, a16, 256, a16, 0, None) == 1
+    assert _rc("fp8rl_quant_act_group", a16 + 8, 16, 256, 256, a16, 256, a16, 0, None) == 3
+    assert _rc("fp8rl_quant_act_group", a16, 0, 256, 256, a16, 256, a16, 0, None) == 0
+
+
+def test_batched_rejects_bad_descriptors(lib):
+    a16 = 1 << 20
+    descs = (fp8rl.WeightDesc * 2)()
+    descs[0] = fp8rl.WeightDesc(a16, a16, a16, 128, 128, 128, 128)
+    descs[1] = fp8rl.WeightDesc(a16 + 2, a16, a16, 128, 128, 128, 128)
+    assert _rc("fp8rl_quant_weight_blockwise_batched", descs, 2, 0, None) == 3
+    assert _rc("fp8rl_quant_weight_blockwise_batched", None, 1, 0, None) == 1
+    assert _rc("fp8rl_quant_weight_blockwise_batched", descs, -1, 0, None) == 1
+    assert _rc("fp8rl_quant_weight_blockwise_batched", descs, 0, 0, None) == 0
+
+
+def test_gemm_rejects_bad_shapes_and_alignment_on_host(lib):
+    a16 = 1 << 20
+    g = "fp8rl_gemm_blockscaled"
+    assert _rc(g, None, a16, a16, a16, a16, 16, 256, 256, 0, None) == 1
+    assert _rc(g, a16, a16, a16, a16, a16, 16, 200, 256, 0, None) == 2  # n % 128
+    assert _rc(g, a16, a16, a16, a16, a16, 16, 256, 300, 0, None) == 2  # k % 128
+    assert _rc(g, a16, a16, a16, a16, a16, -1, 256, 256, 0, None) == 1
+    assert _rc(g, a16 + 8, a16, a16, a16, a16, 16, 256, 256, 0, None) == 3
+    assert _rc(g, a16, a16, a16, a16, a16 + 2, 16, 256, 256, 0, None) == 3
+    assert _rc(g, a16, a16, a16, a16, a16, 16, 256, 256, 9, None) == 1
+    assert _rc(g, a16, a16, a16, a16, a16, 0, 256, 256, 0, None) == 0  # m == 0: no-op
+
+
+def test_grouped_gemm_rejects_bad_arguments_on_host(lib):
+    a16 = 1 << 20
+    g = "fp8rl_grouped_gemm_blockscaled"
+    assert _rc(g, a16, a16, a16, a16, None, 4, 64, 256, 256, a16, 0, None) == 1
+    assert _rc(g, a16, a16, a16, a16, a16, 0, 64, 256, 256, a16, 0, None) == 1
+    assert _rc(g, a16, a16, a16, a16, a16, 4, 64, 200, 256, a16, 0, None) == 2
+    assert _rc(g, a16, a16, a16, a16, a16, 4, 64, 256, 256, a16 + 4, 0, None) == 3
+    assert _rc(g, a16, a16, a16, a16, a16, 4, 0, 256, 256, a16, 0, None) == 0
+
+
+def test_codec_entry_rejects_bad_arguments(lib):
+    assert _rc("fp8rl_e4m3_encode", None, 10, None, None) == 1
+    assert _rc("fp8rl_e4m3_encode", (1 << 20) + 2, 10, 1 << 20, None) == 3
+    assert _rc("fp8rl_e4m3_encode", None, 0, None, None) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(fp8rl, "_lib", None)
+    with pytest.raises(FileNotFoundError):
+        fp8rl.load_library()
