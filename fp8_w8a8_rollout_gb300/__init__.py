@@ -25,7 +25,7 @@ __all__ = [
     "Fp8rlError", "SCALE_FP32", "SCALE_UE8M0", "load_library", "library_path",
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
-    "fp8rl_e4m3_encode", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
+    "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
     "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm",
 ]
 
@@ -79,6 +79,7 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
             "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
             "fp8rl_e4m3_encode": [vp, i64, vp, vp],
+            "fp8rl_debug_set": [i32, i64],
             "fp8rl_sync_status": [vp],
             "fp8rl_status_string": [st],
             "fp8rl_version": [],
@@ -157,6 +158,13 @@ def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_expe
 
 def fp8rl_e4m3_encode(d_in, n, d_out, stream=None) -> None:
     _ok(load_library().fp8rl_e4m3_encode(_p(d_in), n, _p(d_out), _stream(stream)), "fp8rl_e4m3_encode")
+
+
+DEBUG_RESET, DEBUG_GEMM_BN, DEBUG_FAULT_SKIP_KB, DEBUG_TIMEOUT_NS = 0, 1, 2, 3
+
+
+def fp8rl_debug_set(key, value) -> None:
+    _ok(load_library().fp8rl_debug_set(int(key), int(value)), "fp8rl_debug_set")
 
 
 def fp8rl_sync_status(stream=None) -> int:

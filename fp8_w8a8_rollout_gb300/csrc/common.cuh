@@ -49,6 +49,27 @@ __device__ __forceinline__ float scale_fp32(float amax) {
   return amax == 0.0f ? 1.0f : __fdiv_rn(amax, kE4M3Max);
 }
 
+// Correctly rounded x / s from r = RN(1/s), in three fp32 operations
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990: with r the correctly
+// rounded reciprocal and q0 = RN(x r) within one ulp of x / s, the remainder
+// x - q0 s is exact under an FMA and one more FMA gives RN(x / s)).  The
+// remainder is formed as q0 s - x and subtracted, so that x = -0 gives -0.
+// Valid while s, x / s and the remainder stay in the normal range; callers use
+// it only for scales s >= kFastDivMinScale, where every quotient that can round
+// to a non-zero E4M3 code is a normal number.  Checked bit for bit against IEEE
+// division by the GPU tests: every bf16 x against every amax mantissa at
+// exponents across the whole range, both sides of the threshold included (the
+// quotient is unchanged when x and amax share a power-of-two shift away from
+// the ends of the range).
+constexpr float kFastDivMinScale = 0x1p-80f;
+
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(q0, s, -x);
+  return __fmaf_rn(-e, r, q0);
+}
+
 // UE8M0 exponent: smallest e with 448 * 2^e >= amax, in [-127, 127]; zeros: 0.
 // amax is a finite bf16 magnitude, so the fp64 comparison is exact.
 __device__ __forceinline__ int scale_ue8m0_exponent(float amax) {

@@ -1,8 +1,308 @@
-// gemm.cu -- block-scaled W8A8 GEMMs (host validation; the tcgen05 kernels follow).
+// gemm.cu -- block-scaled W8A8 GEMMs on sm_103a tensor cores (tcgen05 + TMEM).
+//
+//   Y[m][n] = bf16_rne( sum_kb sx[kb][m] * sw[n/128][kb] * P_kb[m][n] )
+//
+// P_kb is the product of the E4M3 tiles over one 128-wide K chunk, accumulated
+// in fp32 by the tensor cores; the two chunk scales are applied in fp32 on the
+// way out of TMEM and Y is rounded to bf16 once ("FP8-RL", "Core method":
+// compute-level W8A8 linears with 128x128 weight blocks; "Where Rounding
+// Happens Matters": keep fp32 inside the fused region, round once).
+//
+// One CTA computes a 128 x BN output tile (BN = 128 or 256):
+//   warp 0, one lane   TMA producer: per K chunk, a 128x128 E4M3 tile of X and a
+//                      BN x 128 tile of W (128-byte swizzle) into a ring of
+//                      shared-memory stages;
+//   warp 1, one lane   MMA issuer: four tcgen05.mma (M=128, N=BN, K=32) per chunk
+//                      into one of two TMEM accumulators, then commits;
+//   warps 2, 3         idle (they complete warpgroup 0);
+//   warps 4..          epilogue, one warpgroup per 128 columns: per chunk,
+//                      tcgen05.ld the partial product, fold
+//                      it into fp32 registers with sx * sw, release the TMEM
+//                      buffer (so the tensor cores fill the other one meanwhile);
+//                      finally round to bf16 and store.
+// Every mbarrier wait is bounded; a wait that runs out raises a CTA abort flag
+// and the device error word, and all roles leave through the common teardown,
+// which releases TMEM.
+//
+// The MoE grouped variant is the same kernel over row segments: CTA x-index ->
+// (expert, 128-row tile of that expert's segment) from the device offsets;
+// rows past the segment end are computed and not stored.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace fp8rl {
+
+uint32_t* device_error_word();  // api.cu
+
 namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;     // tile rows (tcgen05 M)
+constexpr int kBK = 128;     // K chunk: one scale block, one 128-byte swizzle row
+constexpr int kUmmaK = 32;   // K of one E4M3 tcgen05.mma
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kEpiWarps = BN / 32;      // one warpgroup per 128 columns
+  static constexpr int kThreads = 128 + BN;      // warpgroup 0: producer, MMA, two idle warps
+  static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  // register split for BN = 256 (384 threads launch with <= 168 each): the
+  // role warpgroup gives registers back, the epilogue warpgroups take them.
+  // 128 * 56 + 256 * 208 = 60416 must not exceed 384 * (registers at launch);
+  // the host checks that before launching.
+  static constexpr bool kSplitRegs = BN == 256;
+  static constexpr int kRoleRegs = 56;
+  static constexpr int kEpiRegs = 208;
+  static constexpr int kMinLaunchRegs = (128 * kRoleRegs + BN * kEpiRegs + kThreads - 1) / kThreads;
+};
+
+struct GemmArgs {
+  const void* sx;            // [K/128][rows], fp32 or UE8M0 bytes
+  const void* sw;            // [experts][N/128][K/128]
+  __nv_bfloat16* y;          // [rows][N]
+  const int32_t* offsets;    // device [experts + 1], or null: one segment [0, rows)
+  int32_t rows, n, k, experts;
+  uint32_t* err;
+  uint64_t timeout_ns;
+  int32_t fault_skip_kb;     // test hook: the producer never fills this K chunk (-1: off)
+};
+
+template <bool UE8M0>
+__device__ __forceinline__ float load_scale(const void* p, int64_t idx) {
+  if (UE8M0) {
+    const uint32_t b = __ldg(static_cast<const uint8_t*>(p) + idx);
+    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+  }
+  return __ldg(static_cast<const float*>(p) + idx);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int BN, bool UE8M0>
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                            const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + C::kStages * C::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* tile = abort_flag + 1;  // expert, first row, segment end
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_kb = a.k / kBK;
+  const int n0 = blockIdx.y * BN;
+
+  // ---- which rows this CTA covers
+  if (warp == 0) {
+    int e = -1, row0 = 0, seg_end = 0;
+    if (a.offsets == nullptr) {
+      row0 = blockIdx.x * kBM;
+      seg_end = a.rows;
+      e = row0 < a.rows ? 0 : -1;
+    } else {
+      // running prefix over experts of their 128-row tile counts, 32 at a time
+      const int target = blockIdx.x;
+      int done = 0;
+      for (int e0 = 0; e0 < a.experts && e < 0; e0 += 32) {
+        const int ex = e0 + lane;
+        int start = 0, end = 0;
+        if (ex < a.experts) {
+          start = min(max(a.offsets[ex], 0), a.rows);
+          end = min(max(a.offsets[ex + 1], 0), a.rows);
+          end = max(end, start);
+        }
+        const int tiles = (end - start + kBM - 1) / kBM;
+        int incl = tiles;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const int excl = incl - tiles;
+        const bool hit = tiles > 0 && target >= done + excl && target < done + incl;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (m) {
+          const int src = __ffs(m) - 1;
+          const int se = __shfl_sync(0xffffffffu, ex, src);
+          const int sst = __shfl_sync(0xffffffffu, start, src);
+          const int sen = __shfl_sync(0xffffffffu, end, src);
+          const int sex = __shfl_sync(0xffffffffu, excl, src);
+          e = se;
+          row0 = sst + (target - done - sex) * kBM;
+          seg_end = sen;
+        }
+        done += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      tile[0] = e;
+      tile[1] = row0;
+      tile[2] = seg_end;
+    }
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), C::kEpiWarps * 32);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int expert = tile[0];
+  if (expert < 0) return;  // the grid is an upper bound on the tiles; CTA-uniform
+  const int row0 = tile[1], seg_end = tile[2];
+
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abortv = abort_flag;
+
+  if (warp < 4) {
+  if (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRoleRegs));
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_x);
+      prefetch_tensormap(&tmap_w);
+      const int wrow0 = expert * a.n + n0;
+      int issued = 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns)) break;
+        issued = kb + 1;
+        if (kb == a.fault_skip_kb) continue;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, row0, fb);
+        tma_load_2d(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
+      }
+      if (*abortv) {
+        // let the copies still in flight land before shared memory is released
+        for (int kb = max(0, issued - C::kStages); kb < issued; ++kb) {
+          if (kb == a.fault_skip_kb) continue;
+          mbar_wait_bounded(smem_u32(&full[kb % C::kStages]), (kb / C::kStages) & 1, nullptr, nullptr,
+                            10000000ull);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        const int buf = kb & 1;
+        const uint32_t bph = (kb >> 1) & 1;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns)) break;
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * BN;
+        const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k)
+          mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                   k > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&empty[s]));
+        mma_commit(smem_u32(&tfull[buf]));
+      }
+      if (*abortv) {
+        // no MMA may still be writing TMEM when it is released
+        mma_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+      }
+    }
+    __syncwarp();
+  }
+  } else {
+    if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 4;
+    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. +31
+    const int half = ew >> 2;   // which 128 columns of the tile
+    const int r = quad * 32 + lane;
+    const int grow = row0 + r;
+    const bool row_ok = grow < seg_end;
+    const int nb = (n0 >> 7) + half;
+    const int64_t sw_base = ((int64_t)expert * (a.n / 128) + nb) * num_kb;
+    float acc[128];
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+    float sx_next = (row_ok && num_kb > 0) ? load_scale<UE8M0>(a.sx, grow) : 0.0f;
+    bool ok = true;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int buf = kb & 1;
+      const uint32_t bph = (kb >> 1) & 1;
+      const float f = sx_next * load_scale<UE8M0>(a.sw, sw_base + kb);
+      if (kb + 1 < num_kb && row_ok) sx_next = load_scale<UE8M0>(a.sx, (int64_t)(kb + 1) * a.rows + grow);
+      ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + half * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(taddr + c * 16, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = __fmaf_rn(__uint_as_float(v[j]), f, acc[c * 16 + j]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[buf]));
+    }
+    if (ok && row_ok && !*abortv) {
+      uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + half * 128);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[j] = make_uint4(pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]), pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
+                            pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 fp8rl_status check_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale,
@@ -11,11 +311,139 @@ fp8rl_status check_gemm(const void* xq, const void* x_scale, const void* wq, con
   if (m < 0 || n < 0 || k < 0) return FP8RL_ERR_INVALID_ARG;
   if (n % 128 || k % 128) return FP8RL_ERR_SHAPE;
   if (m == 0 || n == 0) return FP8RL_OK;
+  if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return FP8RL_ERR_SHAPE;
   if (!xq || !x_scale || !wq || !w_scale || !y) return FP8RL_ERR_INVALID_ARG;
   if (!aligned(xq, 16) || !aligned(wq, 16) || !aligned(y, 16)) return FP8RL_ERR_ALIGNMENT;
   if (fmt == FP8RL_SCALE_FP32 && (!aligned(x_scale, 4) || !aligned(w_scale, 4))) return FP8RL_ERR_ALIGNMENT;
   return FP8RL_OK;
 }
+
+// test hooks (set through fp8rl_debug_set)
+struct Debug {
+  int bn = 0;                     // 0: choose; 128 or 256: force the tile width
+  int fault_skip_kb = -1;         // the producer skips this K chunk (forces a timeout)
+  uint64_t timeout_ns = 2000000000ull;
+};
+Debug g_debug;
+std::mutex g_mu;
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// row-major E4M3 matrix [outer][inner] (inner contiguous), boxes of box_outer rows x 128 bytes
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+};
+
+DeviceInfo device_info() {
+  static DeviceInfo cache[64];
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return {};
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!done[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].ok = major == 10 && minor == 3;
+    cache[dev].sms = sms;
+    done[dev] = true;
+  }
+  return cache[dev];
+}
+
+template <int BN, bool UE8M0>
+fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t grid_x, const GemmArgs& args,
+                    cudaStream_t stream) {
+  using C = Cfg<BN>;
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, xq, args.k, args.rows, kBM)) return FP8RL_ERR_CUDA;
+  if (!make_map(&mw, wq, args.k, (uint64_t)experts * args.n, BN)) return FP8RL_ERR_CUDA;
+  auto kernel = gemm_blockscaled_kernel<BN, UE8M0>;
+  if (C::kSplitRegs) {
+    // setmaxnreg.inc waits until the block has the registers it asks for; make
+    // sure the launch allocation covers the split, or it would wait forever
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8RL_ERR_CUDA;
+    if (fa.numRegs < C::kMinLaunchRegs) return FP8RL_ERR_UNSUPPORTED;
+  }
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return FP8RL_ERR_CUDA;
+  dim3 grid((unsigned)grid_x, (unsigned)(args.n / BN));
+  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, args);
+  return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
+fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void* w_scale,
+                 const int32_t* d_offsets, int64_t experts, int64_t rows, int64_t n, int64_t k, void* y,
+                 fp8rl_scale_fmt fmt, void* stream) {
+  const DeviceInfo di = device_info();
+  if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
+  uint32_t* err = device_error_word();
+  if (!err) return FP8RL_ERR_CUDA;
+  Debug dbg;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    dbg = g_debug;
+  }
+  GemmArgs args{};
+  args.sx = x_scale;
+  args.sw = w_scale;
+  args.y = static_cast<__nv_bfloat16*>(y);
+  args.offsets = d_offsets;
+  args.rows = (int32_t)rows;
+  args.n = (int32_t)n;
+  args.k = (int32_t)k;
+  args.experts = (int32_t)experts;
+  args.err = err;
+  args.timeout_ns = dbg.timeout_ns;
+  args.fault_skip_kb = dbg.fault_skip_kb;
+  const int64_t m_tiles = (rows + kBM - 1) / kBM;
+  const int64_t grid_x = d_offsets ? m_tiles + experts : m_tiles;
+  int bn = dbg.bn;
+  if (bn != 128 && bn != 256) {
+    // wide tiles when there are enough of them to fill every SM
+    bn = (n % 256 == 0 && m_tiles * (n / 256) >= 2 * (int64_t)di.sms) ? 256 : 128;
+  }
+  if (bn == 256 && n % 256) bn = 128;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const bool ue = fmt == FP8RL_SCALE_UE8M0;
+  if (bn == 256)
+    return ue ? launch<256, true>(xq, wq, experts, grid_x, args, cs)
+              : launch<256, false>(xq, wq, experts, grid_x, args, cs);
+  return ue ? launch<128, true>(xq, wq, experts, grid_x, args, cs)
+            : launch<128, false>(xq, wq, experts, grid_x, args, cs);
+}
+
 }  // namespace
 }  // namespace fp8rl
 
@@ -27,8 +455,7 @@ extern "C" FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const v
                                                          fp8rl_scale_fmt fmt, void* stream) {
   fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, m, n, k, fmt);
   if (st != FP8RL_OK || m == 0 || n == 0) return st;
-  (void)stream;
-  return FP8RL_ERR_UNSUPPORTED;
+  return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream);
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_blockscaled(const void* xq, const void* x_scale,
@@ -40,6 +467,27 @@ extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_blockscaled(const void* xq,
   if (num_experts < 1 || !d_offsets) return FP8RL_ERR_INVALID_ARG;
   fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, rows, n, k, fmt);
   if (st != FP8RL_OK || rows == 0 || n == 0) return st;
-  (void)stream;
-  return FP8RL_ERR_UNSUPPORTED;
+  if (num_experts > INT32_MAX / 2 || num_experts * n > INT32_MAX) return FP8RL_ERR_SHAPE;
+  return run(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k, y, fmt, stream);
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  switch (key) {
+    case 1:
+      if (value != 0 && value != 128 && value != 256) return FP8RL_ERR_INVALID_ARG;
+      g_debug.bn = (int)value;
+      return FP8RL_OK;
+    case 2:
+      g_debug.fault_skip_kb = value < 0 ? -1 : (int)value;
+      return FP8RL_OK;
+    case 3:
+      if (value <= 0) return FP8RL_ERR_INVALID_ARG;
+      g_debug.timeout_ns = (uint64_t)value;
+      return FP8RL_OK;
+    case 0:
+      g_debug = Debug{};
+      return FP8RL_OK;
+  }
+  return FP8RL_ERR_INVALID_ARG;
 }

@@ -56,13 +56,22 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
                : "memory");
 }
 
-// 8 bf16 (one uint4) -> 8 E4M3 codes (two 32-bit words), fp32-scale variant
-__device__ __forceinline__ uint2 quant8_div(uint4 v, float s) {
+// 8 bf16 (one uint4) -> 8 E4M3 codes (two 32-bit words), fp32-scale variant:
+// IEEE division for tiny scales, else the three-operation division by the
+// block's correctly rounded reciprocal rcp (same result, see div_by_scale).
+__device__ __forceinline__ uint2 quant8_div(uint4 v, float s, float rcp) {
   uint2 r;
-  r.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
-        (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
-  r.y = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
-        (e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+  if (s >= kFastDivMinScale) {
+    r.x = e4m3x2(div_by_scale(bf16_lo(v.x), s, rcp), div_by_scale(bf16_hi(v.x), s, rcp)) |
+          (e4m3x2(div_by_scale(bf16_lo(v.y), s, rcp), div_by_scale(bf16_hi(v.y), s, rcp)) << 16);
+    r.y = e4m3x2(div_by_scale(bf16_lo(v.z), s, rcp), div_by_scale(bf16_hi(v.z), s, rcp)) |
+          (e4m3x2(div_by_scale(bf16_lo(v.w), s, rcp), div_by_scale(bf16_hi(v.w), s, rcp)) << 16);
+  } else {
+    r.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
+    r.y = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+  }
   return r;
 }
 
@@ -137,10 +146,11 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
         }
       } else {
         const float s = scale_fp32(amax);
+        const float rcp = __frcp_rn(s);
         if (t == 0) static_cast<float*>(D.scale)[local] = s;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          uint2 a = quant8_div(v[i][0], s), b = quant8_div(v[i][1], s);
+          uint2 a = quant8_div(v[i][0], s, rcp), b = quant8_div(v[i][1], s, rcp);
           st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
         }
       }
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
         if (lane16 == 0) static_cast<uint8_t*>(scale)[g[u] * m + row[u]] = (uint8_t)(e + 127);
       } else {
         const float s = scale_fp32(amax);
-        codes = quant8_div(v[u], s);
+        codes = quant8_div(v[u], s, __frcp_rn(s));
         if (lane16 == 0) static_cast<float*>(scale)[g[u] * m + row[u]] = s;
       }
       const int64_t c = g[u] * kBlock + lane16 * 8;

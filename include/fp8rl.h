@@ -193,6 +193,19 @@ FP8RL_API fp8rl_status fp8rl_e4m3_encode(const float* d_in, int64_t n, uint8_t* 
  */
 FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
 
+/*
+ * Test hooks for the GEMMs (no counterpart on the pages), applied to later
+ * launches from any thread:
+ *   key 1  tile width: 0 chooses per shape (default), 128 or 256 forces it;
+ *   key 2  fault injection: the TMA producer skips K chunk `value` (negative:
+ *          off), so the MMA warp's bounded wait runs out and the call reports
+ *          TIMEOUT through fp8rl_sync_status (no trap, no hang);
+ *   key 3  limit of every device-side wait, in nanoseconds (default 2e9);
+ *   key 0  restore all defaults.
+ * Errors: INVALID_ARG for an unknown key or value.
+ */
+FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value);
+
 /* Static, NUL-terminated name of a status code. */
 FP8RL_API const char* fp8rl_status_string(fp8rl_status s);
 

@@ -1,0 +1,235 @@
+"""GPU parity of the block-scaled W8A8 GEMMs (dense and MoE grouped) against
+the fp64 CPU oracle, through the C ABI.
+
+The E4M3 operands and their scales are produced by the ORACLE's quantisers on
+the host and uploaded, so the GEMM is checked on inputs that never passed
+through the CUDA path.  Bar: |gpu - ref| <= 1e-2 |ref| + 1e-3 rms(ref), with
+rms over the whole reference output (over the sampled values where the oracle
+evaluates a sample)."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_w8a8_rollout_gb300 as fp8rl
+import oracle
+from fp8_w8a8_rollout_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [fp8rl.SCALE_FP32, fp8rl.SCALE_UE8M0]
+RTOL, ATOL_RMS = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fp8rl.load_library(build_if_missing=True)
+    yield
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+
+
+@pytest.fixture(params=[0, 128, 256], ids=["bn-auto", "bn128", "bn256"])
+def bn(request):
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, request.param)
+    yield request.param
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, 0)
+
+
+def within(got, ref, rms=None):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if rms is None:
+        rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    err = np.abs(got - ref)
+    bound = RTOL * np.abs(ref) + ATOL_RMS * rms
+    bad = int(np.count_nonzero(err > bound))
+    assert bad == 0, f"{bad}/{ref.size} outside tolerance; worst excess {float((err - bound).max()):.3e}"
+
+
+def oracle_operands(x_bf16, w_bf16, fmt):
+    """Oracle-quantised operands (host numpy) for X [m,k] and W [n,k]."""
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x_bf16), fmt)
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w_bf16), fmt)
+    return xq, sx, wq, sw
+
+
+def to_dev(*arrs):
+    return [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in arrs]
+
+
+def run_gemm(xq, sx, wq, sw, fmt):
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    y = fp8rl.gemm(dx, dsx, dw, dsw, fmt)
+    assert fp8rl.fp8rl_sync_status() == 0
+    return y.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_tiny_linear(fmt, bn):
+    """256x256 weight with one all-zero block, 16 tokens."""
+    w, x = synth.tiny_linear(0)
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    y = run_gemm(xq, sx, wq, sw, fmt)
+    within(y, oracle.gemm_blockscaled(xq, sx, wq, sw, fmt))
+
+
+def test_tiny_linear_zero_block_contributes_nothing():
+    w, x = synth.tiny_linear(0)
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    # the product without K-block 1 for rows 0..127 of W equals Y there
+    xq0, sx0 = xq.copy(), sx.copy()
+    xq0[:, 128:] = 0
+    ref = oracle.gemm_blockscaled(xq0, sx0, wq, sw)
+    within(y[:, :128], ref[:, :128])
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m,n,k", [(1, 128, 128), (15, 256, 256), (129, 384, 1024), (300, 256, 640),
+                                   (128, 512, 128), (257, 128, 384)])
+def test_ragged_shapes(m, n, k, fmt, bn):
+    if bn == 256 and n % 256:
+        pytest.skip("tile width 256 needs n % 256 == 0 (falls back to 128)")
+    x = synth.activation_bf16(m, k, 7, "gemm-ragged", m, n, k)
+    w = synth.weight_bf16(n, k, 8, "gemm-ragged", m, n, k)
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    within(run_gemm(xq, sx, wq, sw, fmt), oracle.gemm_blockscaled(xq, sx, wq, sw, fmt))
+
+
+def test_identity_weight_returns_rounded_activations():
+    m, k = 64, 256
+    x = synth.activation_bf16(m, k, 9, "gemm-id")
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
+    wq = np.zeros((k, k), np.uint8)
+    np.fill_diagonal(wq, 0x38)  # 1.0
+    sw = np.ones((k // 128, k // 128), np.float32)
+    y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    xd = oracle.dequantize(xq, sx.T, 1, 128)
+    # the kernel rounds the exact product once to fp32 (the FMA) and once to bf16
+    expect = torch.from_numpy(xd.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(y, expect)
+
+
+@pytest.mark.parametrize("name,n,k", synth.QWEN3_8B_GEMMS)
+@pytest.mark.parametrize("m", [16, 128])
+def test_qwen3_8b_shapes_small_m_full(name, n, k, m):
+    x = synth.activation_bf16(m, k, 10, "gemm-q", name, m)
+    w = synth.weight_bf16(n, k, 11, "gemm-q", name)
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    within(run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32), oracle.gemm_blockscaled(xq, sx, wq, sw))
+
+
+def sample_positions(m, n, rows_full, count, seed):
+    rng = np.random.default_rng(seed)
+    full_rows = np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, rows_full)]))
+    rr = np.repeat(full_rows, n)
+    cc = np.tile(np.arange(n), full_rows.size)
+    rr = np.concatenate([rr, rng.integers(0, m, count)])
+    cc = np.concatenate([cc, rng.integers(0, n, count)])
+    return rr, cc
+
+
+@pytest.mark.parametrize("name,n,k", synth.QWEN3_8B_GEMMS)
+@pytest.mark.parametrize("m", [1024, 8192])
+def test_qwen3_8b_shapes_large_m_sampled(name, n, k, m):
+    """Full-size launch; the oracle evaluates 4 whole rows plus 4096 random outputs."""
+    x = synth.activation_bf16(m, k, 12, "gemm-q", name, m)
+    w = synth.weight_bf16(n, k, 13, "gemm-q", name)
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    rr, cc = sample_positions(m, n, 2, 4096, m + n)
+    ref = oracle.gemm_blockscaled_at(xq, sx, wq, sw, rr, cc)
+    within(y[rr, cc], ref)
+
+
+def test_ue8m0_large_m_sampled():
+    m, n, k = 8192, 24576, 4096
+    x = synth.activation_bf16(m, k, 14, "gemm-ue")
+    w = synth.weight_bf16(n, k, 15, "gemm-ue")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_UE8M0)
+    y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_UE8M0)
+    rr, cc = sample_positions(m, n, 2, 4096, 3)
+    within(y[rr, cc], oracle.gemm_blockscaled_at(xq, sx, wq, sw, rr, cc, fp8rl.SCALE_UE8M0))
+
+
+def test_m_zero_is_a_no_op():
+    y = torch.full((1, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    xq = torch.zeros((1, 128), dtype=torch.uint8, device="cuda")
+    fp8rl.fp8rl_gemm_blockscaled(xq, xq, xq, xq, y, 0, 128, 128)
+    assert fp8rl.fp8rl_sync_status() == 0 and float(y[0, 0]) == 7.0
+
+
+# --------------------------------------------------------------------------- grouped
+
+def grouped_case(counts, n, k, fmt, seed):
+    offsets = synth.routing_with_counts(counts)
+    rows = int(offsets[-1])
+    e = len(counts)
+    x = synth.normal_bf16((max(rows, 1), k), 1.0, seed, "grp-x", n, k)[:rows]
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x), fmt)
+    ws = synth.moe_expert_weights(n, k, e, seed, 0, f"grp{n}x{k}")
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(ws.reshape(e * n, k)), fmt)
+    wq = wq.reshape(e, n, k)
+    sw = sw.reshape(e, n // 128, k // 128)
+    return offsets, xq, sx, wq, sw
+
+
+def run_grouped(offsets, xq, sx, wq, sw, fmt, fill=None):
+    dx, dsx, dw, dsw, doff = to_dev(xq, sx, wq, sw, offsets)
+    rows, n = xq.shape[0], wq.shape[1]
+    out = torch.empty((rows, n), dtype=torch.bfloat16, device="cuda")
+    if fill is not None:
+        out.fill_(fill)
+    fp8rl.grouped_gemm(dx, dsx, dw, dsw, doff, fmt, out=out)
+    assert fp8rl.fp8rl_sync_status() == 0
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("counts", [[3, 0, 200, 129], [128, 128], [0, 0, 5], [1], [300, 0, 0, 1, 0]])
+def test_grouped_small_full(counts, fmt, bn):
+    n, k = 256, 384
+    offsets, xq, sx, wq, sw = grouped_case(counts, n, k, fmt, sum(counts))
+    y = run_grouped(offsets, xq, sx, wq, sw, fmt)
+    within(y, oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, fmt))
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_grouped_qwen3_30b_a3b_sampled(which):
+    """128 experts, T = 4096 tokens routed top-8 by replayed indices; the
+    oracle evaluates the first and last row of every non-empty segment plus
+    4096 random outputs."""
+    r = synth.moe_routing(4096, 128, 8, seed=0, layer=0)
+    n, k = (1536, 2048) if which == "gate_up" else (2048, 768)
+    rows = int(r.offsets[-1])
+    x = synth.normal_bf16((rows, k), 1.0, 0, "moe-x", which)
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
+    ws = synth.moe_expert_weights(n, k, 128, 0, 0, which)
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(ws.reshape(-1, k)))
+    wq = wq.reshape(128, n, k)
+    sw = sw.reshape(128, n // 128, k // 128)
+    y = run_grouped(r.offsets, xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    rng = np.random.default_rng(5)
+    edge_rows = []
+    for e in range(128):
+        a, b = int(r.offsets[e]), int(r.offsets[e + 1])
+        if b > a:
+            edge_rows += [a, b - 1]
+    er = np.array(edge_rows)
+    rr = np.concatenate([er, rng.integers(0, rows, 4096)])
+    cc = np.concatenate([rng.integers(0, n, er.size), rng.integers(0, n, 4096)])
+    ref = oracle.grouped_gemm_blockscaled_at(xq, sx, wq, sw, r.offsets, rr, cc)
+    within(y[rr, cc], ref)
+
+
+def test_grouped_rows_outside_offsets_untouched():
+    """Offsets that end before `rows`: the trailing rows belong to no expert and
+    are left as they were."""
+    counts = [5, 7]
+    offsets, xq, sx, wq, sw = grouped_case(counts, 128, 128, fp8rl.SCALE_FP32, 1)
+    extra = 9
+    xq2 = np.concatenate([xq, np.zeros((extra, 128), np.uint8)])
+    sx2 = np.concatenate([sx, np.ones((1, extra), np.float32)], axis=1)
+    y = run_grouped(offsets, xq2, sx2, wq, sw, fp8rl.SCALE_FP32, fill=3.0)
+    assert np.all(y[12:] == 3.0)
+    within(y[:12], oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets))

@@ -124,14 +124,14 @@ def test_quotient_domain_exhaustive(fmt):
     division-and-round step up to a shared power of two."""
     all_bits = np.arange(0, 0x7F80, dtype=np.uint32)  # non-negative finite bf16
     mags = (all_bits << 16).view(np.float32)
-    exps = [-133, -130, -126, -100, -40, -7, 0, 3, 9, 60, 120, 127]
+    # exponents across the range, dense near both ends and around amax ~ 2^-71,
+    # where the fp32 path switches between IEEE division and the reciprocal form
+    exps = [-126, -125, -124, -120, -110, -100, -91, -90, -89, -80, -75, -73, -72, -71, -70,
+            -69, -68, -60, -40, -20, -7, -1, 0, 1, 3, 9, 20, 60, 100, 118, 119, 120, 125, 126, 127]
     amaxes = []
     for e in exps:
         for mant in range(128):
-            bits = ((e + 127) << 7 | mant) if e > -127 else None
-            if bits is None:
-                continue
-            amaxes.append(bits)
+            amaxes.append((e + 127) << 7 | mant)
     amaxes += list(range(1, 128))  # subnormal bf16 amax values
     amax_bits = np.array(sorted(set(b for b in amaxes if 0 < b < 0x7F80)), dtype=np.uint16)
     rows = []
