@@ -45,13 +45,16 @@ L2_BYTES = 129 * 2 ** 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="all",
                     help="comma list of extra sections: model,moe_sync,sweep,ue8m0 (or all/none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
+                         "wq:layer[:fmt], aq:M:K[:fmt]")
     return ap.parse_args()
 
 
@@ -102,7 +105,7 @@ class ClockSampler:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits", "-lms", "200"],
+                     "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
@@ -648,9 +651,75 @@ def main_reference(args):
     }))
 
 
+def main_case(args):
+    """One kernel alone, --warmup + --steps launches; prints its median time."""
+    import torch
+
+    import fp8_w8a8_rollout_gb300 as fp8rl
+    from fp8_w8a8_rollout_gb300 import synth
+    dev = torch.device("cuda")
+    fp8rl.load_library()
+    parts = args.case.split(":")
+    kind = parts[0]
+    peaks = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    if kind == "gemm":
+        m, n, k = (int(v) for v in parts[1:4])
+        fmt = int(parts[4]) if len(parts) > 4 else 0
+        w = synth.weight_bf16(n, k, 0, "case", device=dev)
+        wq, sw = fp8rl.quant_weight(w, fmt)
+        x = synth.activation_bf16(m, k, 0, "case-x", device=dev)
+        xq, sx = fp8rl.quant_act(x, fmt)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, m, n, k, fmt)
+        work = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k), 1.0, peaks["hbm_gbs"], fp8_peak)
+    elif kind == "grouped":
+        which = parts[1]
+        n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
+        r = synth.moe_routing(MOE_T, synth.MOE_EXPERTS, synth.MOE_TOPK, 0, 0)
+        rows = int(r.offsets[-1])
+        offsets = torch.from_numpy(r.offsets).to(dev)
+        wb = synth.moe_expert_weights(n, k, synth.MOE_EXPERTS, 0, 0, which, device=dev)
+        wq, sw = fp8rl.quant_weight(wb.view(-1, k))
+        wq = wq.view(synth.MOE_EXPERTS, n, k)
+        sw = sw.view(synth.MOE_EXPERTS, n // 128, k // 128)
+        x = synth.normal_bf16((rows, k), 1.0, 0, "case-x", device=dev)
+        xq, sx = fp8rl.quant_act(x)
+        y = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8rl.fp8rl_grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, synth.MOE_EXPERTS, rows, n, k, y)
+        work = {"flops": gemm_flops(rows, n, k)}
+    elif kind == "wq":
+        fmt = int(parts[2]) if len(parts) > 2 else 0
+        layer = [w for _, w in synth.qwen3_8b_layer(0, 0, device=dev)]
+        outs = fp8rl.quant_weights_batched(layer, fmt)
+        descs = fp8rl.weight_descs([(w, q, sc) for w, (q, sc) in zip(layer, outs)])
+        fn = lambda: fp8rl.fp8rl_quant_weight_blockwise_batched(descs, len(layer), fmt)
+        work = {"bytes": sum(wq_bytes(*w.shape, 4 if fmt == 0 else 1) for w in layer)}
+    elif kind == "aq":
+        m, k = int(parts[1]), int(parts[2])
+        fmt = int(parts[3]) if len(parts) > 3 else 0
+        x = synth.activation_bf16(m, k, 0, "case-x", device=dev)
+        q = torch.empty((m, k), dtype=torch.uint8, device=dev)
+        sc = torch.empty(((k + 127) // 128, m), dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev)
+        fn = lambda: fp8rl.fp8rl_quant_act_group(x, m, k, k, q, k, sc, fmt)
+        work = {"bytes": aq_bytes(m, k, 4 if fmt == 0 else 1)}
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    ms = time_loop(torch, fn, max(1, args.steps), args.warmup)
+    assert fp8rl.fp8rl_sync_status() == 0
+    out = {"case": args.case, "ms": ms}
+    if "flops" in work:
+        out["tflops"] = work["flops"] / ms / 1e9
+    if "bytes" in work:
+        out["gbs"] = work["bytes"] / ms / 1e6
+    print(json.dumps(out))
+
+
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.case:
+        main_case(a)
+    elif a.impl == "reference":
         main_reference(a)
     else:
         main_ours(a)

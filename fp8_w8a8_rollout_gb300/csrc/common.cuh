@@ -71,14 +71,16 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
 }
 
 // UE8M0 exponent: smallest e with 448 * 2^e >= amax, in [-127, 127]; zeros: 0.
-// amax is a finite bf16 magnitude, so the fp64 comparison is exact.
+// Exact integer form: for a normal amax = (1 + m / 2^23) 2^(E - 127) and
+// 448 = 1.75 * 2^8, e = E - 135 when 1 + m / 2^23 <= 1.75 (m <= 0x600000),
+// else E - 134.  A subnormal amax is below 448 * 2^-127 and clamps to -127.
 __device__ __forceinline__ int scale_ue8m0_exponent(float amax) {
-  if (amax == 0.0f) return 0;
-  // start from a bound one below the answer and step up with exact comparisons
-  int e = ilogbf(amax) - 9;
-  if (e < -127) e = -127;
-  while (e < 127 && ldexp(448.0, e) < (double)amax) ++e;
-  return e;
+  const uint32_t b = __float_as_uint(amax) & 0x7FFFFFFFu;
+  if (b == 0) return 0;
+  const int E = (int)(b >> 23);
+  if (E == 0) return -127;
+  const int e = E - 135 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
 // 2^-e as an fp32 (e in [-126, 127] gives a normal number; -127 -> 2^127)

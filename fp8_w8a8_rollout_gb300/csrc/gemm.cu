@@ -59,11 +59,11 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
   // register split for BN = 256 (384 threads launch with <= 168 each): the
   // role warpgroup gives registers back, the epilogue warpgroups take them.
-  // 128 * 56 + 256 * 208 = 60416 must not exceed 384 * (registers at launch);
+  // 128 * 56 + 256 * 224 = 64512 must not exceed 384 * (registers at launch);
   // the host checks that before launching.
   static constexpr bool kSplitRegs = BN == 256;
   static constexpr int kRoleRegs = 56;
-  static constexpr int kEpiRegs = 208;
+  static constexpr int kEpiRegs = 224;
   static constexpr int kMinLaunchRegs = (128 * kRoleRegs + BN * kEpiRegs + kThreads - 1) / kThreads;
 };
 
@@ -274,13 +274,18 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + half * 128;
+      // two 32-column loads in flight per wait
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(taddr + c * 16, v);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(taddr + c * 64, v0);
+        tmem_ld_32x32b_x32(taddr + c * 64 + 32, v1);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[c * 16 + j] = __fmaf_rn(__uint_as_float(v[j]), f, acc[c * 16 + j]);
+        for (int j = 0; j < 32; ++j) {
+          acc[c * 64 + j] = __fmaf_rn(__uint_as_float(v0[j]), f, acc[c * 64 + j]);
+          acc[c * 64 + 32 + j] = __fmaf_rn(__uint_as_float(v1[j]), f, acc[c * 64 + 32 + j]);
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
@@ -394,7 +399,7 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t gri
     // sure the launch allocation covers the split, or it would wait forever
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8RL_ERR_CUDA;
-    if (fa.numRegs < C::kMinLaunchRegs) return FP8RL_ERR_UNSUPPORTED;
+    if (fa.numRegs < C::kMinLaunchRegs) return FP8RL_ERR_UNSUPPORTED;  // the caller retries with 128
   }
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FP8RL_ERR_CUDA;
@@ -437,9 +442,11 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   if (bn == 256 && n % 256) bn = 128;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool ue = fmt == FP8RL_SCALE_UE8M0;
-  if (bn == 256)
-    return ue ? launch<256, true>(xq, wq, experts, grid_x, args, cs)
-              : launch<256, false>(xq, wq, experts, grid_x, args, cs);
+  if (bn == 256) {
+    const fp8rl_status st = ue ? launch<256, true>(xq, wq, experts, grid_x, args, cs)
+                               : launch<256, false>(xq, wq, experts, grid_x, args, cs);
+    if (st != FP8RL_ERR_UNSUPPORTED) return st;
+  }
   return ue ? launch<128, true>(xq, wq, experts, grid_x, args, cs)
             : launch<128, false>(xq, wq, experts, grid_x, args, cs);
 }

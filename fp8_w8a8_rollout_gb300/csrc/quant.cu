@@ -203,58 +203,66 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
 constexpr int kActUnroll = 4;
 
 template <bool UE8M0>
-__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int64_t m,
+__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
                                                         int64_t k, int64_t ldx, uint8_t* __restrict__ q,
                                                         int64_t ldq, void* __restrict__ scale,
-                                                        int64_t groups, int vec) {
+                                                        int32_t groups, int vec) {
   const int lane16 = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
-  const int64_t warp = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t warp_count = (int64_t)gridDim.x * 8;
-  const int64_t tasks = m * groups;
+  const int32_t warp = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int32_t warp_count = gridDim.x * 8;
+  const int32_t tasks = m * groups;  // the host keeps this below 2^31
   constexpr int kPerWarp = 2 * kActUnroll;
-  for (int64_t base = warp * kPerWarp; base < tasks; base += warp_count * kPerWarp) {
+  for (int32_t base = warp * kPerWarp; base < tasks; base += warp_count * kPerWarp) {
+    // (group, row) of this warp's first task; the others follow row by row
+    const int32_t g_base = base / m;
+    const int32_t r_base = base - g_base * m;
     uint4 v[kActUnroll];
-    int64_t row[kActUnroll], g[kActUnroll];
-    bool fast[kActUnroll];
+    int32_t row[kActUnroll], g[kActUnroll];
+    bool fast[kActUnroll], live[kActUnroll];
 #pragma unroll
     for (int u = 0; u < kActUnroll; ++u) {
-      const int64_t task = base + 2 * u + half;
-      g[u] = task / m;
-      row[u] = task - g[u] * m;
-      const int64_t c = g[u] * kBlock + lane16 * 8;
-      fast[u] = task < tasks && vec && (g[u] + 1) * kBlock <= k;
+      int32_t rr = r_base + 2 * u + half, gg = g_base;
+      while (rr >= m) {
+        rr -= m;
+        ++gg;
+      }
+      row[u] = rr;
+      g[u] = gg;
+      live[u] = base + 2 * u + half < tasks;
+      const int64_t c = (int64_t)gg * kBlock + lane16 * 8;
+      fast[u] = live[u] && vec && (int64_t)(gg + 1) * kBlock <= k;
       v[u] = make_uint4(0, 0, 0, 0);
       if (fast[u]) {
-        v[u] = ld_stream(x + row[u] * ldx + c);
-      } else if (task < tasks) {
+        v[u] = ld_stream(x + (int64_t)rr * ldx + c);
+      } else if (live[u]) {
         uint32_t h[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) h[j] = (c + j < k) ? (uint32_t)x[row[u] * ldx + c + j] : 0u;
+        for (int j = 0; j < 8; ++j) h[j] = (c + j < k) ? (uint32_t)x[(int64_t)rr * ldx + c + j] : 0u;
         v[u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
                           h[6] | (h[7] << 16));
       }
     }
 #pragma unroll
     for (int u = 0; u < kActUnroll; ++u) {
-      const int64_t task = base + 2 * u + half;
       const uint32_t acc = absmax_u4(0u, v[u]);
       uint32_t am = max(acc & 0xFFFFu, acc >> 16);
 #pragma unroll
       for (int off = 8; off >= 1; off >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
-      if (task >= tasks) continue;
+      if (!live[u]) continue;
       const float amax = __uint_as_float(am << 16);
+      const int64_t sidx = (int64_t)g[u] * m + row[u];
       uint2 codes;
       if (UE8M0) {
         const int e = scale_ue8m0_exponent(amax);
         codes = quant8_mul(v[u], exp2_neg(e));
-        if (lane16 == 0) static_cast<uint8_t*>(scale)[g[u] * m + row[u]] = (uint8_t)(e + 127);
+        if (lane16 == 0) static_cast<uint8_t*>(scale)[sidx] = (uint8_t)(e + 127);
       } else {
         const float s = scale_fp32(amax);
         codes = quant8_div(v[u], s, __frcp_rn(s));
-        if (lane16 == 0) static_cast<float*>(scale)[g[u] * m + row[u]] = s;
+        if (lane16 == 0) static_cast<float*>(scale)[sidx] = s;
       }
-      const int64_t c = g[u] * kBlock + lane16 * 8;
-      uint8_t* dst = q + row[u] * ldq + c;
+      const int64_t c = (int64_t)g[u] * kBlock + lane16 * 8;
+      uint8_t* dst = q + (int64_t)row[u] * ldq + c;
       if (fast[u]) {
         asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(codes.x), "r"(codes.y) : "memory");
       } else {
@@ -395,19 +403,20 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int6
   if (st != FP8RL_OK || m == 0 || k == 0) return st;
   const int64_t groups = (k + kBlock - 1) / kBlock;
   const int64_t tasks = m * groups;
+  if (tasks > (int64_t)INT32_MAX - (1 << 20)) return FP8RL_ERR_SHAPE;  // 32-bit task numbering
   const int64_t warps = (tasks + 2 * kActUnroll - 1) / (2 * kActUnroll);
   const int64_t want = (warps + 7) / 8;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
   const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (fmt == FP8RL_SCALE_UE8M0)
-    quant_act_kernel<true><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), m, k,
-                                                           ldx, static_cast<uint8_t*>(q_e4m3), ldq,
-                                                           x_scale, groups, vec);
+    quant_act_kernel<true><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), (int32_t)m,
+                                                           k, ldx, static_cast<uint8_t*>(q_e4m3), ldq,
+                                                           x_scale, (int32_t)groups, vec);
   else
-    quant_act_kernel<false><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), m, k,
-                                                            ldx, static_cast<uint8_t*>(q_e4m3), ldq,
-                                                            x_scale, groups, vec);
+    quant_act_kernel<false><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), (int32_t)m,
+                                                            k, ldx, static_cast<uint8_t*>(q_e4m3), ldq,
+                                                            x_scale, (int32_t)groups, vec);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 
