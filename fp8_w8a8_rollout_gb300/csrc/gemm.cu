@@ -56,7 +56,9 @@ struct Cfg {
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static constexpr int kScaleRing = 4;  // K chunks of scales each epilogue thread fetches ahead
+  static constexpr int kRingBytes = BN * kScaleRing * 8;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + kRingBytes;
   // register split for BN = 256 (384 threads launch with <= 168 each): the
   // role warpgroup gives registers back, the epilogue warpgroups take them.
   // 128 * 56 + 256 * 224 = 64512 must not exceed 384 * (registers at launch);
@@ -78,13 +80,22 @@ struct GemmArgs {
   int32_t fault_skip_kb;     // test hook: the producer never fills this K chunk (-1: off)
 };
 
+// Scales are fetched as the aligned 32-bit word that holds them (a UE8M0 byte
+// sits inside its word; the word never crosses the end of the allocation's
+// last 4-byte unit, so it cannot leave mapped memory).
 template <bool UE8M0>
-__device__ __forceinline__ float load_scale(const void* p, int64_t idx) {
+__device__ __forceinline__ const void* scale_word(const void* p, int64_t idx) {
+  if (UE8M0) return static_cast<const uint8_t*>(p) + (idx & ~(int64_t)3);
+  return static_cast<const float*>(p) + idx;
+}
+
+template <bool UE8M0>
+__device__ __forceinline__ float scale_value(uint32_t word, int64_t idx) {
   if (UE8M0) {
-    const uint32_t b = __ldg(static_cast<const uint8_t*>(p) + idx);
+    const uint32_t b = (word >> (8 * (idx & 3))) & 0xFFu;
     return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
   }
-  return __ldg(static_cast<const float*>(p) + idx);
+  return __uint_as_float(word);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -111,6 +122,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* tile = abort_flag + 1;  // expert, first row, segment end
+  // per epilogue thread: kScaleRing slots of {sx word, sw word}
+  const uint32_t ring_base = smem_u32(base_ptr + C::kStages * C::kStageBytes + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
@@ -262,13 +275,30 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     float acc[128];
 #pragma unroll
     for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-    float sx_next = (row_ok && num_kb > 0) ? load_scale<UE8M0>(a.sx, grow) : 0.0f;
+    // the chunk scales of this thread's row and columns, fetched kScaleRing
+    // chunks ahead so that no global-memory latency sits between the tensor
+    // cores finishing a chunk and this thread folding it in
+    const uint32_t ring = ring_base + (uint32_t)(ew * 32 + lane) * C::kScaleRing * 8;
+    const uint8_t* ring_ptr = base_ptr + C::kStages * C::kStageBytes + 256 + (ew * 32 + lane) * C::kScaleRing * 8;
+    auto prefetch = [&](int kb) {
+      if (kb < num_kb) {
+        const uint32_t slot = ring + (uint32_t)(kb % C::kScaleRing) * 8;
+        const int64_t sxi = (int64_t)kb * a.rows + (row_ok ? grow : 0);
+        cp_async_4(slot, scale_word<UE8M0>(a.sx, sxi), row_ok ? 4u : 0u);
+        cp_async_4(slot + 4, scale_word<UE8M0>(a.sw, sw_base + kb), 4u);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int d = 0; d < C::kScaleRing; ++d) prefetch(d);
     bool ok = true;
     for (int kb = 0; kb < num_kb; ++kb) {
       const int buf = kb & 1;
       const uint32_t bph = (kb >> 1) & 1;
-      const float f = sx_next * load_scale<UE8M0>(a.sw, sw_base + kb);
-      if (kb + 1 < num_kb && row_ok) sx_next = load_scale<UE8M0>(a.sx, (int64_t)(kb + 1) * a.rows + grow);
+      cp_async_wait<C::kScaleRing - 1>();
+      const uint32_t* slot = reinterpret_cast<const uint32_t*>(ring_ptr + (kb % C::kScaleRing) * 8);
+      const int64_t sxi = (int64_t)kb * a.rows + (row_ok ? grow : 0);
+      const float f = scale_value<UE8M0>(slot[0], sxi) * scale_value<UE8M0>(slot[1], sw_base + kb);
       ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -289,7 +319,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
+      // refill the slot just read (its value has been consumed by the FMAs above)
+      prefetch(kb + C::kScaleRing);
     }
+    cp_async_wait<0>();  // no scale prefetch may still be landing when the CTA leaves
     if (ok && row_ok && !*abortv) {
       uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + half * 128);
 #pragma unroll

@@ -131,3 +131,11 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(fp8rl, "_lib", None)
     with pytest.raises(FileNotFoundError):
         fp8rl.load_library()
+
+
+def test_debug_hook_validates_on_host(lib):
+    assert _rc("fp8rl_debug_set", 1, 96) == 1
+    assert _rc("fp8rl_debug_set", 3, 0) == 1
+    assert _rc("fp8rl_debug_set", 99, 0) == 1
+    assert _rc("fp8rl_debug_set", 1, 256) == 0
+    assert _rc("fp8rl_debug_set", 0, 0) == 0

@@ -1,0 +1,85 @@
+"""Failure detection without a GPU fault: a device-side wait that can never
+complete (the producer is told to skip one K chunk, so nothing ever arrives on
+that stage's barrier) must run out after its limit, leave the kernel through
+the normal teardown, and be reported as FP8RL_ERR_TIMEOUT on the host; the
+context must stay usable for the next call."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_w8a8_rollout_gb300 as fp8rl
+import oracle
+from fp8_w8a8_rollout_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = 6
+
+
+@pytest.fixture(autouse=True)
+def _reset():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fp8rl.load_library(build_if_missing=True)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+    yield
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+
+
+def operands(m, n, k, seed):
+    x = synth.activation_bf16(m, k, seed, "fault-x")
+    w = synth.weight_bf16(n, k, seed, "fault-w")
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w))
+    return xq, sx, wq, sw
+
+
+def dev(*a):
+    return [torch.from_numpy(np.ascontiguousarray(v)).cuda() for v in a]
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_wait_runs_out_and_is_reported(bn):
+    m, n, k = 256, 512, 512
+    xq, sx, wq, sw = operands(m, n, k, 1)
+    dx, dsx, dw, dsw = dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, bn)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)   # 50 ms
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, 1)         # chunk 1 never arrives
+    fp8rl.gemm(dx, dsx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    # the word is cleared by the read, and the context still works
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+    assert fp8rl.fp8rl_sync_status() == 0
+    y = fp8rl.gemm(dx, dsx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == 0
+    ref = oracle.gemm_blockscaled(xq, sx, wq, sw)
+    got = y.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)
+
+
+def test_grouped_wait_runs_out_and_is_reported():
+    counts = [100, 0, 300]
+    offsets = synth.routing_with_counts(counts)
+    rows, n, k = int(offsets[-1]), 256, 384
+    x = synth.normal_bf16((rows, k), 1.0, 2, "fault-gx")
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
+    ws = synth.moe_expert_weights(n, k, 3, 2, 0, "fault")
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(ws.reshape(-1, k)))
+    dx, dsx, dw, dsw, doff = dev(xq, sx, wq.reshape(3, n, k), sw.reshape(3, n // 128, k // 128), offsets)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, 2)
+    fp8rl.grouped_gemm(dx, dsx, dw, dsw, doff)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+    fp8rl.grouped_gemm(dx, dsx, dw, dsw, doff)
+    assert fp8rl.fp8rl_sync_status() == 0
+
+
+def test_debug_hook_rejects_bad_values():
+    with pytest.raises(fp8rl.Fp8rlError):
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, 96)
+    with pytest.raises(fp8rl.Fp8rlError):
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 0)
+    with pytest.raises(fp8rl.Fp8rlError):
+        fp8rl.fp8rl_debug_set(99, 0)
