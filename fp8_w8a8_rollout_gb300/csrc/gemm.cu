@@ -15,7 +15,8 @@
 //   warp 1, one lane   MMA issuer: four tcgen05.mma (M=128, N=BN, K=32) per chunk
 //                      into one of two TMEM accumulators, then commits;
 //   warps 2, 3         idle (they complete warpgroup 0);
-//   warps 4..          epilogue, one warpgroup per 128 columns: per chunk,
+//   warps 4..          epilogue, 64 accumulator columns per warp (four warps per
+//                      column slice cover the 128 TMEM lanes): per chunk,
 //                      tcgen05.ld the partial product, fold
 //                      it into fp32 registers with sx * sw, release the TMEM
 //                      buffer (so the tensor cores fill the other one meanwhile);
@@ -50,23 +51,24 @@ constexpr int kUmmaK = 32;   // K of one E4M3 tcgen05.mma
 template <int BN>
 struct Cfg {
   static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr int kEpiWarps = BN / 32;      // one warpgroup per 128 columns
-  static constexpr int kThreads = 128 + BN;      // warpgroup 0: producer, MMA, two idle warps
-  static constexpr int kTmemCols = 2 * BN;       // two fp32 accumulators
+  static constexpr int kCols = 64;                      // accumulator columns per epilogue thread
+  static constexpr int kEpiWarps = 4 * (BN / kCols);    // 4 TMEM lane quadrants x column slices
+  static constexpr int kThreads = 128 + kEpiWarps * 32; // warpgroup 0: producer, MMA, two idle warps
+  static constexpr int kTmemCols = 2 * BN;              // two fp32 accumulators
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kScaleRing = 4;  // K chunks of scales each epilogue thread fetches ahead
-  static constexpr int kRingBytes = BN * kScaleRing * 8;
+  static constexpr int kRingBytes = kEpiWarps * 32 * kScaleRing * 8;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + kRingBytes;
-  // register split for BN = 256 (384 threads launch with <= 168 each): the
-  // role warpgroup gives registers back, the epilogue warpgroups take them.
-  // 128 * 56 + 256 * 224 = 64512 must not exceed 384 * (registers at launch);
-  // the host checks that before launching.
+  // register split for BN = 256 (640 threads launch with <= 96 each): the role
+  // warpgroup gives registers back, the four epilogue warpgroups take them.
+  // 128 * kRoleRegs + 512 * kEpiRegs must not exceed 640 * (registers at
+  // launch); the host checks that before launching.
   static constexpr bool kSplitRegs = BN == 256;
-  static constexpr int kRoleRegs = 56;
-  static constexpr int kEpiRegs = 224;
-  static constexpr int kMinLaunchRegs = (128 * kRoleRegs + BN * kEpiRegs + kThreads - 1) / kThreads;
+  static constexpr int kRoleRegs = 32;
+  static constexpr int kEpiRegs = 112;
+  static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
 };
 
 struct GemmArgs {
@@ -265,16 +267,16 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 4;
-    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. +31
-    const int half = ew >> 2;   // which 128 columns of the tile
+    const int quad = warp & 3;   // TMEM lanes this warp may read: 32*quad .. +31
+    const int slice = ew >> 2;   // which kCols columns of the tile
     const int r = quad * 32 + lane;
     const int grow = row0 + r;
     const bool row_ok = grow < seg_end;
-    const int nb = (n0 >> 7) + half;
+    const int nb = (n0 + slice * C::kCols) >> 7;
     const int64_t sw_base = ((int64_t)expert * (a.n / 128) + nb) * num_kb;
-    float acc[128];
+    float acc[C::kCols];
 #pragma unroll
-    for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
     // the chunk scales of this thread's row and columns, fetched kScaleRing
     // chunks ahead so that no global-memory latency sits between the tensor
     // cores finishing a chunk and this thread folding it in
@@ -303,19 +305,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + half * 128;
-      // two 32-column loads in flight per wait
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + slice * C::kCols;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(taddr + c * 64, v0);
-        tmem_ld_32x32b_x32(taddr + c * 64 + 32, v1);
+      for (int c = 0; c < C::kCols / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[c * 64 + j] = __fmaf_rn(__uint_as_float(v0[j]), f, acc[c * 64 + j]);
-          acc[c * 64 + 32 + j] = __fmaf_rn(__uint_as_float(v1[j]), f, acc[c * 64 + 32 + j]);
-        }
+        for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(__uint_as_float(v[j]), f, acc[c * 32 + j]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[buf]));
@@ -324,9 +321,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     }
     cp_async_wait<0>();  // no scale prefetch may still be landing when the CTA leaves
     if (ok && row_ok && !*abortv) {
-      uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + half * 128);
+      uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int j = 0; j < C::kCols / 8; ++j)
         dst[j] = make_uint4(pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]), pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
                             pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
     }

@@ -194,81 +194,97 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
 // activation groups
 // ============================================================================
 
-// A half-warp quantises one 1x128 group: each of its 16 lanes loads 8 bf16.
-// Groups are numbered g-major (task = g * m + row) so that the scale stores of
-// neighbouring half-warps are contiguous in the [K/128][m] scale layout.  A
-// warp takes 2 * kActUnroll consecutive tasks per iteration (half-warp h gets
-// tasks base + 2u + h), issuing all loads before any use.  The loop bound is
-// warp-uniform, so the full-mask shuffles always see all 32 lanes.
-constexpr int kActUnroll = 4;
+// Four lanes quantise one 1x128 group (32 elements each, as four 16-byte
+// pieces interleaved so that the four lanes of a group read 64 contiguous
+// bytes per load).  A warp covers one K group g of 8 consecutive rows per
+// pass and takes kActRows = 16 rows (two passes) per task, so the per-group
+// work (max over 4 lanes, the scale, its reciprocal) is shared by 8 groups per
+// warp instruction, and the 8 scales of a pass land in one 32-byte run of the
+// [K/128][m] scale array.  Tasks are numbered g-major; the loop bound is
+// warp-uniform.
+constexpr int kActRows = 16;
 
 template <bool UE8M0>
 __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
                                                         int64_t k, int64_t ldx, uint8_t* __restrict__ q,
                                                         int64_t ldq, void* __restrict__ scale,
                                                         int32_t groups, int vec) {
-  const int lane16 = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
+  const int lane = threadIdx.x & 31, sub = lane >> 2, part = lane & 3;
   const int32_t warp = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int32_t warp_count = gridDim.x * 8;
-  const int32_t tasks = m * groups;  // the host keeps this below 2^31
-  constexpr int kPerWarp = 2 * kActUnroll;
-  for (int32_t base = warp * kPerWarp; base < tasks; base += warp_count * kPerWarp) {
-    // (group, row) of this warp's first task; the others follow row by row
-    const int32_t g_base = base / m;
-    const int32_t r_base = base - g_base * m;
-    uint4 v[kActUnroll];
-    int32_t row[kActUnroll], g[kActUnroll];
-    bool fast[kActUnroll], live[kActUnroll];
+  const int32_t rblocks = (m + kActRows - 1) / kActRows;
+  const int32_t tasks = rblocks * groups;  // the host keeps m * groups below 2^31
+  for (int32_t t = warp; t < tasks; t += warp_count) {
+    const int32_t g = t / rblocks;
+    const int32_t r0 = (t - g * rblocks) * kActRows;
+    const int64_t c0 = (int64_t)g * kBlock;
+    const bool full_group = vec && c0 + kBlock <= k;
+    uint4 v[2][4];
+    bool live[2];
 #pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-      int32_t rr = r_base + 2 * u + half, gg = g_base;
-      while (rr >= m) {
-        rr -= m;
-        ++gg;
-      }
-      row[u] = rr;
-      g[u] = gg;
-      live[u] = base + 2 * u + half < tasks;
-      const int64_t c = (int64_t)gg * kBlock + lane16 * 8;
-      fast[u] = live[u] && vec && (int64_t)(gg + 1) * kBlock <= k;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (fast[u]) {
-        v[u] = ld_stream(x + (int64_t)rr * ldx + c);
-      } else if (live[u]) {
-        uint32_t h[8];
+    for (int u = 0; u < 2; ++u) {
+      const int32_t row = r0 + u * 8 + sub;
+      live[u] = row < m;
+      const uint16_t* src = x + (int64_t)row * ldx + c0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) h[j] = (c + j < k) ? (uint32_t)x[(int64_t)rr * ldx + c + j] : 0u;
-        v[u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                          h[6] | (h[7] << 16));
+      for (int j = 0; j < 4; ++j) {
+        const int piece = part + 4 * j;  // 8 elements each
+        if (live[u] && full_group) {
+          v[u][j] = ld_stream(src + piece * 8);
+        } else if (live[u]) {
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int64_t c = c0 + piece * 8 + e;
+            h[e] = c < k ? (uint32_t)src[piece * 8 + e] : 0u;
+          }
+          v[u][j] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                               h[6] | (h[7] << 16));
+        } else {
+          v[u][j] = make_uint4(0, 0, 0, 0);
+        }
       }
     }
 #pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-      const uint32_t acc = absmax_u4(0u, v[u]);
-      uint32_t am = max(acc & 0xFFFFu, acc >> 16);
+    for (int u = 0; u < 2; ++u) {
+      const int32_t row = r0 + u * 8 + sub;
+      uint32_t acc = 0;
 #pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, off));
+      for (int j = 0; j < 4; ++j) acc = absmax_u4(acc, v[u][j]);
+      uint32_t am = max(acc & 0xFFFFu, acc >> 16);
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
       if (!live[u]) continue;
       const float amax = __uint_as_float(am << 16);
-      const int64_t sidx = (int64_t)g[u] * m + row[u];
-      uint2 codes;
+      const int64_t sidx = (int64_t)g * m + row;
+      uint2 codes[4];
       if (UE8M0) {
         const int e = scale_ue8m0_exponent(amax);
-        codes = quant8_mul(v[u], exp2_neg(e));
-        if (lane16 == 0) static_cast<uint8_t*>(scale)[sidx] = (uint8_t)(e + 127);
+        const float f = exp2_neg(e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) codes[j] = quant8_mul(v[u][j], f);
+        if (part == 0) static_cast<uint8_t*>(scale)[sidx] = (uint8_t)(e + 127);
       } else {
         const float s = scale_fp32(amax);
-        codes = quant8_div(v[u], s, __frcp_rn(s));
-        if (lane16 == 0) static_cast<float*>(scale)[sidx] = s;
-      }
-      const int64_t c = (int64_t)g[u] * kBlock + lane16 * 8;
-      uint8_t* dst = q + (int64_t)row[u] * ldq + c;
-      if (fast[u]) {
-        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(codes.x), "r"(codes.y) : "memory");
-      } else {
+        const float rcp = __frcp_rn(s);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (c + j < k) dst[j] = (uint8_t)(((j < 4 ? codes.x : codes.y) >> (8 * (j & 3))) & 0xFFu);
+        for (int j = 0; j < 4; ++j) codes[j] = quant8_div(v[u][j], s, rcp);
+        if (part == 0) static_cast<float*>(scale)[sidx] = s;
+      }
+      uint8_t* dst = q + (int64_t)row * ldq + c0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int piece = part + 4 * j;
+        if (full_group) {
+          asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst + piece * 8), "r"(codes[j].x),
+                       "r"(codes[j].y)
+                       : "memory");
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (c0 + piece * 8 + e < k)
+              dst[piece * 8 + e] = (uint8_t)(((e < 4 ? codes[j].x : codes[j].y) >> (8 * (e & 3))) & 0xFFu);
+        }
       }
     }
   }
@@ -303,6 +319,18 @@ int sm_count() {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// resident CTAs per SM of a 256-thread kernel (at least 1), asked once per kernel
+template <typename K>
+int ctas_per_sm(K kernel) {
+  static int cached = 0;
+  if (cached == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
+    cached = n;
+  }
+  return cached;
+}
 
 fp8rl_status check_weight(const fp8rl_weight_desc& d, fp8rl_scale_fmt fmt) {
   if (d.n < 0 || d.k < 0 || d.ldw < d.k || d.ldq < d.k) return FP8RL_ERR_INVALID_ARG;
@@ -404,9 +432,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int6
   const int64_t groups = (k + kBlock - 1) / kBlock;
   const int64_t tasks = m * groups;
   if (tasks > (int64_t)INT32_MAX - (1 << 20)) return FP8RL_ERR_SHAPE;  // 32-bit task numbering
-  const int64_t warps = (tasks + 2 * kActUnroll - 1) / (2 * kActUnroll);
-  const int64_t want = (warps + 7) / 8;
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
+  const int64_t warp_tasks = ((m + kActRows - 1) / kActRows) * groups;
+  const int64_t want = (warp_tasks + 7) / 8;
+  const int occ = fmt == FP8RL_SCALE_UE8M0 ? ctas_per_sm(quant_act_kernel<true>) : ctas_per_sm(quant_act_kernel<false>);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * occ));
   const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (fmt == FP8RL_SCALE_UE8M0)
