@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--case", default=None,
                     help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
                          "wq:layer[:fmt], aq:M:K[:fmt]")
+    ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
+    ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
+    ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
     return ap.parse_args()
 
 
@@ -659,6 +662,12 @@ def main_case(args):
     from fp8_w8a8_rollout_gb300 import synth
     dev = torch.device("cuda")
     fp8rl.load_library()
+    if args.bn:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, args.bn)
+    if args.wait_mode:
+        fp8rl.fp8rl_debug_set(4, args.wait_mode)
+    if args.l2_prefetch >= 0:
+        fp8rl.fp8rl_debug_set(5, args.l2_prefetch)
     parts = args.case.split(":")
     kind = parts[0]
     peaks = load_peaks()
@@ -707,7 +716,8 @@ def main_case(args):
         raise SystemExit(f"unknown case {args.case}")
     ms = time_loop(torch, fn, max(1, args.steps), args.warmup)
     assert fp8rl.fp8rl_sync_status() == 0
-    out = {"case": args.case, "ms": ms}
+    out = {"case": args.case, "ms": ms, "bn": args.bn or "auto", "wait_mode": args.wait_mode,
+           "l2_prefetch": args.l2_prefetch}
     if "flops" in work:
         out["tflops"] = work["flops"] / ms / 1e9
     if "bytes" in work:

@@ -54,18 +54,20 @@ struct Cfg {
   static constexpr int kCols = 64;                      // accumulator columns per epilogue thread
   static constexpr int kEpiWarps = 4 * (BN / kCols);    // 4 TMEM lane quadrants x column slices
   static constexpr int kThreads = 128 + kEpiWarps * 32; // warpgroup 0: producer, MMA, two idle warps
-  static constexpr int kTmemCols = 2 * BN;              // two fp32 accumulators
+  static constexpr int kAccBufs = 512 / BN;             // fp32 accumulators in TMEM (all 512 columns)
+  static constexpr int kTmemCols = kAccBufs * BN;
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kScaleRing = 4;  // K chunks of scales each epilogue thread fetches ahead
-  static constexpr int kRingBytes = kEpiWarps * 32 * kScaleRing * 8;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + kRingBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
   // register split for BN = 256 (640 threads launch with <= 96 each): the role
   // warpgroup gives registers back, the four epilogue warpgroups take them.
   // 128 * kRoleRegs + 512 * kEpiRegs must not exceed 640 * (registers at
   // launch); the host checks that before launching.
   static constexpr bool kSplitRegs = BN == 256;
+  // with registers to spare (BN = 128) the epilogue copies a chunk out of TMEM
+  // and releases the buffer before folding it in
+  static constexpr bool kEarlyRelease = BN == 128;
   static constexpr int kRoleRegs = 32;
   static constexpr int kEpiRegs = 112;
   static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
@@ -80,6 +82,8 @@ struct GemmArgs {
   uint32_t* err;
   uint64_t timeout_ns;
   int32_t fault_skip_kb;     // test hook: the producer never fills this K chunk (-1: off)
+  int32_t wait_mode;         // bit 0: producer and MMA threads poll; bit 1: epilogue polls
+  int32_t l2_prefetch;       // K chunks ahead of the shared-memory loads that are prefetched into L2
 };
 
 // Scales are fetched as the aligned 32-bit word that holds them (a UE8M0 byte
@@ -119,13 +123,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + C::kStages * C::kStageBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + C::kAccBufs;
+  uint64_t* drain = tempty + C::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* tile = abort_flag + 1;  // expert, first row, segment end
-  // per epilogue thread: kScaleRing slots of {sx word, sw word}
-  const uint32_t ring_base = smem_u32(base_ptr + C::kStages * C::kStageBytes + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
@@ -184,9 +186,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), C::kEpiWarps * 32);
+      mbar_init(smem_u32(&tempty[b]), C::kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -212,13 +214,24 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       prefetch_tensormap(&tmap_x);
       prefetch_tensormap(&tmap_w);
       const int wrow0 = expert * a.n + n0;
+      // operands of the first chunks go to L2 at once; later ones a fixed
+      // distance ahead of their shared-memory loads
+      for (int kb = C::kStages; kb < min(num_kb, C::kStages + a.l2_prefetch); ++kb) {
+        tma_prefetch_l2_2d(&tmap_x, kb * kBK, row0);
+        tma_prefetch_l2_2d(&tmap_w, kb * kBK, wrow0);
+      }
       int issued = 0;
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % C::kStages;
         const uint32_t ph = (kb / C::kStages) & 1;
-        if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns)) break;
+        if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) break;
         issued = kb + 1;
         if (kb == a.fault_skip_kb) continue;
+        const int pf = kb + C::kStages + a.l2_prefetch;
+        if (a.l2_prefetch > 0 && pf < num_kb) {
+          tma_prefetch_l2_2d(&tmap_x, pf * kBK, row0);
+          tma_prefetch_l2_2d(&tmap_w, pf * kBK, wrow0);
+        }
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::kStageBytes);
         tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, row0, fb);
@@ -241,10 +254,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % C::kStages;
         const uint32_t ph = (kb / C::kStages) & 1;
-        const int buf = kb & 1;
-        const uint32_t bph = (kb >> 1) & 1;
-        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns)) break;
-        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns)) break;
+        const int buf = kb % C::kAccBufs;
+        const uint32_t bph = (kb / C::kAccBufs) & 1;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) break;
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1)))
+          break;
         tc_fence_after();
         const uint32_t d = tmem + buf * BN;
         const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
@@ -274,58 +288,78 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const bool row_ok = grow < seg_end;
     const int nb = (n0 + slice * C::kCols) >> 7;
     const int64_t sw_base = ((int64_t)expert * (a.n / 128) + nb) * num_kb;
-    float acc[C::kCols];
+    // fp32 accumulators as packed pairs (fma.rn.f32x2: two round-to-nearest
+    // FMAs per instruction, the same results as scalar FMAs)
+    uint64_t acc[C::kCols / 2];
 #pragma unroll
-    for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
-    // the chunk scales of this thread's row and columns, fetched kScaleRing
-    // chunks ahead so that no global-memory latency sits between the tensor
-    // cores finishing a chunk and this thread folding it in
-    const uint32_t ring = ring_base + (uint32_t)(ew * 32 + lane) * C::kScaleRing * 8;
-    const uint8_t* ring_ptr = base_ptr + C::kStages * C::kStageBytes + 256 + (ew * 32 + lane) * C::kScaleRing * 8;
-    auto prefetch = [&](int kb) {
-      if (kb < num_kb) {
-        const uint32_t slot = ring + (uint32_t)(kb % C::kScaleRing) * 8;
-        const int64_t sxi = (int64_t)kb * a.rows + (row_ok ? grow : 0);
-        cp_async_4(slot, scale_word<UE8M0>(a.sx, sxi), row_ok ? 4u : 0u);
-        cp_async_4(slot + 4, scale_word<UE8M0>(a.sw, sw_base + kb), 4u);
-      }
-      cp_async_commit();
+    for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
+    // the chunk scales of this thread's row and column slice, loaded two K
+    // chunks ahead (about one L2 round trip) so that no global-memory latency
+    // sits between the tensor cores finishing a chunk and this thread folding
+    // it in; indices advance by one chunk per iteration
+    int64_t sx_idx = row_ok ? (int64_t)grow : 0;  // sx[kb][grow] = sx[kb * rows + grow]
+    const int64_t sx_step = row_ok ? (int64_t)a.rows : 0;
+    auto ld_scale = [&](const void* base, int64_t i, bool live) -> float {
+      if (!live) return 0.0f;
+      return scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(base, i))), i);
     };
-#pragma unroll
-    for (int d = 0; d < C::kScaleRing; ++d) prefetch(d);
+    float sx0 = ld_scale(a.sx, sx_idx, row_ok && num_kb > 0);
+    float sw0 = ld_scale(a.sw, sw_base, num_kb > 0);
+    float sx1 = ld_scale(a.sx, sx_idx + sx_step, row_ok && num_kb > 1);
+    float sw1 = ld_scale(a.sw, sw_base + 1, num_kb > 1);
+    int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + 2;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
     bool ok = true;
     for (int kb = 0; kb < num_kb; ++kb) {
-      const int buf = kb & 1;
-      const uint32_t bph = (kb >> 1) & 1;
-      cp_async_wait<C::kScaleRing - 1>();
-      const uint32_t* slot = reinterpret_cast<const uint32_t*>(ring_ptr + (kb % C::kScaleRing) * 8);
-      const int64_t sxi = (int64_t)kb * a.rows + (row_ok ? grow : 0);
-      const float f = scale_value<UE8M0>(slot[0], sxi) * scale_value<UE8M0>(slot[1], sw_base + kb);
-      ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
+      const int buf = kb % C::kAccBufs;
+      const uint32_t bph = (kb / C::kAccBufs) & 1;
+      const float f = sx0 * sw0;
+      sx0 = sx1;
+      sw0 = sw1;
+      const bool more = kb + 2 < num_kb;
+      sx1 = ld_scale(a.sx, sx_next, row_ok && more);
+      sw1 = ld_scale(a.sw, sw_next, more);
+      sx_next += sx_step;
+      sw_next += 1;
+      ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + buf * BN + slice * C::kCols;
+      const uint64_t f2 = f32x2(f, f);
+      const uint32_t taddr = t_lane + buf * BN;
+      if (C::kEarlyRelease) {
+        // copy the whole slice out of TMEM, hand the buffer back, then fold
+        uint64_t v[C::kCols / 2];
 #pragma unroll
-      for (int c = 0; c < C::kCols / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, v);
-        tmem_wait_ld();
+        for (int c = 0; c < C::kCols / 32; ++c) tmem_ld_32x32b_x32_pairs(taddr + c * 32, *reinterpret_cast<uint64_t(*)[16]>(&v[c * 16]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[c * 32 + j] = __fmaf_rn(__uint_as_float(v[j]), f, acc[c * 32 + j]);
+        for (int j = 0; j < C::kCols / 2; ++j) acc[j] = fma_f32x2(v[j], f2, acc[j]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::kCols / 32; ++c) {
+          uint64_t v[16];
+          tmem_ld_32x32b_x32_pairs(taddr + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fma_f32x2(v[j], f2, acc[c * 16 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&tempty[buf]));
-      // refill the slot just read (its value has been consumed by the FMAs above)
-      prefetch(kb + C::kScaleRing);
     }
-    cp_async_wait<0>();  // no scale prefetch may still be landing when the CTA leaves
     if (ok && row_ok && !*abortv) {
       uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
 #pragma unroll
-      for (int j = 0; j < C::kCols / 8; ++j)
-        dst[j] = make_uint4(pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]), pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
-                            pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]), pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+      for (int j = 0; j < C::kCols / 8; ++j) {
+        float x[8];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) f32x2_unpack(acc[4 * j + h], x[2 * h], x[2 * h + 1]);
+        dst[j] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                            pack_bf16x2(x[6], x[7]));
+      }
     }
   }
   tc_fence_before();
@@ -357,6 +391,8 @@ fp8rl_status check_gemm(const void* xq, const void* x_scale, const void* wq, con
 struct Debug {
   int bn = 0;                     // 0: choose; 128 or 256: force the tile width
   int fault_skip_kb = -1;         // the producer skips this K chunk (forces a timeout)
+  int wait_mode = 0;              // which roles poll instead of suspending (bits: 1 producer/MMA, 2 epilogue)
+  int l2_prefetch = 0;            // K chunks of L2 prefetch beyond the shared-memory ring
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -462,6 +498,8 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   args.err = err;
   args.timeout_ns = dbg.timeout_ns;
   args.fault_skip_kb = dbg.fault_skip_kb;
+  args.wait_mode = dbg.wait_mode;
+  args.l2_prefetch = dbg.l2_prefetch;
   const int64_t m_tiles = (rows + kBM - 1) / kBM;
   const int64_t grid_x = d_offsets ? m_tiles + experts : m_tiles;
   int bn = dbg.bn;
@@ -521,6 +559,14 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 3:
       if (value <= 0) return FP8RL_ERR_INVALID_ARG;
       g_debug.timeout_ns = (uint64_t)value;
+      return FP8RL_OK;
+    case 4:
+      if (value < 0 || value > 3) return FP8RL_ERR_INVALID_ARG;
+      g_debug.wait_mode = (int)value;
+      return FP8RL_OK;
+    case 5:
+      if (value < 0 || value > 64) return FP8RL_ERR_INVALID_ARG;
+      g_debug.l2_prefetch = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

@@ -51,17 +51,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to hint_ns
+// while the phase is incomplete (it resumes as soon as the phase completes), so
+// that waiting warps neither spin nor load the shared-memory pipe.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of the given parity to complete, for at most limit_ns.
 // Gives up early when another thread has raised *abort.  On running out it
 // raises *abort and sets the timeout bit in the device error word.  Returns
-// false when it gave up.
+// false when it gave up.  With suspend set, each try lets the hardware park
+// the thread for at most 20 us (it resumes when the phase completes), which
+// also bounds how late an abort or the limit is noticed; otherwise the thread
+// polls and checks the clock every 64 tries.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  uint32_t* err_word, uint64_t limit_ns) {
+                                                  uint32_t* err_word, uint64_t limit_ns, bool suspend = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 0) {
+    if (suspend ? mbar_try_wait_suspend(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
+    if (suspend || (i & 63) == 0) {
       if (abort && *abort) return false;
       if (globaltimer() - t0 > limit_ns) {
         if (abort) *abort = 1;
@@ -82,6 +100,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+
+// bring a 2-D box into L2 ahead of its shared-memory load (no completion signal)
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -189,7 +215,47 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// 32 consecutive columns of this thread's lane, waited for and returned as 16
+// packed fp32 pairs (columns 2j, 2j+1) for fma.rn.f32x2
+__device__ __forceinline__ void tmem_ld_32x32b_x32_pairs(uint32_t taddr, uint64_t (&p)[16]) {
+  asm volatile(
+      "{\n\t.reg .b32 r<32>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, "
+      "r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\t"
+      "mov.b64 %3, {r6, r7};\n\tmov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\t"
+      "mov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\tmov.b64 %8, {r16, r17};\n\t"
+      "mov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\t"
+      "mov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\t"
+      "mov.b64 %15, {r30, r31};\n\t}"
+      : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]),
+        "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ packed fp32
+
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// two independent round-to-nearest fp32 FMAs, a * b + c, in one instruction
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 
 }  // namespace ptx
 }  // namespace fp8rl

@@ -201,6 +201,10 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          off), so the MMA warp's bounded wait runs out and the call reports
  *          TIMEOUT through fp8rl_sync_status (no trap, no hang);
  *   key 3  limit of every device-side wait, in nanoseconds (default 2e9);
+ *   key 4  wait style, bit 0: producer and MMA threads poll instead of letting
+ *          the hardware park them; bit 1: the same for the epilogue (default 0);
+ *   key 5  how many K chunks beyond the shared-memory stages the TMA producer
+ *          prefetches into L2 (0..64, default 0: measured slower on GB300);
  *   key 0  restore all defaults.
  * Errors: INVALID_ARG for an unknown key or value.
  */
