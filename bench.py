@@ -361,14 +361,23 @@ def e2e_weight_sync(torch, fp8rl, inp, stream, steps):
 
 
 def time_loop(torch, fn, iters, warmup, flush=None):
-    """Median per-call device time of fn (CUDA events), optional L2 flush between calls."""
+    """Per-call device time of fn (CUDA events around `iters` back-to-back calls;
+    with a flush, the median of single calls each preceded by an L2 flush)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if flush is None:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / iters
     times = []
     for _ in range(iters):
-        if flush is not None:
-            flush()
+        flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()

@@ -31,6 +31,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -60,6 +61,8 @@ struct Cfg {
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static constexpr int kPartPitch = BN + 4;  // floats per row of a split-K partial tile
+  static_assert(kBM * kPartPitch * 4 <= kStages * kStageBytes, "partial tile must fit over the stages");
   // register split for BN = 256 (640 threads launch with <= 96 each): the role
   // warpgroup gives registers back, the four epilogue warpgroups take them.
   // 128 * kRoleRegs + 512 * kEpiRegs must not exceed 640 * (registers at
@@ -84,6 +87,7 @@ struct GemmArgs {
   int32_t fault_skip_kb;     // test hook: the producer never fills this K chunk (-1: off)
   int32_t wait_mode;         // bit 0: producer and MMA threads poll; bit 1: epilogue polls
   int32_t l2_prefetch;       // K chunks ahead of the shared-memory loads that are prefetched into L2
+  int32_t splits;            // K splits; > 1 only for a launch in clusters of `splits` CTAs along z
 };
 
 // Scales are fetched as the aligned 32-bit word that holds them (a UE8M0 byte
@@ -109,7 +113,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int BN, bool UE8M0>
+template <int BN, bool UE8M0, bool SPLITK>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
                             const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
@@ -132,6 +136,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
   const int n0 = blockIdx.y * BN;
+  // split-K: this CTA's K chunks [kb_lo, kb_lo + nloc); the partial tiles of a
+  // cluster are summed through distributed shared memory at the end
+  const int splits = SPLITK ? a.splits : 1;
+  const int split = SPLITK ? (int)cluster_ctarank() : 0;
+  const int kb_lo = (int)((int64_t)num_kb * split / splits);
+  const int nloc = (int)((int64_t)num_kb * (split + 1) / splits) - kb_lo;
 
   // ---- which rows this CTA covers
   if (warp == 0) {
@@ -216,21 +226,22 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int wrow0 = expert * a.n + n0;
       // operands of the first chunks go to L2 at once; later ones a fixed
       // distance ahead of their shared-memory loads
-      for (int kb = C::kStages; kb < min(num_kb, C::kStages + a.l2_prefetch); ++kb) {
-        tma_prefetch_l2_2d(&tmap_x, kb * kBK, row0);
-        tma_prefetch_l2_2d(&tmap_w, kb * kBK, wrow0);
+      for (int it = C::kStages; it < min(nloc, C::kStages + a.l2_prefetch); ++it) {
+        tma_prefetch_l2_2d(&tmap_x, (kb_lo + it) * kBK, row0);
+        tma_prefetch_l2_2d(&tmap_w, (kb_lo + it) * kBK, wrow0);
       }
       int issued = 0;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
+      for (int it = 0; it < nloc; ++it) {
+        const int kb = kb_lo + it;
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
         if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) break;
-        issued = kb + 1;
-        if (kb == a.fault_skip_kb) continue;
-        const int pf = kb + C::kStages + a.l2_prefetch;
-        if (a.l2_prefetch > 0 && pf < num_kb) {
-          tma_prefetch_l2_2d(&tmap_x, pf * kBK, row0);
-          tma_prefetch_l2_2d(&tmap_w, pf * kBK, wrow0);
+        issued = it + 1;
+        if (it == a.fault_skip_kb) continue;
+        const int pf = it + C::kStages + a.l2_prefetch;
+        if (a.l2_prefetch > 0 && pf < nloc) {
+          tma_prefetch_l2_2d(&tmap_x, (kb_lo + pf) * kBK, row0);
+          tma_prefetch_l2_2d(&tmap_w, (kb_lo + pf) * kBK, wrow0);
         }
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::kStageBytes);
@@ -239,9 +250,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       }
       if (*abortv) {
         // let the copies still in flight land before shared memory is released
-        for (int kb = max(0, issued - C::kStages); kb < issued; ++kb) {
-          if (kb == a.fault_skip_kb) continue;
-          mbar_wait_bounded(smem_u32(&full[kb % C::kStages]), (kb / C::kStages) & 1, nullptr, nullptr,
+        for (int it = max(0, issued - C::kStages); it < issued; ++it) {
+          if (it == a.fault_skip_kb) continue;
+          mbar_wait_bounded(smem_u32(&full[it % C::kStages]), (it / C::kStages) & 1, nullptr, nullptr,
                             10000000ull);
         }
       }
@@ -251,11 +262,11 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        const int buf = kb % C::kAccBufs;
-        const uint32_t bph = (kb / C::kAccBufs) & 1;
+      for (int it = 0; it < nloc; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        const int buf = it % C::kAccBufs;
+        const uint32_t bph = (it / C::kAccBufs) & 1;
         if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) break;
         if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1)))
           break;
@@ -297,26 +308,26 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     // chunks ahead (about one L2 round trip) so that no global-memory latency
     // sits between the tensor cores finishing a chunk and this thread folding
     // it in; indices advance by one chunk per iteration
-    int64_t sx_idx = row_ok ? (int64_t)grow : 0;  // sx[kb][grow] = sx[kb * rows + grow]
     const int64_t sx_step = row_ok ? (int64_t)a.rows : 0;
+    int64_t sx_idx = row_ok ? (int64_t)kb_lo * a.rows + grow : 0;  // sx[kb][grow] = sx[kb * rows + grow]
     auto ld_scale = [&](const void* base, int64_t i, bool live) -> float {
       if (!live) return 0.0f;
       return scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(base, i))), i);
     };
-    float sx0 = ld_scale(a.sx, sx_idx, row_ok && num_kb > 0);
-    float sw0 = ld_scale(a.sw, sw_base, num_kb > 0);
-    float sx1 = ld_scale(a.sx, sx_idx + sx_step, row_ok && num_kb > 1);
-    float sw1 = ld_scale(a.sw, sw_base + 1, num_kb > 1);
-    int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + 2;
+    float sx0 = ld_scale(a.sx, sx_idx, row_ok && nloc > 0);
+    float sw0 = ld_scale(a.sw, sw_base + kb_lo, nloc > 0);
+    float sx1 = ld_scale(a.sx, sx_idx + sx_step, row_ok && nloc > 1);
+    float sw1 = ld_scale(a.sw, sw_base + kb_lo + 1, nloc > 1);
+    int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + kb_lo + 2;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
     bool ok = true;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int buf = kb % C::kAccBufs;
-      const uint32_t bph = (kb / C::kAccBufs) & 1;
+    for (int it = 0; it < nloc; ++it) {
+      const int buf = it % C::kAccBufs;
+      const uint32_t bph = (it / C::kAccBufs) & 1;
       const float f = sx0 * sw0;
       sx0 = sx1;
       sw0 = sw1;
-      const bool more = kb + 2 < num_kb;
+      const bool more = it + 2 < nloc;
       sx1 = ld_scale(a.sx, sx_next, row_ok && more);
       sw1 = ld_scale(a.sw, sw_next, more);
       sx_next += sx_step;
@@ -350,17 +361,59 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
       }
     }
-    if (ok && row_ok && !*abortv) {
-      uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
+    if (!SPLITK) {
+      if (ok && row_ok && !*abortv) {
+        uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
 #pragma unroll
-      for (int j = 0; j < C::kCols / 8; ++j) {
-        float x[8];
+        for (int j = 0; j < C::kCols / 8; ++j) {
+          float x[8];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) f32x2_unpack(acc[4 * j + h], x[2 * h], x[2 * h + 1]);
-        dst[j] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                            pack_bf16x2(x[6], x[7]));
+          for (int h = 0; h < 4; ++h) f32x2_unpack(acc[4 * j + h], x[2 * h], x[2 * h + 1]);
+          dst[j] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                              pack_bf16x2(x[6], x[7]));
+        }
+      }
+    } else if (row_ok) {
+      // this split's fp32 partial tile, row-major with a 4-float pad per row,
+      // over the operand stages (every MMA that read them has completed)
+      float4* prow = reinterpret_cast<float4*>(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch +
+                                               slice * C::kCols);
+#pragma unroll
+      for (int j = 0; j < C::kCols / 4; ++j) {
+        float4 v;
+        f32x2_unpack(acc[2 * j], v.x, v.y);
+        f32x2_unpack(acc[2 * j + 1], v.z, v.w);
+        prow[j] = v;
       }
     }
+  }
+  if (SPLITK) {
+    // sum the cluster's partial tiles: rank `split` owns a run of 8-column
+    // chunks; ranks are added in a fixed order, then rounded to bf16 once
+    cluster_sync();
+    if (warp >= 4) {
+      const int quad = warp & 3, slice = (warp - 4) >> 2;
+      const int r = quad * 32 + lane;
+      const int grow = row0 + r;
+      constexpr int kChunks = BN / 8, kSlices = C::kEpiWarps / 4;
+      const int ch_lo = kChunks * split / splits, ch_hi = kChunks * (split + 1) / splits;
+      if (grow < seg_end && !*abortv) {
+        const uint32_t prow = smem_u32(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch);
+        for (int ch = ch_lo + slice; ch < ch_hi; ch += kSlices) {
+          float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int q = 0; q < splits; ++q) {
+            const uint32_t ra = mapa_shared(prow + ch * 32, (uint32_t)q);
+            const float4 u = ld_dsmem_f32x4(ra), w = ld_dsmem_f32x4(ra + 16);
+            x[0] += u.x; x[1] += u.y; x[2] += u.z; x[3] += u.w;
+            x[4] += w.x; x[5] += w.y; x[6] += w.z; x[7] += w.w;
+          }
+          *reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + ch * 8) =
+              make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                         pack_bf16x2(x[6], x[7]));
+        }
+      }
+    }
+    cluster_sync();  // no CTA leaves while its partial may still be read
   }
   tc_fence_before();
   __syncthreads();
@@ -393,6 +446,7 @@ struct Debug {
   int fault_skip_kb = -1;         // the producer skips this K chunk (forces a timeout)
   int wait_mode = 0;              // which roles poll instead of suspending (bits: 1 producer/MMA, 2 epilogue)
   int l2_prefetch = 0;            // K chunks of L2 prefetch beyond the shared-memory ring
+  int splits = 0;                 // 0: choose; 1..8: force the split-K cluster size
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -452,25 +506,98 @@ DeviceInfo device_info() {
   return cache[dev];
 }
 
-template <int BN, bool UE8M0>
-fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t grid_x, const GemmArgs& args,
-                    cudaStream_t stream) {
+// clusters of `splits` CTAs along z that can be resident at once (0: none)
+template <typename K>
+int max_active_clusters(K kernel, dim3 grid, int threads, int smem, int splits) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Per device and kernel instantiation, what does not depend on the call's
+// pointers is established once: the shared-memory opt-in, the register check
+// of the setmaxnreg split, and for each split count whether its clusters fit.
+struct KernelState {
+  bool ready = false;
+  bool regs_ok = false;
+  bool attr_ok = false;
+  int8_t cluster_fits[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+};
+
+template <int BN, bool UE8M0, bool SPLITK>
+KernelState& kernel_state(int dev) {
+  static KernelState st[64];
+  return st[dev];
+}
+
+template <int BN, bool UE8M0, bool SPLITK>
+fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t grid_x, GemmArgs args,
+                    int splits, cudaStream_t stream) {
   using C = Cfg<BN>;
+  auto kernel = gemm_blockscaled_kernel<BN, UE8M0, SPLITK>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
+  KernelState& ks = kernel_state<BN, UE8M0, SPLITK>(dev);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!ks.ready) {
+      cudaFuncAttributes fa;
+      ks.regs_ok = cudaFuncGetAttributes(&fa, kernel) == cudaSuccess &&
+                   // setmaxnreg.inc waits until the block has the registers it asks
+                   // for: the launch allocation must cover the split or it waits forever
+                   (!C::kSplitRegs || fa.numRegs >= C::kMinLaunchRegs);
+      ks.attr_ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==
+                   cudaSuccess;
+      ks.ready = true;
+    }
+    if (!ks.attr_ok) return FP8RL_ERR_CUDA;
+    if (!ks.regs_ok) return FP8RL_ERR_UNSUPPORTED;  // the caller retries with 128-wide tiles
+    // the largest split count not above the request whose clusters can be resident
+    while (SPLITK && splits > 1) {
+      if (ks.cluster_fits[splits] < 0)
+        ks.cluster_fits[splits] =
+            max_active_clusters(kernel, dim3(1, 1, (unsigned)splits), C::kThreads, C::kSmemBytes, splits) >= 1;
+      if (ks.cluster_fits[splits]) break;
+      --splits;
+    }
+  }
+  if (SPLITK && splits == 1) return FP8RL_ERR_UNSUPPORTED;  // the caller launches the plain kernel
   CUtensorMap mx, mw;
   if (!make_map(&mx, xq, args.k, args.rows, kBM)) return FP8RL_ERR_CUDA;
   if (!make_map(&mw, wq, args.k, (uint64_t)experts * args.n, BN)) return FP8RL_ERR_CUDA;
-  auto kernel = gemm_blockscaled_kernel<BN, UE8M0>;
-  if (C::kSplitRegs) {
-    // setmaxnreg.inc waits until the block has the registers it asks for; make
-    // sure the launch allocation covers the split, or it would wait forever
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8RL_ERR_CUDA;
-    if (fa.numRegs < C::kMinLaunchRegs) return FP8RL_ERR_UNSUPPORTED;  // the caller retries with 128
+  args.splits = splits;
+  const dim3 grid((unsigned)grid_x, (unsigned)(args.n / BN), (unsigned)splits);
+  if (!SPLITK) {
+    kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, args);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, args) != cudaSuccess) return FP8RL_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-    return FP8RL_ERR_CUDA;
-  dim3 grid((unsigned)grid_x, (unsigned)(args.n / BN));
-  kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, args);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 
@@ -508,15 +635,33 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
     bn = (n % 256 == 0 && m_tiles * (n / 256) >= 2 * (int64_t)di.sms) ? 256 : 128;
   }
   if (bn == 256 && n % 256) bn = 128;
+  // split K across a cluster when the tiles alone leave SMs idle (dense only):
+  // decode-sized M streams the weights through every SM
+  const int64_t num_kb = k / kBK;
+  int splits = 1;
+  if (!d_offsets) {
+    const int64_t tiles = m_tiles * (n / 128);
+    if (dbg.splits > 0)
+      splits = dbg.splits;
+    else if (m_tiles * (n / bn) < di.sms && tiles < di.sms)
+      splits = (int)std::min<int64_t>(std::min<int64_t>(8, di.sms / tiles), num_kb / 2);
+    splits = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(splits, 8), num_kb));
+  }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool ue = fmt == FP8RL_SCALE_UE8M0;
-  if (bn == 256) {
-    const fp8rl_status st = ue ? launch<256, true>(xq, wq, experts, grid_x, args, cs)
-                               : launch<256, false>(xq, wq, experts, grid_x, args, cs);
+  if (splits > 1) {
+    // split-K clusters use 128-wide tiles
+    const fp8rl_status st = ue ? launch<128, true, true>(xq, wq, experts, grid_x, args, splits, cs)
+                               : launch<128, false, true>(xq, wq, experts, grid_x, args, splits, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
-  return ue ? launch<128, true>(xq, wq, experts, grid_x, args, cs)
-            : launch<128, false>(xq, wq, experts, grid_x, args, cs);
+  if (bn == 256) {
+    const fp8rl_status st = ue ? launch<256, true, false>(xq, wq, experts, grid_x, args, 1, cs)
+                               : launch<256, false, false>(xq, wq, experts, grid_x, args, 1, cs);
+    if (st != FP8RL_ERR_UNSUPPORTED) return st;
+  }
+  return ue ? launch<128, true, false>(xq, wq, experts, grid_x, args, 1, cs)
+            : launch<128, false, false>(xq, wq, experts, grid_x, args, 1, cs);
 }
 
 }  // namespace
@@ -567,6 +712,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 5:
       if (value < 0 || value > 64) return FP8RL_ERR_INVALID_ARG;
       g_debug.l2_prefetch = (int)value;
+      return FP8RL_OK;
+    case 6:
+      if (value < 0 || value > 8) return FP8RL_ERR_INVALID_ARG;
+      g_debug.splits = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

@@ -205,6 +205,8 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          the hardware park them; bit 1: the same for the epilogue (default 0);
  *   key 5  how many K chunks beyond the shared-memory stages the TMA producer
  *          prefetches into L2 (0..64, default 0: measured slower on GB300);
+ *   key 6  split-K cluster size of the dense GEMM: 0 chooses (default), 1..8
+ *          forces it (reduced to what can be resident);
  *   key 0  restore all defaults.
  * Errors: INVALID_ARG for an unknown key or value.
  */

@@ -137,5 +137,7 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 1, 96) == 1
     assert _rc("fp8rl_debug_set", 3, 0) == 1
     assert _rc("fp8rl_debug_set", 99, 0) == 1
+    assert _rc("fp8rl_debug_set", 6, 9) == 1
+    assert _rc("fp8rl_debug_set", 6, 4) == 0
     assert _rc("fp8rl_debug_set", 1, 256) == 0
     assert _rc("fp8rl_debug_set", 0, 0) == 0

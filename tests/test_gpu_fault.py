@@ -83,3 +83,21 @@ def test_debug_hook_rejects_bad_values():
         fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 0)
     with pytest.raises(fp8rl.Fp8rlError):
         fp8rl.fp8rl_debug_set(99, 0)
+
+
+def test_split_k_cluster_wait_runs_out_and_is_reported():
+    m, n, k = 16, 256, 1024
+    xq, sx, wq, sw = operands(m, n, k, 3)
+    dx, dsx, dw, dsw = dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(6, 4)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, 1)
+    fp8rl.gemm(dx, dsx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+    y = fp8rl.gemm(dx, dsx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == 0
+    ref = oracle.gemm_blockscaled(xq, sx, wq, sw)
+    got = y.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)

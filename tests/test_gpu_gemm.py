@@ -233,3 +233,35 @@ def test_grouped_rows_outside_offsets_untouched():
     y = run_grouped(offsets, xq2, sx2, wq, sw, fp8rl.SCALE_FP32, fill=3.0)
     assert np.all(y[12:] == 3.0)
     within(y[:12], oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets))
+
+
+# --------------------------------------------------------------------------- split-K clusters
+
+@pytest.fixture
+def force_splits(request):
+    yield lambda s: fp8rl.fp8rl_debug_set(6, s)
+    fp8rl.fp8rl_debug_set(6, 0)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("splits", [2, 3, 4, 8])
+@pytest.mark.parametrize("m,n,k", [(1, 128, 256), (16, 384, 1280), (100, 256, 640), (128, 128, 1024),
+                                   (200, 256, 2048)])
+def test_split_k_cluster(m, n, k, splits, fmt, force_splits):
+    """K split over a cluster, partial tiles summed through distributed shared
+    memory; uneven splits (k/128 not a multiple of the split count) included."""
+    force_splits(splits)
+    x = synth.activation_bf16(m, k, 21, "splitk", m, n, k)
+    w = synth.weight_bf16(n, k, 22, "splitk", m, n, k)
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    within(run_gemm(xq, sx, wq, sw, fmt), oracle.gemm_blockscaled(xq, sx, wq, sw, fmt))
+
+
+def test_split_k_is_deterministic(force_splits):
+    force_splits(4)
+    x = synth.activation_bf16(16, 4096, 23, "splitk-det")
+    w = synth.weight_bf16(512, 4096, 24, "splitk-det")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    y1 = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    y2 = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    assert np.array_equal(y1, y2)
