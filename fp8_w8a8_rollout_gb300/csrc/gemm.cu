@@ -113,6 +113,65 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Rows of the m-tile with index m_idx: (expert, first row, end of the expert's
+// segment).  Dense: one segment [0, rows).  Grouped: a running prefix over the
+// experts of their 128-row tile counts, 32 experts per step.  Warp-collective.
+struct TileRows {
+  int expert, row0, seg_end;
+};
+
+__device__ __forceinline__ TileRows tile_rows(const GemmArgs& a, int m_idx, int lane) {
+  if (a.offsets == nullptr) return TileRows{0, m_idx * kBM, a.rows};
+  TileRows tr{-1, 0, 0};
+  int done = 0;
+  for (int e0 = 0; e0 < a.experts && tr.expert < 0; e0 += 32) {
+    const int ex = e0 + lane;
+    int start = 0, end = 0;
+    if (ex < a.experts) {
+      start = min(max(a.offsets[ex], 0), a.rows);
+      end = min(max(a.offsets[ex + 1], 0), a.rows);
+      end = max(end, start);
+    }
+    const int tiles = (end - start + kBM - 1) / kBM;
+    int incl = tiles;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int excl = incl - tiles;
+    const bool hit = tiles > 0 && m_idx >= done + excl && m_idx < done + incl;
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      tr.expert = __shfl_sync(0xffffffffu, ex, src);
+      tr.row0 = __shfl_sync(0xffffffffu, start, src) + (m_idx - done - __shfl_sync(0xffffffffu, excl, src)) * kBM;
+      tr.seg_end = __shfl_sync(0xffffffffu, end, src);
+    }
+    done += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return tr;
+}
+
+// number of 128-row tiles over all segments (warp-collective)
+__device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
+  if (a.offsets == nullptr) return (a.rows + kBM - 1) / kBM;
+  int total = 0;
+  for (int e0 = 0; e0 < a.experts; e0 += 32) {
+    const int ex = e0 + lane;
+    int tiles = 0;
+    if (ex < a.experts) {
+      const int start = min(max(a.offsets[ex], 0), a.rows);
+      const int end = max(min(max(a.offsets[ex + 1], 0), a.rows), start);
+      tiles = (end - start + kBM - 1) / kBM;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, off);
+    total += tiles;
+  }
+  return total;
+}
+
 template <int BN, bool UE8M0, bool SPLITK>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
@@ -131,65 +190,23 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   uint64_t* drain = tempty + C::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* tile = abort_flag + 1;  // expert, first row, segment end
+  int* shared_m_tiles = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
-  const int n0 = blockIdx.y * BN;
-  // split-K: this CTA's K chunks [kb_lo, kb_lo + nloc); the partial tiles of a
-  // cluster are summed through distributed shared memory at the end
+  const int n_tiles = a.n / BN;
+  // split-K: one tile per CTA (m-tile blockIdx.x, n-tile blockIdx.y), this
+  // CTA's K chunks [kb_lo, kb_lo + nloc); the partial tiles of a cluster are
+  // summed through distributed shared memory at the end.  Otherwise the CTA is
+  // persistent: tiles blockIdx.x, blockIdx.x + gridDim.x, ... (m-tile fastest).
   const int splits = SPLITK ? a.splits : 1;
   const int split = SPLITK ? (int)cluster_ctarank() : 0;
   const int kb_lo = (int)((int64_t)num_kb * split / splits);
   const int nloc = (int)((int64_t)num_kb * (split + 1) / splits) - kb_lo;
 
-  // ---- which rows this CTA covers
   if (warp == 0) {
-    int e = -1, row0 = 0, seg_end = 0;
-    if (a.offsets == nullptr) {
-      row0 = blockIdx.x * kBM;
-      seg_end = a.rows;
-      e = row0 < a.rows ? 0 : -1;
-    } else {
-      // running prefix over experts of their 128-row tile counts, 32 at a time
-      const int target = blockIdx.x;
-      int done = 0;
-      for (int e0 = 0; e0 < a.experts && e < 0; e0 += 32) {
-        const int ex = e0 + lane;
-        int start = 0, end = 0;
-        if (ex < a.experts) {
-          start = min(max(a.offsets[ex], 0), a.rows);
-          end = min(max(a.offsets[ex + 1], 0), a.rows);
-          end = max(end, start);
-        }
-        const int tiles = (end - start + kBM - 1) / kBM;
-        int incl = tiles;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += v;
-        }
-        const int excl = incl - tiles;
-        const bool hit = tiles > 0 && target >= done + excl && target < done + incl;
-        const unsigned m = __ballot_sync(0xffffffffu, hit);
-        if (m) {
-          const int src = __ffs(m) - 1;
-          const int se = __shfl_sync(0xffffffffu, ex, src);
-          const int sst = __shfl_sync(0xffffffffu, start, src);
-          const int sen = __shfl_sync(0xffffffffu, end, src);
-          const int sex = __shfl_sync(0xffffffffu, excl, src);
-          e = se;
-          row0 = sst + (target - done - sex) * kBM;
-          seg_end = sen;
-        }
-        done += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-    if (lane == 0) {
-      tile[0] = e;
-      tile[1] = row0;
-      tile[2] = seg_end;
-    }
+    const int mt = SPLITK ? 0 : count_m_tiles(a, lane);
+    if (lane == 0) *shared_m_tiles = mt;
   }
   if (threadIdx.x == 32) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -205,9 +222,20 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
-  const int expert = tile[0];
-  if (expert < 0) return;  // the grid is an upper bound on the tiles; CTA-uniform
-  const int row0 = tile[1], seg_end = tile[2];
+  const int m_tiles = *shared_m_tiles;
+  const int total_tiles = SPLITK ? 1 : m_tiles * n_tiles;
+  const int first_tile = SPLITK ? 0 : (int)blockIdx.x;
+  const int tile_stride = SPLITK ? 1 : (int)gridDim.x;
+  if (first_tile >= total_tiles) return;  // CTA-uniform: more CTAs than tiles
+  auto tile_coords = [&](int t, int& m_idx, int& n_tile) {
+    if (SPLITK) {
+      m_idx = blockIdx.x;
+      n_tile = blockIdx.y;
+    } else {
+      m_idx = t % m_tiles;
+      n_tile = t / m_tiles;
+    }
+  };
 
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
@@ -217,77 +245,88 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   volatile int* abortv = abort_flag;
 
   if (warp < 4) {
-  if (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRoleRegs));
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_x);
-      prefetch_tensormap(&tmap_w);
-      const int wrow0 = expert * a.n + n0;
-      // operands of the first chunks go to L2 at once; later ones a fixed
-      // distance ahead of their shared-memory loads
-      for (int it = C::kStages; it < min(nloc, C::kStages + a.l2_prefetch); ++it) {
-        tma_prefetch_l2_2d(&tmap_x, (kb_lo + it) * kBK, row0);
-        tma_prefetch_l2_2d(&tmap_w, (kb_lo + it) * kBK, wrow0);
+    if (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRoleRegs));
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        prefetch_tensormap(&tmap_x);
+        prefetch_tensormap(&tmap_w);
       }
-      int issued = 0;
-      for (int it = 0; it < nloc; ++it) {
-        const int kb = kb_lo + it;
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) break;
-        issued = it + 1;
-        if (it == a.fault_skip_kb) continue;
-        const int pf = it + C::kStages + a.l2_prefetch;
-        if (a.l2_prefetch > 0 && pf < nloc) {
-          tma_prefetch_l2_2d(&tmap_x, (kb_lo + pf) * kBK, row0);
-          tma_prefetch_l2_2d(&tmap_w, (kb_lo + pf) * kBK, wrow0);
+      uint32_t g = 0;  // chunks issued by this CTA so far (position in the stage ring)
+      bool alive = true;
+      for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
+        int m_idx, n_tile;
+        tile_coords(t, m_idx, n_tile);
+        const TileRows tr = tile_rows(a, m_idx, lane);
+        if (lane == 0) {
+          const int wrow0 = tr.expert * a.n + n_tile * BN;
+          for (int it = 0; it < nloc; ++it, ++g) {
+            const int kb = kb_lo + it;
+            const int s = g % C::kStages;
+            const uint32_t ph = (g / C::kStages) & 1;
+            if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
+              alive = false;
+              break;
+            }
+            if ((int)g == a.fault_skip_kb) continue;
+            if (a.l2_prefetch > 0 && it + a.l2_prefetch < nloc) {
+              tma_prefetch_l2_2d(&tmap_x, (kb + a.l2_prefetch) * kBK, tr.row0);
+              tma_prefetch_l2_2d(&tmap_w, (kb + a.l2_prefetch) * kBK, wrow0);
+            }
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, tr.row0, fb);
+            tma_load_2d(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
+          }
         }
-        const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, C::kStageBytes);
-        tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, row0, fb);
-        tma_load_2d(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
+        alive = __shfl_sync(0xffffffffu, alive, 0);
       }
-      if (*abortv) {
+      if (lane == 0 && *abortv) {
         // let the copies still in flight land before shared memory is released
-        for (int it = max(0, issued - C::kStages); it < issued; ++it) {
-          if (it == a.fault_skip_kb) continue;
-          mbar_wait_bounded(smem_u32(&full[it % C::kStages]), (it / C::kStages) & 1, nullptr, nullptr,
-                            10000000ull);
+        for (uint32_t j = g > (uint32_t)C::kStages ? g - C::kStages : 0; j < g; ++j) {
+          if ((int)j == a.fault_skip_kb) continue;
+          mbar_wait_bounded(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1, nullptr, nullptr, 10000000ull);
         }
       }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-      for (int it = 0; it < nloc; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        const int buf = it % C::kAccBufs;
-        const uint32_t bph = (it / C::kAccBufs) & 1;
-        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) break;
-        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1)))
-          break;
-        tc_fence_after();
-        const uint32_t d = tmem + buf * BN;
-        const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+        const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
+        uint32_t g = 0;  // chunks consumed (stage ring and TMEM ring position)
+        bool alive = true;
+        for (int tt = 0; tt < my_tiles && alive; ++tt) {
+          for (int it = 0; it < nloc; ++it, ++g) {
+            const int s = g % C::kStages;
+            const uint32_t ph = (g / C::kStages) & 1;
+            const int buf = g % C::kAccBufs;
+            const uint32_t bph = (g / C::kAccBufs) & 1;
+            if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1)) ||
+                !mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
+                                   !(a.wait_mode & 1))) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + buf * BN;
+            const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
 #pragma unroll
-        for (int k = 0; k < kBK / kUmmaK; ++k)
-          mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
-                   k > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&empty[s]));
-        mma_commit(smem_u32(&tfull[buf]));
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                       k > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&empty[s]));
+            mma_commit(smem_u32(&tfull[buf]));
+          }
+        }
+        if (*abortv) {
+          // no MMA may still be writing TMEM when it is released
+          mma_commit(smem_u32(drain));
+          mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+        }
       }
-      if (*abortv) {
-        // no MMA may still be writing TMEM when it is released
-        mma_commit(smem_u32(drain));
-        mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
-      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
     if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
     // ------------------------------------------------------------ epilogue
@@ -295,95 +334,103 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const int quad = warp & 3;   // TMEM lanes this warp may read: 32*quad .. +31
     const int slice = ew >> 2;   // which kCols columns of the tile
     const int r = quad * 32 + lane;
-    const int grow = row0 + r;
-    const bool row_ok = grow < seg_end;
-    const int nb = (n0 + slice * C::kCols) >> 7;
-    const int64_t sw_base = ((int64_t)expert * (a.n / 128) + nb) * num_kb;
-    // fp32 accumulators as packed pairs (fma.rn.f32x2: two round-to-nearest
-    // FMAs per instruction, the same results as scalar FMAs)
-    uint64_t acc[C::kCols / 2];
-#pragma unroll
-    for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
-    // the chunk scales of this thread's row and column slice, loaded two K
-    // chunks ahead (about one L2 round trip) so that no global-memory latency
-    // sits between the tensor cores finishing a chunk and this thread folding
-    // it in; indices advance by one chunk per iteration
-    const int64_t sx_step = row_ok ? (int64_t)a.rows : 0;
-    int64_t sx_idx = row_ok ? (int64_t)kb_lo * a.rows + grow : 0;  // sx[kb][grow] = sx[kb * rows + grow]
-    auto ld_scale = [&](const void* base, int64_t i, bool live) -> float {
-      if (!live) return 0.0f;
-      return scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(base, i))), i);
-    };
-    float sx0 = ld_scale(a.sx, sx_idx, row_ok && nloc > 0);
-    float sw0 = ld_scale(a.sw, sw_base + kb_lo, nloc > 0);
-    float sx1 = ld_scale(a.sx, sx_idx + sx_step, row_ok && nloc > 1);
-    float sw1 = ld_scale(a.sw, sw_base + kb_lo + 1, nloc > 1);
-    int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + kb_lo + 2;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
+    auto ld_scale = [&](const void* p, int64_t i, bool live) -> float {
+      if (!live) return 0.0f;
+      return scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(p, i))), i);
+    };
+    uint32_t g = 0;  // chunks folded so far (TMEM ring position)
     bool ok = true;
-    for (int it = 0; it < nloc; ++it) {
-      const int buf = it % C::kAccBufs;
-      const uint32_t bph = (it / C::kAccBufs) & 1;
-      const float f = sx0 * sw0;
-      sx0 = sx1;
-      sw0 = sw1;
-      const bool more = it + 2 < nloc;
-      sx1 = ld_scale(a.sx, sx_next, row_ok && more);
-      sw1 = ld_scale(a.sw, sw_next, more);
-      sx_next += sx_step;
-      sw_next += 1;
-      ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t f2 = f32x2(f, f);
-      const uint32_t taddr = t_lane + buf * BN;
-      if (C::kEarlyRelease) {
-        // copy the whole slice out of TMEM, hand the buffer back, then fold
-        uint64_t v[C::kCols / 2];
+    for (int t = first_tile; t < total_tiles && ok; t += tile_stride) {
+      int m_idx, n_tile;
+      tile_coords(t, m_idx, n_tile);
+      const TileRows tr = tile_rows(a, m_idx, lane);
+      const int n0 = n_tile * BN;
+      const int grow = tr.row0 + r;
+      const bool row_ok = grow < tr.seg_end;
+      const int nb = (n0 + slice * C::kCols) >> 7;
+      const int64_t sw_base = ((int64_t)tr.expert * (a.n / 128) + nb) * num_kb + kb_lo;
+      // fp32 accumulators as packed pairs (fma.rn.f32x2: two round-to-nearest
+      // FMAs per instruction, the same results as scalar FMAs)
+      uint64_t acc[C::kCols / 2];
 #pragma unroll
-        for (int c = 0; c < C::kCols / 32; ++c) tmem_ld_32x32b_x32_pairs(taddr + c * 32, *reinterpret_cast<uint64_t(*)[16]>(&v[c * 16]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
+      for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
+      // the chunk scales of this thread's row and column slice, loaded two K
+      // chunks ahead (about one L2 round trip) so that no global-memory latency
+      // sits between the tensor cores finishing a chunk and this thread folding
+      // it in; indices advance by one chunk per iteration
+      const int64_t sx_step = row_ok ? (int64_t)a.rows : 0;
+      const int64_t sx_idx = row_ok ? (int64_t)kb_lo * a.rows + grow : 0;  // sx[kb][grow]
+      float sx0 = ld_scale(a.sx, sx_idx, row_ok && nloc > 0);
+      float sw0 = ld_scale(a.sw, sw_base, nloc > 0);
+      float sx1 = ld_scale(a.sx, sx_idx + sx_step, row_ok && nloc > 1);
+      float sw1 = ld_scale(a.sw, sw_base + 1, nloc > 1);
+      int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + 2;
+      for (int it = 0; it < nloc; ++it, ++g) {
+        const int buf = g % C::kAccBufs;
+        const uint32_t bph = (g / C::kAccBufs) & 1;
+        const float f = sx0 * sw0;
+        sx0 = sx1;
+        sw0 = sw1;
+        const bool more = it + 2 < nloc;
+        sx1 = ld_scale(a.sx, sx_next, row_ok && more);
+        sw1 = ld_scale(a.sw, sw_next, more);
+        sx_next += sx_step;
+        sw_next += 1;
+        ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t f2 = f32x2(f, f);
+        const uint32_t taddr = t_lane + buf * BN;
+        if (C::kEarlyRelease) {
+          // copy the whole slice out of TMEM, hand the buffer back, then fold
+          uint64_t v[C::kCols / 2];
 #pragma unroll
-        for (int j = 0; j < C::kCols / 2; ++j) acc[j] = fma_f32x2(v[j], f2, acc[j]);
-      } else {
+          for (int c = 0; c < C::kCols / 32; ++c)
+            tmem_ld_32x32b_x32_pairs(taddr + c * 32, *reinterpret_cast<uint64_t(*)[16]>(&v[c * 16]));
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
 #pragma unroll
-        for (int c = 0; c < C::kCols / 32; ++c) {
-          uint64_t v[16];
-          tmem_ld_32x32b_x32_pairs(taddr + c * 32, v);
+          for (int j = 0; j < C::kCols / 2; ++j) acc[j] = fma_f32x2(v[j], f2, acc[j]);
+        } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fma_f32x2(v[j], f2, acc[c * 16 + j]);
+          for (int c = 0; c < C::kCols / 32; ++c) {
+            uint64_t v[16];
+            tmem_ld_32x32b_x32_pairs(taddr + c * 32, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fma_f32x2(v[j], f2, acc[c * 16 + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
       }
-    }
-    if (!SPLITK) {
-      if (ok && row_ok && !*abortv) {
-        uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
+      if (!SPLITK) {
+        if (ok && row_ok && !*abortv) {
+          uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
 #pragma unroll
-        for (int j = 0; j < C::kCols / 8; ++j) {
-          float x[8];
+          for (int j = 0; j < C::kCols / 8; ++j) {
+            float x[8];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) f32x2_unpack(acc[4 * j + h], x[2 * h], x[2 * h + 1]);
-          dst[j] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                              pack_bf16x2(x[6], x[7]));
+            for (int h = 0; h < 4; ++h) f32x2_unpack(acc[4 * j + h], x[2 * h], x[2 * h + 1]);
+            dst[j] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                                pack_bf16x2(x[6], x[7]));
+          }
         }
-      }
-    } else if (row_ok) {
-      // this split's fp32 partial tile, row-major with a 4-float pad per row,
-      // over the operand stages (every MMA that read them has completed)
-      float4* prow = reinterpret_cast<float4*>(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch +
-                                               slice * C::kCols);
+      } else if (row_ok) {
+        // this split's fp32 partial tile, row-major with a 4-float pad per row,
+        // over the operand stages (every MMA that read them has completed)
+        float4* prow = reinterpret_cast<float4*>(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch +
+                                                 slice * C::kCols);
 #pragma unroll
-      for (int j = 0; j < C::kCols / 4; ++j) {
-        float4 v;
-        f32x2_unpack(acc[2 * j], v.x, v.y);
-        f32x2_unpack(acc[2 * j + 1], v.z, v.w);
-        prow[j] = v;
+        for (int j = 0; j < C::kCols / 4; ++j) {
+          float4 v;
+          f32x2_unpack(acc[2 * j], v.x, v.y);
+          f32x2_unpack(acc[2 * j + 1], v.z, v.w);
+          prow[j] = v;
+        }
       }
     }
   }
@@ -394,10 +441,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     if (warp >= 4) {
       const int quad = warp & 3, slice = (warp - 4) >> 2;
       const int r = quad * 32 + lane;
-      const int grow = row0 + r;
+      const TileRows tr = tile_rows(a, blockIdx.x, lane);
+      const int grow = tr.row0 + r;
+      const int n0 = blockIdx.y * BN;
       constexpr int kChunks = BN / 8, kSlices = C::kEpiWarps / 4;
       const int ch_lo = kChunks * split / splits, ch_hi = kChunks * (split + 1) / splits;
-      if (grow < seg_end && !*abortv) {
+      if (grow < tr.seg_end && !*abortv) {
         const uint32_t prow = smem_u32(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch);
         for (int ch = ch_lo + slice; ch < ch_hi; ch += kSlices) {
           float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -545,8 +594,8 @@ KernelState& kernel_state(int dev) {
 }
 
 template <int BN, bool UE8M0, bool SPLITK>
-fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t grid_x, GemmArgs args,
-                    int splits, cudaStream_t stream) {
+fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_tiles_bound, int sms,
+                    GemmArgs args, int splits, cudaStream_t stream) {
   using C = Cfg<BN>;
   auto kernel = gemm_blockscaled_kernel<BN, UE8M0, SPLITK>;
   int dev = 0;
@@ -580,7 +629,11 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t gri
   if (!make_map(&mx, xq, args.k, args.rows, kBM)) return FP8RL_ERR_CUDA;
   if (!make_map(&mw, wq, args.k, (uint64_t)experts * args.n, BN)) return FP8RL_ERR_CUDA;
   args.splits = splits;
-  const dim3 grid((unsigned)grid_x, (unsigned)(args.n / BN), (unsigned)splits);
+  // split-K: one CTA per (m-tile, n-tile, split); otherwise persistent CTAs,
+  // at most one per SM, striding over the tiles
+  const int64_t tiles_bound = m_tiles_bound * (args.n / BN);
+  const dim3 grid = SPLITK ? dim3((unsigned)m_tiles_bound, (unsigned)(args.n / BN), (unsigned)splits)
+                           : dim3((unsigned)std::min<int64_t>(tiles_bound, sms), 1, 1);
   if (!SPLITK) {
     kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, args);
   } else {
@@ -628,7 +681,6 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   args.wait_mode = dbg.wait_mode;
   args.l2_prefetch = dbg.l2_prefetch;
   const int64_t m_tiles = (rows + kBM - 1) / kBM;
-  const int64_t grid_x = d_offsets ? m_tiles + experts : m_tiles;
   int bn = dbg.bn;
   if (bn != 128 && bn != 256) {
     // wide tiles when there are enough of them to fill every SM
@@ -649,19 +701,22 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool ue = fmt == FP8RL_SCALE_UE8M0;
+  // an upper bound on the 128-row tiles (grouped: every expert may end in a partial tile)
+  const int64_t mt_bound = d_offsets ? m_tiles + experts : m_tiles;
+  const int sms = di.sms;
   if (splits > 1) {
     // split-K clusters use 128-wide tiles
-    const fp8rl_status st = ue ? launch<128, true, true>(xq, wq, experts, grid_x, args, splits, cs)
-                               : launch<128, false, true>(xq, wq, experts, grid_x, args, splits, cs);
+    const fp8rl_status st = ue ? launch<128, true, true>(xq, wq, experts, mt_bound, sms, args, splits, cs)
+                               : launch<128, false, true>(xq, wq, experts, mt_bound, sms, args, splits, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
   if (bn == 256) {
-    const fp8rl_status st = ue ? launch<256, true, false>(xq, wq, experts, grid_x, args, 1, cs)
-                               : launch<256, false, false>(xq, wq, experts, grid_x, args, 1, cs);
+    const fp8rl_status st = ue ? launch<256, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                               : launch<256, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
-  return ue ? launch<128, true, false>(xq, wq, experts, grid_x, args, 1, cs)
-            : launch<128, false, false>(xq, wq, experts, grid_x, args, 1, cs);
+  return ue ? launch<128, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+            : launch<128, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
 }
 
 }  // namespace
