@@ -26,7 +26,7 @@ __all__ = [
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
     "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
-    "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm",
+    "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm", "HostWeightSync",
 ]
 
 SCALE_FP32 = 0
@@ -254,3 +254,71 @@ def grouped_gemm(xq, x_scale, wq, w_scale, d_offsets, fmt=SCALE_FP32, out=None, 
     fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, e, rows, n, k, out, fmt,
                                    stream)
     return out
+
+
+class HostWeightSync:
+    """Weight sync from host memory: bf16 weights in pinned host buffers are
+    copied to the GPU, quantised (128x128 blocks) and the E4M3 codes and scales
+    copied back to pinned host buffers, as a three-stream pipeline (copy in,
+    quantise, copy out) over chunks of whole 128-row block rows, so that both
+    copy directions overlap the kernels and each other.
+
+    Each chunk is an independent sub-matrix: its codes and scale rows are
+    exactly those of the whole matrix.  Device staging is allocated once, at
+    construction (`chunk_rows` rows per slot, `slots` slots); `run()` then only
+    enqueues work on the caller's device."""
+
+    def __init__(self, host_weights, host_codes, host_scales, fmt=SCALE_FP32, chunk_bytes=32 << 20,
+                 slots=3, device=None):
+        device = torch.device(device or "cuda")
+        self.fmt = fmt
+        self.items = []
+        for w, q, s in zip(host_weights, host_codes, host_scales):
+            n, k = w.shape
+            rows = max(128, (chunk_bytes // (2 * k)) // 128 * 128)
+            for r0 in range(0, n, rows):
+                r1 = min(n, r0 + rows)
+                self.items.append((w[r0:r1], q[r0:r1], s[r0 // 128:(r1 + 127) // 128], r1 - r0, k))
+        # flat staging, viewed per chunk as contiguous [n][k] / [n/128][k/128]
+        elems = max(it[3] * it[4] for it in self.items)
+        blocks = max(((it[3] + 127) // 128) * ((it[4] + 127) // 128) for it in self.items)
+        self.slots = [(torch.empty(elems, dtype=torch.bfloat16, device=device),
+                       torch.empty(elems, dtype=torch.uint8, device=device),
+                       torch.empty(blocks, dtype=_scale_dtype(fmt), device=device))
+                      for _ in range(slots)]
+        self.s_in = torch.cuda.Stream(device)
+        self.s_q = torch.cuda.Stream(device)
+        self.s_out = torch.cuda.Stream(device)
+        self.ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(slots)]
+        self.h2d_bytes = sum(w.numel() * 2 for w in host_weights)
+        self.d2h_bytes = sum(q.numel() + s.numel() * s.element_size() for q, s in zip(host_codes, host_scales))
+
+    def run(self):
+        """Enqueue one full weight sync; returns immediately (the caller syncs)."""
+        cur = torch.cuda.current_stream()
+        for st in (self.s_in, self.s_q, self.s_out):
+            st.wait_stream(cur)
+        nslot = len(self.slots)
+        for i, (w, q, s, n, k) in enumerate(self.items):
+            j = i % nslot
+            dw, dq, ds = self.slots[j]
+            e_in, e_q, e_out = self.ev[j]
+            nb, kb = (n + 127) // 128, (k + 127) // 128
+            dw_v = dw[:n * k].view(n, k)
+            dq_v = dq[:n * k].view(n, k)
+            ds_v = ds[:nb * kb].view(nb, kb)
+            if i >= nslot:
+                self.s_in.wait_event(e_out)      # the slot's previous chunk has left the GPU
+            with torch.cuda.stream(self.s_in):
+                dw_v.copy_(w, non_blocking=True)
+                e_in.record(self.s_in)
+            self.s_q.wait_event(e_in)
+            fp8rl_quant_weight_blockwise(dw_v, n, k, k, dq_v, k, ds_v, self.fmt, self.s_q)
+            e_q.record(self.s_q)
+            self.s_out.wait_event(e_q)
+            with torch.cuda.stream(self.s_out):
+                q.copy_(dq_v, non_blocking=True)
+                s.copy_(ds_v, non_blocking=True)
+                e_out.record(self.s_out)
+        for st in (self.s_in, self.s_q, self.s_out):
+            cur.wait_stream(st)

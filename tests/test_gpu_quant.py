@@ -185,3 +185,24 @@ def test_status_is_ok_after_quantisers():
     x = torch.zeros((4, 128), dtype=torch.bfloat16, device="cuda")
     fp8rl.quant_act(x)
     assert fp8rl.fp8rl_sync_status() == 0
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_host_weight_sync_pipeline_bit_exact(fmt):
+    """Host-to-host weight sync in small chunks (many more chunks than staging
+    slots, ragged shapes) equals the oracle on every matrix."""
+    shapes = [(384, 256), (200, 300), (1024, 128), (130, 640)]
+    ws = [synth.weight_bf16(n, k, 6, "hostsync", n, k) for n, k in shapes]
+    host_w = [w.pin_memory() for w in ws]
+    sdt = torch.float32 if fmt == fp8rl.SCALE_FP32 else torch.uint8
+    host_q = [torch.empty((n, k), dtype=torch.uint8, pin_memory=True) for n, k in shapes]
+    host_s = [torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=sdt, pin_memory=True) for n, k in shapes]
+    hs = fp8rl.HostWeightSync(host_w, host_q, host_s, fmt=fmt, chunk_bytes=64 * 1024, slots=2)
+    assert len(hs.items) > 2 * len(hs.slots)
+    for _ in range(2):
+        hs.run()
+    torch.cuda.synchronize()
+    for w, q, s in zip(ws, host_q, host_s):
+        qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(w), fmt)
+        assert np.array_equal(q.numpy(), qo)
+        assert np.array_equal(s.numpy().view(np.uint8), so.view(np.uint8))
