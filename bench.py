@@ -58,6 +58,7 @@ def parse():
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
     ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
+    ap.add_argument("--graph", action="store_true", help="with --case: also time replays of a CUDA graph")
     return ap.parse_args()
 
 
@@ -383,6 +384,32 @@ def time_loop(torch, fn, iters, warmup, flush=None):
     return statistics.median(times)
 
 
+def time_graph(torch, fn, reps, warmup=3):
+    """Per-call device time of fn replayed from a CUDA graph (captures `reps`
+    calls once; times graph replays), so host call overhead does not show."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        g.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / (3 * reps)
+
+
 def section_model_sync(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
     """Full-model weight sync: 36 layers x 7 linears (~6.95e9 params) in one pass."""
     weights = []
@@ -454,7 +481,8 @@ def section_sweep(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
                 a = sets[it[0] % len(sets)]
                 it[0] += 1
                 fp8rl.fp8rl_gemm_blockscaled(a[0], a[1], a[2], a[3], a[4], m, n, k, fmt)
-            ms = time_loop(torch, call, 20, 5)
+            # replayed from a CUDA graph: device time of back-to-back launches
+            ms = time_graph(torch, call, max(20, len(sets) * 2))
             r = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k, 4 if fmt == 0 else 1), ms,
                           peaks["hbm_gbs"], fp8_peak)
             res[f"{name}_m{m}"] = {"m": m, "n": n, "k": k, "ms": ms, "tflops": r["tflops"],
@@ -722,6 +750,8 @@ def main_case(args):
     assert fp8rl.fp8rl_sync_status() == 0
     out = {"case": args.case, "ms": ms, "bn": args.bn or "auto", "wait_mode": args.wait_mode,
            "l2_prefetch": args.l2_prefetch}
+    if args.graph:
+        out["ms_graph"] = time_graph(torch, fn, max(10, args.steps))
     if "flops" in work:
         out["tflops"] = work["flops"] / ms / 1e9
     if "bytes" in work:

@@ -49,15 +49,17 @@ constexpr int kBM = 128;     // tile rows (tcgen05 M)
 constexpr int kBK = 128;     // K chunk: one scale block, one 128-byte swizzle row
 constexpr int kUmmaK = 32;   // K of one E4M3 tcgen05.mma
 
-template <int BN>
+template <int BN, int AROWS = kBM>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  // operand stages: as many as fit in about 200 KB of shared memory
+  static constexpr int kStageBytesRaw = AROWS * kBK + BN * kBK;
+  static constexpr int kStages = (200 * 1024) / kStageBytesRaw > 12 ? 12 : (200 * 1024) / kStageBytesRaw;
   static constexpr int kCols = 64;                      // accumulator columns per epilogue thread
   static constexpr int kEpiWarps = 4 * (BN / kCols);    // 4 TMEM lane quadrants x column slices
   static constexpr int kThreads = 128 + kEpiWarps * 32; // warpgroup 0: producer, MMA, two idle warps
   static constexpr int kAccBufs = 512 / BN;             // fp32 accumulators in TMEM (all 512 columns)
   static constexpr int kTmemCols = kAccBufs * BN;
-  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kABytes = AROWS * kBK;  // activation rows loaded per stage
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
@@ -172,11 +174,15 @@ __device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
   return total;
 }
 
-template <int BN, bool UE8M0, bool SPLITK>
-__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
+// AROWS < 128 (decode-sized M, at most AROWS rows in the only m-tile): each
+// stage holds just AROWS activation rows; the M = 128 MMA reads the rest of
+// its A rows from whatever shared memory follows, which only feeds accumulator
+// rows >= AROWS that are never stored.
+template <int BN, int AROWS, bool UE8M0, bool SPLITK>
+__global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
                             const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, AROWS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   // split-K: one tile per CTA (m-tile blockIdx.x, n-tile blockIdx.y), this
   // CTA's K chunks [kb_lo, kb_lo + nloc); the partial tiles of a cluster are
   // summed through distributed shared memory at the end.  Otherwise the CTA is
-  // persistent: tiles blockIdx.x, blockIdx.x + gridDim.x, ... (m-tile fastest).
+  // persistent: tiles blockIdx.x, blockIdx.x + gridDim.x, ...
   const int splits = SPLITK ? a.splits : 1;
   const int split = SPLITK ? (int)cluster_ctarank() : 0;
   const int kb_lo = (int)((int64_t)num_kb * split / splits);
@@ -231,9 +237,17 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     if (SPLITK) {
       m_idx = blockIdx.x;
       n_tile = blockIdx.y;
-    } else {
+    } else if (a.offsets == nullptr) {
+      // dense: m-tile fastest, so that the tiles in flight share a few weight
+      // n-tiles and the whole (smaller) activation matrix stays in L2
       m_idx = t % m_tiles;
       n_tile = t / m_tiles;
+    } else {
+      // grouped: n-tile fastest, so that each activation tile is read once for
+      // all n-tiles of its expert and each expert's weights serve its few
+      // m-tiles back to back
+      m_idx = t / n_tiles;
+      n_tile = t % n_tiles;
     }
   };
 
@@ -335,9 +349,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     const int slice = ew >> 2;   // which kCols columns of the tile
     const int r = quad * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
-    auto ld_scale = [&](const void* p, int64_t i, bool live) -> float {
-      if (!live) return 0.0f;
-      return scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(p, i))), i);
+    // raw scale words are loaded ahead and decoded only when used, so that the
+    // load's latency stays hidden for both formats
+    auto ld_word = [&](const void* p, int64_t i, bool live) -> uint32_t {
+      return live ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(p, i))) : 0u;
     };
     uint32_t g = 0;  // chunks folded so far (TMEM ring position)
     bool ok = true;
@@ -348,6 +363,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int n0 = n_tile * BN;
       const int grow = tr.row0 + r;
       const bool row_ok = grow < tr.seg_end;
+      const bool warp_idle = AROWS < kBM && tr.row0 + quad * 32 >= tr.seg_end;  // warp-uniform
       const int nb = (n0 + slice * C::kCols) >> 7;
       const int64_t sw_base = ((int64_t)tr.expert * (a.n / 128) + nb) * num_kb + kb_lo;
       // fp32 accumulators as packed pairs (fma.rn.f32x2: two round-to-nearest
@@ -361,20 +377,23 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       // it in; indices advance by one chunk per iteration
       const int64_t sx_step = row_ok ? (int64_t)a.rows : 0;
       const int64_t sx_idx = row_ok ? (int64_t)kb_lo * a.rows + grow : 0;  // sx[kb][grow]
-      float sx0 = ld_scale(a.sx, sx_idx, row_ok && nloc > 0);
-      float sw0 = ld_scale(a.sw, sw_base, nloc > 0);
-      float sx1 = ld_scale(a.sx, sx_idx + sx_step, row_ok && nloc > 1);
-      float sw1 = ld_scale(a.sw, sw_base + 1, nloc > 1);
+      uint32_t sx0 = ld_word(a.sx, sx_idx, row_ok && nloc > 0);
+      uint32_t sw0 = ld_word(a.sw, sw_base, nloc > 0);
+      uint32_t sx1 = ld_word(a.sx, sx_idx + sx_step, row_ok && nloc > 1);
+      uint32_t sw1 = ld_word(a.sw, sw_base + 1, nloc > 1);
+      int64_t sx_cur = sx_idx, sw_cur = sw_base;  // indices of the words in sx0 / sw0
       int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + 2;
       for (int it = 0; it < nloc; ++it, ++g) {
         const int buf = g % C::kAccBufs;
         const uint32_t bph = (g / C::kAccBufs) & 1;
-        const float f = sx0 * sw0;
+        const float f = row_ok ? scale_value<UE8M0>(sx0, sx_cur) * scale_value<UE8M0>(sw0, sw_cur) : 0.0f;
         sx0 = sx1;
         sw0 = sw1;
+        sx_cur += sx_step;
+        sw_cur += 1;
         const bool more = it + 2 < nloc;
-        sx1 = ld_scale(a.sx, sx_next, row_ok && more);
-        sw1 = ld_scale(a.sw, sw_next, more);
+        sx1 = ld_word(a.sx, sx_next, row_ok && more);
+        sw1 = ld_word(a.sw, sw_next, more);
         sx_next += sx_step;
         sw_next += 1;
         ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
@@ -383,7 +402,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         tc_fence_after();
         const uint64_t f2 = f32x2(f, f);
         const uint32_t taddr = t_lane + buf * BN;
-        if (C::kEarlyRelease) {
+        if (warp_idle) {
+          // every row of this warp is past the segment: nothing to fold
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+        } else if (C::kEarlyRelease) {
           // copy the whole slice out of TMEM, hand the buffer back, then fold
           uint64_t v[C::kCols / 2];
 #pragma unroll
@@ -587,20 +611,20 @@ struct KernelState {
   int8_t cluster_fits[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
 };
 
-template <int BN, bool UE8M0, bool SPLITK>
+template <int BN, int AROWS, bool UE8M0, bool SPLITK>
 KernelState& kernel_state(int dev) {
   static KernelState st[64];
   return st[dev];
 }
 
-template <int BN, bool UE8M0, bool SPLITK>
+template <int BN, int AROWS, bool UE8M0, bool SPLITK>
 fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_tiles_bound, int sms,
                     GemmArgs args, int splits, cudaStream_t stream) {
-  using C = Cfg<BN>;
-  auto kernel = gemm_blockscaled_kernel<BN, UE8M0, SPLITK>;
+  using C = Cfg<BN, AROWS>;
+  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, SPLITK>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
-  KernelState& ks = kernel_state<BN, UE8M0, SPLITK>(dev);
+  KernelState& ks = kernel_state<BN, AROWS, UE8M0, SPLITK>(dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!ks.ready) {
@@ -626,7 +650,7 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
   }
   if (SPLITK && splits == 1) return FP8RL_ERR_UNSUPPORTED;  // the caller launches the plain kernel
   CUtensorMap mx, mw;
-  if (!make_map(&mx, xq, args.k, args.rows, kBM)) return FP8RL_ERR_CUDA;
+  if (!make_map(&mx, xq, args.k, args.rows, AROWS)) return FP8RL_ERR_CUDA;
   if (!make_map(&mw, wq, args.k, (uint64_t)experts * args.n, BN)) return FP8RL_ERR_CUDA;
   args.splits = splits;
   // split-K: one CTA per (m-tile, n-tile, split); otherwise persistent CTAs,
@@ -704,19 +728,29 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   // an upper bound on the 128-row tiles (grouped: every expert may end in a partial tile)
   const int64_t mt_bound = d_offsets ? m_tiles + experts : m_tiles;
   const int sms = di.sms;
+  // decode-sized M: load only 32 activation rows per stage (deeper weight pipeline)
+  const bool short_a = !d_offsets && rows <= 32;
   if (splits > 1) {
     // split-K clusters use 128-wide tiles
-    const fp8rl_status st = ue ? launch<128, true, true>(xq, wq, experts, mt_bound, sms, args, splits, cs)
-                               : launch<128, false, true>(xq, wq, experts, mt_bound, sms, args, splits, cs);
+    fp8rl_status st;
+    if (short_a)
+      st = ue ? launch<128, 32, true, true>(xq, wq, experts, mt_bound, sms, args, splits, cs)
+              : launch<128, 32, false, true>(xq, wq, experts, mt_bound, sms, args, splits, cs);
+    else
+      st = ue ? launch<128, kBM, true, true>(xq, wq, experts, mt_bound, sms, args, splits, cs)
+              : launch<128, kBM, false, true>(xq, wq, experts, mt_bound, sms, args, splits, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
+  if (short_a)
+    return ue ? launch<128, 32, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+              : launch<128, 32, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
   if (bn == 256) {
-    const fp8rl_status st = ue ? launch<256, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-                               : launch<256, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+    const fp8rl_status st = ue ? launch<256, kBM, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                               : launch<256, kBM, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
-  return ue ? launch<128, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-            : launch<128, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+  return ue ? launch<128, kBM, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+            : launch<128, kBM, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
 }
 
 }  // namespace
