@@ -57,24 +57,30 @@ struct Cfg {
   static constexpr int kCols = 64;                      // accumulator columns per epilogue thread
   static constexpr int kEpiWarps = 4 * (BN / kCols);    // 4 TMEM lane quadrants x column slices
   static constexpr int kThreads = 128 + kEpiWarps * 32; // warpgroup 0: producer, MMA, two idle warps
-  static constexpr int kAccBufs = 512 / BN;             // fp32 accumulators in TMEM (all 512 columns)
-  static constexpr int kTmemCols = kAccBufs * BN;
+  // K chunks handed from the MMA issuer to the epilogue per synchronisation:
+  // a 128-wide tile's TMEM buffer holds two chunk partials side by side
+  static constexpr int kGroup = BN == 128 ? 2 : 1;
+  static constexpr int kAccBufs = 512 / (BN * kGroup);   // TMEM buffers (all 512 columns)
+  static constexpr int kTmemCols = kAccBufs * BN * kGroup;
   static constexpr int kABytes = AROWS * kBK;  // activation rows loaded per stage
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  // chunk-scale ring filled by the scale-loader warp: per K chunk the tile's
+  // 128 activation scales and its BN/128 weight scales, as fp32
+  static constexpr int kScaleSlots = 16;
+  static constexpr int kScaleSlotFloats = kBM + 4;
+  static constexpr int kBookBytes = 1024;  // barriers and small shared state
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4;
   static constexpr int kPartPitch = BN + 4;  // floats per row of a split-K partial tile
   static_assert(kBM * kPartPitch * 4 <= kStages * kStageBytes, "partial tile must fit over the stages");
+  static_assert((2 * kStages + 2 * kAccBufs + 2 * kScaleSlots + 1) * 8 + 16 <= kBookBytes, "bookkeeping");
   // register split for BN = 256 (640 threads launch with <= 96 each): the role
   // warpgroup gives registers back, the four epilogue warpgroups take them.
   // 128 * kRoleRegs + 512 * kEpiRegs must not exceed 640 * (registers at
   // launch); the host checks that before launching.
   static constexpr bool kSplitRegs = BN == 256;
-  // with registers to spare (BN = 128) the epilogue copies a chunk out of TMEM
-  // and releases the buffer before folding it in
-  static constexpr bool kEarlyRelease = BN == 128;
-  static constexpr int kRoleRegs = 32;
-  static constexpr int kEpiRegs = 112;
+  static constexpr int kRoleRegs = 56;
+  static constexpr int kEpiRegs = 104;
   static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
 };
 
@@ -194,9 +200,12 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + C::kAccBufs;
   uint64_t* drain = tempty + C::kAccBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sfull = drain + 1;                // scale slot filled (1 arrival: the loader)
+  uint64_t* sempty = sfull + C::kScaleSlots;  // scale slot read (one arrival per epilogue warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::kScaleSlots);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* shared_m_tiles = abort_flag + 1;
+  float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
@@ -224,6 +233,10 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       mbar_init(smem_u32(&tempty[b]), C::kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int q = 0; q < C::kScaleSlots; ++q) {
+      mbar_init(smem_u32(&sfull[q]), 1);
+      mbar_init(smem_u32(&sempty[q]), C::kEpiWarps);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -308,29 +321,36 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
         const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
-        uint32_t g = 0;  // chunks consumed (stage ring and TMEM ring position)
+        uint32_t g = 0;  // chunks consumed (stage ring position)
+        uint32_t c = 0;  // chunk groups handed to the epilogue (TMEM ring position)
         bool alive = true;
         for (int tt = 0; tt < my_tiles && alive; ++tt) {
-          for (int it = 0; it < nloc; ++it, ++g) {
-            const int s = g % C::kStages;
-            const uint32_t ph = (g / C::kStages) & 1;
-            const int buf = g % C::kAccBufs;
-            const uint32_t bph = (g / C::kAccBufs) & 1;
-            if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1)) ||
-                !mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
+          for (int it = 0; it < nloc && alive; it += C::kGroup, ++c) {
+            const int gsz = min(C::kGroup, nloc - it);
+            const int buf = c % C::kAccBufs;
+            const uint32_t bph = (c / C::kAccBufs) & 1;
+            if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
                                    !(a.wait_mode & 1))) {
               alive = false;
               break;
             }
-            tc_fence_after();
-            const uint32_t d = tmem + buf * BN;
-            const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+            for (int j = 0; j < gsz; ++j, ++g) {
+              const int s = g % C::kStages;
+              const uint32_t ph = (g / C::kStages) & 1;
+              if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
+                alive = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d = tmem + (buf * C::kGroup + j) * BN;
+              const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
 #pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k)
-              mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
-                       k > 0 ? 1u : 0u);
-            mma_commit(smem_u32(&empty[s]));
-            mma_commit(smem_u32(&tfull[buf]));
+              for (int k = 0; k < kBK / kUmmaK; ++k)
+                mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                         k > 0 ? 1u : 0u);
+              mma_commit(smem_u32(&empty[s]));
+            }
+            if (alive) mma_commit(smem_u32(&tfull[buf]));
           }
         }
         if (*abortv) {
@@ -340,6 +360,60 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
         }
       }
       __syncwarp();
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- scale loader
+      // Runs up to kScaleSlots K chunks ahead of the epilogue, so the latency
+      // of these small loads never paces the pipeline.  Lane l loads the
+      // activation scales of rows l, l+32, l+64, l+96 of the tile.
+      uint32_t gs = 0;
+      bool alive = true;
+      for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
+        int m_idx, n_tile;
+        tile_coords(t, m_idx, n_tile);
+        const TileRows tr = tile_rows(a, m_idx, lane);
+        const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
+        // batches of kLoadBatch chunks: all their loads first, then the stores
+        constexpr int kLoadBatch = 4;
+        for (int it0 = 0; it0 < nloc && alive; it0 += kLoadBatch) {
+          float v[kLoadBatch][4];
+          float w[kLoadBatch];
+#pragma unroll
+          for (int b = 0; b < kLoadBatch; ++b) {
+            const int kb = kb_lo + it0 + b;
+            const bool live = it0 + b < nloc;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int grow = tr.row0 + lane + 32 * j;
+              const int64_t i = (int64_t)kb * a.rows + grow;
+              v[b][j] = (live && grow < tr.seg_end)
+                            ? scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, i))), i)
+                            : 0.0f;
+            }
+            w[b] = 0.0f;
+            if (live && lane < BN / 128) {
+              const int64_t i = sw_row + (int64_t)lane * num_kb + kb;
+              w[b] = scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, i))), i);
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < kLoadBatch; ++b) {
+            if (it0 + b >= nloc) break;
+            const int q = gs % C::kScaleSlots;
+            const uint32_t ph = (gs / C::kScaleSlots) & 1;
+            const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ph ^ 1, abortv, a.err, a.timeout_ns,
+                                               !(a.wait_mode & 1));
+            alive = __all_sync(0xffffffffu, got);
+            if (!alive) break;
+            float* slot = scale_ring + q * C::kScaleSlotFloats;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) slot[lane + 32 * j] = v[b][j];
+            if (lane < BN / 128) slot[kBM + lane] = w[b];
+            __syncwarp();  // orders the lanes' stores before lane 0's release
+            if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
+            ++gs;
+          }
+        }
+      }
     }
   } else {
     if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
@@ -349,12 +423,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
     const int slice = ew >> 2;   // which kCols columns of the tile
     const int r = quad * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
-    // raw scale words are loaded ahead and decoded only when used, so that the
-    // load's latency stays hidden for both formats
-    auto ld_word = [&](const void* p, int64_t i, bool live) -> uint32_t {
-      return live ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(p, i))) : 0u;
-    };
-    uint32_t g = 0;  // chunks folded so far (TMEM ring position)
+    uint32_t g = 0;   // chunk groups folded so far (TMEM ring position)
+    uint32_t gs = 0;  // chunks whose scales were taken (scale ring position)
     bool ok = true;
     for (int t = first_tile; t < total_tiles && ok; t += tile_stride) {
       int m_idx, n_tile;
@@ -365,82 +435,68 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       const bool row_ok = grow < tr.seg_end;
       const bool warp_idle = AROWS < kBM && tr.row0 + quad * 32 >= tr.seg_end;  // warp-uniform
       const int nb = (n0 + slice * C::kCols) >> 7;
-      const int64_t sw_base = ((int64_t)tr.expert * (a.n / 128) + nb) * num_kb + kb_lo;
       // fp32 accumulators as packed pairs (fma.rn.f32x2: two round-to-nearest
       // FMAs per instruction, the same results as scalar FMAs)
       uint64_t acc[C::kCols / 2];
 #pragma unroll
       for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
-      // the chunk scales of this thread's row and column slice, loaded two K
-      // chunks ahead (about one L2 round trip) so that no global-memory latency
-      // sits between the tensor cores finishing a chunk and this thread folding
-      // it in; indices advance by one chunk per iteration
-      const int64_t sx_step = row_ok ? (int64_t)a.rows : 0;
-      const int64_t sx_idx = row_ok ? (int64_t)kb_lo * a.rows + grow : 0;  // sx[kb][grow]
-      uint32_t sx0 = ld_word(a.sx, sx_idx, row_ok && nloc > 0);
-      uint32_t sw0 = ld_word(a.sw, sw_base, nloc > 0);
-      uint32_t sx1 = ld_word(a.sx, sx_idx + sx_step, row_ok && nloc > 1);
-      uint32_t sw1 = ld_word(a.sw, sw_base + 1, nloc > 1);
-      int64_t sx_cur = sx_idx, sw_cur = sw_base;  // indices of the words in sx0 / sw0
-      int64_t sx_next = sx_idx + 2 * sx_step, sw_next = sw_base + 2;
-      for (int it = 0; it < nloc; ++it, ++g) {
+      const int sw_lane = nb - (n0 >> 7);  // which of the tile's weight scales
+      for (int it = 0; it < nloc; it += C::kGroup, ++g) {
+        const int gsz = min(C::kGroup, nloc - it);
         const int buf = g % C::kAccBufs;
         const uint32_t bph = (g / C::kAccBufs) & 1;
-        const float f = row_ok ? scale_value<UE8M0>(sx0, sx_cur) * scale_value<UE8M0>(sw0, sw_cur) : 0.0f;
-        sx0 = sx1;
-        sw0 = sw1;
-        sx_cur += sx_step;
-        sw_cur += 1;
-        const bool more = it + 2 < nloc;
-        sx1 = ld_word(a.sx, sx_next, row_ok && more);
-        sw1 = ld_word(a.sw, sw_next, more);
-        sx_next += sx_step;
-        sw_next += 1;
         ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t f2 = f32x2(f, f);
-        const uint32_t taddr = t_lane + buf * BN;
-        if (warp_idle) {
-          // every row of this warp is past the segment: nothing to fold
-          tc_fence_before();
+        for (int j = 0; j < gsz; ++j, ++gs) {
+          const int q = gs % C::kScaleSlots;
+          ok = mbar_wait_bounded(smem_u32(&sfull[q]), (gs / C::kScaleSlots) & 1, abortv, a.err, a.timeout_ns,
+                                 !(a.wait_mode & 2));
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const float* slot = scale_ring + q * C::kScaleSlotFloats;
+          const float f = slot[r] * slot[kBM + sw_lane];
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
-        } else if (C::kEarlyRelease) {
-          // copy the whole slice out of TMEM, hand the buffer back, then fold
-          uint64_t v[C::kCols / 2];
+          if (lane == 0) mbar_arrive(smem_u32(&sempty[q]));  // the values are in registers
+          if (warp_idle) continue;  // every row of this warp is past the segment
+          const uint64_t f2 = f32x2(f, f);
+          const uint32_t taddr = t_lane + (buf * C::kGroup + j) * BN;
 #pragma unroll
-          for (int c = 0; c < C::kCols / 32; ++c)
-            tmem_ld_32x32b_x32_pairs(taddr + c * 32, *reinterpret_cast<uint64_t(*)[16]>(&v[c * 16]));
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
-#pragma unroll
-          for (int j = 0; j < C::kCols / 2; ++j) acc[j] = fma_f32x2(v[j], f2, acc[j]);
-        } else {
-#pragma unroll
-          for (int c = 0; c < C::kCols / 32; ++c) {
+          for (int cc = 0; cc < C::kCols / 32; ++cc) {
             uint64_t v[16];
-            tmem_ld_32x32b_x32_pairs(taddr + c * 32, v);
+            tmem_ld_32x32b_x32_pairs(taddr + cc * 32, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fma_f32x2(v[j], f2, acc[c * 16 + j]);
+            for (int q = 0; q < 16; ++q) acc[cc * 16 + q] = fma_f32x2(v[q], f2, acc[cc * 16 + q]);
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
       }
       if (!SPLITK) {
         if (ok && row_ok && !*abortv) {
+          // the row segment leaves as full 32-byte sectors (one 256-bit store
+          // per 16 columns) when the output allows it
           uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
+          const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
 #pragma unroll
-          for (int j = 0; j < C::kCols / 8; ++j) {
-            float x[8];
+          for (int j = 0; j < C::kCols / 16; ++j) {
+            uint4 h[2];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) f32x2_unpack(acc[4 * j + h], x[2 * h], x[2 * h + 1]);
-            dst[j] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+            for (int e = 0; e < 2; ++e) {
+              float x[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) f32x2_unpack(acc[8 * j + 4 * e + q], x[2 * q], x[2 * q + 1]);
+              h[e] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                                 pack_bf16x2(x[6], x[7]));
+            }
+            if (wide) {
+              st_global_v8(dst + 2 * j, h[0], h[1]);
+            } else {
+              dst[2 * j] = h[0];
+              dst[2 * j + 1] = h[1];
+            }
           }
         }
       } else if (row_ok) {

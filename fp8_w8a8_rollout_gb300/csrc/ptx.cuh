@@ -51,6 +51,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase (returns at once either way)
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The same test, letting the hardware suspend the thread for up to hint_ns
 // while the phase is incomplete (it resumes as soon as the phase completes), so
 // that waiting warps neither spin nor load the shared-memory pipe.
@@ -72,13 +85,13 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
 // false when it gave up.  With suspend set, each try lets the hardware park
 // the thread for at most 20 us (it resumes when the phase completes), which
 // also bounds how late an abort or the limit is noticed; otherwise the thread
-// polls and checks the clock every 64 tries.
+// spins on the non-blocking test and checks the clock every 64 tries.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   uint32_t* err_word, uint64_t limit_ns, bool suspend = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (suspend ? mbar_try_wait_suspend(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
+    if (suspend ? mbar_try_wait_suspend(bar, parity, 20000u) : mbar_test_wait(bar, parity)) return true;
     if (suspend || (i & 63) == 0) {
       if (abort && *abort) return false;
       if (globaltimer() - t0 > limit_ns) {
@@ -266,6 +279,14 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+// ------------------------------------------------------------------ 256-bit store
+
+__device__ __forceinline__ void st_global_v8(void* p, uint4 lo, uint4 hi) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(lo.x), "r"(lo.y),
+               "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+               : "memory");
 }
 
 // ------------------------------------------------------------------ packed fp32
