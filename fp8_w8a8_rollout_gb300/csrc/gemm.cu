@@ -375,8 +375,10 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
         // batches of kLoadBatch chunks: all their loads first, then the stores
         constexpr int kLoadBatch = 4;
         for (int it0 = 0; it0 < nloc && alive; it0 += kLoadBatch) {
-          float v[kLoadBatch][4];
-          float w[kLoadBatch];
+          // raw words first (all loads of the batch in flight), decoded at the store
+          uint32_t v[kLoadBatch][4];
+          uint32_t w[kLoadBatch];
+          int64_t vi[kLoadBatch][4], wi[kLoadBatch];
 #pragma unroll
           for (int b = 0; b < kLoadBatch; ++b) {
             const int kb = kb_lo + it0 + b;
@@ -384,16 +386,14 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int grow = tr.row0 + lane + 32 * j;
-              const int64_t i = (int64_t)kb * a.rows + grow;
+              vi[b][j] = (int64_t)kb * a.rows + grow;
               v[b][j] = (live && grow < tr.seg_end)
-                            ? scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, i))), i)
-                            : 0.0f;
+                            ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, vi[b][j])))
+                            : 0u;
             }
-            w[b] = 0.0f;
-            if (live && lane < BN / 128) {
-              const int64_t i = sw_row + (int64_t)lane * num_kb + kb;
-              w[b] = scale_value<UE8M0>(__ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, i))), i);
-            }
+            wi[b] = sw_row + (int64_t)(lane < BN / 128 ? lane : 0) * num_kb + kb;
+            w[b] = (live && lane < BN / 128) ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, wi[b])))
+                                               : 0u;
           }
 #pragma unroll
           for (int b = 0; b < kLoadBatch; ++b) {
@@ -406,8 +406,9 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
             if (!alive) break;
             float* slot = scale_ring + q * C::kScaleSlotFloats;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) slot[lane + 32 * j] = v[b][j];
-            if (lane < BN / 128) slot[kBM + lane] = w[b];
+            for (int j = 0; j < 4; ++j)
+              slot[lane + 32 * j] = tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
+            if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
             __syncwarp();  // orders the lanes' stores before lane 0's release
             if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
             ++gs;
