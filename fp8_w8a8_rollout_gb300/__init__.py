@@ -269,10 +269,23 @@ class HostWeightSync:
     enqueues work on the caller's device."""
 
     def __init__(self, host_weights, host_codes, host_scales, fmt=SCALE_FP32, chunk_bytes=32 << 20,
-                 slots=3, device=None):
+                 slots=3, device=None, direct=False):
         device = torch.device(device or "cuda")
         self.fmt = fmt
         self.items = []
+        self.direct = direct
+        self.h2d_bytes = sum(w.numel() * 2 for w in host_weights)
+        self.d2h_bytes = sum(q.numel() + s.numel() * s.element_size() for q, s in zip(host_codes, host_scales))
+        if direct:
+            # the quantiser reads the pinned bf16 weights and writes the codes and
+            # scales in host memory itself (over the CPU-GPU link): one batched
+            # launch, no staging copies
+            for t in list(host_weights) + list(host_codes) + list(host_scales):
+                if not t.is_pinned():
+                    raise ValueError("direct mode needs pinned host tensors")
+            self.descs = weight_descs(list(zip(host_weights, host_codes, host_scales)))
+            self.count = len(host_weights)
+            return
         for w, q, s in zip(host_weights, host_codes, host_scales):
             n, k = w.shape
             rows = max(128, (chunk_bytes // (2 * k)) // 128 * 128)
@@ -290,11 +303,12 @@ class HostWeightSync:
         self.s_q = torch.cuda.Stream(device)
         self.s_out = torch.cuda.Stream(device)
         self.ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(slots)]
-        self.h2d_bytes = sum(w.numel() * 2 for w in host_weights)
-        self.d2h_bytes = sum(q.numel() + s.numel() * s.element_size() for q, s in zip(host_codes, host_scales))
 
     def run(self):
         """Enqueue one full weight sync; returns immediately (the caller syncs)."""
+        if self.direct:
+            fp8rl_quant_weight_blockwise_batched(self.descs, self.count, self.fmt)
+            return
         cur = torch.cuda.current_stream()
         for st in (self.s_in, self.s_q, self.s_out):
             st.wait_stream(cur)

@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
 constexpr int kActRows = 16;
 
 template <bool UE8M0>
-__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
+__global__ void __launch_bounds__(256, 4) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
                                                         int64_t k, int64_t ldx, uint8_t* __restrict__ q,
                                                         int64_t ldq, void* __restrict__ scale,
                                                         int32_t groups, int vec) {

@@ -206,3 +206,19 @@ def test_host_weight_sync_pipeline_bit_exact(fmt):
         qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(w), fmt)
         assert np.array_equal(q.numpy(), qo)
         assert np.array_equal(s.numpy().view(np.uint8), so.view(np.uint8))
+
+
+def test_host_weight_sync_direct_bit_exact():
+    """The quantiser reading pinned host weights and writing pinned host codes."""
+    shapes = [(384, 256), (200, 300)]
+    ws = [synth.weight_bf16(n, k, 7, "hostdirect", n, k) for n, k in shapes]
+    host_w = [w.pin_memory() for w in ws]
+    host_q = [torch.empty((n, k), dtype=torch.uint8, pin_memory=True) for n, k in shapes]
+    host_s = [torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=torch.float32, pin_memory=True)
+              for n, k in shapes]
+    hs = fp8rl.HostWeightSync(host_w, host_q, host_s, direct=True)
+    hs.run()
+    torch.cuda.synchronize()
+    for w, q, s in zip(ws, host_q, host_s):
+        qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(w))
+        assert np.array_equal(q.numpy(), qo) and np.array_equal(s.numpy(), so)
