@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
     ap.add_argument("--graph", action="store_true", help="with --case: also time replays of a CUDA graph")
+    ap.add_argument("--streamk", type=int, default=-1,
+                    help="with --case gemm: call the workspace entry point; 0 chooses, 1 never, 2 always stream-K")
+    ap.add_argument("--streamk-grid", type=int, default=0, help="with --streamk: stream-K CTA count (0: one per SM)")
     return ap.parse_args()
 
 
@@ -719,7 +722,13 @@ def main_case(args):
         x = synth.activation_bf16(m, k, 0, "case-x", device=dev)
         xq, sx = fp8rl.quant_act(x, fmt)
         y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        fn = lambda: fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, m, n, k, fmt)
+        if args.streamk >= 0:
+            fp8rl.fp8rl_debug_set(fp8rl.DEBUG_STREAMK, args.streamk)
+            fp8rl.fp8rl_debug_set(fp8rl.DEBUG_STREAMK_GRID, args.streamk_grid)
+            ws = fp8rl.gemm_workspace(dev)
+            fn = lambda: fp8rl.fp8rl_gemm_blockscaled_ws(xq, sx, wq, sw, y, m, n, k, fmt, ws, ws.numel())
+        else:
+            fn = lambda: fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, m, n, k, fmt)
         work = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k), 1.0, peaks["hbm_gbs"], fp8_peak)
     elif kind == "grouped":
         which = parts[1]
@@ -756,7 +765,7 @@ def main_case(args):
     ms = time_loop(torch, fn, max(1, args.steps), args.warmup)
     assert fp8rl.fp8rl_sync_status() == 0
     out = {"case": args.case, "ms": ms, "bn": args.bn or "auto", "wait_mode": args.wait_mode,
-           "l2_prefetch": args.l2_prefetch}
+           "l2_prefetch": args.l2_prefetch, "streamk": args.streamk}
     if args.graph:
         out["ms_graph"] = time_graph(torch, fn, max(10, args.steps))
     if "flops" in work:

@@ -25,6 +25,7 @@ __all__ = [
     "Fp8rlError", "SCALE_FP32", "SCALE_UE8M0", "load_library", "library_path",
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
+    "fp8rl_gemm_workspace_size", "fp8rl_gemm_blockscaled_ws", "gemm_workspace",
     "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
     "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm", "HostWeightSync",
 ]
@@ -77,6 +78,8 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_quant_weight_blockwise_batched": [ctypes.POINTER(WeightDesc), i32, st, vp],
             "fp8rl_quant_act_group": [vp, i64, i64, i64, vp, i64, vp, st, vp],
             "fp8rl_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
+            "fp8rl_gemm_workspace_size": [ctypes.POINTER(ctypes.c_size_t)],
+            "fp8rl_gemm_blockscaled_ws": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp, ctypes.c_size_t, vp],
             "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
             "fp8rl_e4m3_encode": [vp, i64, vp, vp],
             "fp8rl_debug_set": [i32, i64],
@@ -148,6 +151,20 @@ def fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt=SCALE_
         "fp8rl_gemm_blockscaled")
 
 
+def fp8rl_gemm_workspace_size() -> int:
+    n = ctypes.c_size_t(0)
+    _ok(load_library().fp8rl_gemm_workspace_size(ctypes.byref(n)), "fp8rl_gemm_workspace_size")
+    return int(n.value)
+
+
+def fp8rl_gemm_blockscaled_ws(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt, workspace,
+                              workspace_bytes, stream=None) -> None:
+    _ok(load_library().fp8rl_gemm_blockscaled_ws(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
+                                                 _p(y_bf16), m, n, k, fmt, _p(workspace),
+                                                 int(workspace_bytes), _stream(stream)),
+        "fp8rl_gemm_blockscaled_ws")
+
+
 def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k,
                                    y_bf16, fmt=SCALE_FP32, stream=None) -> None:
     _ok(load_library().fp8rl_grouped_gemm_blockscaled(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
@@ -161,6 +178,7 @@ def fp8rl_e4m3_encode(d_in, n, d_out, stream=None) -> None:
 
 
 DEBUG_RESET, DEBUG_GEMM_BN, DEBUG_FAULT_SKIP_KB, DEBUG_TIMEOUT_NS = 0, 1, 2, 3
+DEBUG_WAIT_MODE, DEBUG_L2_PREFETCH, DEBUG_SPLITS, DEBUG_STREAMK, DEBUG_STREAMK_GRID = 4, 5, 6, 7, 8
 
 
 def fp8rl_debug_set(key, value) -> None:
@@ -235,13 +253,26 @@ def quant_act(x: torch.Tensor, fmt=SCALE_FP32, stream=None):
     return q, s
 
 
-def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None):
-    """bf16 Y [m, n] = block-scaled X W^T."""
+def gemm_workspace(device=None) -> torch.Tensor:
+    """A zero-filled workspace for fp8rl_gemm_blockscaled_ws on `device`."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        nbytes = fp8rl_gemm_workspace_size()
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None, workspace=None):
+    """bf16 Y [m, n] = block-scaled X W^T.  With a workspace (gemm_workspace),
+    shapes that fill the SMs unevenly run the stream-K schedule."""
     m, k = xq.shape
     n = wq.shape[0]
     if out is None:
         out = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device)
-    fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, out, m, n, k, fmt, stream)
+    if workspace is None:
+        fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, out, m, n, k, fmt, stream)
+    else:
+        fp8rl_gemm_blockscaled_ws(xq, x_scale, wq, w_scale, out, m, n, k, fmt, workspace,
+                                  workspace.numel() * workspace.element_size(), stream)
     return out
 
 

@@ -33,6 +33,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -73,13 +74,13 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4;
   static constexpr int kPartPitch = BN + 4;  // floats per row of a split-K partial tile
   static_assert(kBM * kPartPitch * 4 <= kStages * kStageBytes, "partial tile must fit over the stages");
-  static_assert((2 * kStages + 2 * kAccBufs + 2 * kScaleSlots + 1) * 8 + 16 <= kBookBytes, "bookkeeping");
+  static_assert((2 * kStages + 2 * kAccBufs + 2 * kScaleSlots + 2) * 8 + 16 <= kBookBytes, "bookkeeping");
   // register split for BN = 256 (640 threads launch with <= 96 each): the role
   // warpgroup gives registers back, the four epilogue warpgroups take them.
   // 128 * kRoleRegs + 512 * kEpiRegs must not exceed 640 * (registers at
   // launch); the host checks that before launching.
   static constexpr bool kSplitRegs = BN == 256;
-  static constexpr int kRoleRegs = 56;
+  static constexpr int kRoleRegs = 64;
   static constexpr int kEpiRegs = 104;
   static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
 };
@@ -96,7 +97,93 @@ struct GemmArgs {
   int32_t wait_mode;         // bit 0: producer and MMA threads poll; bit 1: epilogue polls
   int32_t l2_prefetch;       // K chunks ahead of the shared-memory loads that are prefetched into L2
   int32_t splits;            // K splits; > 1 only for a launch in clusters of `splits` CTAs along z
+  // stream-K (cooperative launch): partial tiles meet in a caller-provided workspace
+  uint32_t* ws_head;         // [0] epoch of the last completed launch, [1] CTAs finished in this launch
+  uint32_t* ws_flag;         // [gridDim.x] slot of CTA b holds this launch's partial: == epoch + 1
+  // [gridDim.x][BN / 4][32] float4: one 128 x BN fp32 partial tile per CTA,
+  // stored as each epilogue thread holds it (warp, 4-column step, lane), so
+  // that every warp-wide access is 512 contiguous bytes
+  float* ws_part;
 };
+
+// The (tile, first K chunk, end K chunk) segments one CTA works through, in
+// order.  Data-parallel: whole tiles blockIdx.x, +gridDim.x, ...  Stream-K: the
+// CTA's share of all tiles' K iterations, which may begin inside one tile and
+// end inside another.  Split-K cluster: one segment of the CTA's own tile.
+// kernel schedules
+constexpr int kDataParallel = 0;  // persistent CTAs stride over whole tiles
+constexpr int kSplitK = 1;        // one tile per cluster, its K chunks split over the cluster's CTAs
+constexpr int kStreamK = 2;       // the K iterations of all tiles divided evenly over the CTAs
+
+template <int MODE>
+struct Schedule {
+  // data-parallel (and the first part of stream-K): u = next whole tile, below
+  // dp_tiles.  Stream-K: then the CTA's share [v, v_end) of the K iterations of
+  // the remaining tiles.  Split-K cluster: the CTA's K chunks [u, v_end), once.
+  // (The host keeps gridDim.x x the stream-K iteration count below 2^31.)
+  int u, dp_tiles, num_kb;
+  int v, v_end;
+  __device__ __forceinline__ bool next(int& t, int& lo, int& hi) {
+    if (MODE == kSplitK) {
+      if (u > (int)v_end) return false;
+      t = 0;
+      lo = u;
+      hi = (int)v_end;
+      u = (int)v_end + 1;
+      return true;
+    }
+    if (u < dp_tiles) {
+      t = u;
+      u += gridDim.x;
+      lo = 0;
+      hi = num_kb;
+      return true;
+    }
+    if (MODE != kStreamK || v >= v_end) return false;
+    const int r = v / num_kb;
+    t = dp_tiles + r;
+    lo = v - r * num_kb;
+    hi = min(num_kb, lo + (v_end - v));
+    v += hi - lo;
+    return true;
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Stream-K tile owner, for one thread's n4 x 4 columns: `srow` (shared
+// memory) holds this CTA's partial; the same values of the partial tile of
+// every CTA after this one whose K range starts inside the tile (the tile's
+// iterations end at tile_end) are added in CTA order, each once its flag shows
+// this launch's epoch.  part0: the thread's first float4 in slot 0; the next
+// steps follow 32 float4 apart.  Warp-collective.  Kept out of line so that
+// its registers are not added to the epilogue's.
+__device__ __noinline__ bool streamk_fold(float4* srow, const float* part0, int64_t slot_floats,
+                                          const uint32_t* flags, uint32_t epoch, uint32_t tile_end, uint32_t iters,
+                                          int n4, bool row_ok, volatile int* abortv, uint32_t* err,
+                                          uint64_t timeout_ns) {
+  for (uint32_t q = blockIdx.x + 1; q < gridDim.x && q * iters / gridDim.x < tile_end; ++q) {
+    bool ok = flag_wait_bounded(flags + q, epoch, abortv, err, timeout_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    if (!row_ok) continue;
+    const float* part = part0 + (int64_t)q * slot_floats;
+#pragma unroll 8
+    for (int j = 0; j < n4; ++j) {
+      const float4 v = ld_cg_f32x4(part + 128 * j);
+      float4 w = srow[j];
+      w.x += v.x;
+      w.y += v.y;
+      w.z += v.z;
+      w.w += v.w;
+      srow[j] = w;
+    }
+  }
+  return true;
+}
 
 // Scales are fetched as the aligned 32-bit word that holds them (a UE8M0 byte
 // sits inside its word; the word never crosses the end of the allocation's
@@ -107,8 +194,10 @@ __device__ __forceinline__ const void* scale_word(const void* p, int64_t idx) {
   return static_cast<const float*>(p) + idx;
 }
 
+// idx: the scale's element index, or only its low 32 bits (the byte position
+// within the word is idx mod 4)
 template <bool UE8M0>
-__device__ __forceinline__ float scale_value(uint32_t word, int64_t idx) {
+__device__ __forceinline__ float scale_value(uint32_t word, uint32_t idx) {
   if (UE8M0) {
     const uint32_t b = (word >> (8 * (idx & 3))) & 0xFFu;
     return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
@@ -116,10 +205,6 @@ __device__ __forceinline__ float scale_value(uint32_t word, int64_t idx) {
   return __uint_as_float(word);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // Rows of the m-tile with index m_idx: (expert, first row, end of the expert's
 // segment).  Dense: one segment [0, rows).  Grouped: a running prefix over the
@@ -184,11 +269,13 @@ __device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
 // stage holds just AROWS activation rows; the M = 128 MMA reads the rest of
 // its A rows from whatever shared memory follows, which only feeds accumulator
 // rows >= AROWS that are never stored.
-template <int BN, int AROWS, bool UE8M0, bool SPLITK>
+template <int BN, int AROWS, bool UE8M0, int MODE>
 __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
                             const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
   using C = Cfg<BN, AROWS>;
+  constexpr bool SPLITK = MODE == kSplitK;
+  constexpr bool STREAMK = MODE == kStreamK;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -202,9 +289,11 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
   uint64_t* drain = tempty + C::kAccBufs;
   uint64_t* sfull = drain + 1;                // scale slot filled (1 arrival: the loader)
   uint64_t* sempty = sfull + C::kScaleSlots;  // scale slot read (one arrival per epilogue warp)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::kScaleSlots);
+  uint64_t* published = sempty + C::kScaleSlots;  // stream-K partial stored (one arrival per epilogue warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(published + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* shared_m_tiles = abort_flag + 1;
+  uint32_t* shared_epoch = reinterpret_cast<uint32_t*>(shared_m_tiles + 1);
   float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -233,19 +322,58 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       mbar_init(smem_u32(&tempty[b]), C::kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(published), C::kEpiWarps);
     for (int q = 0; q < C::kScaleSlots; ++q) {
       mbar_init(smem_u32(&sfull[q]), 1);
       mbar_init(smem_u32(&sempty[q]), C::kEpiWarps);
     }
     *abort_flag = 0;
+    // stream-K flags of this launch carry the value epoch + 1; the epoch in the
+    // workspace header advances only after every CTA has read it (below)
+    if (STREAMK) *shared_epoch = ld_acquire_gpu(a.ws_head) + 1;
     fence_barrier_init();
   }
   __syncthreads();
   const int m_tiles = *shared_m_tiles;
   const int total_tiles = SPLITK ? 1 : m_tiles * n_tiles;
-  const int first_tile = SPLITK ? 0 : (int)blockIdx.x;
-  const int tile_stride = SPLITK ? 1 : (int)gridDim.x;
-  if (first_tile >= total_tiles) return;  // CTA-uniform: more CTAs than tiles
+  Schedule<MODE> sched0;
+  sched0.num_kb = num_kb;
+  // stream-K: whole waves of tiles first (data-parallel, in the same order as
+  // the data-parallel kernel); the last partial wave plus one full wave are
+  // divided by K iterations
+  int sk_tiles = 0;
+  if (STREAMK) {
+    const int rem = total_tiles % (int)gridDim.x;
+    sk_tiles = rem == 0 ? 0 : rem + (total_tiles >= (int)gridDim.x ? (int)gridDim.x : 0);
+  }
+  const int sk_iters = sk_tiles * num_kb;
+  if (SPLITK) {
+    sched0.u = kb_lo;
+    sched0.dp_tiles = 0;
+    sched0.v = kb_lo + nloc;
+    sched0.v_end = kb_lo + nloc;
+  } else {
+    sched0.u = blockIdx.x;
+    sched0.dp_tiles = total_tiles - sk_tiles;
+    sched0.v = STREAMK ? (int)(blockIdx.x * (uint32_t)sk_iters / gridDim.x) : 0;
+    sched0.v_end = STREAMK ? (int)((blockIdx.x + 1) * (uint32_t)sk_iters / gridDim.x) : 0;
+  }
+  // The last stream-K CTA to finish advances the workspace epoch: every CTA
+  // read the old one before it counted itself as finished.
+  auto streamk_finish = [&]() {
+    if (STREAMK && threadIdx.x == 0) {
+      const uint32_t before = atom_add_acq_rel_gpu(a.ws_head + 1, 1u);
+      if (before == gridDim.x - 1) {
+        a.ws_head[1] = 0;
+        st_release_gpu(a.ws_head, *shared_epoch);
+      }
+    }
+  };
+  // CTA-uniform: nothing to do (more CTAs than tiles or iterations)
+  if (!SPLITK && sched0.u >= sched0.dp_tiles && sched0.v >= sched0.v_end) {
+    streamk_finish();
+    return;
+  }
   auto tile_coords = [&](int t, int& m_idx, int& n_tile) {
     if (SPLITK) {
       m_idx = blockIdx.x;
@@ -281,14 +409,17 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       }
       uint32_t g = 0;  // chunks issued by this CTA so far (position in the stage ring)
       bool alive = true;
-      for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
+      Schedule<MODE> sch = sched0;
+      int t, lo, hi;
+      while (alive && sch.next(t, lo, hi)) {
         int m_idx, n_tile;
         tile_coords(t, m_idx, n_tile);
         const TileRows tr = tile_rows(a, m_idx, lane);
         if (lane == 0) {
           const int wrow0 = tr.expert * a.n + n_tile * BN;
-          for (int it = 0; it < nloc; ++it, ++g) {
-            const int kb = kb_lo + it;
+          const int nseg = hi - lo;
+          for (int it = 0; it < nseg; ++it, ++g) {
+            const int kb = lo + it;
             const int s = g % C::kStages;
             const uint32_t ph = (g / C::kStages) & 1;
             if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
@@ -296,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
               break;
             }
             if ((int)g == a.fault_skip_kb) continue;
-            if (a.l2_prefetch > 0 && it + a.l2_prefetch < nloc) {
+            if (a.l2_prefetch > 0 && it + a.l2_prefetch < nseg) {
               tma_prefetch_l2_2d(&tmap_x, (kb + a.l2_prefetch) * kBK, tr.row0);
               tma_prefetch_l2_2d(&tmap_w, (kb + a.l2_prefetch) * kBK, wrow0);
             }
@@ -320,13 +451,15 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-        const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
         uint32_t g = 0;  // chunks consumed (stage ring position)
         uint32_t c = 0;  // chunk groups handed to the epilogue (TMEM ring position)
         bool alive = true;
-        for (int tt = 0; tt < my_tiles && alive; ++tt) {
-          for (int it = 0; it < nloc && alive; it += C::kGroup, ++c) {
-            const int gsz = min(C::kGroup, nloc - it);
+        Schedule<MODE> sch = sched0;
+        int t, lo, hi;
+        while (alive && sch.next(t, lo, hi)) {
+          const int nseg = hi - lo;
+          for (int it = 0; it < nseg && alive; it += C::kGroup, ++c) {
+            const int gsz = min(C::kGroup, nseg - it);
             const int buf = c % C::kAccBufs;
             const uint32_t bph = (c / C::kAccBufs) & 1;
             if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
@@ -367,37 +500,46 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
       // activation scales of rows l, l+32, l+64, l+96 of the tile.
       uint32_t gs = 0;
       bool alive = true;
-      for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
+      Schedule<MODE> sch = sched0;
+      int t, lo, hi;
+      while (alive && sch.next(t, lo, hi)) {
         int m_idx, n_tile;
         tile_coords(t, m_idx, n_tile);
         const TileRows tr = tile_rows(a, m_idx, lane);
         const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
+        const int nseg = hi - lo;
         // batches of kLoadBatch chunks: all their loads first, then the stores
         constexpr int kLoadBatch = 4;
-        for (int it0 = 0; it0 < nloc && alive; it0 += kLoadBatch) {
+        for (int it0 = 0; it0 < nseg && alive; it0 += kLoadBatch) {
           // raw words first (all loads of the batch in flight), decoded at the store
           uint32_t v[kLoadBatch][4];
           uint32_t w[kLoadBatch];
-          int64_t vi[kLoadBatch][4], wi[kLoadBatch];
+          // low bits of the indices (byte position): kept from the load, or (in
+          // the stream-K kernel, which has fewer registers to spare) recomputed
+          constexpr bool kKeepIdx = MODE != kStreamK;
+          uint32_t vi[kLoadBatch][4], wi[kLoadBatch];
+          const int64_t wbase = sw_row + (int64_t)(lane < BN / 128 ? lane : 0) * num_kb;
 #pragma unroll
           for (int b = 0; b < kLoadBatch; ++b) {
-            const int kb = kb_lo + it0 + b;
-            const bool live = it0 + b < nloc;
+            const int kb = lo + it0 + b;
+            const bool live = it0 + b < nseg;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int grow = tr.row0 + lane + 32 * j;
-              vi[b][j] = (int64_t)kb * a.rows + grow;
+              const int64_t idx = (int64_t)kb * a.rows + grow;
+              vi[b][j] = (uint32_t)idx;
               v[b][j] = (live && grow < tr.seg_end)
-                            ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, vi[b][j])))
+                            ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, idx)))
                             : 0u;
             }
-            wi[b] = sw_row + (int64_t)(lane < BN / 128 ? lane : 0) * num_kb + kb;
-            w[b] = (live && lane < BN / 128) ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, wi[b])))
+            const int64_t widx = wbase + kb;
+            wi[b] = (uint32_t)widx;
+            w[b] = (live && lane < BN / 128) ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, widx)))
                                                : 0u;
           }
 #pragma unroll
           for (int b = 0; b < kLoadBatch; ++b) {
-            if (it0 + b >= nloc) break;
+            if (it0 + b >= nseg) break;
             const int q = gs % C::kScaleSlots;
             const uint32_t ph = (gs / C::kScaleSlots) & 1;
             const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ph ^ 1, abortv, a.err, a.timeout_ns,
@@ -405,16 +547,31 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
             alive = __all_sync(0xffffffffu, got);
             if (!alive) break;
             float* slot = scale_ring + q * C::kScaleSlotFloats;
+            const uint32_t kb = (uint32_t)(lo + it0 + b);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              slot[lane + 32 * j] = tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
-            if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
+            for (int j = 0; j < 4; ++j) {
+              const int grow = tr.row0 + lane + 32 * j;
+              const uint32_t idx = kKeepIdx ? vi[b][j] : kb * (uint32_t)a.rows + (uint32_t)grow;
+              slot[lane + 32 * j] = grow < tr.seg_end ? scale_value<UE8M0>(v[b][j], idx) : 0.0f;
+            }
+            const uint32_t widx = kKeepIdx ? wi[b] : (uint32_t)wbase + kb;
+            if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], widx);
             __syncwarp();  // orders the lanes' stores before lane 0's release
             if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
             ++gs;
           }
         }
       }
+    } else if (STREAMK && lane == 0) {
+      // ---------------------------------------------------------- publisher
+      // A CTA whose stream-K share starts inside a tile computes that tile's
+      // later K chunks first and publishes the partial: once every epilogue
+      // warp has stored its part, the flag of this CTA's slot is raised.  A
+      // warp that gave up never arrives; then nothing is published, and the
+      // tile's owner gives up as well.
+      if (sched0.v < sched0.v_end && sched0.v % num_kb != 0 &&
+          mbar_wait_bounded(smem_u32(published), 0, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2)) && !*abortv)
+        st_release_gpu(a.ws_flag + blockIdx.x, *shared_epoch);
     }
   } else {
     if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
@@ -427,7 +584,10 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
     uint32_t g = 0;   // chunk groups folded so far (TMEM ring position)
     uint32_t gs = 0;  // chunks whose scales were taken (scale ring position)
     bool ok = true;
-    for (int t = first_tile; t < total_tiles && ok; t += tile_stride) {
+    Schedule<MODE> sch = sched0;
+    int t, lo, hi;
+    while (ok && sch.next(t, lo, hi)) {
+      const int nseg = hi - lo;
       int m_idx, n_tile;
       tile_coords(t, m_idx, n_tile);
       const TileRows tr = tile_rows(a, m_idx, lane);
@@ -442,8 +602,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
       const int sw_lane = nb - (n0 >> 7);  // which of the tile's weight scales
-      for (int it = 0; it < nloc; it += C::kGroup, ++g) {
-        const int gsz = min(C::kGroup, nloc - it);
+      for (int it = 0; it < nseg; it += C::kGroup, ++g) {
+        const int gsz = min(C::kGroup, nseg - it);
         const int buf = g % C::kAccBufs;
         const uint32_t bph = (g / C::kAccBufs) & 1;
         ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
@@ -475,7 +635,67 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
       }
-      if (!SPLITK) {
+      bool store_y = !SPLITK;
+      if (STREAMK && !(lo == 0 && hi == num_kb)) {
+        if (lo > 0) {
+          // a later part of tile t (a CTA has at most one, in its first
+          // stream-K segment): publish the partial in this CTA's slot
+          store_y = false;
+          if (ok && row_ok) {
+            float4* slot = reinterpret_cast<float4*>(a.ws_part + (int64_t)blockIdx.x * kBM * BN) +
+                           ew * (C::kCols / 4) * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < C::kCols / 4; ++j) {
+              float4 v;
+              f32x2_unpack(acc[2 * j], v.x, v.y);
+              f32x2_unpack(acc[2 * j + 1], v.z, v.w);
+              slot[32 * j] = v;
+            }
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(published));  // warp 3 raises the flag
+        } else {
+          // the head of tile t, which is this CTA's last segment: every MMA has
+          // completed, so the operand stages are idle.  The accumulators wait
+          // there (padded rows, as for split-K) while the parts that the
+          // following CTAs published are added in CTA order; the sums leave
+          // from there.
+          store_y = false;
+          float4* srow = reinterpret_cast<float4*>(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch +
+                                                   slice * C::kCols);
+#pragma unroll
+          for (int j = 0; j < C::kCols / 4; ++j) {
+            float4 v;
+            f32x2_unpack(acc[2 * j], v.x, v.y);
+            f32x2_unpack(acc[2 * j + 1], v.z, v.w);
+            srow[j] = v;
+          }
+          const bool folded =
+              streamk_fold(srow, a.ws_part + (int64_t)(ew * (C::kCols / 4) * 32 + lane) * 4, (int64_t)kBM * BN, a.ws_flag,
+                           *shared_epoch, (uint32_t)((t - sch.dp_tiles + 1) * num_kb), (uint32_t)sk_iters,
+                           C::kCols / 4, ok && row_ok, abortv, a.err, a.timeout_ns);
+          if (folded && ok && row_ok && !*abortv) {
+            uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
+            const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
+#pragma unroll 1
+            for (int j = 0; j < C::kCols / 16; ++j) {
+              const float4 s0 = srow[4 * j], s1 = srow[4 * j + 1], s2 = srow[4 * j + 2], s3 = srow[4 * j + 3];
+              const uint4 h0 = make_uint4(pack_bf16x2(s0.x, s0.y), pack_bf16x2(s0.z, s0.w),
+                                          pack_bf16x2(s1.x, s1.y), pack_bf16x2(s1.z, s1.w));
+              const uint4 h1 = make_uint4(pack_bf16x2(s2.x, s2.y), pack_bf16x2(s2.z, s2.w),
+                                          pack_bf16x2(s3.x, s3.y), pack_bf16x2(s3.z, s3.w));
+              if (wide) {
+                st_global_v8(dst + 2 * j, h0, h1);
+              } else {
+                dst[2 * j] = h0;
+                dst[2 * j + 1] = h1;
+              }
+            }
+          }
+        }
+      }
+      if (store_y) {
         if (ok && row_ok && !*abortv) {
           // the row segment leaves as full 32-byte sectors (one 256-bit store
           // per 16 columns) when the output allows it
@@ -500,7 +720,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
             }
           }
         }
-      } else if (row_ok) {
+      } else if (SPLITK && row_ok) {
         // this split's fp32 partial tile, row-major with a 4-float pad per row,
         // over the operand stages (every MMA that read them has completed)
         float4* prow = reinterpret_cast<float4*>(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch +
@@ -551,6 +771,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  streamk_finish();
 }
 
 // ---------------------------------------------------------------- host side
@@ -577,6 +798,8 @@ struct Debug {
   int wait_mode = 0;              // which roles poll instead of suspending (bits: 1 producer/MMA, 2 epilogue)
   int l2_prefetch = 0;            // K chunks of L2 prefetch beyond the shared-memory ring
   int splits = 0;                 // 0: choose; 1..8: force the split-K cluster size
+  int streamk = 0;                // with a workspace: 0 choose, 1 never, 2 always (dense, M > 32)
+  int streamk_grid = 0;           // 0: one CTA per SM (at most one per K iteration); else this many
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -668,20 +891,35 @@ struct KernelState {
   int8_t cluster_fits[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
 };
 
-template <int BN, int AROWS, bool UE8M0, bool SPLITK>
+template <int BN, int AROWS, bool UE8M0, int MODE>
 KernelState& kernel_state(int dev) {
   static KernelState st[64];
   return st[dev];
 }
 
-template <int BN, int AROWS, bool UE8M0, bool SPLITK>
+// Stream-K workspace: a 256-byte header (epoch, finished-CTA count), one flag
+// word per CTA, then one 128 x 256 fp32 partial tile per CTA.
+struct StreamKLayout {
+  size_t flag_off, part_off, bytes;
+};
+
+StreamKLayout streamk_layout(int max_ctas) {
+  StreamKLayout l;
+  l.flag_off = 256;
+  l.part_off = l.flag_off + (((size_t)max_ctas * 4 + 255) / 256) * 256;
+  l.bytes = l.part_off + (size_t)max_ctas * kBM * 256 * 4;
+  return l;
+}
+
+template <int BN, int AROWS, bool UE8M0, int MODE>
 fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_tiles_bound, int sms,
-                    GemmArgs args, int splits, cudaStream_t stream) {
+                    GemmArgs args, int splits, cudaStream_t stream, int streamk_grid = 0) {
   using C = Cfg<BN, AROWS>;
-  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, SPLITK>;
+  constexpr bool SPLITK = MODE == kSplitK;
+  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
-  KernelState& ks = kernel_state<BN, AROWS, UE8M0, SPLITK>(dev);
+  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE>(dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!ks.ready) {
@@ -713,9 +951,30 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
   // split-K: one CTA per (m-tile, n-tile, split); otherwise persistent CTAs,
   // at most one per SM, striding over the tiles
   const int64_t tiles_bound = m_tiles_bound * (args.n / BN);
-  const dim3 grid = SPLITK ? dim3((unsigned)m_tiles_bound, (unsigned)(args.n / BN), (unsigned)splits)
-                           : dim3((unsigned)std::min<int64_t>(tiles_bound, sms), 1, 1);
-  if (!SPLITK) {
+  dim3 grid = SPLITK ? dim3((unsigned)m_tiles_bound, (unsigned)(args.n / BN), (unsigned)splits)
+                     : dim3((unsigned)std::min<int64_t>(tiles_bound, sms), 1, 1);
+  if (MODE == kStreamK) {
+    // stream-K: every CTA gets at least one K iteration (dense: the tile count
+    // is exact); the launch is cooperative because tile owners wait for the
+    // CTAs that hold the rest of their tiles
+    const int64_t iters = tiles_bound * (args.k / kBK);
+    const int want = streamk_grid > 0 ? streamk_grid : sms;
+    grid = dim3((unsigned)std::min<int64_t>(iters, std::min(want, sms)), 1, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, args) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8RL_ERR_CUDA;
+    }
+  } else if (!SPLITK) {
     kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, args);
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -737,7 +996,7 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
 
 fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void* w_scale,
                  const int32_t* d_offsets, int64_t experts, int64_t rows, int64_t n, int64_t k, void* y,
-                 fp8rl_scale_fmt fmt, void* stream) {
+                 fp8rl_scale_fmt fmt, void* stream, void* workspace = nullptr) {
   const DeviceInfo di = device_info();
   if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
   uint32_t* err = device_error_word();
@@ -762,11 +1021,14 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   args.wait_mode = dbg.wait_mode;
   args.l2_prefetch = dbg.l2_prefetch;
   const int64_t m_tiles = (rows + kBM - 1) / kBM;
+  // Tile width by estimated time: whole waves of tiles x the time of one tile.
+  // Measured on GB300 (K = 4096): a 128 x 256 tile takes ~1.35x as long as a
+  // 128 x 128 one (half the operand traffic per flop).
+  const int64_t sms64 = di.sms;
+  const int64_t cost128 = (m_tiles * (n / 128) + sms64 - 1) / sms64 * 100;
+  const int64_t cost256 = n % 256 ? INT64_MAX : (m_tiles * (n / 256) + sms64 - 1) / sms64 * 135;
   int bn = dbg.bn;
-  if (bn != 128 && bn != 256) {
-    // wide tiles when there are enough of them to fill every SM
-    bn = (n % 256 == 0 && m_tiles * (n / 256) >= 2 * (int64_t)di.sms) ? 256 : 128;
-  }
+  if (bn != 128 && bn != 256) bn = (d_offsets ? m_tiles * (n / 256) >= 2 * sms64 : cost256 <= cost128) ? 256 : 128;
   if (bn == 256 && n % 256) bn = 128;
   // split K across a cluster when the tiles alone leave SMs idle (dense only):
   // decode-sized M streams the weights through every SM
@@ -787,27 +1049,53 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   const int sms = di.sms;
   // decode-sized M: load only 32 activation rows per stage (deeper weight pipeline)
   const bool short_a = !d_offsets && rows <= 32;
+  if (workspace && !d_offsets && !short_a && dbg.streamk != 1) {
+    // stream-K when whole tiles would leave the last wave of SMs mostly idle
+    // (measured on GB300: it pays when that wave is at most ~30% full, between
+    // one and eight waves; with less than one wave, whole tiles are faster)
+    const int sbn = (dbg.bn == 128 || n % 256) ? 128 : 256;
+    const int64_t tiles = m_tiles * (n / sbn);
+    const bool uneven = splits == 1 && tiles > sms64 && tiles < 8 * sms64 && (tiles % sms64) * 10 <= 3 * sms64;
+    // the kernel counts stream-K iterations (at most two waves of tiles) times
+    // the grid in 32 bits
+    const bool fits = 2 * (int64_t)sms * num_kb * sms < ((int64_t)1 << 31);
+    if (fits && (dbg.streamk == 2 || uneven)) {
+      const StreamKLayout l = streamk_layout(sms);
+      char* ws = static_cast<char*>(workspace);
+      args.ws_head = reinterpret_cast<uint32_t*>(ws);
+      args.ws_flag = reinterpret_cast<uint32_t*>(ws + l.flag_off);
+      args.ws_part = reinterpret_cast<float*>(ws + l.part_off);
+      fp8rl_status st;
+      if (sbn == 256) {
+        st = ue ? launch<256, kBM, true, kStreamK>(xq, wq, experts, mt_bound, sms, args, 1, cs, dbg.streamk_grid)
+                : launch<256, kBM, false, kStreamK>(xq, wq, experts, mt_bound, sms, args, 1, cs, dbg.streamk_grid);
+        if (st != FP8RL_ERR_UNSUPPORTED) return st;
+      }
+      return ue ? launch<128, kBM, true, kStreamK>(xq, wq, experts, mt_bound, sms, args, 1, cs, dbg.streamk_grid)
+                : launch<128, kBM, false, kStreamK>(xq, wq, experts, mt_bound, sms, args, 1, cs, dbg.streamk_grid);
+    }
+  }
   if (splits > 1) {
     // split-K clusters use 128-wide tiles
     fp8rl_status st;
     if (short_a)
-      st = ue ? launch<128, 32, true, true>(xq, wq, experts, mt_bound, sms, args, splits, cs)
-              : launch<128, 32, false, true>(xq, wq, experts, mt_bound, sms, args, splits, cs);
+      st = ue ? launch<128, 32, true, kSplitK>(xq, wq, experts, mt_bound, sms, args, splits, cs)
+              : launch<128, 32, false, kSplitK>(xq, wq, experts, mt_bound, sms, args, splits, cs);
     else
-      st = ue ? launch<128, kBM, true, true>(xq, wq, experts, mt_bound, sms, args, splits, cs)
-              : launch<128, kBM, false, true>(xq, wq, experts, mt_bound, sms, args, splits, cs);
+      st = ue ? launch<128, kBM, true, kSplitK>(xq, wq, experts, mt_bound, sms, args, splits, cs)
+              : launch<128, kBM, false, kSplitK>(xq, wq, experts, mt_bound, sms, args, splits, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
   if (short_a)
-    return ue ? launch<128, 32, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-              : launch<128, 32, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+    return ue ? launch<128, 32, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+              : launch<128, 32, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
   if (bn == 256) {
-    const fp8rl_status st = ue ? launch<256, kBM, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-                               : launch<256, kBM, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+    const fp8rl_status st = ue ? launch<256, kBM, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                               : launch<256, kBM, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
-  return ue ? launch<128, kBM, true, false>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-            : launch<128, kBM, false, false>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+  return ue ? launch<128, kBM, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+            : launch<128, kBM, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
 }
 
 }  // namespace
@@ -822,6 +1110,31 @@ extern "C" FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const v
   fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, m, n, k, fmt);
   if (st != FP8RL_OK || m == 0 || n == 0) return st;
   return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream);
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_gemm_workspace_size(size_t* bytes) {
+  if (!bytes) return FP8RL_ERR_INVALID_ARG;
+  *bytes = 0;
+  const DeviceInfo di = device_info();
+  if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
+  *bytes = streamk_layout(di.sms).bytes;
+  return FP8RL_OK;
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_gemm_blockscaled_ws(const void* xq, const void* x_scale,
+                                                            const void* wq, const void* w_scale, void* y,
+                                                            int64_t m, int64_t n, int64_t k,
+                                                            fp8rl_scale_fmt fmt, void* workspace,
+                                                            size_t workspace_bytes, void* stream) {
+  fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, m, n, k, fmt);
+  if (st != FP8RL_OK) return st;
+  if (!workspace) return FP8RL_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FP8RL_ERR_ALIGNMENT;
+  if (m == 0 || n == 0) return FP8RL_OK;
+  const DeviceInfo di = device_info();
+  if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
+  if (workspace_bytes < streamk_layout(di.sms).bytes) return FP8RL_ERR_INVALID_ARG;
+  return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream, workspace);
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_blockscaled(const void* xq, const void* x_scale,
@@ -862,6 +1175,14 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 6:
       if (value < 0 || value > 8) return FP8RL_ERR_INVALID_ARG;
       g_debug.splits = (int)value;
+      return FP8RL_OK;
+    case 7:
+      if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
+      g_debug.streamk = (int)value;
+      return FP8RL_OK;
+    case 8:
+      if (value < 0 || value > 1024) return FP8RL_ERR_INVALID_ARG;
+      g_debug.streamk_grid = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

@@ -289,6 +289,54 @@ __device__ __forceinline__ void st_global_v8(void* p, uint4 lo, uint4 hi) {
                : "memory");
 }
 
+// ------------------------------------------------------------------ inter-CTA flags
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// L2-coherent vector load (not through L1): data another CTA published
+__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Wait until *flag == value, for at most limit_ns (same abort and error-word
+// conventions as mbar_wait_bounded).
+__device__ __forceinline__ bool flag_wait_bounded(const uint32_t* flag, uint32_t value, volatile int* abort,
+                                                  uint32_t* err_word, uint64_t limit_ns) {
+  if (ld_acquire_gpu(flag) == value) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) == value) return true;
+    if ((i & 15) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        if (abort) *abort = 1;
+        if (err_word) atomicOr(err_word, 1u);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ packed fp32
 
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {

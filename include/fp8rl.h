@@ -45,6 +45,7 @@
 #ifndef FP8RL_H
 #define FP8RL_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -151,6 +152,43 @@ FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const void* x_scal
                                               void* stream);
 
 /*
+ * Bytes of workspace that fp8rl_gemm_blockscaled_ws needs on the current
+ * device (a 256-byte header, one flag word and one 128 x 256 fp32 tile per SM;
+ * about 20 MB on a 152-SM part).  The size does not depend on the shape.
+ * Errors: INVALID_ARG (null bytes), UNSUPPORTED (not an sm_103 device).
+ */
+FP8RL_API fp8rl_status fp8rl_gemm_workspace_size(size_t* bytes);
+
+/*
+ * fp8rl_gemm_blockscaled with a caller-provided workspace, which lets shapes
+ * whose 128-row tiles would fill the SMs unevenly (e.g. m = 1024) use a
+ * stream-K schedule: the K iterations of all tiles are divided evenly over one
+ * cooperative wave of CTAs; a CTA that computes the later K chunks of a tile
+ * publishes its fp32 partial tile in the workspace, and the CTA holding the
+ * tile's first chunks adds the published parts in CTA order and rounds to
+ * bf16 once.  The arithmetic per output element is that of
+ * fp8rl_gemm_blockscaled (same per-chunk products and scales) with the fp32
+ * chunk partial sums added in a different, fixed order; results are
+ * deterministic for a given shape and device.  Other shapes run exactly as in
+ * fp8rl_gemm_blockscaled and leave the workspace untouched.
+ *   workspace        device, 256-byte aligned, at least
+ *                    fp8rl_gemm_workspace_size bytes, owned by the caller.
+ *                    Zero-fill it once before its first use; the library
+ *                    keeps it consistent from then on (also after a TIMEOUT).
+ *                    Calls that may run at the same time (other streams or
+ *                    threads) need workspaces of their own.
+ *   workspace_bytes  its size
+ * Other arguments as fp8rl_gemm_blockscaled.
+ * Errors: as fp8rl_gemm_blockscaled; a null or short workspace is
+ *         INVALID_ARG, a misaligned one ALIGNMENT.
+ */
+FP8RL_API fp8rl_status fp8rl_gemm_blockscaled_ws(const void* xq, const void* x_scale, const void* wq,
+                                                 const void* w_scale, void* y_bf16, int64_t m,
+                                                 int64_t n, int64_t k, fp8rl_scale_fmt fmt,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 void* stream);
+
+/*
  * Grouped (MoE expert) block-scaled GEMM over row segments: for every expert e,
  * rows offsets[e] .. offsets[e+1]-1 of X are multiplied by expert e's weights
  * ("Method steps", step 1: MoE fc1 / fc2 are quantised; "MoE RL routing
@@ -207,6 +245,10 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          prefetches into L2 (0..64, default 0: measured slower on GB300);
  *   key 6  split-K cluster size of the dense GEMM: 0 chooses (default), 1..8
  *          forces it (reduced to what can be resident);
+ *   key 7  stream-K in fp8rl_gemm_blockscaled_ws: 0 chooses per shape
+ *          (default), 1 never, 2 always (m > 32);
+ *   key 8  stream-K CTA count: 0 one per SM (default), else min(value, SMs),
+ *          at most one per K iteration (1..1024);
  *   key 0  restore all defaults.
  * Errors: INVALID_ARG for an unknown key or value.
  */

@@ -110,6 +110,17 @@ def test_gemm_rejects_bad_shapes_and_alignment_on_host(lib):
     assert _rc(g, a16, a16, a16, a16, a16, 0, 256, 256, 0, None) == 0  # m == 0: no-op
 
 
+def test_workspace_gemm_rejects_bad_arguments_on_host(lib):
+    a16 = 1 << 20
+    g = "fp8rl_gemm_blockscaled_ws"
+    # a null or misaligned workspace, then the checks shared with the plain GEMM
+    assert _rc(g, a16, a16, a16, a16, a16, 16, 256, 256, 0, None, 1 << 30, None) == 1
+    assert _rc(g, a16, a16, a16, a16, a16, 16, 256, 256, 0, a16 + 16, 1 << 30, None) == 3
+    assert _rc(g, a16, a16, a16, a16, a16, 16, 200, 256, 0, a16, 1 << 30, None) == 2
+    assert _rc(g, a16, a16, a16, a16, a16, 0, 256, 256, 0, a16, 0, None) == 0  # m == 0: no-op
+    assert _rc("fp8rl_gemm_workspace_size", None) == 1
+
+
 def test_grouped_gemm_rejects_bad_arguments_on_host(lib):
     a16 = 1 << 20
     g = "fp8rl_grouped_gemm_blockscaled"
@@ -139,5 +150,9 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 99, 0) == 1
     assert _rc("fp8rl_debug_set", 6, 9) == 1
     assert _rc("fp8rl_debug_set", 6, 4) == 0
+    assert _rc("fp8rl_debug_set", 7, 3) == 1
+    assert _rc("fp8rl_debug_set", 8, 1025) == 1
+    assert _rc("fp8rl_debug_set", 7, 2) == 0
+    assert _rc("fp8rl_debug_set", 8, 7) == 0
     assert _rc("fp8rl_debug_set", 1, 256) == 0
     assert _rc("fp8rl_debug_set", 0, 0) == 0

@@ -101,3 +101,30 @@ def test_split_k_cluster_wait_runs_out_and_is_reported():
     got = y.float().cpu().numpy()
     rms = float(np.sqrt(np.mean(ref ** 2)))
     assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)
+
+
+def test_stream_k_owner_wait_runs_out_and_workspace_recovers():
+    """One tile of ten K chunks over three stream-K CTAs ([0,3) owner, [3,6),
+    [6,10)).  Only the last CTA has a fourth chunk, and it is the one skipped:
+    that CTA's MMA wait runs out and it publishes nothing, so the owner's wait
+    for its flag runs out as well.  The workspace needs no clean-up: the next
+    call with it is correct."""
+    m, n, k = 64, 256, 1280
+    xq, sx, wq, sw = operands(m, n, k, 5)
+    dx, dsx, dw, dsw = dev(xq, sx, wq, sw)
+    ws = fp8rl.gemm_workspace()
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_STREAMK, 2)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_STREAMK_GRID, 3)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, 256)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, 3)
+    fp8rl.gemm(dx, dsx, dw, dsw, workspace=ws)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, -1)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 2_000_000_000)
+    y = fp8rl.gemm(dx, dsx, dw, dsw, workspace=ws)
+    assert fp8rl.fp8rl_sync_status() == 0
+    ref = oracle.gemm_blockscaled(xq, sx, wq, sw)
+    got = y.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)

@@ -265,3 +265,86 @@ def test_split_k_is_deterministic(force_splits):
     y1 = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
     y2 = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
     assert np.array_equal(y1, y2)
+
+
+# --------------------------------------------------------------------------- stream-K (workspace)
+
+@pytest.fixture(scope="module")
+def workspace():
+    return fp8rl.gemm_workspace()
+
+
+@pytest.fixture
+def force_streamk():
+    def set_(grid, bn=0):
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_STREAMK, 2)
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_STREAMK_GRID, grid)
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, bn)
+    yield set_
+    for key in (fp8rl.DEBUG_STREAMK, fp8rl.DEBUG_STREAMK_GRID, fp8rl.DEBUG_GEMM_BN):
+        fp8rl.fp8rl_debug_set(key, 0)
+
+
+def run_gemm_ws(xq, sx, wq, sw, fmt, ws):
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    y = fp8rl.gemm(dx, dsx, dw, dsw, fmt, workspace=ws)
+    assert fp8rl.fp8rl_sync_status() == 0
+    return y.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("m,n,k,grid", [
+    (33, 256, 1280, 4),     # one tile of 10 K chunks over 4 CTAs: two CTAs hold only inner chunks
+    (129, 256, 1024, 3),    # two m-tiles, ranges crossing tile boundaries
+    (300, 512, 640, 7),     # ragged rows, 7 CTAs
+    (256, 256, 256, 16),    # fewer K iterations than CTAs asked for: one iteration per CTA
+    (1000, 768, 2048, 0),   # one CTA per SM
+    (128, 1024, 128, 5),    # a single K chunk per tile: no tile is ever split
+])
+def test_stream_k_forced(m, n, k, grid, bn, fmt, workspace, force_streamk):
+    if bn == 256 and n % 256:
+        pytest.skip("tile width 256 needs n % 256 == 0")
+    force_streamk(grid, bn)
+    x = synth.activation_bf16(m, k, 31, "streamk", m, n, k)
+    w = synth.weight_bf16(n, k, 32, "streamk", m, n, k)
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    within(run_gemm_ws(xq, sx, wq, sw, fmt, workspace), oracle.gemm_blockscaled(xq, sx, wq, sw, fmt))
+
+
+@pytest.mark.parametrize("name,n,k", synth.QWEN3_8B_GEMMS)
+def test_stream_k_qwen3_8b_m1024_sampled(name, n, k, workspace):
+    """At M = 1024 the workspace entry point chooses stream-K on its own where
+    whole tiles would leave the last wave nearly empty (qkv, gate-up) and whole
+    tiles elsewhere; 4 whole rows + 4096 random outputs."""
+    m = 1024
+    x = synth.activation_bf16(m, k, 12, "gemm-q", name, m)
+    w = synth.weight_bf16(n, k, 13, "gemm-q", name)
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    y = run_gemm_ws(xq, sx, wq, sw, fp8rl.SCALE_FP32, workspace)
+    rr, cc = sample_positions(m, n, 2, 4096, m + n)
+    within(y[rr, cc], oracle.gemm_blockscaled_at(xq, sx, wq, sw, rr, cc))
+
+
+def test_stream_k_repeated_calls_are_identical(workspace, force_streamk):
+    """Every call advances the workspace epoch; five calls in a row give the
+    same bits, and the same as a fresh workspace."""
+    force_streamk(9, 256)
+    x = synth.activation_bf16(200, 2048, 33, "streamk-det")
+    w = synth.weight_bf16(512, 2048, 34, "streamk-det")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    ys = [run_gemm_ws(xq, sx, wq, sw, fp8rl.SCALE_FP32, workspace) for _ in range(5)]
+    ys.append(run_gemm_ws(xq, sx, wq, sw, fp8rl.SCALE_FP32, fp8rl.gemm_workspace()))
+    for y in ys[1:]:
+        assert np.array_equal(ys[0], y)
+    within(ys[0], oracle.gemm_blockscaled(xq, sx, wq, sw))
+
+
+def test_stream_k_short_workspace_is_rejected(workspace):
+    xq = torch.zeros((64, 128), dtype=torch.uint8, device="cuda")
+    s = torch.ones((1, 64), dtype=torch.float32, device="cuda")
+    y = torch.empty((64, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fp8rl.Fp8rlError) as e:
+        fp8rl.fp8rl_gemm_blockscaled_ws(xq, s, xq, s, y, 64, 128, 128, fp8rl.SCALE_FP32, workspace,
+                                        workspace.numel() - 1)
+    assert e.value.status == 1

@@ -222,3 +222,54 @@ def test_host_weight_sync_direct_bit_exact():
     for w, q, s in zip(ws, host_q, host_s):
         qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(w))
         assert np.array_equal(q.numpy(), qo) and np.array_equal(s.numpy(), so)
+
+
+def _sampled_block_parity(ws, outs, fmt, samples, seed):
+    """Compare randomly chosen 128x128 blocks (and their scales) of device
+    results with the oracle run on just those blocks."""
+    rng = np.random.default_rng(seed)
+    for _ in range(samples):
+        i = int(rng.integers(len(ws)))
+        w = ws[i]
+        q, s = outs[i]
+        n, k = w.shape
+        nb = int(rng.integers((n + 127) // 128))
+        kb = int(rng.integers((k + 127) // 128))
+        blk = w[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
+        qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(blk), fmt)
+        assert np.array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128].cpu().numpy(), qo)
+        assert np.array_equal(s[nb:nb + 1, kb:kb + 1].cpu().numpy().view(np.uint8), so.view(np.uint8))
+
+
+@pytest.mark.slow
+def test_full_model_weight_sync_sampled():
+    """36 Qwen3-8B-shaped layers (252 matrices, 6.95e9 parameters) in the
+    single batched launch the benchmark times; 256 sampled blocks."""
+    dev = torch.device("cuda")
+    ws = []
+    for layer in range(synth.QWEN3_8B_LAYERS):
+        ws += [w for _, w in synth.qwen3_8b_layer(layer, 1000, device=dev)]
+    outs = fp8rl.quant_weights_batched(ws)
+    torch.cuda.synchronize()
+    _sampled_block_parity(ws, outs, fp8rl.SCALE_FP32, 256, 1)
+    del ws, outs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", FMTS)
+def test_moe_expert_weight_sync_sampled(fmt):
+    """48 layers x 128 experts x (gate-up, down) of a Qwen3-30B-A3B-shaped model
+    (2.9e10 parameters, 58 GB of bf16) in one batched launch; 256 sampled blocks."""
+    dev = torch.device("cuda")
+    ws = []
+    for layer in range(synth.MOE_LAYERS):
+        for which, n, k in (("gate_up", 2 * synth.MOE_INTER, synth.MOE_HIDDEN),
+                            ("down", synth.MOE_HIDDEN, synth.MOE_INTER)):
+            ws.append(synth.normal_bf16((synth.MOE_EXPERTS * n, k), synth.WEIGHT_STD, 1000, "moe-sync",
+                                        layer, which, device=dev))
+    outs = fp8rl.quant_weights_batched(ws, fmt)
+    torch.cuda.synchronize()
+    _sampled_block_parity(ws, outs, fmt, 256, 2)
+    del ws, outs
+    torch.cuda.empty_cache()
