@@ -26,6 +26,7 @@ __all__ = [
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
     "fp8rl_gemm_workspace_size", "fp8rl_gemm_blockscaled_ws", "gemm_workspace",
+    "fp8rl_gemm_blockscaled_static",
     "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
     "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm", "HostWeightSync",
 ]
@@ -80,6 +81,7 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
             "fp8rl_gemm_workspace_size": [ctypes.POINTER(ctypes.c_size_t)],
             "fp8rl_gemm_blockscaled_ws": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp, ctypes.c_size_t, vp],
+            "fp8rl_gemm_blockscaled_static": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
             "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
             "fp8rl_e4m3_encode": [vp, i64, vp, vp],
             "fp8rl_debug_set": [i32, i64],
@@ -163,6 +165,13 @@ def fp8rl_gemm_blockscaled_ws(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt, wo
                                                  _p(y_bf16), m, n, k, fmt, _p(workspace),
                                                  int(workspace_bytes), _stream(stream)),
         "fp8rl_gemm_blockscaled_ws")
+
+
+def fp8rl_gemm_blockscaled_static(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt=SCALE_FP32,
+                                  stream=None) -> None:
+    _ok(load_library().fp8rl_gemm_blockscaled_static(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
+                                                     _p(y_bf16), m, n, k, fmt, _stream(stream)),
+        "fp8rl_gemm_blockscaled_static")
 
 
 def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k,

@@ -41,6 +41,7 @@
 namespace fp8rl {
 
 uint32_t* device_error_word();  // api.cu
+void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* status);  // static_scratch.cu
 
 namespace {
 
@@ -1135,6 +1136,20 @@ extern "C" FP8RL_API fp8rl_status fp8rl_gemm_blockscaled_ws(const void* xq, cons
   if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
   if (workspace_bytes < streamk_layout(di.sms).bytes) return FP8RL_ERR_INVALID_ARG;
   return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream, workspace);
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_gemm_blockscaled_static(const void* xq, const void* x_scale,
+                                                                const void* wq, const void* w_scale, void* y,
+                                                                int64_t m, int64_t n, int64_t k,
+                                                                fp8rl_scale_fmt fmt, void* stream) {
+  fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, m, n, k, fmt);
+  if (st != FP8RL_OK || m == 0 || n == 0) return st;
+  const DeviceInfo di = device_info();
+  if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
+  const StreamKLayout l = streamk_layout(di.sms);
+  void* scratch = static_gemm_scratch(l.bytes, l.part_off, &st);
+  if (!scratch) return st;
+  return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream, scratch);
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_blockscaled(const void* xq, const void* x_scale,

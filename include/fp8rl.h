@@ -189,6 +189,34 @@ FP8RL_API fp8rl_status fp8rl_gemm_blockscaled_ws(const void* xq, const void* x_s
                                                  void* stream);
 
 /*
+ * fp8rl_gemm_blockscaled_ws without a caller workspace: the stream-K scratch
+ * is a fixed 24 MiB device array inside the library, so the call allocates
+ * nothing.  (No counterpart in the method's description: a convenience of
+ * this library.)  Meant for callers that cannot allocate device memory on
+ * their path: C code with no device allocator of its own, or loops where an
+ * allocation could synchronise the device or fail under memory pressure.
+ *   Set-up: the first call on each device, with that device current, looks
+ *   the array up and zeroes its header and flags (a synchronous memset and
+ *   device synchronisation); make that first call before any stream capture
+ *   begins.  Later calls only launch.
+ *   Capacity: the scratch the stream-K schedule needs (a 1 KB header and
+ *   flags, one 128 x 256 fp32 tile per SM: 19.9 MB on 152 SMs) must fit in
+ *   24 MiB; a device that needs more gets UNSUPPORTED and nothing runs.
+ *   Races: every call on a device shares the one array.  Calls that may run
+ *   at the same time (on different streams, or from different threads
+ *   without ordering) corrupt each other's partial tiles; issue them on one
+ *   stream, or give each concurrent caller its own workspace through
+ *   fp8rl_gemm_blockscaled_ws.
+ * Results are bit-identical to fp8rl_gemm_blockscaled_ws for the same
+ * arguments.  Arguments and errors as fp8rl_gemm_blockscaled; CUDA if the
+ * first-call set-up fails.
+ */
+FP8RL_API fp8rl_status fp8rl_gemm_blockscaled_static(const void* xq, const void* x_scale,
+                                                     const void* wq, const void* w_scale,
+                                                     void* y_bf16, int64_t m, int64_t n, int64_t k,
+                                                     fp8rl_scale_fmt fmt, void* stream);
+
+/*
  * Grouped (MoE expert) block-scaled GEMM over row segments: for every expert e,
  * rows offsets[e] .. offsets[e+1]-1 of X are multiplied by expert e's weights
  * ("Method steps", step 1: MoE fc1 / fc2 are quantised; "MoE RL routing
