@@ -70,6 +70,47 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
   return __fmaf_rn(-e, r, q0);
 }
 
+// ------------------------------------------------------------------ fp32 pairs
+// Two IEEE fp32 operations per instruction (mul/fma.rn.f32x2, no flush of
+// subnormals): the same results as the scalar operations on each half.
+
+__device__ __forceinline__ uint64_t pair_of(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pair_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pair_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// two E4M3 codes (low byte from the low half) of an fp32 pair
+__device__ __forceinline__ uint32_t e4m3x2_pair(uint64_t p) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+  return e4m3x2(lo, hi);
+}
+
+// div_by_scale on the two bf16 values of word w, as pairs.  Written from -x
+// (one XOR of the packed sign bits): q0 = (-x)(-r) = RN(x r), the remainder
+// q0 s + (-x) and q = q0 + e (-r) round exactly as the scalar form, signed
+// zeros included.
+__device__ __forceinline__ uint64_t div_by_scale_pair(uint32_t w, uint64_t s2, uint64_t nr2) {
+  const uint32_t nw = w ^ 0x80008000u;
+  const uint64_t nx = pair_of(bf16_lo(nw), bf16_hi(nw));
+  const uint64_t q0 = pair_mul(nx, nr2);
+  const uint64_t e = pair_fma(q0, s2, nx);
+  return pair_fma(e, nr2, q0);
+}
+
 // UE8M0 exponent: smallest e with 448 * 2^e >= amax, in [-127, 127]; zeros: 0.
 // Exact integer form: for a normal amax = (1 + m / 2^23) 2^(E - 127) and
 // 448 = 1.75 * 2^8, e = E - 135 when 1 + m / 2^23 <= 1.75 (m <= 0x600000),

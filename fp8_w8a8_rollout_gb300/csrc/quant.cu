@@ -50,6 +50,11 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+// a hint: fetch the line holding p into L2 (p must point into the tensor)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -62,10 +67,9 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
 __device__ __forceinline__ uint2 quant8_div(uint4 v, float s, float rcp) {
   uint2 r;
   if (s >= kFastDivMinScale) {
-    r.x = e4m3x2(div_by_scale(bf16_lo(v.x), s, rcp), div_by_scale(bf16_hi(v.x), s, rcp)) |
-          (e4m3x2(div_by_scale(bf16_lo(v.y), s, rcp), div_by_scale(bf16_hi(v.y), s, rcp)) << 16);
-    r.y = e4m3x2(div_by_scale(bf16_lo(v.z), s, rcp), div_by_scale(bf16_hi(v.z), s, rcp)) |
-          (e4m3x2(div_by_scale(bf16_lo(v.w), s, rcp), div_by_scale(bf16_hi(v.w), s, rcp)) << 16);
+    const uint64_t s2 = pair_of(s, s), nr2 = pair_of(-rcp, -rcp);
+    r.x = e4m3x2_pair(div_by_scale_pair(v.x, s2, nr2)) | (e4m3x2_pair(div_by_scale_pair(v.y, s2, nr2)) << 16);
+    r.y = e4m3x2_pair(div_by_scale_pair(v.z, s2, nr2)) | (e4m3x2_pair(div_by_scale_pair(v.w, s2, nr2)) << 16);
   } else {
     r.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
           (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
@@ -77,9 +81,11 @@ __device__ __forceinline__ uint2 quant8_div(uint4 v, float s, float rcp) {
 
 // the same with an exact power-of-two multiplier (UE8M0 variant)
 __device__ __forceinline__ uint2 quant8_mul(uint4 v, float f) {
+  const uint64_t f2 = pair_of(f, f);
+  auto one = [&](uint32_t w) { return e4m3x2_pair(pair_mul(pair_of(bf16_lo(w), bf16_hi(w)), f2)); };
   uint2 r;
-  r.x = e4m3x2(bf16_lo(v.x) * f, bf16_hi(v.x) * f) | (e4m3x2(bf16_lo(v.y) * f, bf16_hi(v.y) * f) << 16);
-  r.y = e4m3x2(bf16_lo(v.z) * f, bf16_hi(v.z) * f) | (e4m3x2(bf16_lo(v.w) * f, bf16_hi(v.w) * f) << 16);
+  r.x = one(v.x) | (one(v.y) << 16);
+  r.y = one(v.z) | (one(v.w) << 16);
   return r;
 }
 
@@ -196,16 +202,97 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
 
 // Four lanes quantise one 1x128 group (32 elements each, as four 16-byte
 // pieces interleaved so that the four lanes of a group read 64 contiguous
-// bytes per load).  A warp covers one K group g of 8 consecutive rows per
-// pass and takes kActRows = 16 rows (two passes) per task, so the per-group
-// work (max over 4 lanes, the scale, its reciprocal) is shared by 8 groups per
-// warp instruction, and the 8 scales of a pass land in one 32-byte run of the
-// [K/128][m] scale array.  Tasks are numbered g-major; the loop bound is
-// warp-uniform.
-constexpr int kActRows = 16;
+// bytes per load).  A warp task is one K group g of kActRows = 8 consecutive
+// rows, so the per-group work (max over 4 lanes, the scale, its reciprocal)
+// is shared by 8 groups per warp instruction, and the 8 scales land in one
+// 32-byte run of the [K/128][m] scale array.  Tasks are numbered g-major and
+// taken with a warp-uniform stride; each warp loads its next task before it
+// quantises the current one, so its loads stay in flight while it computes.
+constexpr int kActRows = 8;
+
+struct ActTask {
+  int32_t row;  // this lane's row
+  int64_t c0;   // first column of the group
+  bool live, full;
+};
+
+__device__ __forceinline__ ActTask act_task(int32_t t, int32_t rblocks, int32_t m, int64_t k, int vec, int sub) {
+  ActTask a;
+  const int32_t g = t / rblocks;
+  a.row = (t - g * rblocks) * kActRows + sub;
+  a.c0 = (int64_t)g * kBlock;
+  a.live = a.row < m;
+  a.full = vec && a.c0 + kBlock <= k;
+  return a;
+}
+
+__device__ __forceinline__ void act_load(const uint16_t* __restrict__ x, int64_t ldx, int64_t k, const ActTask& a,
+                                         int part, uint4 (&v)[4]) {
+  const uint16_t* src = x + (int64_t)a.row * ldx + a.c0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int piece = part + 4 * j;  // 8 elements each
+    if (a.live && a.full) {
+      v[j] = ld_stream(src + piece * 8);
+    } else if (a.live) {
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int64_t c = a.c0 + piece * 8 + e;
+        h[e] = c < k ? (uint32_t)src[piece * 8 + e] : 0u;
+      }
+      v[j] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    } else {
+      v[j] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
 
 template <bool UE8M0>
-__global__ void __launch_bounds__(256, 4) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
+__device__ __forceinline__ void act_quant_store(const uint4 (&v)[4], const ActTask& a, int32_t m, int64_t k,
+                                                uint8_t* __restrict__ q, int64_t ldq, void* __restrict__ scale,
+                                                int part) {
+  uint32_t acc = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc = absmax_u4(acc, v[j]);
+  uint32_t am = max(acc & 0xFFFFu, acc >> 16);
+  am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+  if (!a.live) return;
+  const float amax = __uint_as_float(am << 16);
+  const int64_t sidx = (a.c0 / kBlock) * m + a.row;
+  uint2 codes[4];
+  if (UE8M0) {
+    const int e = scale_ue8m0_exponent(amax);
+    const float f = exp2_neg(e);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) codes[j] = quant8_mul(v[j], f);
+    if (part == 0) static_cast<uint8_t*>(scale)[sidx] = (uint8_t)(e + 127);
+  } else {
+    const float s = scale_fp32(amax);
+    const float rcp = __frcp_rn(s);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) codes[j] = quant8_div(v[j], s, rcp);
+    if (part == 0) static_cast<float*>(scale)[sidx] = s;
+  }
+  uint8_t* dst = q + (int64_t)a.row * ldq + a.c0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int piece = part + 4 * j;
+    if (a.full) {
+      asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst + piece * 8), "r"(codes[j].x), "r"(codes[j].y)
+                   : "memory");
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (a.c0 + piece * 8 + e < k)
+          dst[piece * 8 + e] = (uint8_t)(((e < 4 ? codes[j].x : codes[j].y) >> (8 * (e & 3))) & 0xFFu);
+    }
+  }
+}
+
+template <bool UE8M0>
+__global__ void __launch_bounds__(256, 3) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
                                                         int64_t k, int64_t ldx, uint8_t* __restrict__ q,
                                                         int64_t ldq, void* __restrict__ scale,
                                                         int32_t groups, int vec) {
@@ -214,79 +301,24 @@ __global__ void __launch_bounds__(256, 4) quant_act_kernel(const uint16_t* __res
   const int32_t warp_count = gridDim.x * 8;
   const int32_t rblocks = (m + kActRows - 1) / kActRows;
   const int32_t tasks = rblocks * groups;  // the host keeps m * groups below 2^31
-  for (int32_t t = warp; t < tasks; t += warp_count) {
-    const int32_t g = t / rblocks;
-    const int32_t r0 = (t - g * rblocks) * kActRows;
-    const int64_t c0 = (int64_t)g * kBlock;
-    const bool full_group = vec && c0 + kBlock <= k;
-    uint4 v[2][4];
-    bool live[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int32_t row = r0 + u * 8 + sub;
-      live[u] = row < m;
-      const uint16_t* src = x + (int64_t)row * ldx + c0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int piece = part + 4 * j;  // 8 elements each
-        if (live[u] && full_group) {
-          v[u][j] = ld_stream(src + piece * 8);
-        } else if (live[u]) {
-          uint32_t h[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int64_t c = c0 + piece * 8 + e;
-            h[e] = c < k ? (uint32_t)src[piece * 8 + e] : 0u;
-          }
-          v[u][j] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                               h[6] | (h[7] << 16));
-        } else {
-          v[u][j] = make_uint4(0, 0, 0, 0);
-        }
-      }
+  if (warp >= tasks) return;
+  uint4 va[4], vb[4];
+  ActTask ta = act_task(warp, rblocks, m, k, vec, sub);
+  act_load(x, ldx, k, ta, part, va);
+  // two tasks per trip, so that the two register sets keep fixed names
+  for (int32_t t = warp; t < tasks; t += 2 * warp_count) {
+    const int32_t t1 = t + warp_count, t2 = t + 2 * warp_count;
+    ActTask tb;
+    if (t1 < tasks) {
+      tb = act_task(t1, rblocks, m, k, vec, sub);
+      act_load(x, ldx, k, tb, part, vb);
     }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int32_t row = r0 + u * 8 + sub;
-      uint32_t acc = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc = absmax_u4(acc, v[u][j]);
-      uint32_t am = max(acc & 0xFFFFu, acc >> 16);
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-      if (!live[u]) continue;
-      const float amax = __uint_as_float(am << 16);
-      const int64_t sidx = (int64_t)g * m + row;
-      uint2 codes[4];
-      if (UE8M0) {
-        const int e = scale_ue8m0_exponent(amax);
-        const float f = exp2_neg(e);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) codes[j] = quant8_mul(v[u][j], f);
-        if (part == 0) static_cast<uint8_t*>(scale)[sidx] = (uint8_t)(e + 127);
-      } else {
-        const float s = scale_fp32(amax);
-        const float rcp = __frcp_rn(s);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) codes[j] = quant8_div(v[u][j], s, rcp);
-        if (part == 0) static_cast<float*>(scale)[sidx] = s;
-      }
-      uint8_t* dst = q + (int64_t)row * ldq + c0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int piece = part + 4 * j;
-        if (full_group) {
-          asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst + piece * 8), "r"(codes[j].x),
-                       "r"(codes[j].y)
-                       : "memory");
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (c0 + piece * 8 + e < k)
-              dst[piece * 8 + e] = (uint8_t)(((e < 4 ? codes[j].x : codes[j].y) >> (8 * (e & 3))) & 0xFFu);
-        }
-      }
+    act_quant_store<UE8M0>(va, ta, m, k, q, ldq, scale, part);
+    if (t2 < tasks) {
+      ta = act_task(t2, rblocks, m, k, vec, sub);
+      act_load(x, ldx, k, ta, part, va);
     }
+    if (t1 < tasks) act_quant_store<UE8M0>(vb, tb, m, k, q, ldq, scale, part);
   }
 }
 
@@ -347,7 +379,10 @@ constexpr int kWeightCtasPerSm = 4;  // 256 threads each, about 64 registers
 template <int MAXD>
 fp8rl_status launch_weight(const WBatch<MAXD>& b, fp8rl_scale_fmt fmt, cudaStream_t stream) {
   if (b.total_blocks == 0) return FP8RL_OK;
-  const int64_t grid = std::min<int64_t>(b.total_blocks, (int64_t)sm_count() * kWeightCtasPerSm);
+  // the same whole number of blocks for every CTA (no partly idle last round)
+  const int64_t resident = (int64_t)sm_count() * kWeightCtasPerSm;
+  const int64_t per_cta = (b.total_blocks + resident - 1) / resident;
+  const int64_t grid = (b.total_blocks + per_cta - 1) / per_cta;
   if (fmt == FP8RL_SCALE_UE8M0)
     quant_weight_kernel<MAXD, true><<<(unsigned)grid, 256, 0, stream>>>(b);
   else
@@ -433,9 +468,13 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int6
   const int64_t tasks = m * groups;
   if (tasks > (int64_t)INT32_MAX - (1 << 20)) return FP8RL_ERR_SHAPE;  // 32-bit task numbering
   const int64_t warp_tasks = ((m + kActRows - 1) / kActRows) * groups;
-  const int64_t want = (warp_tasks + 7) / 8;
   const int occ = fmt == FP8RL_SCALE_UE8M0 ? ctas_per_sm(quant_act_kernel<true>) : ctas_per_sm(quant_act_kernel<false>);
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * occ));
+  // Every warp gets the same whole number of tasks (the last round of a
+  // striding loop is otherwise partly idle: 3.37 tasks per resident warp at
+  // 8192 x 4096 left a third of the warps working in the fourth round).
+  const int64_t resident_warps = (int64_t)sm_count() * occ * 8;
+  const int64_t per_warp = (warp_tasks + resident_warps - 1) / resident_warps;
+  const int64_t grid = std::max<int64_t>(1, (warp_tasks + 8 * per_warp - 1) / (8 * per_warp));
   const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (fmt == FP8RL_SCALE_UE8M0)
