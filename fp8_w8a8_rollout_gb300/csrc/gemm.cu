@@ -81,9 +81,12 @@ struct Cfg {
   // 128 * kRoleRegs + 512 * kEpiRegs must not exceed 640 * (registers at
   // launch); the host checks that before launching.
   static constexpr bool kSplitRegs = BN == 256;
-  static constexpr int kRoleRegs = 64;
+  static constexpr int kRoleRegs = 56;
+  static constexpr int kRoleRegsStreamK = 64;  // its schedule state needs a little more
   static constexpr int kEpiRegs = 104;
-  static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
+  static constexpr int kMinLaunchRegs =
+      (128 * (kRoleRegsStreamK > kRoleRegs ? kRoleRegsStreamK : kRoleRegs) + kEpiWarps * 32 * kEpiRegs + kThreads - 1) /
+      kThreads;
 };
 
 struct GemmArgs {
@@ -184,6 +187,26 @@ __device__ __noinline__ bool streamk_fold(float4* srow, const float* part0, int6
     }
   }
   return true;
+}
+
+// Calls fn(t, lo, nseg) for the segments of this CTA in order, while fn
+// returns true.  The data-parallel and split-K kernels keep a plain loop over
+// whole tiles (the role warps' loops are latency-critical: measured on GB300,
+// driving them through the general schedule cost the data-parallel kernel
+// ~4%); only the stream-K kernel walks the general schedule.
+template <int MODE, typename F>
+__device__ __forceinline__ void for_each_segment(const Schedule<MODE>& s0, int total_tiles, F&& fn) {
+  if constexpr (MODE == kStreamK) {
+    Schedule<MODE> s = s0;
+    int t, lo, hi;
+    while (s.next(t, lo, hi))
+      if (!fn(t, lo, hi - lo)) return;
+  } else if constexpr (MODE == kSplitK) {
+    fn(0, s0.u, s0.v_end - s0.u);
+  } else {
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x)
+      if (!fn(t, 0, s0.num_kb)) return;
+  }
 }
 
 // Scales are fetched as the aligned 32-bit word that holds them (a UE8M0 byte
@@ -401,178 +424,320 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
   volatile int* abortv = abort_flag;
 
   if (warp < 4) {
-    if (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRoleRegs));
-    if (warp == 0) {
-      // ---------------------------------------------------------- TMA producer
-      if (lane == 0) {
-        prefetch_tensormap(&tmap_x);
-        prefetch_tensormap(&tmap_w);
-      }
-      uint32_t g = 0;  // chunks issued by this CTA so far (position in the stage ring)
-      bool alive = true;
-      Schedule<MODE> sch = sched0;
-      int t, lo, hi;
-      while (alive && sch.next(t, lo, hi)) {
-        int m_idx, n_tile;
-        tile_coords(t, m_idx, n_tile);
-        const TileRows tr = tile_rows(a, m_idx, lane);
-        if (lane == 0) {
-          const int wrow0 = tr.expert * a.n + n_tile * BN;
-          const int nseg = hi - lo;
-          for (int it = 0; it < nseg; ++it, ++g) {
-            const int kb = lo + it;
-            const int s = g % C::kStages;
-            const uint32_t ph = (g / C::kStages) & 1;
-            if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
-              alive = false;
-              break;
+    if (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(STREAMK ? C::kRoleRegsStreamK : C::kRoleRegs));
+    if constexpr (!STREAMK) {
+      // Data-parallel and split-K: plain loops over whole tiles (or the
+      // cluster's one tile).  These loops are latency-critical; measured on
+      // GB300, driving them through the general segment schedule (below)
+      // cost the data-parallel kernel ~4% (fp32 scales) to ~9% (UE8M0).
+      const int first_tile = SPLITK ? 0 : (int)blockIdx.x;
+      const int tile_stride = SPLITK ? 1 : (int)gridDim.x;
+        if (warp == 0) {
+          // ---------------------------------------------------------- TMA producer
+          if (lane == 0) {
+            prefetch_tensormap(&tmap_x);
+            prefetch_tensormap(&tmap_w);
+          }
+          uint32_t g = 0;  // chunks issued by this CTA so far (position in the stage ring)
+          bool alive = true;
+          for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
+            int m_idx, n_tile;
+            tile_coords(t, m_idx, n_tile);
+            const TileRows tr = tile_rows(a, m_idx, lane);
+            if (lane == 0) {
+              const int wrow0 = tr.expert * a.n + n_tile * BN;
+              for (int it = 0; it < nloc; ++it, ++g) {
+                const int kb = kb_lo + it;
+                const int s = g % C::kStages;
+                const uint32_t ph = (g / C::kStages) & 1;
+                if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
+                  alive = false;
+                  break;
+                }
+                if ((int)g == a.fault_skip_kb) continue;
+                if (a.l2_prefetch > 0 && it + a.l2_prefetch < nloc) {
+                  tma_prefetch_l2_2d(&tmap_x, (kb + a.l2_prefetch) * kBK, tr.row0);
+                  tma_prefetch_l2_2d(&tmap_w, (kb + a.l2_prefetch) * kBK, wrow0);
+                }
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, C::kStageBytes);
+                tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, tr.row0, fb);
+                tma_load_2d(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
+              }
             }
-            if ((int)g == a.fault_skip_kb) continue;
-            if (a.l2_prefetch > 0 && it + a.l2_prefetch < nseg) {
-              tma_prefetch_l2_2d(&tmap_x, (kb + a.l2_prefetch) * kBK, tr.row0);
-              tma_prefetch_l2_2d(&tmap_w, (kb + a.l2_prefetch) * kBK, wrow0);
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+          }
+          if (lane == 0 && *abortv) {
+            // let the copies still in flight land before shared memory is released
+            for (uint32_t j = g > (uint32_t)C::kStages ? g - C::kStages : 0; j < g; ++j) {
+              if ((int)j == a.fault_skip_kb) continue;
+              mbar_wait_bounded(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1, nullptr, nullptr, 10000000ull);
             }
-            const uint32_t fb = smem_u32(&full[s]);
-            mbar_arrive_expect_tx(fb, C::kStageBytes);
-            tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, tr.row0, fb);
-            tma_load_2d(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
+          }
+          __syncwarp();
+        } else if (warp == 1) {
+          // ---------------------------------------------------------- MMA issuer
+          if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+            const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
+            uint32_t g = 0;  // chunks consumed (stage ring position)
+            uint32_t c = 0;  // chunk groups handed to the epilogue (TMEM ring position)
+            bool alive = true;
+            for (int tt = 0; tt < my_tiles && alive; ++tt) {
+              for (int it = 0; it < nloc && alive; it += C::kGroup, ++c) {
+                const int gsz = min(C::kGroup, nloc - it);
+                const int buf = c % C::kAccBufs;
+                const uint32_t bph = (c / C::kAccBufs) & 1;
+                if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
+                                       !(a.wait_mode & 1))) {
+                  alive = false;
+                  break;
+                }
+                for (int j = 0; j < gsz; ++j, ++g) {
+                  const int s = g % C::kStages;
+                  const uint32_t ph = (g / C::kStages) & 1;
+                  if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
+                    alive = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  const uint32_t d = tmem + (buf * C::kGroup + j) * BN;
+                  const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+    #pragma unroll
+                  for (int k = 0; k < kBK / kUmmaK; ++k)
+                    mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                             k > 0 ? 1u : 0u);
+                  mma_commit(smem_u32(&empty[s]));
+                }
+                if (alive) mma_commit(smem_u32(&tfull[buf]));
+              }
+            }
+            if (*abortv) {
+              // no MMA may still be writing TMEM when it is released
+              mma_commit(smem_u32(drain));
+              mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+            }
+          }
+          __syncwarp();
+        } else if (warp == 2) {
+          // ---------------------------------------------------------- scale loader
+          // Runs up to kScaleSlots K chunks ahead of the epilogue, so the latency
+          // of these small loads never paces the pipeline.  Lane l loads the
+          // activation scales of rows l, l+32, l+64, l+96 of the tile.
+          uint32_t gs = 0;
+          bool alive = true;
+          for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
+            int m_idx, n_tile;
+            tile_coords(t, m_idx, n_tile);
+            const TileRows tr = tile_rows(a, m_idx, lane);
+            const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
+            // batches of kLoadBatch chunks: all their loads first, then the stores
+            constexpr int kLoadBatch = 4;
+            for (int it0 = 0; it0 < nloc && alive; it0 += kLoadBatch) {
+              // raw words first (all loads of the batch in flight), decoded at the store
+              uint32_t v[kLoadBatch][4];
+              uint32_t w[kLoadBatch];
+              int64_t vi[kLoadBatch][4], wi[kLoadBatch];
+    #pragma unroll
+              for (int b = 0; b < kLoadBatch; ++b) {
+                const int kb = kb_lo + it0 + b;
+                const bool live = it0 + b < nloc;
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int grow = tr.row0 + lane + 32 * j;
+                  vi[b][j] = (int64_t)kb * a.rows + grow;
+                  v[b][j] = (live && grow < tr.seg_end)
+                                ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, vi[b][j])))
+                                : 0u;
+                }
+                wi[b] = sw_row + (int64_t)(lane < BN / 128 ? lane : 0) * num_kb + kb;
+                w[b] = (live && lane < BN / 128) ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, wi[b])))
+                                                   : 0u;
+              }
+    #pragma unroll
+              for (int b = 0; b < kLoadBatch; ++b) {
+                if (it0 + b >= nloc) break;
+                const int q = gs % C::kScaleSlots;
+                const uint32_t ph = (gs / C::kScaleSlots) & 1;
+                const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ph ^ 1, abortv, a.err, a.timeout_ns,
+                                                   !(a.wait_mode & 1));
+                alive = __all_sync(0xffffffffu, got);
+                if (!alive) break;
+                float* slot = scale_ring + q * C::kScaleSlotFloats;
+    #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  slot[lane + 32 * j] = tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
+                if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
+                __syncwarp();  // orders the lanes' stores before lane 0's release
+                if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
+                ++gs;
+              }
+            }
           }
         }
-        alive = __shfl_sync(0xffffffffu, alive, 0);
-      }
-      if (lane == 0 && *abortv) {
-        // let the copies still in flight land before shared memory is released
-        for (uint32_t j = g > (uint32_t)C::kStages ? g - C::kStages : 0; j < g; ++j) {
-          if ((int)j == a.fault_skip_kb) continue;
-          mbar_wait_bounded(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1, nullptr, nullptr, 10000000ull);
+    } else {
+      // stream-K: the CTA's segments, possibly starting and ending inside tiles
+      if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+          prefetch_tensormap(&tmap_x);
+          prefetch_tensormap(&tmap_w);
         }
-      }
-      __syncwarp();
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-        uint32_t g = 0;  // chunks consumed (stage ring position)
-        uint32_t c = 0;  // chunk groups handed to the epilogue (TMEM ring position)
+        uint32_t g = 0;  // chunks issued by this CTA so far (position in the stage ring)
         bool alive = true;
-        Schedule<MODE> sch = sched0;
-        int t, lo, hi;
-        while (alive && sch.next(t, lo, hi)) {
-          const int nseg = hi - lo;
-          for (int it = 0; it < nseg && alive; it += C::kGroup, ++c) {
-            const int gsz = min(C::kGroup, nseg - it);
-            const int buf = c % C::kAccBufs;
-            const uint32_t bph = (c / C::kAccBufs) & 1;
-            if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
-                                   !(a.wait_mode & 1))) {
-              alive = false;
-              break;
-            }
-            for (int j = 0; j < gsz; ++j, ++g) {
+        for_each_segment<MODE>(sched0, total_tiles, [&](int t, int lo, int nseg) {
+          int m_idx, n_tile;
+          tile_coords(t, m_idx, n_tile);
+          const TileRows tr = tile_rows(a, m_idx, lane);
+          if (lane == 0) {
+            const int wrow0 = tr.expert * a.n + n_tile * BN;
+            for (int it = 0; it < nseg; ++it, ++g) {
+              const int kb = lo + it;
               const int s = g % C::kStages;
               const uint32_t ph = (g / C::kStages) & 1;
-              if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
+              if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
                 alive = false;
                 break;
               }
-              tc_fence_after();
-              const uint32_t d = tmem + (buf * C::kGroup + j) * BN;
-              const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
-#pragma unroll
-              for (int k = 0; k < kBK / kUmmaK; ++k)
-                mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
-                         k > 0 ? 1u : 0u);
-              mma_commit(smem_u32(&empty[s]));
+              if ((int)g == a.fault_skip_kb) continue;
+              if (a.l2_prefetch > 0 && it + a.l2_prefetch < nseg) {
+                tma_prefetch_l2_2d(&tmap_x, (kb + a.l2_prefetch) * kBK, tr.row0);
+                tma_prefetch_l2_2d(&tmap_w, (kb + a.l2_prefetch) * kBK, wrow0);
+              }
+              const uint32_t fb = smem_u32(&full[s]);
+              mbar_arrive_expect_tx(fb, C::kStageBytes);
+              tma_load_2d(sA + s * C::kABytes, &tmap_x, kb * kBK, tr.row0, fb);
+              tma_load_2d(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
             }
-            if (alive) mma_commit(smem_u32(&tfull[buf]));
+          }
+          alive = __shfl_sync(0xffffffffu, alive, 0);
+          return alive;
+        });
+        if (lane == 0 && *abortv) {
+          // let the copies still in flight land before shared memory is released
+          for (uint32_t j = g > (uint32_t)C::kStages ? g - C::kStages : 0; j < g; ++j) {
+            if ((int)j == a.fault_skip_kb) continue;
+            mbar_wait_bounded(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1, nullptr, nullptr, 10000000ull);
           }
         }
-        if (*abortv) {
-          // no MMA may still be writing TMEM when it is released
-          mma_commit(smem_u32(drain));
-          mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+        __syncwarp();
+      } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+          constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+          uint32_t g = 0;  // chunks consumed (stage ring position)
+          uint32_t c = 0;  // chunk groups handed to the epilogue (TMEM ring position)
+          bool alive = true;
+          for_each_segment<MODE>(sched0, total_tiles, [&](int, int, int nseg) {
+            for (int it = 0; it < nseg && alive; it += C::kGroup, ++c) {
+              const int gsz = min(C::kGroup, nseg - it);
+              const int buf = c % C::kAccBufs;
+              const uint32_t bph = (c / C::kAccBufs) & 1;
+              if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
+                                     !(a.wait_mode & 1))) {
+                alive = false;
+                break;
+              }
+              for (int j = 0; j < gsz; ++j, ++g) {
+                const int s = g % C::kStages;
+                const uint32_t ph = (g / C::kStages) & 1;
+                if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 1))) {
+                  alive = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (buf * C::kGroup + j) * BN;
+                const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+  #pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k)
+                  mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                           k > 0 ? 1u : 0u);
+                mma_commit(smem_u32(&empty[s]));
+              }
+              if (alive) mma_commit(smem_u32(&tfull[buf]));
+            }
+            return alive;
+          });
+          if (*abortv) {
+            // no MMA may still be writing TMEM when it is released
+            mma_commit(smem_u32(drain));
+            mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+          }
         }
-      }
-      __syncwarp();
-    } else if (warp == 2) {
-      // ---------------------------------------------------------- scale loader
-      // Runs up to kScaleSlots K chunks ahead of the epilogue, so the latency
-      // of these small loads never paces the pipeline.  Lane l loads the
-      // activation scales of rows l, l+32, l+64, l+96 of the tile.
-      uint32_t gs = 0;
-      bool alive = true;
-      Schedule<MODE> sch = sched0;
-      int t, lo, hi;
-      while (alive && sch.next(t, lo, hi)) {
-        int m_idx, n_tile;
-        tile_coords(t, m_idx, n_tile);
-        const TileRows tr = tile_rows(a, m_idx, lane);
-        const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
-        const int nseg = hi - lo;
-        // batches of kLoadBatch chunks: all their loads first, then the stores
-        constexpr int kLoadBatch = 4;
-        for (int it0 = 0; it0 < nseg && alive; it0 += kLoadBatch) {
-          // raw words first (all loads of the batch in flight), decoded at the store
-          uint32_t v[kLoadBatch][4];
-          uint32_t w[kLoadBatch];
-          // low bits of the indices (byte position): kept from the load, or (in
-          // the stream-K kernel, which has fewer registers to spare) recomputed
-          constexpr bool kKeepIdx = MODE != kStreamK;
-          uint32_t vi[kLoadBatch][4], wi[kLoadBatch];
+        __syncwarp();
+      } else if (warp == 2) {
+        // ---------------------------------------------------------- scale loader
+        // Runs up to kScaleSlots K chunks ahead of the epilogue, so the latency
+        // of these small loads never paces the pipeline.  Lane l loads the
+        // activation scales of rows l, l+32, l+64, l+96 of the tile.
+        uint32_t gs = 0;
+        bool alive = true;
+        for_each_segment<MODE>(sched0, total_tiles, [&](int t, int lo, int nseg) {
+          int m_idx, n_tile;
+          tile_coords(t, m_idx, n_tile);
+          const TileRows tr = tile_rows(a, m_idx, lane);
+          const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
+          // batches of kLoadBatch chunks: all their loads first, then the stores
+          constexpr int kLoadBatch = 4;
+          // low bits of the scales' element indices (a UE8M0 scale's byte
+          // position within its word) are recomputed at the store: this kernel
+          // has fewer registers to spare
           const int64_t wbase = sw_row + (int64_t)(lane < BN / 128 ? lane : 0) * num_kb;
+          for (int it0 = 0; it0 < nseg && alive; it0 += kLoadBatch) {
+            // raw words first (all loads of the batch in flight), decoded at the store
+            uint32_t v[kLoadBatch][4];
+            uint32_t w[kLoadBatch];
 #pragma unroll
-          for (int b = 0; b < kLoadBatch; ++b) {
-            const int kb = lo + it0 + b;
-            const bool live = it0 + b < nseg;
+            for (int b = 0; b < kLoadBatch; ++b) {
+              const int kb = lo + it0 + b;
+              const bool live = it0 + b < nseg;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int grow = tr.row0 + lane + 32 * j;
-              const int64_t idx = (int64_t)kb * a.rows + grow;
-              vi[b][j] = (uint32_t)idx;
-              v[b][j] = (live && grow < tr.seg_end)
-                            ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, idx)))
-                            : 0u;
+              for (int j = 0; j < 4; ++j) {
+                const int grow = tr.row0 + lane + 32 * j;
+                v[b][j] = (live && grow < tr.seg_end)
+                              ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sx, (int64_t)kb * a.rows + grow)))
+                              : 0u;
+              }
+              w[b] = (live && lane < BN / 128)
+                         ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, wbase + kb)))
+                         : 0u;
             }
-            const int64_t widx = wbase + kb;
-            wi[b] = (uint32_t)widx;
-            w[b] = (live && lane < BN / 128) ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, widx)))
-                                               : 0u;
-          }
 #pragma unroll
-          for (int b = 0; b < kLoadBatch; ++b) {
-            if (it0 + b >= nseg) break;
-            const int q = gs % C::kScaleSlots;
-            const uint32_t ph = (gs / C::kScaleSlots) & 1;
-            const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ph ^ 1, abortv, a.err, a.timeout_ns,
-                                               !(a.wait_mode & 1));
-            alive = __all_sync(0xffffffffu, got);
-            if (!alive) break;
-            float* slot = scale_ring + q * C::kScaleSlotFloats;
-            const uint32_t kb = (uint32_t)(lo + it0 + b);
+            for (int b = 0; b < kLoadBatch; ++b) {
+              if (it0 + b >= nseg) break;
+              const int q = gs % C::kScaleSlots;
+              const uint32_t ph = (gs / C::kScaleSlots) & 1;
+              const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ph ^ 1, abortv, a.err, a.timeout_ns,
+                                                 !(a.wait_mode & 1));
+              alive = __all_sync(0xffffffffu, got);
+              if (!alive) break;
+              float* slot = scale_ring + q * C::kScaleSlotFloats;
+              const uint32_t kb = (uint32_t)(lo + it0 + b);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int grow = tr.row0 + lane + 32 * j;
-              const uint32_t idx = kKeepIdx ? vi[b][j] : kb * (uint32_t)a.rows + (uint32_t)grow;
-              slot[lane + 32 * j] = grow < tr.seg_end ? scale_value<UE8M0>(v[b][j], idx) : 0.0f;
+              for (int j = 0; j < 4; ++j) {
+                const int grow = tr.row0 + lane + 32 * j;
+                slot[lane + 32 * j] =
+                    grow < tr.seg_end ? scale_value<UE8M0>(v[b][j], kb * (uint32_t)a.rows + (uint32_t)grow) : 0.0f;
+              }
+              if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], (uint32_t)wbase + kb);
+              __syncwarp();  // orders the lanes' stores before lane 0's release
+              if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
+              ++gs;
             }
-            const uint32_t widx = kKeepIdx ? wi[b] : (uint32_t)wbase + kb;
-            if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], widx);
-            __syncwarp();  // orders the lanes' stores before lane 0's release
-            if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
-            ++gs;
           }
-        }
+          return alive;
+        });
+      } else if (STREAMK && lane == 0) {
+        // ---------------------------------------------------------- publisher
+        // A CTA whose stream-K share starts inside a tile computes that tile's
+        // later K chunks first and publishes the partial: once every epilogue
+        // warp has stored its part, the flag of this CTA's slot is raised.  A
+        // warp that gave up never arrives; then nothing is published, and the
+        // tile's owner gives up as well.
+        if (sched0.v < sched0.v_end && sched0.v % num_kb != 0 &&
+            mbar_wait_bounded(smem_u32(published), 0, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2)) && !*abortv)
+          st_release_gpu(a.ws_flag + blockIdx.x, *shared_epoch);
       }
-    } else if (STREAMK && lane == 0) {
-      // ---------------------------------------------------------- publisher
-      // A CTA whose stream-K share starts inside a tile computes that tile's
-      // later K chunks first and publishes the partial: once every epilogue
-      // warp has stored its part, the flag of this CTA's slot is raised.  A
-      // warp that gave up never arrives; then nothing is published, and the
-      // tile's owner gives up as well.
-      if (sched0.v < sched0.v_end && sched0.v % num_kb != 0 &&
-          mbar_wait_bounded(smem_u32(published), 0, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2)) && !*abortv)
-        st_release_gpu(a.ws_flag + blockIdx.x, *shared_epoch);
     }
   } else {
     if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
