@@ -64,6 +64,8 @@ def _load():
         lib.oracle_quant_weight_blockwise.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32]
         lib.oracle_quant_weight_blockwise.restype = i32
         lib.oracle_quant_act_group.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32]
+        lib.oracle_quant_group_f32.restype = i32
+        lib.oracle_quant_group_f32.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32]
         lib.oracle_quant_act_group.restype = i32
         lib.oracle_gemm_blockscaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32]
         lib.oracle_gemm_blockscaled.restype = i32
@@ -174,6 +176,64 @@ def quant_act_group(x_bf16_bits: np.ndarray, fmt: int = SCALE_FP32, threads: int
                                         threads or default_threads())
     _check(rc, "quant_act_group")
     return q, s
+
+
+def quant_group_f32(x_f32: np.ndarray, fmt: int = SCALE_FP32, threads: int | None = None):
+    """1x128 group quantisation of an fp32 matrix [m, k] (values never rounded
+    to bf16).  Returns (q uint8 [m,k], scale [ceil(k/128), m] fp32 or uint8)."""
+    x = _c(x_f32, np.float32)
+    m, k = x.shape
+    q = np.empty((m, k), dtype=np.uint8)
+    s = np.empty(((k + 127) // 128, m), dtype=_scale_dtype(fmt))
+    rc = _load().oracle_quant_group_f32(_ptr(x), m, k, k, _ptr(q), k, _ptr(s), fmt, threads or default_threads())
+    _check(rc, "quant_group_f32")
+    return q, s
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU (swish) in fp64: x * sigmoid(x) = x / (1 + exp(-x)).  The gated
+    MLP of the pages' Qwen3 models applies SiLU to the gate projection and
+    multiplies by the up projection (SwiGLU)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """SiLU(gate) * up, elementwise, in fp64."""
+    return silu(gate) * np.asarray(up, dtype=np.float64)
+
+
+def interleave_gate_up_rows(rows: int) -> np.ndarray:
+    """Row order of the fused gate-up weight that the fused kernel consumes:
+    128-row blocks alternate gate, up, gate, up ...; returns, for each row of
+    the interleaved matrix, its row in [gate; up] (rows = 2 * inter)."""
+    inter = rows // 2
+    idx = np.empty(rows, dtype=np.int64)
+    for b in range(inter // 128):
+        idx[256 * b:256 * b + 128] = np.arange(128 * b, 128 * b + 128)
+        idx[256 * b + 128:256 * b + 256] = inter + np.arange(128 * b, 128 * b + 128)
+    return idx
+
+
+def gemm_swiglu_quant(xq, sx, wq_il, sw_il, fmt_w: int = SCALE_FP32, fmt_h: int = SCALE_FP32,
+                      offsets=None, threads: int | None = None):
+    """Reference of the fused gate-up path: the block-scaled GEMM against the
+    interleaved gate-up weight (dense, or grouped by `offsets`), de-interleaved
+    into gate and up, h = SiLU(gate) * up in fp64, rounded once to fp32, then
+    quantised in 1x128 groups.  Returns (h fp64 [m, inter], hq, h_scale)."""
+    if offsets is None:
+        y = gemm_blockscaled(xq, sx, wq_il, sw_il, fmt_w, threads)
+    else:
+        y = grouped_gemm_blockscaled(xq, sx, wq_il, sw_il, offsets, fmt_w, threads)
+    rows = y.shape[1]
+    inter = rows // 2
+    order = interleave_gate_up_rows(rows)
+    plain = np.empty_like(y)
+    plain[:, order] = y          # column j of y is row order[j] of [gate; up]
+    h = swiglu(plain[:, :inter], plain[:, inter:])
+    hq, hs = quant_group_f32(h.astype(np.float32), fmt_h, threads)
+    return h, hq, hs
 
 
 # --------------------------------------------------------------------------- GEMMs

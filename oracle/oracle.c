@@ -39,6 +39,11 @@
  *      128 columns); scales are stored K-group-major: scale[g][m].
  *  R7  Ragged edges: amax is taken over the valid elements of a partial
  *      block or group only.
+ *  R8  Fused gate-up path (a "next" step: act-quant fused into the producing
+ *      GEMM): the SwiGLU output SiLU(gate) * up is kept in fp32 (never rounded
+ *      to bf16) and quantised in 1x128 groups by the same steps (R1-R6) as a
+ *      bf16 activation; "Where Rounding Happens Matters", "the overall
+ *      scheme".  The fp64 SiLU lives in the Python wrapper.
  *
  * Everything is computed the plain way: decode and encode by explicit search
  * over the format's code table, fp64 dot products for the GEMM, no blocking.
@@ -353,6 +358,85 @@ ORACLE_API int oracle_quant_act_group(const uint16_t* x, int64_t m, int64_t k, i
     c.fmt = fmt;
     c.groups = (k + 127) / 128;
     parallel_for(m, threads, aq_item, &c);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* fp32 activations: the same 1x128 group quantisation of values that were   */
+/* never rounded to bf16 (the fused gate-up -> SwiGLU -> quantise path keeps  */
+/* the SwiGLU output in fp32; "Where Rounding Happens Matters", "the overall  */
+/* scheme").  Steps as above: amax over the group in fp32, R1/R4/R5 scale,   */
+/* R3 fp32 quotient, R2 rounding.                                             */
+/* ------------------------------------------------------------------------ */
+
+static void quantize_group_f32(const float* x, int64_t cols, uint8_t* q, int fmt, float* scale_f32,
+                               uint8_t* scale_u8)
+{
+    float amax = 0.0f;
+    for (int64_t c = 0; c < cols; ++c) {
+        float a = fabsf(x[c]);
+        if (a > amax)
+            amax = a;
+    }
+    if (fmt == SCALE_UE8M0) {
+        int e = scale_ue8m0_exponent(amax);
+        *scale_u8 = (uint8_t)(e + 127);
+        for (int64_t c = 0; c < cols; ++c)
+            q[c] = encode_value(ldexp((double)x[c], -e));
+    } else {
+        float scale = scale_fp32(amax);
+        *scale_f32 = scale;
+        for (int64_t c = 0; c < cols; ++c) {
+            float quotient = x[c] / scale; /* R3 */
+            q[c] = encode_value((double)quotient);
+        }
+    }
+}
+
+typedef struct {
+    const float* x;
+    int64_t m, k, ldx;
+    uint8_t* q;
+    int64_t ldq;
+    void* scale;
+    int fmt;
+    int64_t groups;
+} aqf_ctx;
+
+static void aqf_item(void* p, int64_t row)
+{
+    aqf_ctx* c = (aqf_ctx*)p;
+    for (int64_t g = 0; g < c->groups; ++g) {
+        int64_t c0 = g * 128;
+        int64_t cols = c->k - c0 < 128 ? c->k - c0 : 128;
+        float sf = 0.0f;
+        uint8_t su = 0;
+        quantize_group_f32(c->x + row * c->ldx + c0, cols, c->q + row * c->ldq + c0, c->fmt, &sf, &su);
+        if (c->fmt == SCALE_UE8M0)
+            ((uint8_t*)c->scale)[g * c->m + row] = su;
+        else
+            ((float*)c->scale)[g * c->m + row] = sf;
+    }
+}
+
+/* X: fp32 [m][k] (row stride ldx).  Q: E4M3 [m][k] (row stride ldq).
+ * scale: [ceil(k/128)][m], fp32 or UE8M0 bytes (R6 layout). */
+ORACLE_API int oracle_quant_group_f32(const float* x, int64_t m, int64_t k, int64_t ldx, uint8_t* q,
+                                      int64_t ldq, void* scale, int fmt, int threads)
+{
+    aqf_ctx c;
+    if (m < 0 || k < 0 || ldx < k || ldq < k || (fmt != SCALE_FP32 && fmt != SCALE_UE8M0))
+        return 1;
+    c.x = x;
+    c.m = m;
+    c.k = k;
+    c.ldx = ldx;
+    c.q = q;
+    c.ldq = ldq;
+    c.scale = scale;
+    c.fmt = fmt;
+    c.groups = (k + 127) / 128;
+    parallel_for(m, threads, aqf_item, &c);
     return 0;
 }
 

@@ -456,3 +456,102 @@ def test_routing_replay_offsets_are_prefix_sums():
         toks = r.token_of_row[r.offsets[e]:r.offsets[e + 1]]
         assert np.all(np.diff(toks) > 0)
         assert all(e in r.topk[t] for t in toks)
+
+
+# --------------------------------------------------------------------------- fused gate-up path (fp32 groups, SwiGLU)
+
+def _fp32_groups(m, k, seed):
+    """fp32 values with a wide per-row range and non-bf16 mantissas."""
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(m, k)) * np.exp(rng.normal(size=(m, 1)) * 2.0)
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("m,k", [(4, 256), (3, 300), (2, 128), (1, 5)])
+def test_fp32_group_quant_is_rne_of_fp32_quotient(m, k):
+    """Codes = library RNE cast of the IEEE fp32 quotient x / s (R2, R3), with
+    s = amax / 448 of each 1x128 group computed in fp32 by the library."""
+    x = _fp32_groups(m, k, 11)
+    q, s = oracle.quant_group_f32(x)
+    groups = (k + 127) // 128
+    assert s.shape == (groups, m)
+    for g in range(groups):
+        blk = x[:, g * 128:(g + 1) * 128]
+        amax = np.abs(blk).max(axis=1).astype(np.float32)
+        assert np.array_equal(s[g], np.where(amax == 0, np.float32(1), amax / np.float32(448)))
+        quotient = (blk / s[g][:, None]).astype(np.float32)
+        lib = torch.from_numpy(quotient).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        assert np.array_equal(q[:, g * 128:(g + 1) * 128], lib.numpy())
+
+
+def test_fp32_group_quant_amax_maps_to_448_and_error_bound():
+    x = _fp32_groups(8, 384, 12)
+    q, s = oracle.quant_group_f32(x)
+    table = oracle.e4m3_decode_table()
+    srep = np.repeat(s.T.astype(np.float64), 128, axis=1)
+    for r in range(8):
+        for g in range(3):
+            c = int(np.argmax(np.abs(x[r, g * 128:(g + 1) * 128]))) + g * 128
+            assert q[r, c] & 0x7F == 0x7E  # the group maximum is exactly +-448
+    v = np.abs(x.astype(np.float64) / srep)
+    with np.errstate(divide="ignore"):
+        ulp = np.where(v < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(v, 1e-300))) - 3))
+    assert np.all(np.abs(table[q] * srep - x) <= 0.5 * ulp * srep + 2.0 ** -23 * np.abs(x))
+
+
+def test_fp32_group_quant_zero_group_and_ue8m0_bounds():
+    x = _fp32_groups(3, 256, 13)
+    x[1, 128:] = 0.0
+    q, s = oracle.quant_group_f32(x)
+    assert s[1, 1] == 1.0 and np.all(q[1, 128:] == 0)
+    qu, su = oracle.quant_group_f32(x, oracle.SCALE_UE8M0)
+    assert su[1, 1] == 127 and np.all(qu[1, 128:] == 0)
+    for r in (0, 2):
+        for g in range(2):
+            blk = x[r, g * 128:(g + 1) * 128].astype(np.float64)
+            sc = 2.0 ** (int(su[g, r]) - 127)
+            assert sc >= np.abs(blk).max() / 448 > sc / 2
+            assert np.array_equal(qu[r, g * 128:(g + 1) * 128], brute_force_encode(blk / sc))
+
+
+def test_silu_closed_forms():
+    x = np.linspace(-30.0, 30.0, 601)
+    # x sigmoid(x) - (-x) sigmoid(-x) = x (sigmoid(x) + sigmoid(-x) = 1)
+    assert np.allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=0, atol=1e-12)
+    assert oracle.silu(np.array([0.0]))[0] == 0.0
+    assert oracle.silu(np.array([1.0]))[0] == pytest.approx(math.e / (1.0 + math.e), rel=1e-15)
+    assert oracle.silu(np.array([60.0]))[0] == pytest.approx(60.0, rel=1e-15)
+    assert abs(oracle.silu(np.array([-800.0]))[0]) == 0.0
+    up = np.array([2.0, -3.0, 0.5])
+    gate = np.array([1.0, 0.0, -1.0])
+    assert np.allclose(oracle.swiglu(gate, up), up * gate / (1.0 + np.exp(-gate)), rtol=1e-15)
+
+
+def test_gate_up_interleave_is_a_row_permutation_in_128_blocks():
+    order = oracle.interleave_gate_up_rows(768)
+    assert sorted(order.tolist()) == list(range(768))
+    # blocks alternate: gate block b, then up block b
+    assert np.array_equal(order[:128], np.arange(128))
+    assert np.array_equal(order[128:256], 384 + np.arange(128))
+    assert np.array_equal(order[256:384], 128 + np.arange(128))
+    assert np.array_equal(order[640:768], 384 + 256 + np.arange(128))
+
+
+def test_fused_reference_equals_unfused_steps():
+    """gemm_swiglu_quant on the interleaved weight = the plain GEMM on [gate; up],
+    SiLU(gate) * up, fp32 rounding, group quantisation (each step by hand)."""
+    rng = np.random.default_rng(14)
+    m, k, inter = 40, 256, 256
+    x = torch.from_numpy(rng.normal(size=(m, k)).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy((rng.normal(size=(2 * inter, k)) * 0.05).astype(np.float32)).to(torch.bfloat16)
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
+    order = oracle.interleave_gate_up_rows(2 * inter)
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w[torch.from_numpy(order)]))
+    h, hq, hs = oracle.gemm_swiglu_quant(xq, sx, wq, sw)
+    wq_plain, sw_plain = oracle.quant_weight_blockwise(synth.bf16_bits(w))
+    y = oracle.gemm_blockscaled(xq, sx, wq_plain, sw_plain)
+    gate, up = y[:, :inter], y[:, inter:]
+    h_ref = gate / (1.0 + np.exp(-gate)) * up
+    assert np.allclose(h, h_ref, rtol=1e-14, atol=0)
+    hq_ref, hs_ref = oracle.quant_group_f32(h_ref.astype(np.float32))
+    assert np.array_equal(hq, hq_ref) and np.array_equal(hs, hs_ref)
