@@ -49,12 +49,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="all",
-                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0 (or all/none)")
+                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused (or all/none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--case", default=None,
                     help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
-                         "wq:layer[:fmt], aq:M:K[:fmt]")
+                         "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt]")
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
     ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
@@ -519,6 +519,68 @@ def section_ue8m0(torch, synth, fp8rl, dev, seed, peaks, have_gemm):
     return res
 
 
+def fused_mlp_inputs(torch, synth, fp8rl, dev, seed, m, fmt, moe=False):
+    """Gate/up weights quantised straight into the interleaved layout, and the
+    quantised activations, for the dense Qwen3-8B MLP or the Qwen3-30B-A3B
+    experts (T = 4096, top-8)."""
+    if moe:
+        inter, k, e = synth.MOE_INTER, synth.MOE_HIDDEN, synth.MOE_EXPERTS
+        gate = synth.moe_expert_weights(inter, k, e, seed, 0, "gate", device=dev)
+        up = synth.moe_expert_weights(inter, k, e, seed, 0, "up", device=dev)
+        r = synth.moe_routing(MOE_T, e, synth.MOE_TOPK, seed, 0)
+        offsets = torch.from_numpy(r.offsets).to(dev)
+        m = int(r.offsets[-1])
+        x = synth.normal_bf16((m, k), 1.0, seed, "fused-moe-x", device=dev)
+    else:
+        inter, k = 12288, 4096
+        gate = synth.weight_bf16(inter, k, seed, "fused-gate", device=dev)
+        up = synth.weight_bf16(inter, k, seed, "fused-up", device=dev)
+        offsets = None
+        x = synth.activation_bf16(m, k, seed, "fused-x", device=dev)
+    wq, sw = fp8rl.quant_gate_up_interleaved(gate, up, fmt)
+    del gate, up
+    xq, sx = fp8rl.quant_act(x, fmt)
+    return {"m": m, "inter": inter, "k": k, "wq": wq, "sw": sw, "xq": xq, "sx": sx, "offsets": offsets,
+            "experts": synth.MOE_EXPERTS if moe else 1}
+
+
+def section_fused_mlp(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
+    """The fused gate-up path (GEMM + SiLU(gate) * up + 1x128 quantisation in
+    one kernel) against the two kernels it replaces: the gate-up GEMM to bf16
+    and the activation quantiser on the [m, inter] intermediate (the separate
+    SwiGLU pass of an unfused path is not even counted)."""
+    res = {}
+    for name, moe, m in (("qwen3_8b_mlp_m8192", False, STEP_M), ("qwen3_30b_a3b_experts_t4096", True, 0)):
+        d = fused_mlp_inputs(torch, synth, fp8rl, dev, seed, m, fmt, moe)
+        m, inter, k = d["m"], d["inter"], d["k"]
+        hq = torch.empty((m, inter), dtype=torch.uint8, device=dev)
+        hs = torch.empty((inter // 128, m), dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev)
+        y = torch.empty((m, 2 * inter), dtype=torch.bfloat16, device=dev)
+        q2 = torch.empty((m, inter), dtype=torch.uint8, device=dev)
+        if moe:
+            fused = lambda: fp8rl.fp8rl_grouped_gemm_swiglu_quant(d["xq"], d["sx"], d["wq"], d["sw"], d["offsets"],
+                                                                 d["experts"], m, inter, k, hq, hs, fmt)
+            gemm = lambda: fp8rl.fp8rl_grouped_gemm_blockscaled(d["xq"], d["sx"], d["wq"], d["sw"], d["offsets"],
+                                                               d["experts"], m, 2 * inter, k, y, fmt)
+        else:
+            fused = lambda: fp8rl.fp8rl_gemm_swiglu_quant(d["xq"], d["sx"], d["wq"], d["sw"], m, inter, k, hq, hs,
+                                                         fmt)
+            gemm = lambda: fp8rl.fp8rl_gemm_blockscaled(d["xq"], d["sx"], d["wq"], d["sw"], y, m, 2 * inter, k,
+                                                       fmt)
+        aq = lambda: fp8rl.fp8rl_quant_act_group(y, m, inter, 2 * inter, q2, inter, hs, fmt)
+        t_fused = time_loop(torch, fused, 20, 5)
+        t_gemm = time_loop(torch, gemm, 20, 5)
+        t_aq = time_loop(torch, aq, 20, 5)
+        flops = 2.0 * m * 2 * inter * k
+        res[name] = {"m": m, "inter": inter, "k": k, "fused_ms": t_fused, "unfused_gemm_ms": t_gemm,
+                     "unfused_act_quant_ms": t_aq, "saved_ms": t_gemm + t_aq - t_fused,
+                     "fused_tflops": flops / t_fused / 1e9,
+                     "fused_frac_fp8": flops / t_fused / 1e9 / (2.0 * peaks["bf16_tflops_sustained"])}
+        del d, hq, hs, y, q2
+        torch.cuda.empty_cache()
+    return res
+
+
 def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt):
     w = synth.weight_bf16(n, k, seed, "ue8m0", name, device=dev)
     wq, sw = fp8rl.quant_weight(w, fmt)
@@ -621,7 +683,7 @@ def main_ours(args):
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
     wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
-        {"model", "moe_sync", "sweep", "ue8m0"} if args.sections == "all" else set())
+        {"model", "moe_sync", "sweep", "ue8m0", "fused"} if args.sections == "all" else set())
     del inp
     torch.cuda.empty_cache()
     if "model" in wanted:
@@ -632,6 +694,8 @@ def main_ours(args):
         sections["gemm_sweep_qwen3_8b"] = section_sweep(torch, synth, fp8rl, dev, seed, peaks)
     if "ue8m0" in wanted:
         sections["ue8m0"] = section_ue8m0(torch, synth, fp8rl, dev, seed, peaks, have_gemm)
+    if "fused" in wanted and have_gemm:
+        sections["fused_mlp"] = section_fused_mlp(torch, synth, fp8rl, dev, seed, peaks)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_sample(synth)
@@ -745,6 +809,19 @@ def main_case(args):
         y = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
         fn = lambda: fp8rl.fp8rl_grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, synth.MOE_EXPERTS, rows, n, k, y)
         work = {"flops": gemm_flops(rows, n, k)}
+    elif kind in ("fused", "fused_moe"):
+        fmt = int(parts[-1]) if (kind == "fused" and len(parts) > 2) or (kind == "fused_moe" and len(parts) > 1) else 0
+        d = fused_mlp_inputs(torch, synth, fp8rl, dev, 0, int(parts[1]) if kind == "fused" else 0, fmt,
+                             kind == "fused_moe")
+        m, inter, k = d["m"], d["inter"], d["k"]
+        hq = torch.empty((m, inter), dtype=torch.uint8, device=dev)
+        hs = torch.empty((inter // 128, m), dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev)
+        if kind == "fused_moe":
+            fn = lambda: fp8rl.fp8rl_grouped_gemm_swiglu_quant(d["xq"], d["sx"], d["wq"], d["sw"], d["offsets"],
+                                                              d["experts"], m, inter, k, hq, hs, fmt)
+        else:
+            fn = lambda: fp8rl.fp8rl_gemm_swiglu_quant(d["xq"], d["sx"], d["wq"], d["sw"], m, inter, k, hq, hs, fmt)
+        work = {"flops": 2.0 * m * 2 * inter * k}
     elif kind == "wq":
         fmt = int(parts[2]) if len(parts) > 2 else 0
         layer = [w for _, w in synth.qwen3_8b_layer(0, 0, device=dev)]

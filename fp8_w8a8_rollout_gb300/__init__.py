@@ -26,7 +26,8 @@ __all__ = [
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
     "fp8rl_gemm_workspace_size", "fp8rl_gemm_blockscaled_ws", "gemm_workspace",
-    "fp8rl_gemm_blockscaled_static",
+    "fp8rl_gemm_blockscaled_static", "fp8rl_gemm_swiglu_quant", "fp8rl_grouped_gemm_swiglu_quant",
+    "gemm_swiglu_quant", "grouped_gemm_swiglu_quant", "quant_gate_up_interleaved",
     "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
     "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm", "HostWeightSync",
 ]
@@ -82,6 +83,8 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_gemm_workspace_size": [ctypes.POINTER(ctypes.c_size_t)],
             "fp8rl_gemm_blockscaled_ws": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp, ctypes.c_size_t, vp],
             "fp8rl_gemm_blockscaled_static": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
+            "fp8rl_gemm_swiglu_quant": [vp, vp, vp, vp, i64, i64, i64, vp, vp, st, vp],
+            "fp8rl_grouped_gemm_swiglu_quant": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, st, vp],
             "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
             "fp8rl_e4m3_encode": [vp, i64, vp, vp],
             "fp8rl_debug_set": [i32, i64],
@@ -172,6 +175,21 @@ def fp8rl_gemm_blockscaled_static(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt
     _ok(load_library().fp8rl_gemm_blockscaled_static(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
                                                      _p(y_bf16), m, n, k, fmt, _stream(stream)),
         "fp8rl_gemm_blockscaled_static")
+
+
+def fp8rl_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, m, inter, k, hq, h_scale,
+                            fmt=SCALE_FP32, stream=None) -> None:
+    _ok(load_library().fp8rl_gemm_swiglu_quant(_p(xq), _p(x_scale), _p(wq_gate_up), _p(w_scale_gate_up), m,
+                                               inter, k, _p(hq), _p(h_scale), fmt, _stream(stream)),
+        "fp8rl_gemm_swiglu_quant")
+
+
+def fp8rl_grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, num_experts, rows,
+                                    inter, k, hq, h_scale, fmt=SCALE_FP32, stream=None) -> None:
+    _ok(load_library().fp8rl_grouped_gemm_swiglu_quant(_p(xq), _p(x_scale), _p(wq_gate_up),
+                                                       _p(w_scale_gate_up), _p(d_offsets), num_experts, rows,
+                                                       inter, k, _p(hq), _p(h_scale), fmt, _stream(stream)),
+        "fp8rl_grouped_gemm_swiglu_quant")
 
 
 def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k,
@@ -293,6 +311,65 @@ def grouped_gemm(xq, x_scale, wq, w_scale, d_offsets, fmt=SCALE_FP32, out=None, 
         out = torch.empty((rows, n), dtype=torch.bfloat16, device=xq.device)
     fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, e, rows, n, k, out, fmt,
                                    stream)
+    return out
+
+
+def quant_gate_up_interleaved(gate: torch.Tensor, up: torch.Tensor, fmt=SCALE_FP32, stream=None,
+                              out=None):
+    """Quantise a gate and an up weight ([..., inter, k] bf16, optionally with
+    leading expert dimensions) straight into the interleaved fused layout that
+    fp8rl_gemm_swiglu_quant consumes: 128-row blocks alternate gate, up.  One
+    batched quantiser pass (one descriptor per 128-row block); returns
+    (q [..., 2 * inter, k] uint8, scale [..., 2 * inter / 128, k / 128])."""
+    if gate.shape != up.shape or gate.dtype != torch.bfloat16 or up.dtype != torch.bfloat16:
+        raise ValueError("gate and up must be bf16 tensors of one shape")
+    *lead, inter, k = gate.shape
+    if inter % 128 or k % 128:
+        raise ValueError("inter and k must be multiples of 128")
+    g2 = gate.reshape(-1, inter, k)
+    u2 = up.reshape(-1, inter, k)
+    if g2.stride(2) != 1 or u2.stride(2) != 1:
+        raise ValueError("weights need unit column stride")
+    experts = g2.shape[0]
+    if out is None:
+        q = torch.empty((experts, 2 * inter, k), dtype=torch.uint8, device=gate.device)
+        sc = torch.empty((experts, 2 * inter // 128, k // 128), dtype=_scale_dtype(fmt), device=gate.device)
+    else:
+        q, sc = (t.view(experts, *t.shape[-2:]) for t in out)
+    items = []
+    for e in range(experts):
+        for b in range(inter // 128):
+            for half, src in ((0, g2[e]), (1, u2[e])):
+                row = 256 * b + 128 * half
+                items.append((src[128 * b:128 * b + 128], q[e, row:row + 128], sc[e, row // 128:row // 128 + 1]))
+    for i in range(0, len(items), 256):
+        chunk = items[i:i + 256]
+        fp8rl_quant_weight_blockwise_batched(weight_descs(chunk), len(chunk), fmt, stream)
+    return q.view(*lead, 2 * inter, k), sc.view(*lead, 2 * inter // 128, k // 128)
+
+
+def gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, fmt=SCALE_FP32, out=None, stream=None):
+    """(hq [m, inter] uint8, h_scale [inter/128, m]) of SiLU(gate) * up."""
+    m, k = xq.shape
+    inter = wq_gate_up.shape[0] // 2
+    if out is None:
+        out = (torch.empty((m, inter), dtype=torch.uint8, device=xq.device),
+               torch.empty((inter // 128, m), dtype=_scale_dtype(fmt), device=xq.device))
+    fp8rl_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, m, inter, k, out[0], out[1], fmt, stream)
+    return out
+
+
+def grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, fmt=SCALE_FP32, out=None,
+                              stream=None):
+    """Grouped (MoE) form of gemm_swiglu_quant."""
+    rows, k = xq.shape
+    e, n2, _ = wq_gate_up.shape
+    inter = n2 // 2
+    if out is None:
+        out = (torch.empty((rows, inter), dtype=torch.uint8, device=xq.device),
+               torch.empty((inter // 128, rows), dtype=_scale_dtype(fmt), device=xq.device))
+    fp8rl_grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, e, rows, inter, k,
+                                    out[0], out[1], fmt, stream)
     return out
 
 

@@ -51,7 +51,9 @@ constexpr int kBM = 128;     // tile rows (tcgen05 M)
 constexpr int kBK = 128;     // K chunk: one scale block, one 128-byte swizzle row
 constexpr int kUmmaK = 32;   // K of one E4M3 tcgen05.mma
 
-template <int BN, int AROWS = kBM>
+// EPI 0: bf16 Y.  EPI 1: the fused gate-up epilogue (SiLU(gate) * up kept in
+// fp32, quantised to E4M3 in 1x128 groups); needs 256-wide tiles.
+template <int BN, int AROWS = kBM, int EPI = 0>
 struct Cfg {
   // operand stages: as many as fit in about 200 KB of shared memory
   static constexpr int kStageBytesRaw = AROWS * kBK + BN * kBK;
@@ -72,7 +74,11 @@ struct Cfg {
   static constexpr int kScaleSlots = 16;
   static constexpr int kScaleSlotFloats = kBM + 4;
   static constexpr int kBookBytes = 1024;  // barriers and small shared state
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4;
+  // fused epilogue: per-row maxima of the four column slices, two tiles deep
+  static constexpr int kRedBytes = EPI ? 2 * 4 * kBM * 4 : 0;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4 + kRedBytes;
+  static_assert(EPI == 0 || BN == 256, "the fused epilogue pairs 128 gate with 128 up columns");
   static constexpr int kPartPitch = BN + 4;  // floats per row of a split-K partial tile
   static_assert(kBM * kPartPitch * 4 <= kStages * kStageBytes, "partial tile must fit over the stages");
   static_assert((2 * kStages + 2 * kAccBufs + 2 * kScaleSlots + 2) * 8 + 16 <= kBookBytes, "bookkeeping");
@@ -102,6 +108,10 @@ struct GemmArgs {
   int32_t l2_prefetch;       // K chunks ahead of the shared-memory loads that are prefetched into L2
   int32_t splits;            // K splits; > 1 only for a launch in clusters of `splits` CTAs along z
   // stream-K (cooperative launch): partial tiles meet in a caller-provided workspace
+  // fused gate-up epilogue: h = SiLU(gate) * up, [rows][n / 2] E4M3 codes and
+  // [n / 256][rows] scales (the weight's 128-row blocks alternate gate, up)
+  uint8_t* hq;
+  void* h_scale;
   uint32_t* ws_head;         // [0] epoch of the last completed launch, [1] CTAs finished in this launch
   uint32_t* ws_flag;         // [gridDim.x] slot of CTA b holds this launch's partial: == epoch + 1
   // [gridDim.x][BN / 4][32] float4: one 128 x BN fp32 partial tile per CTA,
@@ -293,11 +303,12 @@ __device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
 // stage holds just AROWS activation rows; the M = 128 MMA reads the rest of
 // its A rows from whatever shared memory follows, which only feeds accumulator
 // rows >= AROWS that are never stored.
-template <int BN, int AROWS, bool UE8M0, int MODE>
-__global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0>
+__global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
                             const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
-  using C = Cfg<BN, AROWS>;
+  using C = Cfg<BN, AROWS, EPI>;
+  static_assert(EPI == 0 || MODE == kDataParallel, "the fused epilogue needs whole tiles");
   constexpr bool SPLITK = MODE == kSplitK;
   constexpr bool STREAMK = MODE == kStreamK;
   extern __shared__ uint8_t smem_raw[];
@@ -319,6 +330,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
   int* shared_m_tiles = abort_flag + 1;
   uint32_t* shared_epoch = reinterpret_cast<uint32_t*>(shared_m_tiles + 1);
   float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
+  float* row_max = scale_ring + C::kScaleSlots * C::kScaleSlotFloats;  // fused epilogue only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
@@ -746,7 +758,10 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
     const int quad = warp & 3;   // TMEM lanes this warp may read: 32*quad .. +31
     const int slice = ew >> 2;   // which kCols columns of the tile
     const int r = quad * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
+    // EPI 0: columns [kCols * slice, +kCols).  EPI 1: gate columns
+    // [32 * slice, +32) and the matching up columns 128 further on.
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + (EPI ? 32 * slice : slice * C::kCols);
+    uint32_t tiles_done = 0;  // fused epilogue: which half of row_max
     uint32_t g = 0;   // chunk groups folded so far (TMEM ring position)
     uint32_t gs = 0;  // chunks whose scales were taken (scale ring position)
     bool ok = true;
@@ -783,16 +798,18 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const float* slot = scale_ring + q * C::kScaleSlotFloats;
-          const float f = slot[r] * slot[kBM + sw_lane];
+          const float f = slot[r] * slot[kBM + (EPI ? 0 : sw_lane)];
+          const float f_up = EPI ? slot[r] * slot[kBM + 1] : f;  // the up half's weight block
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sempty[q]));  // the values are in registers
           if (warp_idle) continue;  // every row of this warp is past the segment
-          const uint64_t f2 = f32x2(f, f);
           const uint32_t taddr = t_lane + (buf * C::kGroup + j) * BN;
 #pragma unroll
           for (int cc = 0; cc < C::kCols / 32; ++cc) {
+            const float fc = cc == 0 ? f : f_up;
+            const uint64_t f2 = f32x2(fc, fc);
             uint64_t v[16];
-            tmem_ld_32x32b_x32_pairs(taddr + cc * 32, v);
+            tmem_ld_32x32b_x32_pairs(taddr + cc * (EPI ? 128 : 32), v);
 #pragma unroll
             for (int q = 0; q < 16; ++q) acc[cc * 16 + q] = fma_f32x2(v[q], f2, acc[cc * 16 + q]);
           }
@@ -800,6 +817,87 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));  // one arrival per warp
+      }
+      if constexpr (EPI == 1) {
+        // h = SiLU(gate) * up for this thread's 32 columns, kept in fp32 (the
+        // single rounding of the fused region is the E4M3 one below); SiLU
+        // with the fast exponential and division intrinsics (a few ulp)
+        float hmax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float g0, g1, u0, u1;
+          f32x2_unpack(acc[j], g0, g1);
+          f32x2_unpack(acc[16 + j], u0, u1);
+          const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+          const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+          acc[j] = f32x2(h0, h1);
+          hmax = fmaxf(hmax, fmaxf(fabsf(h0), fabsf(h1)));
+        }
+        // the group is the row's 128 h columns, held by the four warps of this
+        // TMEM lane quadrant: their maxima meet in shared memory (two buffers:
+        // a warp may start the next tile's exchange while another still reads
+        // this one) behind the quadrant's own barrier
+        float* red = row_max + (tiles_done++ & 1) * 4 * kBM;
+        red[slice * kBM + r] = hmax;
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + quad) : "memory");
+        // every warp reaches its quadrant's barrier for every tile (a warp whose
+        // wait ran out still finishes the tile), and all of them leave here
+        // once any wait has run out
+        if (*abortv) break;
+        const float amax = fmaxf(fmaxf(red[r], red[kBM + r]), fmaxf(red[2 * kBM + r], red[3 * kBM + r]));
+        if (ok && row_ok) {
+          uint32_t w[8];
+          if (UE8M0) {
+            const int e = scale_ue8m0_exponent(amax);
+            const float fs = exp2_neg(e);
+            const uint64_t f2 = f32x2(fs, fs);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float h0, h1, h2, h3;
+              f32x2_unpack(mul_f32x2(acc[2 * j], f2), h0, h1);
+              f32x2_unpack(mul_f32x2(acc[2 * j + 1], f2), h2, h3);
+              w[j] = e4m3x2(h0, h1) | (e4m3x2(h2, h3) << 16);
+            }
+            if (slice == 0) static_cast<uint8_t*>(a.h_scale)[(int64_t)n_tile * a.rows + grow] = (uint8_t)(e + 127);
+          } else {
+            const float sc = scale_fp32(amax);
+            const float rc = __frcp_rn(sc);
+            if (sc >= kFastDivMinScale) {
+              // the correctly rounded quotient h / sc, on pairs (formed from
+              // -h so that every rounding, signed zeros included, matches the
+              // scalar sequence q0 = h r, e = q0 sc - h, q = q0 - e r)
+              const uint64_t s2 = f32x2(sc, sc), nr2 = f32x2(-rc, -rc);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                uint32_t half[2];
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                  const uint64_t nx = acc[2 * j + p] ^ 0x8000000080000000ull;
+                  const uint64_t q0 = mul_f32x2(nx, nr2);
+                  const uint64_t e = fma_f32x2(q0, s2, nx);
+                  float q_lo, q_hi;
+                  f32x2_unpack(fma_f32x2(e, nr2, q0), q_lo, q_hi);
+                  half[p] = e4m3x2(q_lo, q_hi);
+                }
+                w[j] = half[0] | (half[1] << 16);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float h[4];
+                f32x2_unpack(acc[2 * j], h[0], h[1]);
+                f32x2_unpack(acc[2 * j + 1], h[2], h[3]);
+                w[j] = e4m3x2(__fdiv_rn(h[0], sc), __fdiv_rn(h[1], sc)) |
+                       (e4m3x2(__fdiv_rn(h[2], sc), __fdiv_rn(h[3], sc)) << 16);
+              }
+            }
+            if (slice == 0) static_cast<float*>(a.h_scale)[(int64_t)n_tile * a.rows + grow] = sc;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(a.hq + (int64_t)grow * (a.n / 2) + n_tile * 128 + slice * 32);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        continue;
       }
       bool store_y = !SPLITK;
       if (STREAMK && !(lo == 0 && hi == num_kb)) {
@@ -1057,7 +1155,7 @@ struct KernelState {
   int8_t cluster_fits[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
 };
 
-template <int BN, int AROWS, bool UE8M0, int MODE>
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI>
 KernelState& kernel_state(int dev) {
   static KernelState st[64];
   return st[dev];
@@ -1077,15 +1175,15 @@ StreamKLayout streamk_layout(int max_ctas) {
   return l;
 }
 
-template <int BN, int AROWS, bool UE8M0, int MODE>
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0>
 fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_tiles_bound, int sms,
                     GemmArgs args, int splits, cudaStream_t stream, int streamk_grid = 0) {
-  using C = Cfg<BN, AROWS>;
+  using C = Cfg<BN, AROWS, EPI>;
   constexpr bool SPLITK = MODE == kSplitK;
-  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE>;
+  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE, EPI>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
-  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE>(dev);
+  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE, EPI>(dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!ks.ready) {
@@ -1264,6 +1362,43 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
             : launch<128, kBM, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
 }
 
+// The fused gate-up GEMM: the same kernel with the SwiGLU-quantise epilogue,
+// 256-wide tiles (128 gate + the matching 128 up columns), whole tiles.
+fp8rl_status run_swiglu(const void* xq, const void* x_scale, const void* wq, const void* w_scale,
+                        const int32_t* d_offsets, int64_t experts, int64_t rows, int64_t inter, int64_t k,
+                        void* hq, void* h_scale, fp8rl_scale_fmt fmt, void* stream) {
+  const DeviceInfo di = device_info();
+  if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
+  uint32_t* err = device_error_word();
+  if (!err) return FP8RL_ERR_CUDA;
+  Debug dbg;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    dbg = g_debug;
+  }
+  GemmArgs args{};
+  args.sx = x_scale;
+  args.sw = w_scale;
+  args.offsets = d_offsets;
+  args.rows = (int32_t)rows;
+  args.n = (int32_t)(2 * inter);
+  args.k = (int32_t)k;
+  args.experts = (int32_t)experts;
+  args.err = err;
+  args.timeout_ns = dbg.timeout_ns;
+  args.fault_skip_kb = dbg.fault_skip_kb;
+  args.wait_mode = dbg.wait_mode;
+  args.l2_prefetch = dbg.l2_prefetch;
+  args.hq = static_cast<uint8_t*>(hq);
+  args.h_scale = h_scale;
+  const int64_t m_tiles = (rows + kBM - 1) / kBM;
+  const int64_t mt_bound = d_offsets ? m_tiles + experts : m_tiles;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return fmt == FP8RL_SCALE_UE8M0
+             ? launch<256, kBM, true, kDataParallel, 1>(xq, wq, experts, mt_bound, di.sms, args, 1, cs)
+             : launch<256, kBM, false, kDataParallel, 1>(xq, wq, experts, mt_bound, di.sms, args, 1, cs);
+}
+
 }  // namespace
 }  // namespace fp8rl
 
@@ -1328,6 +1463,33 @@ extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_blockscaled(const void* xq,
   if (st != FP8RL_OK || rows == 0 || n == 0) return st;
   if (num_experts > INT32_MAX / 2 || num_experts * n > INT32_MAX) return FP8RL_ERR_SHAPE;
   return run(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k, y, fmt, stream);
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_gemm_swiglu_quant(const void* xq, const void* x_scale,
+                                                          const void* wq_gate_up, const void* w_scale_gate_up,
+                                                          int64_t m, int64_t inter, int64_t k, void* hq,
+                                                          void* h_scale, fp8rl_scale_fmt fmt, void* stream) {
+  if (inter < 0) return FP8RL_ERR_INVALID_ARG;
+  fp8rl_status st = check_gemm(xq, x_scale, wq_gate_up, w_scale_gate_up, hq, m, 2 * inter, k, fmt);
+  if (st != FP8RL_OK || m == 0 || inter == 0) return st;
+  if (!h_scale) return FP8RL_ERR_INVALID_ARG;
+  if (fmt == FP8RL_SCALE_FP32 && !aligned(h_scale, 4)) return FP8RL_ERR_ALIGNMENT;
+  if (2 * inter > INT32_MAX) return FP8RL_ERR_SHAPE;
+  return run_swiglu(xq, x_scale, wq_gate_up, w_scale_gate_up, nullptr, 1, m, inter, k, hq, h_scale, fmt, stream);
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_swiglu_quant(
+    const void* xq, const void* x_scale, const void* wq_gate_up, const void* w_scale_gate_up,
+    const int32_t* d_offsets, int64_t num_experts, int64_t rows, int64_t inter, int64_t k, void* hq,
+    void* h_scale, fp8rl_scale_fmt fmt, void* stream) {
+  if (num_experts < 1 || !d_offsets || inter < 0) return FP8RL_ERR_INVALID_ARG;
+  fp8rl_status st = check_gemm(xq, x_scale, wq_gate_up, w_scale_gate_up, hq, rows, 2 * inter, k, fmt);
+  if (st != FP8RL_OK || rows == 0 || inter == 0) return st;
+  if (!h_scale) return FP8RL_ERR_INVALID_ARG;
+  if (fmt == FP8RL_SCALE_FP32 && !aligned(h_scale, 4)) return FP8RL_ERR_ALIGNMENT;
+  if (num_experts > INT32_MAX / 2 || num_experts * 2 * inter > INT32_MAX) return FP8RL_ERR_SHAPE;
+  return run_swiglu(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, num_experts, rows, inter, k, hq, h_scale,
+                    fmt, stream);
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {

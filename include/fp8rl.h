@@ -152,6 +152,49 @@ FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const void* x_scal
                                               void* stream);
 
 /*
+ * Fused gate-up projection of a gated MLP: the block-scaled GEMM against the
+ * fused gate/up weight, SiLU(gate) * up computed from the fp32 accumulators
+ * (never rounded to bf16), and that result quantised to E4M3 in 1x128 groups
+ * along its columns, ready to be the down projection's activation ("Method
+ * steps", step 1: activations quantised dynamically; "Where Rounding Happens
+ * Matters", "the overall scheme": keep the fused region's intermediate in fp32
+ * and round once).  Replaces the bf16 gate-up output, the SwiGLU and the
+ * activation quantisation pass of the unfused path.
+ *   xq, x_scale      as fp8rl_gemm_blockscaled, [m][k] and [k/128][m]
+ *   wq_gate_up       device, E4M3 [2 * inter][k]: the gate and up weights with
+ *                    their 128-row blocks interleaved: gate rows 0..127, up
+ *                    rows 0..127, gate rows 128..255, up rows 128..255, ...
+ *                    (a row order, not arithmetic: the 128x128 block
+ *                    quantisation of either layout is the same)
+ *   w_scale_gate_up  device, [2 * inter / 128][k/128], in the same block order
+ *   hq               device, E4M3 [m][inter] (row stride inter)
+ *   h_scale          device, [inter/128][m] (layout of fp8rl_quant_act_group)
+ * inter and k must be multiples of 128 (SHAPE otherwise).  fmt applies to the
+ * input scales and to h_scale alike.  Alignment and errors as
+ * fp8rl_gemm_blockscaled (hq takes the place of y_bf16).
+ */
+FP8RL_API fp8rl_status fp8rl_gemm_swiglu_quant(const void* xq, const void* x_scale, const void* wq_gate_up,
+                                               const void* w_scale_gate_up, int64_t m, int64_t inter,
+                                               int64_t k, void* hq, void* h_scale, fp8rl_scale_fmt fmt,
+                                               void* stream);
+
+/*
+ * The same fused gate-up path over MoE expert row segments (the expert
+ * layout of fp8rl_grouped_gemm_blockscaled): expert e's rows
+ * offsets[e] .. offsets[e+1]-1 use wq_gate_up[e], each expert's weight with
+ * the interleaved block order above.
+ *   wq_gate_up       device, E4M3 [num_experts][2 * inter][k]
+ *   w_scale_gate_up  device, [num_experts][2 * inter / 128][k/128]
+ *   hq               device, E4M3 [rows][inter];  h_scale [inter/128][rows]
+ * Errors: as fp8rl_grouped_gemm_blockscaled.
+ */
+FP8RL_API fp8rl_status fp8rl_grouped_gemm_swiglu_quant(const void* xq, const void* x_scale,
+                                                       const void* wq_gate_up, const void* w_scale_gate_up,
+                                                       const int32_t* d_offsets, int64_t num_experts,
+                                                       int64_t rows, int64_t inter, int64_t k, void* hq,
+                                                       void* h_scale, fp8rl_scale_fmt fmt, void* stream);
+
+/*
  * Bytes of workspace that fp8rl_gemm_blockscaled_ws needs on the current
  * device (a 256-byte header, one flag word and one 128 x 256 fp32 tile per SM;
  * about 20 MB on a 152-SM part).  The size does not depend on the shape.

@@ -121,6 +121,21 @@ def test_workspace_gemm_rejects_bad_arguments_on_host(lib):
     assert _rc("fp8rl_gemm_workspace_size", None) == 1
 
 
+def test_fused_gate_up_rejects_bad_arguments_on_host(lib):
+    a16 = 1 << 20
+    g = "fp8rl_gemm_swiglu_quant"
+    assert _rc(g, None, a16, a16, a16, 16, 128, 256, a16, a16, 0, None) == 1
+    assert _rc(g, a16, a16, a16, a16, 16, 100, 256, a16, a16, 0, None) == 2   # inter % 128
+    assert _rc(g, a16, a16, a16, a16, 16, 128, 200, a16, a16, 0, None) == 2   # k % 128
+    assert _rc(g, a16, a16, a16, a16, 16, 128, 256, a16 + 8, a16, 0, None) == 3  # hq alignment
+    assert _rc(g, a16, a16, a16, a16, 16, 128, 256, a16, None, 0, None) == 1
+    assert _rc(g, a16, a16, a16, a16, 0, 128, 256, a16, a16, 0, None) == 0    # m == 0: no-op
+    gg = "fp8rl_grouped_gemm_swiglu_quant"
+    assert _rc(gg, a16, a16, a16, a16, None, 4, 64, 128, 256, a16, a16, 0, None) == 1
+    assert _rc(gg, a16, a16, a16, a16, a16, 4, 64, 100, 256, a16, a16, 0, None) == 2
+    assert _rc(gg, a16, a16, a16, a16, a16, 4, 0, 128, 256, a16, a16, 0, None) == 0
+
+
 def test_grouped_gemm_rejects_bad_arguments_on_host(lib):
     a16 = 1 << 20
     g = "fp8rl_grouped_gemm_blockscaled"

@@ -128,3 +128,24 @@ def test_stream_k_owner_wait_runs_out_and_workspace_recovers():
     got = y.float().cpu().numpy()
     rms = float(np.sqrt(np.mean(ref ** 2)))
     assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)
+
+
+def test_fused_epilogue_wait_runs_out_and_is_reported():
+    """The fused gate-up epilogue exchanges row maxima behind a barrier of all
+    epilogue warps; a wait that runs out must still end the kernel (every
+    warp leaves together) and be reported, and the next call must work."""
+    m, inter, k = 300, 256, 512
+    x = synth.activation_bf16(m, k, 6, "fault-fx")
+    w = synth.weight_bf16(2 * inter, k, 6, "fault-fw")
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w[torch.from_numpy(oracle.interleave_gate_up_rows(2 * inter))]))
+    dx, dsx, dw, dsw = dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, 1)  # each CTA's second K chunk never arrives
+    fp8rl.gemm_swiglu_quant(dx, dsx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_RESET, 0)
+    hq, hs = fp8rl.gemm_swiglu_quant(dx, dsx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == 0
+    h_ref, hq_ref, hs_ref = oracle.gemm_swiglu_quant(xq, sx, wq, sw)
+    assert np.all(np.abs(hs.cpu().numpy() - hs_ref) <= 1e-4 * hs_ref)
