@@ -64,6 +64,10 @@ def _load():
         lib.oracle_quant_weight_blockwise.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32]
         lib.oracle_quant_weight_blockwise.restype = i32
         lib.oracle_quant_act_group.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32]
+        lib.oracle_kv_calibrate.restype = i32
+        lib.oracle_kv_calibrate.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp]
+        lib.oracle_kv_append.restype = i32
+        lib.oracle_kv_append.argtypes = [vp, vp, i64, i64, i64, i64, vp, vp, vp, i64, i64, vp]
         lib.oracle_quant_group_f32.restype = i32
         lib.oracle_quant_group_f32.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32]
         lib.oracle_quant_act_group.restype = i32
@@ -188,6 +192,38 @@ def quant_group_f32(x_f32: np.ndarray, fmt: int = SCALE_FP32, threads: int | Non
     rc = _load().oracle_quant_group_f32(_ptr(x), m, k, k, _ptr(q), k, _ptr(s), fmt, threads or default_threads())
     _check(rc, "quant_group_f32")
     return q, s
+
+
+def kv_calibrate(k_bf16_bits: np.ndarray, v_bf16_bits: np.ndarray, q_bf16_bits: np.ndarray | None = None):
+    """Per-tensor fp32 scales (amax / 448) of the calibration pass's K, V
+    [tokens, kv_dim] and optionally Q [tokens, q_dim]: float32 [3] (k, v, q;
+    q is 0 without a Q tensor)."""
+    k = _c(k_bf16_bits, np.uint16)
+    v = _c(v_bf16_bits, np.uint16)
+    t, d = k.shape
+    scales = np.zeros(3, np.float32)
+    if q_bf16_bits is None:
+        rc = _load().oracle_kv_calibrate(_ptr(k), _ptr(v), None, t, d, d, d, 0, 0, _ptr(scales))
+    else:
+        q = _c(q_bf16_bits, np.uint16)
+        rc = _load().oracle_kv_calibrate(_ptr(k), _ptr(v), _ptr(q), t, d, d, d, q.shape[1], q.shape[1],
+                                         _ptr(scales))
+    _check(rc, "kv_calibrate")
+    return scales
+
+
+def kv_append(k_bf16_bits, v_bf16_bits, slots, k_cache, v_cache, scales):
+    """Quantise rows of K and V into the caches (uint8 [num_slots, kv_dim],
+    updated in place) at `slots` (int32 [tokens]; out-of-range: skipped)."""
+    k = _c(k_bf16_bits, np.uint16)
+    v = _c(v_bf16_bits, np.uint16)
+    sl = _c(slots, np.int32)
+    sc = _c(scales, np.float32)
+    assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
+    t, d = k.shape
+    rc = _load().oracle_kv_append(_ptr(k), _ptr(v), t, d, d, d, _ptr(sl), _ptr(k_cache), _ptr(v_cache),
+                                  k_cache.shape[1], k_cache.shape[0], _ptr(sc))
+    _check(rc, "kv_append")
 
 
 def silu(x: np.ndarray) -> np.ndarray:

@@ -44,6 +44,14 @@
  *      to bf16) and quantised in 1x128 groups by the same steps (R1-R6) as a
  *      bf16 activation; "Where Rounding Happens Matters", "the overall
  *      scheme".  The fp64 SiLU lives in the Python wrapper.
+ *  R9  KV cache (a "next" step; "Method steps", step 3: the K/V quantisation
+ *      scales are recomputed from the first forward of every RL step, before
+ *      its rollout): one fp32 scale per tensor (the pages do not fix the
+ *      granularity; per tensor is the plainest reading), scale = amax / 448
+ *      of that calibration pass (R1, R4), and every K or V row written to the
+ *      cache afterwards is quantised with it (R2, R3: values above the
+ *      calibrated range saturate at +-448).  A slot index outside
+ *      [0, num_slots) (padding) writes nothing.
  *
  * Everything is computed the plain way: decode and encode by explicit search
  * over the format's code table, fp64 dot products for the GEMM, no blocking.
@@ -437,6 +445,60 @@ ORACLE_API int oracle_quant_group_f32(const float* x, int64_t m, int64_t k, int6
     c.fmt = fmt;
     c.groups = (k + 127) / 128;
     parallel_for(m, threads, aqf_item, &c);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV cache: per-step per-tensor calibration and quantised append (R9)       */
+/* ------------------------------------------------------------------------ */
+
+static float tensor_amax_bf16(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld)
+{
+    float amax = 0.0f;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float a = fabsf(bf16_to_f32(x[r * ld + c]));
+            if (a > amax)
+                amax = a;
+        }
+    return amax;
+}
+
+/* scales[0] = K scale, scales[1] = V scale, scales[2] = Q scale (q may be
+ * null: scales[2] is left alone).  K and V are [tokens][kv_dim], Q is
+ * [tokens][q_dim], bf16, with row strides ldk, ldv, ldq. */
+ORACLE_API int oracle_kv_calibrate(const uint16_t* k, const uint16_t* v, const uint16_t* q, int64_t tokens,
+                                   int64_t kv_dim, int64_t ldk, int64_t ldv, int64_t q_dim, int64_t ldq,
+                                   float* scales)
+{
+    if (tokens < 0 || kv_dim < 0 || ldk < kv_dim || ldv < kv_dim || (q && (q_dim < 0 || ldq < q_dim)))
+        return 1;
+    scales[0] = scale_fp32(tensor_amax_bf16(k, tokens, kv_dim, ldk));
+    scales[1] = scale_fp32(tensor_amax_bf16(v, tokens, kv_dim, ldv));
+    if (q)
+        scales[2] = scale_fp32(tensor_amax_bf16(q, tokens, q_dim, ldq));
+    return 0;
+}
+
+/* Row t of K and V goes to cache row slots[t] (E4M3, row stride ldc) when
+ * 0 <= slots[t] < num_slots; other cache rows are not touched. */
+ORACLE_API int oracle_kv_append(const uint16_t* k, const uint16_t* v, int64_t tokens, int64_t kv_dim, int64_t ldk,
+                                int64_t ldv, const int32_t* slots, uint8_t* k_cache, uint8_t* v_cache, int64_t ldc,
+                                int64_t num_slots, const float* scales)
+{
+    if (tokens < 0 || kv_dim < 0 || ldk < kv_dim || ldv < kv_dim || ldc < kv_dim)
+        return 1;
+    for (int64_t t = 0; t < tokens; ++t) {
+        int64_t slot = slots[t];
+        if (slot < 0 || slot >= num_slots)
+            continue;
+        for (int64_t c = 0; c < kv_dim; ++c) {
+            float qk = bf16_to_f32(k[t * ldk + c]) / scales[0]; /* R3 */
+            float qv = bf16_to_f32(v[t * ldv + c]) / scales[1];
+            k_cache[slot * ldc + c] = encode_value((double)qk);
+            v_cache[slot * ldc + c] = encode_value((double)qv);
+        }
+    }
     return 0;
 }
 

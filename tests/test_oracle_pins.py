@@ -555,3 +555,51 @@ def test_fused_reference_equals_unfused_steps():
     assert np.allclose(h, h_ref, rtol=1e-14, atol=0)
     hq_ref, hs_ref = oracle.quant_group_f32(h_ref.astype(np.float32))
     assert np.array_equal(hq, hq_ref) and np.array_equal(hs, hs_ref)
+
+
+# --------------------------------------------------------------------------- KV cache (per-step calibration, append)
+
+def _kv(tokens, dim, seed, spread=1.0):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(tokens, dim)) * spread
+    return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+
+
+def test_kv_calibrate_is_tensor_amax_over_448():
+    k, v, q = _kv(50, 256, 21), _kv(50, 256, 22, 3.0), _kv(50, 512, 23, 0.1)
+    s = oracle.kv_calibrate(synth.bf16_bits(k), synth.bf16_bits(v), synth.bf16_bits(q))
+    for i, t in enumerate((k, v, q)):
+        amax = np.float32(t.float().abs().max().item())
+        assert s[i] == amax / np.float32(448)
+    s0 = oracle.kv_calibrate(synth.bf16_bits(torch.zeros_like(k)), synth.bf16_bits(v))
+    assert s0[0] == 1.0 and s0[2] == 0.0
+
+
+def test_kv_append_codes_slots_and_saturation():
+    tokens, dim, slots_total = 40, 256, 64
+    k, v = _kv(tokens, dim, 24), _kv(tokens, dim, 25, 2.0)
+    s = oracle.kv_calibrate(synth.bf16_bits(k[:20]), synth.bf16_bits(v[:20]))  # calibrated on a prefix
+    rng = np.random.default_rng(26)
+    slots = rng.permutation(slots_total)[:tokens].astype(np.int32)
+    slots[3] = -1        # padding
+    slots[7] = 10 ** 6   # outside the cache
+    kc = np.full((slots_total, dim), 0x55, np.uint8)
+    vc = np.full((slots_total, dim), 0x55, np.uint8)
+    oracle.kv_append(synth.bf16_bits(k), synth.bf16_bits(v), slots, kc, vc, s)
+    for cache, x, sc in ((kc, k, s[0]), (vc, v, s[1])):
+        quotient = (x.float().numpy() / np.float32(sc)).astype(np.float32)  # IEEE fp32 division
+        lib = torch.from_numpy(quotient).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        for t in range(tokens):
+            if 0 <= slots[t] < slots_total:
+                assert np.array_equal(cache[slots[t]], lib[t])
+        untouched = np.setdiff1d(np.arange(slots_total), slots[(slots >= 0) & (slots < slots_total)])
+        assert np.all(cache[untouched] == 0x55)
+    # tokens after the calibration prefix may exceed its range: they saturate
+    beyond = np.abs(k.float().numpy()) / s[0] > 448
+    if beyond.any():
+        t, c = np.argwhere(beyond)[0]
+        assert kc[slots[t], c] & 0x7F == 0x7E
+    # the calibration tensor's own maximum maps to exactly +-448
+    t, c = np.unravel_index(np.argmax(np.abs(k[:20].float().numpy())), (20, dim))
+    if 0 <= slots[t] < slots_total:
+        assert kc[slots[t], c] & 0x7F == 0x7E
