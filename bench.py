@@ -49,12 +49,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="all",
-                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused (or all/none)")
+                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused,kv (or all/none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--case", default=None,
                     help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
-                         "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt]")
+                         "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt], kv:TOKENS")
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
     ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
@@ -581,6 +581,43 @@ def section_fused_mlp(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
     return res
 
 
+KV_DIM, Q_DIM = 1024, 4096  # Qwen3-8B: 8 KV heads and 32 query heads of 128
+
+
+def kv_inputs(torch, synth, dev, seed, tokens, slots_total):
+    k = synth.normal_bf16((tokens, KV_DIM), 1.0, seed, "bench-kv-k", device=dev)
+    v = synth.normal_bf16((tokens, KV_DIM), 1.0, seed, "bench-kv-v", device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    slots = torch.randperm(slots_total, generator=gen, device=dev)[:tokens].to(torch.int32)
+    kc = torch.empty((slots_total, KV_DIM), dtype=torch.uint8, device=dev)
+    vc = torch.empty((slots_total, KV_DIM), dtype=torch.uint8, device=dev)
+    return k, v, slots, kc, vc
+
+
+def section_kv_cache(torch, synth, fp8rl, dev, seed, peaks):
+    """FP8 KV cache of one Qwen3-8B layer: the per-step scale calibration over
+    a prefill (K, V and Q of 8192 tokens), a prefill-size append (32768
+    tokens into a 65536-slot cache) and a decode-size append (256 tokens)."""
+    res = {}
+    k, v, _, _, _ = kv_inputs(torch, synth, dev, seed, STEP_M, STEP_M)
+    q = synth.normal_bf16((STEP_M, Q_DIM), 1.0, seed, "bench-kv-q", device=dev)
+    scales = torch.zeros(3, dtype=torch.float32, device=dev)
+    t = time_loop(torch, lambda: fp8rl.kv_calibrate(k, v, q, out=scales), 20, 5)
+    b = STEP_M * (2 * KV_DIM + Q_DIM) * 2
+    res["calibrate_prefill_8192"] = {"ms": t, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"]}
+    for name, tokens in (("append_prefill_32768", 32768), ("append_decode_256", 256)):
+        k, v, slots, kc, vc = kv_inputs(torch, synth, dev, seed, tokens, 65536)
+        fn = lambda: fp8rl.kv_append(k, v, slots, kc, vc, scales)
+        t = time_loop(torch, fn, 20, 5)
+        b = tokens * KV_DIM * 2 * 3 + tokens * 4  # bf16 in, E4M3 out, K and V; slot indices
+        entry = {"ms": t, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"]}
+        if tokens < 1024:
+            entry["ms_graph"] = time_graph(torch, fn, 50)
+        res[name] = entry
+    return res
+
+
 def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt):
     w = synth.weight_bf16(n, k, seed, "ue8m0", name, device=dev)
     wq, sw = fp8rl.quant_weight(w, fmt)
@@ -683,7 +720,7 @@ def main_ours(args):
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
     wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
-        {"model", "moe_sync", "sweep", "ue8m0", "fused"} if args.sections == "all" else set())
+        {"model", "moe_sync", "sweep", "ue8m0", "fused", "kv"} if args.sections == "all" else set())
     del inp
     torch.cuda.empty_cache()
     if "model" in wanted:
@@ -696,6 +733,8 @@ def main_ours(args):
         sections["ue8m0"] = section_ue8m0(torch, synth, fp8rl, dev, seed, peaks, have_gemm)
     if "fused" in wanted and have_gemm:
         sections["fused_mlp"] = section_fused_mlp(torch, synth, fp8rl, dev, seed, peaks)
+    if "kv" in wanted:
+        sections["kv_cache_qwen3_8b_layer"] = section_kv_cache(torch, synth, fp8rl, dev, seed, peaks)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_sample(synth)
@@ -822,6 +861,12 @@ def main_case(args):
         else:
             fn = lambda: fp8rl.fp8rl_gemm_swiglu_quant(d["xq"], d["sx"], d["wq"], d["sw"], m, inter, k, hq, hs, fmt)
         work = {"flops": 2.0 * m * 2 * inter * k}
+    elif kind == "kv":
+        tokens = int(parts[1])
+        k, v, slots, kc, vc = kv_inputs(torch, synth, dev, 0, tokens, max(65536, tokens))
+        scales = fp8rl.kv_calibrate(k, v)
+        fn = lambda: fp8rl.kv_append(k, v, slots, kc, vc, scales)
+        work = {"bytes": tokens * KV_DIM * 2 * 3 + tokens * 4}
     elif kind == "wq":
         fmt = int(parts[2]) if len(parts) > 2 else 0
         layer = [w for _, w in synth.qwen3_8b_layer(0, 0, device=dev)]

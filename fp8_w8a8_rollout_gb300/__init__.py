@@ -28,6 +28,7 @@ __all__ = [
     "fp8rl_gemm_workspace_size", "fp8rl_gemm_blockscaled_ws", "gemm_workspace",
     "fp8rl_gemm_blockscaled_static", "fp8rl_gemm_swiglu_quant", "fp8rl_grouped_gemm_swiglu_quant",
     "gemm_swiglu_quant", "grouped_gemm_swiglu_quant", "quant_gate_up_interleaved",
+    "fp8rl_kv_calibrate", "fp8rl_kv_append", "kv_calibrate", "kv_append",
     "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
     "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm", "HostWeightSync",
 ]
@@ -84,6 +85,8 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_gemm_blockscaled_ws": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp, ctypes.c_size_t, vp],
             "fp8rl_gemm_blockscaled_static": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
             "fp8rl_gemm_swiglu_quant": [vp, vp, vp, vp, i64, i64, i64, vp, vp, st, vp],
+            "fp8rl_kv_calibrate": [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, vp],
+            "fp8rl_kv_append": [vp, vp, i64, i64, i64, i64, vp, vp, vp, i64, i64, vp, vp],
             "fp8rl_grouped_gemm_swiglu_quant": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, st, vp],
             "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
             "fp8rl_e4m3_encode": [vp, i64, vp, vp],
@@ -190,6 +193,21 @@ def fp8rl_grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_
                                                        _p(w_scale_gate_up), _p(d_offsets), num_experts, rows,
                                                        inter, k, _p(hq), _p(h_scale), fmt, _stream(stream)),
         "fp8rl_grouped_gemm_swiglu_quant")
+
+
+def fp8rl_kv_calibrate(k_bf16, v_bf16, q_bf16, tokens, kv_dim, ldk, ldv, q_dim, ldq, d_scales,
+                       stream=None) -> None:
+    _ok(load_library().fp8rl_kv_calibrate(_p(k_bf16), _p(v_bf16), _p(q_bf16), tokens, kv_dim, ldk, ldv, q_dim,
+                                          ldq, _p(d_scales), _stream(stream)),
+        "fp8rl_kv_calibrate")
+
+
+def fp8rl_kv_append(k_bf16, v_bf16, tokens, kv_dim, ldk, ldv, d_slot_mapping, k_cache, v_cache, ld_cache,
+                    num_slots, d_scales, stream=None) -> None:
+    _ok(load_library().fp8rl_kv_append(_p(k_bf16), _p(v_bf16), tokens, kv_dim, ldk, ldv, _p(d_slot_mapping),
+                                       _p(k_cache), _p(v_cache), ld_cache, num_slots, _p(d_scales),
+                                       _stream(stream)),
+        "fp8rl_kv_append")
 
 
 def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k,
@@ -371,6 +389,27 @@ def grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offset
     fp8rl_grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, e, rows, inter, k,
                                     out[0], out[1], fmt, stream)
     return out
+
+
+def kv_calibrate(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor | None = None, out=None, stream=None):
+    """Per-tensor fp32 scales (device float [3]: K, V, Q) of a calibration pass."""
+    for name, t in (("k", k), ("v", v)) + ((("q", q),) if q is not None else ()):
+        _check_bf16_2d(t, name)
+    scales = out if out is not None else torch.zeros(3, dtype=torch.float32, device=k.device)
+    tokens, dim = k.shape
+    fp8rl_kv_calibrate(k, v, q, tokens, dim, k.stride(0), v.stride(0), 0 if q is None else q.shape[1],
+                       0 if q is None else q.stride(0), scales, stream)
+    return scales
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """Quantise rows of K and V into the E4M3 caches ([num_slots, kv_dim] uint8)."""
+    _check_bf16_2d(k, "k")
+    _check_bf16_2d(v, "v")
+    tokens, dim = k.shape
+    fp8rl_kv_append(k, v, tokens, dim, k.stride(0), v.stride(0), slot_mapping, k_cache, v_cache,
+                    k_cache.stride(0), k_cache.shape[0], scales, stream)
 
 
 class HostWeightSync:

@@ -127,6 +127,43 @@ __device__ __forceinline__ int scale_ue8m0_exponent(float amax) {
 // 2^-e as an fp32 (e in [-126, 127] gives a normal number; -127 -> 2^127)
 __device__ __forceinline__ float exp2_neg(int e) { return __int_as_float((127 - e) << 23); }
 
+// ------------------------------------------------------------------ eight values
+
+// 8 bf16 (one uint4) -> 8 E4M3 codes (two 32-bit words), fp32-scale variant:
+// IEEE division for tiny scales, else the three-operation division by the
+// block's correctly rounded reciprocal rcp (same result, see div_by_scale).
+__device__ __forceinline__ uint2 quant8_div(uint4 v, float s, float rcp) {
+  uint2 r;
+  if (s >= kFastDivMinScale) {
+    const uint64_t s2 = pair_of(s, s), nr2 = pair_of(-rcp, -rcp);
+    r.x = e4m3x2_pair(div_by_scale_pair(v.x, s2, nr2)) | (e4m3x2_pair(div_by_scale_pair(v.y, s2, nr2)) << 16);
+    r.y = e4m3x2_pair(div_by_scale_pair(v.z, s2, nr2)) | (e4m3x2_pair(div_by_scale_pair(v.w, s2, nr2)) << 16);
+  } else {
+    r.x = e4m3x2(__fdiv_rn(bf16_lo(v.x), s), __fdiv_rn(bf16_hi(v.x), s)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(v.y), s), __fdiv_rn(bf16_hi(v.y), s)) << 16);
+    r.y = e4m3x2(__fdiv_rn(bf16_lo(v.z), s), __fdiv_rn(bf16_hi(v.z), s)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(v.w), s), __fdiv_rn(bf16_hi(v.w), s)) << 16);
+  }
+  return r;
+}
+
+// the same with an exact power-of-two multiplier (UE8M0 variant)
+__device__ __forceinline__ uint2 quant8_mul(uint4 v, float f) {
+  const uint64_t f2 = pair_of(f, f);
+  auto one = [&](uint32_t w) { return e4m3x2_pair(pair_mul(pair_of(bf16_lo(w), bf16_hi(w)), f2)); };
+  uint2 r;
+  r.x = one(v.x) | (one(v.y) << 16);
+  r.y = one(v.z) | (one(v.w) << 16);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t absmax_u4(uint32_t acc, uint4 v) {
+  acc = absmax_bf16x2(acc, v.x);
+  acc = absmax_bf16x2(acc, v.y);
+  acc = absmax_bf16x2(acc, v.z);
+  return absmax_bf16x2(acc, v.w);
+}
+
 // ------------------------------------------------------------------ errors
 
 // bits recorded in a device error word

@@ -131,6 +131,43 @@ FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int64_t m, int6
                                              fp8rl_scale_fmt fmt, void* stream);
 
 /*
+ * FP8 KV cache, per-step scale calibration ("Method steps", step 3: the
+ * K/V quantisation scales are recomputed from the first forward of every RL
+ * step, before its rollout, so that they follow the freshly synced weights).
+ * One fp32 scale per tensor (the pages leave the granularity open; per tensor
+ * is the plain reading): scale = amax / 448 over the calibration pass, 1.0 for
+ * an all-zero tensor.
+ *   k_bf16, v_bf16  device, bf16 [tokens][kv_dim], row strides ldk, ldv
+ *   q_bf16          device, bf16 [tokens][q_dim] (row stride ldq), or null
+ *   d_scales        device, float [3] (q given) or [2]: K, V (, Q) scales;
+ *                   written on the stream, never read back on the host
+ * Errors: INVALID_ARG (negative sizes, short strides, null pointers),
+ *         ALIGNMENT (element alignment), CUDA.
+ */
+FP8RL_API fp8rl_status fp8rl_kv_calibrate(const void* k_bf16, const void* v_bf16, const void* q_bf16,
+                                          int64_t tokens, int64_t kv_dim, int64_t ldk, int64_t ldv,
+                                          int64_t q_dim, int64_t ldq, float* d_scales, void* stream);
+
+/*
+ * Quantised append to the FP8 KV cache: row t of K and V, divided by the
+ * calibrated scale (IEEE fp32 quotient), rounded to nearest-even E4M3 and
+ * saturated at +-448, is written to cache row d_slot_mapping[t] (the flat
+ * slot index of a paged cache: block * block_size + offset).  Slots outside
+ * [0, num_slots), e.g. -1 for padding, are skipped; slot values are device
+ * data and are not read on the host.
+ *   k_bf16, v_bf16  device, bf16 [tokens][kv_dim], row strides ldk, ldv
+ *   d_slot_mapping  device, int32 [tokens]
+ *   k_cache, v_cache device, E4M3 [num_slots][ld_cache]
+ *   d_scales        device, float [2]: the K and V scales of fp8rl_kv_calibrate
+ * Rows that are 16-byte aligned go through the vector path; any layout is
+ * accepted.  Errors: INVALID_ARG, ALIGNMENT (element alignment), CUDA.
+ */
+FP8RL_API fp8rl_status fp8rl_kv_append(const void* k_bf16, const void* v_bf16, int64_t tokens, int64_t kv_dim,
+                                       int64_t ldk, int64_t ldv, const int32_t* d_slot_mapping, void* k_cache,
+                                       void* v_cache, int64_t ld_cache, int64_t num_slots, const float* d_scales,
+                                       void* stream);
+
+/*
  * Block-scaled W8A8 GEMM: Y = X W^T with E4M3 operands, fp32 accumulation per
  * 128-wide K chunk on the tensor cores, the two chunk scales applied in fp32,
  * and one bf16 round-to-nearest-even at the end ("Core method": W8A8
