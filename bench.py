@@ -38,6 +38,37 @@ METRIC = "weight-sync quant GB/s; W8A8 block-scaled GEMM TFLOPS; % of roofline, 
 UNIT = "GB/s"
 WORKLOAD = "qwen3-8b-layer"
 STEP_M = 8192          # tokens in the step's forward batch
+
+# DRAM bytes (read + write) per launch of the dominant kernel, taken from one
+# ncu capture of the same launch (profiles/gemm_blockscaled_gate_up_8192x24576x4096.md).
+# Reported only while the GEMM's sources are those the capture was taken with.
+TRAFFIC = {
+    "gemm_gate_up": {
+        "bytes": 143.554048e6 + 375.021824e6,
+        "sources": {
+            "gemm.cu": "e39b93ef1c1fb9bdd221562bbb92bbbb9317c61a85455eee8eae7421d3e8a9dc",
+            "ptx.cuh": "613b01290ee01f74857e5a4258a8635bbae7f4fdd53931a2c5771ba86a9391b5",
+            "common.cuh": "ce22f13b50d69d05f583fb60eb22375700c10e0326d46e23e9ac29b79ecfa620",
+        },
+    },
+}
+
+
+def captured_traffic(kernel: str):
+    """The captured DRAM bytes of `kernel`, or None if its sources changed since."""
+    import hashlib
+    entry = TRAFFIC.get(kernel)
+    if entry is None:
+        return None
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "fp8_w8a8_rollout_gb300", "csrc")
+    for name, digest in entry["sources"].items():
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return entry["bytes"]
 MOE_T = 4096           # tokens of the MoE layer (x top-8 = 32768 grouped rows)
 L2_BYTES = 129 * 2 ** 20
 
@@ -715,7 +746,7 @@ def main_ours(args):
     dominant = max(roofs, key=lambda k: roofs[k]["ms"])
     d = roofs[dominant]
     roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
-                "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                "unit": d["unit"], "frac": d["frac"], "traffic": captured_traffic(dominant),
                 "peak_source": f"{peaks['source']} ({'hbm_gbs' if d['bound'] == 'hbm' else '2 x bf16_tflops_sustained'})"}
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
