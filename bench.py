@@ -730,11 +730,7 @@ def main_ours(args):
         raise RuntimeError(f"device reported {fp8rl.STATUS.get(status, status)}")
     sync_ms = timer.avg_ms("weight_sync")
     wbytes = sum(wq_bytes(*w.shape) for w in inp["weights"])
-    t = torch.tensor([total_ms, sync_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, sync_ms = float(t[0]), float(t[1])
-    value = world * wbytes / sync_ms / 1e6
+    total_ms, sync_ms, value = aggregate_over_ranks(dist, torch, total_ms, sync_ms, wbytes, world, dev)
 
     if rank != 0:
         if world > 1:
@@ -795,6 +791,17 @@ def main_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def aggregate_over_ranks(dist, torch, total_ms, sync_ms, wbytes, world, device):
+    """Replicas (weak scaling): the timed region's and the weight-sync phase's
+    times are the maximum over ranks; the value is the bytes all ranks synced
+    divided by that time.  Returns (total_ms, sync_ms, GB/s)."""
+    t = torch.tensor([total_ms, sync_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, sync_ms = float(t[0]), float(t[1])
+    return total_ms, sync_ms, world * wbytes / sync_ms / 1e6
 
 
 def main_reference(args):

@@ -39,12 +39,12 @@
  *      128 columns); scales are stored K-group-major: scale[g][m].
  *  R7  Ragged edges: amax is taken over the valid elements of a partial
  *      block or group only.
- *  R8  Fused gate-up path (a "next" step: act-quant fused into the producing
+ *  R12 Fused gate-up path (a "next" step: act-quant fused into the producing
  *      GEMM): the SwiGLU output SiLU(gate) * up is kept in fp32 (never rounded
  *      to bf16) and quantised in 1x128 groups by the same steps (R1-R6) as a
  *      bf16 activation; "Where Rounding Happens Matters", "the overall
  *      scheme".  The fp64 SiLU lives in the Python wrapper.
- *  R9  KV cache (a "next" step; "Method steps", step 3: the K/V quantisation
+ *  R13 KV cache (a "next" step; "Method steps", step 3: the K/V quantisation
  *      scales are recomputed from the first forward of every RL step, before
  *      its rollout): one fp32 scale per tensor (the pages do not fix the
  *      granularity; per tensor is the plainest reading), scale = amax / 448
@@ -449,7 +449,7 @@ ORACLE_API int oracle_quant_group_f32(const float* x, int64_t m, int64_t k, int6
 }
 
 /* ------------------------------------------------------------------------ */
-/* KV cache: per-step per-tensor calibration and quantised append (R9)       */
+/* KV cache: per-step per-tensor calibration and quantised append (R13)      */
 /* ------------------------------------------------------------------------ */
 
 static float tensor_amax_bf16(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld)
