@@ -804,14 +804,24 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           if (lane == 0) mbar_arrive(smem_u32(&sempty[q]));  // the values are in registers
           if (warp_idle) continue;  // every row of this warp is past the segment
           const uint32_t taddr = t_lane + (buf * C::kGroup + j) * BN;
+          if constexpr (!C::kSplitRegs && EPI == 0 && C::kCols == 64) {
+            // registers to spare (no split): the chunk's 64 columns in one
+            // TMEM round trip instead of two
+            const uint64_t f2 = f32x2(f, f);
+            uint64_t v[32];
+            tmem_ld_32x32b_x64_pairs(taddr, v);
 #pragma unroll
-          for (int cc = 0; cc < C::kCols / 32; ++cc) {
-            const float fc = cc == 0 ? f : f_up;
-            const uint64_t f2 = f32x2(fc, fc);
-            uint64_t v[16];
-            tmem_ld_32x32b_x32_pairs(taddr + cc * (EPI ? 128 : 32), v);
+            for (int q = 0; q < 32; ++q) acc[q] = fma_f32x2(v[q], f2, acc[q]);
+          } else {
 #pragma unroll
-            for (int q = 0; q < 16; ++q) acc[cc * 16 + q] = fma_f32x2(v[q], f2, acc[cc * 16 + q]);
+            for (int cc = 0; cc < C::kCols / 32; ++cc) {
+              const float fc = cc == 0 ? f : f_up;
+              const uint64_t f2 = f32x2(fc, fc);
+              uint64_t v[16];
+              tmem_ld_32x32b_x32_pairs(taddr + cc * (EPI ? 128 : 32), v);
+#pragma unroll
+              for (int q = 0; q < 16; ++q) acc[cc * 16 + q] = fma_f32x2(v[q], f2, acc[cc * 16 + q]);
+            }
           }
         }
         tc_fence_before();
@@ -1001,27 +1011,39 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   }
   if (SPLITK) {
     // sum the cluster's partial tiles: rank `split` owns a run of 8-column
-    // chunks; ranks are added in a fixed order, then rounded to bf16 once
+    // chunks of every valid row; the (row, chunk) items are spread over all
+    // epilogue threads (neighbouring threads take neighbouring chunks), each
+    // issues every rank's loads before adding them in rank order, then rounds
+    // to bf16 once
     cluster_sync();
     if (warp >= 4) {
-      const int quad = warp & 3, slice = (warp - 4) >> 2;
-      const int r = quad * 32 + lane;
       const TileRows tr = tile_rows(a, blockIdx.x, lane);
-      const int grow = tr.row0 + r;
+      const int rows = min(kBM, tr.seg_end - tr.row0);
       const int n0 = blockIdx.y * BN;
-      constexpr int kChunks = BN / 8, kSlices = C::kEpiWarps / 4;
+      constexpr int kChunks = BN / 8;
       const int ch_lo = kChunks * split / splits, ch_hi = kChunks * (split + 1) / splits;
-      if (grow < tr.seg_end && !*abortv) {
-        const uint32_t prow = smem_u32(reinterpret_cast<float*>(base_ptr) + r * C::kPartPitch);
-        for (int ch = ch_lo + slice; ch < ch_hi; ch += kSlices) {
+      const int nch = ch_hi - ch_lo;
+      const uint32_t part0 = smem_u32(base_ptr);
+      if (!*abortv && nch > 0) {
+        for (int item = threadIdx.x - 128; item < rows * nch; item += C::kEpiWarps * 32) {
+          const int r = item / nch, ch = ch_lo + (item - r * nch);
+          const uint32_t src = part0 + (uint32_t)(r * C::kPartPitch + ch * 8) * 4u;
+          float4 u[8], w[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < splits) {
+              const uint32_t ra = mapa_shared(src, (uint32_t)q);
+              u[q] = ld_dsmem_f32x4(ra);
+              w[q] = ld_dsmem_f32x4(ra + 16);
+            }
           float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int q = 0; q < splits; ++q) {
-            const uint32_t ra = mapa_shared(prow + ch * 32, (uint32_t)q);
-            const float4 u = ld_dsmem_f32x4(ra), w = ld_dsmem_f32x4(ra + 16);
-            x[0] += u.x; x[1] += u.y; x[2] += u.z; x[3] += u.w;
-            x[4] += w.x; x[5] += w.y; x[6] += w.z; x[7] += w.w;
-          }
-          *reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + ch * 8) =
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q < splits) {
+              x[0] += u[q].x; x[1] += u[q].y; x[2] += u[q].z; x[3] += u[q].w;
+              x[4] += w[q].x; x[5] += w[q].y; x[6] += w[q].z; x[7] += w[q].w;
+            }
+          *reinterpret_cast<uint4*>(a.y + (int64_t)(tr.row0 + r) * a.n + n0 + ch * 8) =
               make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                          pack_bf16x2(x[6], x[7]));
         }
@@ -1152,7 +1174,7 @@ struct KernelState {
   bool ready = false;
   bool regs_ok = false;
   bool attr_ok = false;
-  int8_t cluster_fits[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  int cluster_capacity[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // clusters resident at once
 };
 
 template <int BN, int AROWS, bool UE8M0, int MODE, int EPI>
@@ -1198,12 +1220,15 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
     }
     if (!ks.attr_ok) return FP8RL_ERR_CUDA;
     if (!ks.regs_ok) return FP8RL_ERR_UNSUPPORTED;  // the caller retries with 128-wide tiles
-    // the largest split count not above the request whose clusters can be resident
+    // the largest split count not above the request whose clusters (one per
+    // tile) are all resident at once: measured on GB300, clusters of 3 fit 46
+    // at a time, so 48 tiles split three ways ran as two waves
+    const int64_t cluster_count = m_tiles_bound * (args.n / BN);
     while (SPLITK && splits > 1) {
-      if (ks.cluster_fits[splits] < 0)
-        ks.cluster_fits[splits] =
-            max_active_clusters(kernel, dim3(1, 1, (unsigned)splits), C::kThreads, C::kSmemBytes, splits) >= 1;
-      if (ks.cluster_fits[splits]) break;
+      if (ks.cluster_capacity[splits] < 0)
+        ks.cluster_capacity[splits] =
+            max_active_clusters(kernel, dim3(1, 1, (unsigned)splits), C::kThreads, C::kSmemBytes, splits);
+      if (ks.cluster_capacity[splits] >= cluster_count) break;
       --splits;
     }
   }

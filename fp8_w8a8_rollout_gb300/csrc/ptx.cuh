@@ -249,6 +249,52 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32_pairs(uint32_t taddr, uint64_
       : "memory");
 }
 
+// 64 consecutive columns of this thread's lane in one load and one wait,
+// returned as 32 packed fp32 pairs (columns 2j, 2j+1)
+__device__ __forceinline__ void tmem_ld_32x32b_x64_pairs(uint32_t taddr, uint64_t (&p)[32]) {
+  asm volatile(
+      "{\n\t.reg .b32 r<64>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31, r32, r33, r34, r35, r36, r37, r38, r39, r40, r41, r42, r43, r44, r45, r46, r47, r48, r49, r50, r51, r52, r53, r54, r55, r56, r57, r58, r59, r60, r61, r62, r63}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {r0, r1};\n\t"
+      "mov.b64 %1, {r2, r3};\n\t"
+      "mov.b64 %2, {r4, r5};\n\t"
+      "mov.b64 %3, {r6, r7};\n\t"
+      "mov.b64 %4, {r8, r9};\n\t"
+      "mov.b64 %5, {r10, r11};\n\t"
+      "mov.b64 %6, {r12, r13};\n\t"
+      "mov.b64 %7, {r14, r15};\n\t"
+      "mov.b64 %8, {r16, r17};\n\t"
+      "mov.b64 %9, {r18, r19};\n\t"
+      "mov.b64 %10, {r20, r21};\n\t"
+      "mov.b64 %11, {r22, r23};\n\t"
+      "mov.b64 %12, {r24, r25};\n\t"
+      "mov.b64 %13, {r26, r27};\n\t"
+      "mov.b64 %14, {r28, r29};\n\t"
+      "mov.b64 %15, {r30, r31};\n\t"
+      "mov.b64 %16, {r32, r33};\n\t"
+      "mov.b64 %17, {r34, r35};\n\t"
+      "mov.b64 %18, {r36, r37};\n\t"
+      "mov.b64 %19, {r38, r39};\n\t"
+      "mov.b64 %20, {r40, r41};\n\t"
+      "mov.b64 %21, {r42, r43};\n\t"
+      "mov.b64 %22, {r44, r45};\n\t"
+      "mov.b64 %23, {r46, r47};\n\t"
+      "mov.b64 %24, {r48, r49};\n\t"
+      "mov.b64 %25, {r50, r51};\n\t"
+      "mov.b64 %26, {r52, r53};\n\t"
+      "mov.b64 %27, {r54, r55};\n\t"
+      "mov.b64 %28, {r56, r57};\n\t"
+      "mov.b64 %29, {r58, r59};\n\t"
+      "mov.b64 %30, {r60, r61};\n\t"
+      "mov.b64 %31, {r62, r63};\n\t"
+      "}"
+      : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]), "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]), "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]), "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ clusters
