@@ -44,10 +44,10 @@ STEP_M = 8192          # tokens in the step's forward batch
 # Reported only while the GEMM's sources are those the capture was taken with.
 TRAFFIC = {
     "gemm_gate_up": {
-        "bytes": 143.554048e6 + 375.021824e6,
+        "bytes": 142.233856e6 + 374.807552e6,
         "sources": {
-            "gemm.cu": "e39b93ef1c1fb9bdd221562bbb92bbbb9317c61a85455eee8eae7421d3e8a9dc",
-            "ptx.cuh": "613b01290ee01f74857e5a4258a8635bbae7f4fdd53931a2c5771ba86a9391b5",
+            "gemm.cu": "853a1b4464eafdd7fa4f70a5755ecc8a2e2f19dab366aa90c6843fe70a561ec1",
+            "ptx.cuh": "cc21b686c76ecef323c84f536a43bd0f7ca9e54117acd193a2f79a8f60e5685e",
             "common.cuh": "ce22f13b50d69d05f583fb60eb22375700c10e0326d46e23e9ac29b79ecfa620",
         },
     },
