@@ -15,7 +15,9 @@ Recipes (every tensor has its own stream id under one seed):
   [1536, 2048] and a down [2048, 768] bf16 matrix ~ N(0, 0.02); T tokens route
   to top-8 experts by the softmax of N(0, 1) router logits (ties go to the lower
   expert index).  The indices are fixed integers, replayed as the R3 post
-  describes, and token rows are grouped by expert in increasing token order.
+  describes; the combine weights are the chosen experts' renormalised
+  probabilities.  Grouping the token rows by expert is the dispatch step,
+  not part of this module.
 
 Small inputs are drawn with numpy on the host (``device='cpu'``); the
 multi-gigabyte benchmark inputs are drawn with torch's generator directly on
@@ -153,30 +155,26 @@ def qwen3_8b_layer(layer: int = 0, seed: int = 0, device="cpu", shapes=QWEN3_8B_
 
 @dataclass
 class Routing:
-    topk: np.ndarray        # int32 [T, 8] expert indices (fixed, replayed)
-    offsets: np.ndarray     # int32 [E + 1], exclusive prefix sum of rows per expert
-    token_of_row: np.ndarray  # int32 [T * 8], which token each grouped row came from
+    topk: np.ndarray   # int32 [T, k] expert indices (fixed, replayed)
+    gate: np.ndarray   # fp32 [T, k] the router's weights of those experts (renormalised over the k)
 
 
 def moe_routing(tokens: int = MOE_TOKENS, experts: int = MOE_EXPERTS, topk: int = MOE_TOPK,
                 seed: int = 0, layer: int = 0) -> Routing:
     """Top-k experts per token from softmax(N(0,1) logits); lower index wins ties.
 
-    The indices are drawn once and then treated as fixed integers: the grouped
-    GEMM never sees the logits."""
+    The indices are drawn once and then treated as fixed integers (the
+    dispatch never sees the logits).  The combine weights are the chosen
+    experts' softmax probabilities renormalised to sum to 1, as the MoE layer
+    of Qwen3-30B-A3B forms them."""
     logits = _np_rng(seed, "router", layer).standard_normal((tokens, experts))
     p = np.exp(logits - logits.max(axis=1, keepdims=True))
     p /= p.sum(axis=1, keepdims=True)
     order = np.argsort(-p, axis=1, kind="stable")  # stable: equal p keeps the lower index first
     idx = order[:, :topk].astype(np.int32)
-    counts = np.bincount(idx.reshape(-1), minlength=experts)
-    offsets = np.zeros(experts + 1, dtype=np.int32)
-    offsets[1:] = np.cumsum(counts)
-    # rows of expert e: the (token, slot) pairs routed to e, in increasing token order
-    flat_expert = idx.reshape(-1)
-    flat_token = np.repeat(np.arange(tokens, dtype=np.int32), topk)
-    perm = np.argsort(flat_expert, kind="stable")
-    return Routing(topk=idx, offsets=offsets, token_of_row=flat_token[perm])
+    w = np.take_along_axis(p, order[:, :topk], axis=1)
+    w = (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+    return Routing(topk=idx, gate=w)
 
 
 def routing_with_counts(counts, seed: int = 0) -> np.ndarray:

@@ -5,10 +5,14 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 its Python binding) never imports, links or calls it, and it shares no code
 with them.
 
-The arithmetic lives in ``oracle.c`` (plain C, fp64 where the pages leave the
-precision open); this module only compiles it with gcc and marshals numpy
-arrays.  See the header of ``oracle.c`` for what each function follows and the
-readings taken where the FP8-RL pages are silent.
+The quantisation, GEMM and KV-cache arithmetic lives in ``oracle.c`` (plain
+C, fp64 where the pages leave the precision open); this module compiles it
+with gcc and marshals numpy arrays.  See the header of ``oracle.c`` for what
+each function follows and the readings taken where the FP8-RL pages are
+silent.  The SwiGLU helpers below, the MoE dispatch/combine
+(``moe_routing.py``) and the TIS weight / mismatch KL (``tis.py``) are plain
+fp64 numpy and Python loops, each module with its own header of citations
+and readings.
 """
 from __future__ import annotations
 
@@ -367,3 +371,16 @@ def dequantize(q: np.ndarray, scale: np.ndarray, block_rows: int, block_cols: in
     r_idx = np.arange(q.shape[0]) // block_rows
     c_idx = np.arange(q.shape[1]) // block_cols
     return vals * s[r_idx][:, c_idx]
+
+
+from .moe_routing import combine as moe_combine  # noqa: E402
+from .moe_routing import dispatch_plan as moe_dispatch_plan  # noqa: E402
+from .moe_routing import gather_rows as moe_gather_rows  # noqa: E402
+from .tis import TIS_CLIP, mismatch_kl, tis_weights  # noqa: E402
+
+
+def moe_dispatch_quant(x_bf16_bits: np.ndarray, token_of_row: np.ndarray, fmt: int = SCALE_FP32):
+    """Grouped activation of the dispatch: gathered token rows, quantised in
+    1x128 groups.  Returns (codes [R, K], scales [K/128, R], live rows)."""
+    from .moe_routing import dispatch_quant
+    return dispatch_quant(x_bf16_bits, token_of_row, fmt, quant_act_group)

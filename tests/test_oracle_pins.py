@@ -443,19 +443,12 @@ def test_grouped_gemm_rejects_bad_offsets():
         oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, np.array([0, 1, 3], np.int32))
 
 
-def test_routing_replay_offsets_are_prefix_sums():
+def test_routing_generator_draws_distinct_topk_with_normalised_gates():
     r = synth.moe_routing(tokens=64, experts=16, topk=4, seed=0)
-    assert r.topk.shape == (64, 4)
-    # distinct experts per token, offsets consistent with the indices
+    assert r.topk.shape == (64, 4) and r.gate.shape == (64, 4)
     assert all(len(set(row)) == 4 for row in r.topk.tolist())
-    counts = np.bincount(r.topk.reshape(-1), minlength=16)
-    assert np.array_equal(np.diff(r.offsets), counts)
-    assert r.offsets[-1] == 64 * 4
-    # rows of one expert come in increasing token order
-    for e in range(16):
-        toks = r.token_of_row[r.offsets[e]:r.offsets[e + 1]]
-        assert np.all(np.diff(toks) > 0)
-        assert all(e in r.topk[t] for t in toks)
+    assert np.allclose(r.gate.sum(axis=1), 1.0, atol=1e-6)
+    assert np.all(np.diff(r.gate, axis=1) <= 0)  # descending probability
 
 
 # --------------------------------------------------------------------------- fused gate-up path (fp32 groups, SwiGLU)
@@ -603,3 +596,137 @@ def test_kv_append_codes_slots_and_saturation():
     t, c = np.unravel_index(np.argmax(np.abs(k[:20].float().numpy())), (20, dim))
     if 0 <= slots[t] < slots_total:
         assert kc[slots[t], c] & 0x7F == 0x7E
+
+
+# --------------------------------------------------------------------------- MoE dispatch / combine (routing replay)
+
+def _golden_list(g, key, dtype):
+    return np.array([dtype(v) for v in g[key].split(",")])
+
+
+def test_dispatch_plan_and_combine_worked_example():
+    g = read_golden("moe_dispatch_worked_example.txt")
+    idx = _golden_list(g, "indices", int).reshape(4, 2)
+    off, rop, tor = oracle.moe_dispatch_plan(idx, int(g["experts"]))
+    assert off.tolist() == _golden_list(g, "offsets", int).tolist()
+    assert rop.tolist() == _golden_list(g, "row_of_pair", int).tolist()
+    assert tor.tolist() == _golden_list(g, "token_of_row", int).tolist()
+    y = np.array([[r + 1, -(r + 1) / 2] for r in range(8)])
+    out = oracle.moe_combine(y, rop, _golden_list(g, "gate", float).reshape(4, 2))
+    assert out.reshape(-1).tolist() == _golden_list(g, "combine_out", float).tolist()
+
+
+@pytest.mark.parametrize("tokens,k,experts,drop", [(64, 8, 16, 0.0), (37, 3, 5, 0.2), (1, 1, 1, 0.0), (0, 8, 4, 0.0)])
+def test_dispatch_plan_is_the_stable_sort_by_expert(tokens, k, experts, drop):
+    """Equal to numpy's stable argsort of the flattened expert ids (the
+    special case the plan reduces to), with dropped pairs left out."""
+    rng = np.random.default_rng(tokens * 7 + k)
+    idx = rng.integers(0, experts, size=(tokens, k))
+    idx[rng.random((tokens, k)) < drop] = -1
+    idx[rng.random((tokens, k)) < drop / 2] = experts + 3  # also out of range
+    off, rop, tor = oracle.moe_dispatch_plan(idx, experts)
+    flat = idx.reshape(-1)
+    live = np.flatnonzero((flat >= 0) & (flat < experts))
+    order = live[np.argsort(flat[live], kind="stable")]
+    assert np.array_equal(np.diff(off), np.bincount(flat[live], minlength=experts))
+    assert off[-1] == live.size
+    assert np.array_equal(rop[order], np.arange(live.size))  # pair -> row
+    assert np.all(rop[np.setdiff1d(np.arange(flat.size), live)] == -1)
+    assert np.array_equal(tor[:live.size], order // k) and np.all(tor[live.size:] == -1)
+
+
+def test_dispatch_quant_rows_equal_each_token_row_quantised_alone():
+    tokens, k, experts, hidden = 12, 3, 5, 300
+    rng = np.random.default_rng(3)
+    idx = rng.integers(-1, experts, size=(tokens, k))
+    x = synth.normal_bf16((tokens, hidden), 1.0, 7, "pin-dispatch")
+    xb = synth.bf16_bits(x)
+    _, _, tor = oracle.moe_dispatch_plan(idx, experts)
+    q, s, live = oracle.moe_dispatch_quant(xb, tor)
+    for r in np.flatnonzero(live):
+        qr, sr = oracle.quant_act_group(xb[tor[r]:tor[r] + 1])
+        assert np.array_equal(q[r], qr[0]) and np.array_equal(s[:, r], sr[:, 0])
+
+
+def test_combine_one_hot_selects_rows_and_ignores_slot_order():
+    tokens, k, experts, n = 10, 4, 6, 7
+    rng = np.random.default_rng(4)
+    idx = np.stack([rng.permutation(experts)[:k] for _ in range(tokens)])
+    _, rop, _ = oracle.moe_dispatch_plan(idx, experts)
+    y = rng.standard_normal((tokens * k, n))
+    hot = np.zeros((tokens, k))
+    hot[np.arange(tokens), rng.integers(0, k, tokens)] = 1.0
+    out = oracle.moe_combine(y, rop, hot)
+    sel = rop.reshape(tokens, k)[hot == 1]
+    assert np.array_equal(out, y[sel])
+    # permuting each token's slots (indices and gates together) changes nothing but rounding
+    gate = rng.random((tokens, k))
+    perm = np.stack([rng.permutation(k) for _ in range(tokens)])
+    _, rop_p, _ = oracle.moe_dispatch_plan(np.take_along_axis(idx, perm, 1), experts)
+    # the same (token, expert) pair owns the same row in both plans, as rows
+    # are ordered by token within a segment and a token holds an expert once
+    a = oracle.moe_combine(y, rop, gate)
+    b = oracle.moe_combine(y, rop_p, np.take_along_axis(gate, perm, 1))
+    assert np.allclose(a, b, rtol=1e-14, atol=1e-14)
+
+
+def test_dispatch_then_identity_experts_then_combine_returns_tokens():
+    """With every expert the identity and gates summing to 1, the round trip
+    gives back each token row up to its 1x128 quantisation error."""
+    tokens, k, experts, hidden = 16, 4, 8, 256
+    r = synth.moe_routing(tokens, experts, k, seed=5)
+    x = synth.normal_bf16((tokens, hidden), 1.0, 8, "pin-roundtrip")
+    xb = synth.bf16_bits(x)
+    _, rop, tor = oracle.moe_dispatch_plan(r.topk, experts)
+    q, s, _ = oracle.moe_dispatch_quant(xb, tor)
+    y = oracle.dequantize(q, s.T, 1, 128)
+    out = oracle.moe_combine(y, rop, r.gate.astype(np.float64))
+    xf = x.float().numpy().astype(np.float64)
+    # per element: half an E4M3 ulp at that magnitude (<= 2^-4 relative) times
+    # the weight, plus the subnormal floor scale * 2^-10, summed over slots
+    smax = s.max()
+    assert np.all(np.abs(out - xf) <= 2.0 ** -4 * np.abs(xf) + smax * 2.0 ** -10 + 1e-6)
+
+
+# --------------------------------------------------------------------------- TIS weight and mismatch KL
+
+def test_tis_weight_closed_forms_and_truncation():
+    lr = np.zeros(6, np.float32)
+    lt = np.array([0.0, math.log(1.5), math.log(3.0), -50.0, math.log(2.0) + 1e-3, 10.0], np.float32)
+    w = oracle.tis_weights(lt, lr)
+    assert w[0] == 1.0
+    assert abs(w[1] - 1.5) < 1e-6 and w[2] == 2.0 and w[4] == 2.0 and w[5] == 2.0
+    assert abs(w[3] - math.exp(-50.0)) < 1e-30
+    # the ratio of probabilities, not of log-probabilities: shifting both sides
+    # by the same amount leaves it unchanged
+    assert np.allclose(oracle.tis_weights(lt - 3.0, lr - 3.0), w, rtol=1e-6)
+    # masked-out tokens weigh 0
+    mask = np.array([1, 0, 1, 0, 1, 1], np.uint8)
+    assert np.array_equal(oracle.tis_weights(lt, lr, mask), np.where(mask == 1, w, 0.0))
+
+
+def test_mismatch_kl_constant_gap_mask_and_empty():
+    lt = np.full(10, -2.0, np.float32)
+    lr = np.full(10, -1.75, np.float32)
+    mean, total, count = oracle.mismatch_kl(lt, lr)
+    assert (mean, total, count) == (0.25, 2.5, 10)
+    mask = np.zeros(10, np.uint8)
+    assert oracle.mismatch_kl(lt, lr, mask) == (0.0, 0.0, 0)
+    mask[[1, 4]] = 1
+    lr2 = lr.copy()
+    lr2[0] = 100.0  # masked out: no effect
+    assert oracle.mismatch_kl(lt, lr2, mask) == (0.25, 0.5, 2)
+
+
+def test_mismatch_kl_estimates_kl_of_rollout_from_training_policy():
+    """Tokens sampled from the rollout policy p: the mean of log p - log q
+    converges to KL(p || q), a closed form over the vocabulary."""
+    rng = np.random.default_rng(11)
+    vocab, n = 50, 400_000
+    p = rng.dirichlet(np.ones(vocab))
+    q = 0.8 * p + 0.2 * rng.dirichlet(np.ones(vocab))
+    kl = float(np.sum(p * (np.log(p) - np.log(q))))
+    tok = rng.choice(vocab, size=n, p=p)
+    mean, _, count = oracle.mismatch_kl(np.log(q)[tok], np.log(p)[tok])
+    sd = float(np.std(np.log(p)[tok] - np.log(q)[tok]))
+    assert count == n and abs(mean - kl) < 5 * sd / math.sqrt(n)
