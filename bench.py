@@ -80,12 +80,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="all",
-                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused,kv (or all/none)")
+                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused,kv,moe_layer,tis "
+                         "(or all/none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--case", default=None,
                     help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
-                         "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt], kv:TOKENS")
+                         "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt], kv:TOKENS, "
+                         "moe_plan, moe_dispatch, moe_combine, tis[:RESPONSES]")
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
     ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
@@ -272,9 +274,7 @@ def build_step_inputs(torch, synth, fp8rl, dev, seed, have_gemm):
         y = torch.empty((STEP_M, n), dtype=torch.bfloat16, device=dev)
         inp["gemms"].append((name, n, k, x, xq, sx, wq, sw, y))
     # MoE expert pair, one layer
-    r = synth.moe_routing(MOE_T, synth.MOE_EXPERTS, synth.MOE_TOPK, seed, 0)
-    offsets = torch.from_numpy(r.offsets).to(dev)
-    rows = int(r.offsets[-1])
+    _, offsets, _, _, rows = moe_plan_for(torch, synth, fp8rl, dev, seed)
     moe = {"offsets": offsets, "rows": rows, "pairs": []}
     for which, n, k in (("gate_up", 2 * synth.MOE_INTER, synth.MOE_HIDDEN),
                         ("down", synth.MOE_HIDDEN, synth.MOE_INTER)):
@@ -395,6 +395,24 @@ def e2e_weight_sync(torch, fp8rl, inp, stream, steps):
             "h2d_bytes_per_step": r["h2d_bytes_per_step"], "d2h_bytes_per_step": r["d2h_bytes_per_step"],
             "mode": best, "modes": {m: round(v["value"], 1) for m, v in results.items()},
             "matches_device_result": r["matches_device_result"]}
+
+
+def l2_flusher(torch, dev, mb=512):
+    """A call that reads a buffer 4x the L2 (129 MB), so that the next timed
+    call starts with none of its inputs in L2.  A read leaves clean lines: a
+    flush by writing would leave 129 MB of dirty lines whose write-back the
+    timed kernel would pay for."""
+    buf = torch.ones(mb << 18, dtype=torch.float32, device=dev)
+    return lambda: buf.sum()
+
+
+def moe_plan_for(torch, synth, fp8rl, dev, seed, tokens=None):
+    """The replayed top-8 routing of the Qwen3-30B-A3B-shaped layer and its
+    dispatch plan, made by the library's plan kernels: (routing, offsets,
+    row_of_pair, token_of_row, routed rows)."""
+    r = synth.moe_routing(tokens or MOE_T, synth.MOE_EXPERTS, synth.MOE_TOPK, seed, 0)
+    off, rop, tor = fp8rl.moe_plan(torch.from_numpy(r.topk).to(dev), synth.MOE_EXPERTS)
+    return r, off, rop, tor, int(off[-1].item())
 
 
 def time_loop(torch, fn, iters, warmup, flush=None):
@@ -558,9 +576,7 @@ def fused_mlp_inputs(torch, synth, fp8rl, dev, seed, m, fmt, moe=False):
         inter, k, e = synth.MOE_INTER, synth.MOE_HIDDEN, synth.MOE_EXPERTS
         gate = synth.moe_expert_weights(inter, k, e, seed, 0, "gate", device=dev)
         up = synth.moe_expert_weights(inter, k, e, seed, 0, "up", device=dev)
-        r = synth.moe_routing(MOE_T, e, synth.MOE_TOPK, seed, 0)
-        offsets = torch.from_numpy(r.offsets).to(dev)
-        m = int(r.offsets[-1])
+        _, offsets, _, _, m = moe_plan_for(torch, synth, fp8rl, dev, seed)
         x = synth.normal_bf16((m, k), 1.0, seed, "fused-moe-x", device=dev)
     else:
         inter, k = 12288, 4096
@@ -647,6 +663,78 @@ def section_kv_cache(torch, synth, fp8rl, dev, seed, peaks):
             entry["ms_graph"] = time_graph(torch, fn, 50)
         res[name] = entry
     return res
+
+
+def moe_layer_inputs(torch, synth, fp8rl, dev, seed):
+    """Replayed routing of T = 4096 tokens (top-8 of 128 experts), the plan
+    buffers, the hidden states [T, 2048] bf16, the grouped gate-up input
+    buffers and a down output [T * 8, 2048] bf16 to combine."""
+    t, e, k, h = MOE_T, synth.MOE_EXPERTS, synth.MOE_TOPK, synth.MOE_HIDDEN
+    r = synth.moe_routing(t, e, k, seed, 0)
+    rows = t * k
+    d = {"t": t, "e": e, "k": k, "h": h, "rows": rows,
+         "topk": torch.from_numpy(r.topk).to(dev), "gate": torch.from_numpy(r.gate).to(dev),
+         "ws": torch.empty(fp8rl.fp8rl_moe_plan_workspace_size(t, k, e), dtype=torch.uint8, device=dev),
+         "off": torch.empty(e + 1, dtype=torch.int32, device=dev),
+         "rop": torch.empty(rows, dtype=torch.int32, device=dev),
+         "tor": torch.empty(rows, dtype=torch.int32, device=dev),
+         "x": synth.normal_bf16((t, h), 1.0, seed, "bench-moe-layer-x", device=dev),
+         "xq": torch.empty((rows, h), dtype=torch.uint8, device=dev),
+         "sx": torch.empty((h // 128, rows), dtype=torch.float32, device=dev),
+         "y": synth.normal_bf16((rows, h), 1.0, seed, "bench-moe-layer-y", device=dev),
+         "out": torch.empty((t, h), dtype=torch.bfloat16, device=dev)}
+    d["plan"] = lambda: fp8rl.fp8rl_moe_plan(d["topk"], t, k, e, d["off"], d["rop"], d["tor"], d["ws"],
+                                             d["ws"].numel())
+    d["dispatch"] = lambda: fp8rl.fp8rl_moe_dispatch_quant(d["x"], t, h, h, d["rop"], k, rows, d["xq"], h, d["sx"],
+                                                           0)
+    d["combine"] = lambda: fp8rl.fp8rl_moe_combine(d["y"], h, h, d["rop"], d["gate"], t, k, d["out"], h)
+    d["plan"]()
+    # algorithmic bytes: hidden states read once, codes + scales + row map
+    # written; combine: k expert rows read, one row written, plus the map
+    d["dispatch_bytes"] = 2 * t * h + rows * h + 4 * rows * (h // 128) + 4 * rows
+    d["combine_bytes"] = 2 * rows * h + 2 * t * h + 8 * rows
+    return d
+
+
+def section_moe_layer(torch, synth, fp8rl, dev, seed, peaks):
+    """The MoE layer around the grouped GEMMs (Qwen3-30B-A3B shape, T = 4096,
+    top-8 of 128 experts, hidden 2048): the dispatch plan of the replayed
+    indices, the dispatch with 1x128 quantisation into the grouped gate-up
+    input, and the weighted combine of the down outputs.  The working sets are
+    near or below the L2 size, so L2 is flushed before every timed call."""
+    hbm = peaks["hbm_gbs"]
+    flush = l2_flusher(torch, dev)
+    d = moe_layer_inputs(torch, synth, fp8rl, dev, seed)
+    res = {"tokens": d["t"], "experts": d["e"], "topk": d["k"], "hidden": d["h"], "l2": "flushed before each call"}
+    res["plan"] = {"ms": time_loop(torch, d["plan"], 20, 5, flush), "ms_graph": time_graph(torch, d["plan"], 50),
+                   "launches": 1 if d["rows"] <= 8192 and d["e"] <= 256 else 3}
+    for name in ("dispatch", "combine"):
+        t = time_loop(torch, d[name], 20, 5, flush)
+        b = d[name + "_bytes"]
+        res[name] = {"ms": t, "bytes": b, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / hbm}
+    # context: the plain quantiser over an already-gathered [T * 8, 2048] input
+    rows, h = d["rows"], d["h"]
+    aq = lambda: fp8rl.fp8rl_quant_act_group(d["y"], rows, h, h, d["xq"], h, d["sx"], 0)
+    t = time_loop(torch, aq, 20, 5, flush)
+    res["act_quant_gathered_rows"] = {"ms": t, "gbs": aq_bytes(rows, h) / t / 1e6}
+    return res
+
+
+def section_tis(torch, synth, fp8rl, dev, seed, peaks):
+    """Token-level TIS weights and the mismatch KL over a rollout batch of
+    512 responses x 16384 tokens (8.4 M tokens, 13 bytes each; L2 flushed
+    before every timed call, as the 109 MB working set fits in L2)."""
+    flush = l2_flusher(torch, dev)
+    lt, lr, m = synth.rollout_logprobs(seed=seed, device=dev)
+    n = lt.numel()
+    ws = torch.empty(fp8rl.fp8rl_tis_workspace_size(n), dtype=torch.uint8, device=dev)
+    w = torch.empty(n, dtype=torch.float32, device=dev)
+    kl = torch.empty(3, dtype=torch.float64, device=dev)
+    fn = lambda: fp8rl.fp8rl_tis_weights(lt, lr, m, n, 2.0, w, kl, ws, ws.numel())
+    t = time_loop(torch, fn, 20, 5, flush)
+    b = 13 * n
+    return {"tokens": n, "ms": t, "bytes": b, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"],
+            "launches": 2, "l2": "flushed before each call"}
 
 
 def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt):
@@ -747,7 +835,8 @@ def main_ours(args):
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
     wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
-        {"model", "moe_sync", "sweep", "ue8m0", "fused", "kv"} if args.sections == "all" else set())
+        {"model", "moe_sync", "sweep", "ue8m0", "fused", "kv", "moe_layer", "tis"} if args.sections == "all"
+        else set())
     del inp
     torch.cuda.empty_cache()
     if "model" in wanted:
@@ -762,6 +851,10 @@ def main_ours(args):
         sections["fused_mlp"] = section_fused_mlp(torch, synth, fp8rl, dev, seed, peaks)
     if "kv" in wanted:
         sections["kv_cache_qwen3_8b_layer"] = section_kv_cache(torch, synth, fp8rl, dev, seed, peaks)
+    if "moe_layer" in wanted:
+        sections["moe_dispatch_combine_qwen3_30b_a3b"] = section_moe_layer(torch, synth, fp8rl, dev, seed, peaks)
+    if "tis" in wanted:
+        sections["tis_rollout_512x16384"] = section_tis(torch, synth, fp8rl, dev, seed, peaks)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_sample(synth)
@@ -874,9 +967,7 @@ def main_case(args):
     elif kind == "grouped":
         which = parts[1]
         n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
-        r = synth.moe_routing(MOE_T, synth.MOE_EXPERTS, synth.MOE_TOPK, 0, 0)
-        rows = int(r.offsets[-1])
-        offsets = torch.from_numpy(r.offsets).to(dev)
+        _, offsets, _, _, rows = moe_plan_for(torch, synth, fp8rl, dev, 0)
         wb = synth.moe_expert_weights(n, k, synth.MOE_EXPERTS, 0, 0, which, device=dev)
         wq, sw = fp8rl.quant_weight(wb.view(-1, k))
         wq = wq.view(synth.MOE_EXPERTS, n, k)
@@ -905,6 +996,19 @@ def main_case(args):
         scales = fp8rl.kv_calibrate(k, v)
         fn = lambda: fp8rl.kv_append(k, v, slots, kc, vc, scales)
         work = {"bytes": tokens * KV_DIM * 2 * 3 + tokens * 4}
+    elif kind in ("moe_plan", "moe_dispatch", "moe_combine"):
+        d = moe_layer_inputs(torch, synth, fp8rl, dev, 0)
+        fn = d[kind[4:]]
+        work = {"bytes": d[kind[4:] + "_bytes"]} if kind != "moe_plan" else {}
+    elif kind == "tis":
+        lt, lr, msk = synth.rollout_logprobs(int(parts[1]) if len(parts) > 1 else synth.ROLLOUT_RESPONSES,
+                                             device=dev)
+        n = lt.numel()
+        ws = torch.empty(fp8rl.fp8rl_tis_workspace_size(n), dtype=torch.uint8, device=dev)
+        w = torch.empty(n, dtype=torch.float32, device=dev)
+        kl = torch.empty(3, dtype=torch.float64, device=dev)
+        fn = lambda: fp8rl.fp8rl_tis_weights(lt, lr, msk, n, 2.0, w, kl, ws, ws.numel())
+        work = {"bytes": 13 * n}
     elif kind == "wq":
         fmt = int(parts[2]) if len(parts) > 2 else 0
         layer = [w for _, w in synth.qwen3_8b_layer(0, 0, device=dev)]

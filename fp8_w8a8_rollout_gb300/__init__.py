@@ -90,6 +90,12 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_grouped_gemm_swiglu_quant": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, vp, st, vp],
             "fp8rl_grouped_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, st, vp],
             "fp8rl_e4m3_encode": [vp, i64, vp, vp],
+            "fp8rl_moe_plan_workspace_size": [i64, i64, i64],
+            "fp8rl_moe_plan": [vp, i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp],
+            "fp8rl_moe_dispatch_quant": [vp, i64, i64, i64, vp, i64, i64, vp, i64, vp, st, vp],
+            "fp8rl_moe_combine": [vp, i64, i64, vp, vp, i64, i64, vp, i64, vp],
+            "fp8rl_tis_workspace_size": [i64],
+            "fp8rl_tis_weights": [vp, vp, vp, i64, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
             "fp8rl_debug_set": [i32, i64],
             "fp8rl_sync_status": [vp],
             "fp8rl_status_string": [st],
@@ -100,6 +106,8 @@ def load_library(build_if_missing: bool = False):
             fn.argtypes = args
             fn.restype = st
         lib.fp8rl_status_string.restype = ctypes.c_char_p
+        lib.fp8rl_moe_plan_workspace_size.restype = ctypes.c_size_t
+        lib.fp8rl_tis_workspace_size.restype = ctypes.c_size_t
         lib.fp8rl_version.restype = i32
         _lib = lib
         return lib
@@ -208,6 +216,41 @@ def fp8rl_kv_append(k_bf16, v_bf16, tokens, kv_dim, ldk, ldv, d_slot_mapping, k_
                                        _p(k_cache), _p(v_cache), ld_cache, num_slots, _p(d_scales),
                                        _stream(stream)),
         "fp8rl_kv_append")
+
+
+def fp8rl_moe_plan_workspace_size(tokens, topk, experts) -> int:
+    return int(load_library().fp8rl_moe_plan_workspace_size(tokens, topk, experts))
+
+
+def fp8rl_moe_plan(d_topk, tokens, topk, experts, d_offsets, d_row_of_pair, d_token_of_row, d_workspace,
+                   workspace_bytes, stream=None) -> None:
+    _ok(load_library().fp8rl_moe_plan(_p(d_topk), tokens, topk, experts, _p(d_offsets), _p(d_row_of_pair),
+                                      _p(d_token_of_row), _p(d_workspace), workspace_bytes, _stream(stream)),
+        "fp8rl_moe_plan")
+
+
+def fp8rl_moe_dispatch_quant(x_bf16, tokens, k, ldx, d_row_of_pair, topk, rows, q_e4m3, ldq, x_scale,
+                             fmt=SCALE_FP32, stream=None) -> None:
+    _ok(load_library().fp8rl_moe_dispatch_quant(_p(x_bf16), tokens, k, ldx, _p(d_row_of_pair), topk, rows,
+                                                _p(q_e4m3), ldq, _p(x_scale), fmt, _stream(stream)),
+        "fp8rl_moe_dispatch_quant")
+
+
+def fp8rl_moe_combine(y_bf16, n, ldy, d_row_of_pair, d_gate, tokens, topk, out_bf16, ldo, stream=None) -> None:
+    _ok(load_library().fp8rl_moe_combine(_p(y_bf16), n, ldy, _p(d_row_of_pair), _p(d_gate), tokens, topk,
+                                         _p(out_bf16), ldo, _stream(stream)),
+        "fp8rl_moe_combine")
+
+
+def fp8rl_tis_workspace_size(n) -> int:
+    return int(load_library().fp8rl_tis_workspace_size(n))
+
+
+def fp8rl_tis_weights(d_lp_train, d_lp_rollout, d_mask, n, clip, d_w, d_kl, d_workspace, workspace_bytes,
+                      stream=None) -> None:
+    _ok(load_library().fp8rl_tis_weights(_p(d_lp_train), _p(d_lp_rollout), _p(d_mask), n, clip, _p(d_w),
+                                         _p(d_kl), _p(d_workspace), workspace_bytes, _stream(stream)),
+        "fp8rl_tis_weights")
 
 
 def fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, num_experts, rows, n, k,
@@ -410,6 +453,75 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_ca
     tokens, dim = k.shape
     fp8rl_kv_append(k, v, tokens, dim, k.stride(0), v.stride(0), slot_mapping, k_cache, v_cache,
                     k_cache.stride(0), k_cache.shape[0], scales, stream)
+
+
+def moe_plan(topk: torch.Tensor, experts: int, workspace: torch.Tensor | None = None, stream=None):
+    """Dispatch plan of replayed top-k indices (device int32 [T, k]): returns
+    device int32 (offsets [E+1], row_of_pair [T*k], token_of_row [T*k])."""
+    if topk.dtype != torch.int32 or topk.dim() != 2 or not topk.is_contiguous():
+        raise ValueError("topk must be a contiguous int32 [tokens, k] tensor")
+    tokens, k = topk.shape
+    dev = topk.device
+    need = fp8rl_moe_plan_workspace_size(tokens, k, experts)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    offsets = torch.empty(experts + 1, dtype=torch.int32, device=dev)
+    row_of_pair = torch.empty(tokens * k, dtype=torch.int32, device=dev)
+    token_of_row = torch.empty(tokens * k, dtype=torch.int32, device=dev)
+    fp8rl_moe_plan(topk, tokens, k, experts, offsets, row_of_pair, token_of_row, workspace, workspace.numel(),
+                   stream)
+    return offsets, row_of_pair, token_of_row
+
+
+def moe_dispatch_quant(x: torch.Tensor, row_of_pair: torch.Tensor, topk: int, fmt=SCALE_FP32, out=None,
+                       stream=None):
+    """The grouped activation of the dispatch: token t's 1x128 quantisation in
+    rows row_of_pair[t * topk + j], (codes uint8 [R, K], scales [K/128, R]
+    fp32 or uint8) with R = tokens * topk."""
+    _check_bf16_2d(x, "x")
+    tokens, k = x.shape
+    rows = row_of_pair.numel()
+    if rows != tokens * topk:
+        raise ValueError("row_of_pair must have tokens * topk entries")
+    if out is None:
+        q = torch.empty((rows, k), dtype=torch.uint8, device=x.device)
+        sdt = torch.float32 if fmt == SCALE_FP32 else torch.uint8
+        s = torch.empty(((k + 127) // 128, rows), dtype=sdt, device=x.device)
+    else:
+        q, s = out
+    fp8rl_moe_dispatch_quant(x, tokens, k, x.stride(0), row_of_pair, topk, rows, q, q.stride(0), s, fmt, stream)
+    return q, s
+
+
+def moe_combine(y: torch.Tensor, row_of_pair: torch.Tensor, gate: torch.Tensor, out=None, stream=None):
+    """bf16 [T, N]: each token's expert output rows weighted by its gates."""
+    _check_bf16_2d(y, "y")
+    if gate.dtype != torch.float32 or gate.dim() != 2 or not gate.is_contiguous():
+        raise ValueError("gate must be a contiguous fp32 [tokens, k] tensor")
+    tokens, k = gate.shape
+    n = y.shape[1]
+    o = out if out is not None else torch.empty((tokens, n), dtype=torch.bfloat16, device=y.device)
+    fp8rl_moe_combine(y, n, y.stride(0), row_of_pair, gate, tokens, k, o, o.stride(0), stream)
+    return o
+
+
+def tis_weights(lp_train: torch.Tensor, lp_rollout: torch.Tensor, mask: torch.Tensor | None = None,
+                clip: float = 2.0, workspace: torch.Tensor | None = None, out=None, stream=None):
+    """(w fp32 [n], kl fp64 [3] = mean, sum, count) on the device."""
+    for name, t in (("lp_train", lp_train), ("lp_rollout", lp_rollout)):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 tensor")
+    if mask is not None and (mask.dtype != torch.uint8 or not mask.is_contiguous()):
+        raise ValueError("mask must be a contiguous uint8 tensor")
+    n = lp_train.numel()
+    dev = lp_train.device
+    need = fp8rl_tis_workspace_size(n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    w, kl = out if out is not None else (torch.empty(n, dtype=torch.float32, device=dev),
+                                         torch.empty(3, dtype=torch.float64, device=dev))
+    fp8rl_tis_weights(lp_train, lp_rollout, mask, n, clip, w, kl, workspace, workspace.numel(), stream)
+    return w, kl
 
 
 class HostWeightSync:

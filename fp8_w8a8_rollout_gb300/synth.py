@@ -202,3 +202,33 @@ def moe_expert_weights(n: int, k: int, experts: int, seed: int, layer: int, whic
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns of a bf16 tensor (a host copy)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------- rollout log-probabilities (TIS)
+
+ROLLOUT_RESPONSES = 512
+ROLLOUT_MAX_LEN = 16384
+
+
+def rollout_logprobs(responses: int = ROLLOUT_RESPONSES, max_len: int = ROLLOUT_MAX_LEN, seed: int = 0,
+                     device="cpu"):
+    """Per-token log-probabilities of a padded rollout batch, flattened
+    [responses * max_len]: (lp_train fp32, lp_rollout fp32, mask uint8).
+
+    Response lengths ~ uniform{1..max_len}; mask = 1 on a response's tokens,
+    0 on its padding.  lp_rollout = -Exp(mean 0.5) (mostly confident
+    samples); lp_train = lp_rollout + N(0, 0.05), and for 1 % of tokens an
+    extra N(0, 1) (tokens where the two precisions disagree), so that some
+    ratios pass the truncation."""
+    n = responses * max_len
+    g = _torch_gen(device, seed, "rollout", "len")
+    lens = torch.randint(1, max_len + 1, (responses,), generator=g, device=device)
+    pos = torch.arange(max_len, device=device)
+    mask = (pos[None, :] < lens[:, None]).reshape(n).to(torch.uint8)
+    g = _torch_gen(device, seed, "rollout", "lp")
+    lp_rollout = torch.empty(n, device=device, dtype=torch.float32).exponential_(2.0, generator=g).neg_()
+    noise = torch.randn(n, generator=g, device=device, dtype=torch.float32).mul_(0.05)
+    big = torch.rand(n, generator=g, device=device, dtype=torch.float32) < 0.01
+    noise += torch.randn(n, generator=g, device=device, dtype=torch.float32) * big
+    lp_train = lp_rollout + noise
+    return lp_train, lp_rollout, mask

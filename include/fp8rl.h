@@ -362,6 +362,90 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  */
 FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value);
 
+/*
+ * MoE dispatch plan from replayed routing indices (routing-replay page,
+ * "R3: Rollout Routing Replay": the rollout's recorded top-k expert indices
+ * per token decide which experts a token's rows go to).  Pair p = t * topk + j
+ * is token t's slot j.  Rows of expert e's segment [offsets[e], offsets[e+1])
+ * hold the pairs routed to e in increasing p (the stable order; the pages fix
+ * none).  An index outside [0, experts) drops its pair.
+ *   d_topk          device, int32 [tokens][topk], 1 <= topk <= 32
+ *   d_offsets       device, int32 [experts + 1] out (offsets[experts] = routed pairs)
+ *   d_row_of_pair   device, int32 [tokens * topk] out: the row of each pair, -1 if dropped
+ *   d_token_of_row  device, int32 [tokens * topk] out: the token of each row, -1 past
+ *                   offsets[experts]
+ *   d_workspace     device scratch of fp8rl_moe_plan_workspace_size() bytes, owned by
+ *                   the caller; needs no initial contents; one call at a time per buffer
+ * 1 <= experts <= 8192.  Three launches on `stream`; deterministic.
+ * Errors: INVALID_ARG (sizes, null pointers, workspace too small), SHAPE
+ *         (experts > 8192, tokens * topk >= 2^31 - 4096), ALIGNMENT (4 bytes), CUDA.
+ */
+FP8RL_API size_t fp8rl_moe_plan_workspace_size(int64_t tokens, int64_t topk, int64_t experts);
+FP8RL_API fp8rl_status fp8rl_moe_plan(const int32_t* d_topk, int64_t tokens, int64_t topk, int64_t experts,
+                                      int32_t* d_offsets, int32_t* d_row_of_pair, int32_t* d_token_of_row,
+                                      void* d_workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * MoE dispatch with 1x128 activation quantisation: for every routed pair
+ * p = t * topk + j, row d_row_of_pair[p] of the grouped activation is x[t]
+ * quantised exactly as fp8rl_quant_act_group quantises a row (FP8-RL page,
+ * "Method steps", step 1: activations quantised dynamically in every
+ * forward).  Each token row is read and quantised once and its codes and
+ * scales are written to all of its rows; pairs with row -1 (dropped) or a
+ * row outside [0, rows) write nothing, and rows no pair names are left as
+ * they were (the grouped GEMM never reads them).
+ *   x_bf16          device, bf16 [tokens][ldx], 16-byte aligned
+ *   d_row_of_pair   device, int32 [tokens * topk] (fp8rl_moe_plan's output), 1 <= topk <= 32
+ *   q_e4m3          device, E4M3 [rows][ldq] out, 16-byte aligned
+ *   x_scale         device, [ceil(k/128)][rows] fp32 or UE8M0 bytes out
+ * Errors: INVALID_ARG, SHAPE (tokens * ceil(k/128) >= 2^31 - 2^20), ALIGNMENT, CUDA.
+ */
+FP8RL_API fp8rl_status fp8rl_moe_dispatch_quant(const void* x_bf16, int64_t tokens, int64_t k, int64_t ldx,
+                                                const int32_t* d_row_of_pair, int64_t topk, int64_t rows,
+                                                void* q_e4m3, int64_t ldq, void* x_scale, fp8rl_scale_fmt fmt,
+                                                void* stream);
+
+/*
+ * MoE combine: out[t] = sum over j of gate[t][j] * y[row_of_pair[t * topk + j]],
+ * fp32 multiply-adds in slot order, rounded once to bf16 (nearest-even);
+ * slots with row -1 add nothing.  The gates are an input: the router's
+ * weights of the recorded experts (replaying indices fixes which experts run,
+ * not how their outputs are weighted).
+ *   y_bf16          device, bf16 [rows][ldy] (the grouped GEMM's output)
+ *   d_row_of_pair   device, int32 [tokens * topk] (fp8rl_moe_plan's output)
+ *   d_gate          device, fp32 [tokens][topk]
+ *   out_bf16        device, bf16 [tokens][ldo]
+ * 1 <= topk <= 32.  Errors: INVALID_ARG, SHAPE (tokens * ceil(n/8) >= 2^31 - 2^20),
+ *         ALIGNMENT (element alignment), CUDA.
+ */
+FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t n, int64_t ldy, const int32_t* d_row_of_pair,
+                                         const float* d_gate, int64_t tokens, int64_t topk, void* out_bf16,
+                                         int64_t ldo, void* stream);
+
+/*
+ * Token-level truncated importance sampling weights and the mismatch KL
+ * estimate.  FP8-RL page, "Method steps", step 4: w = pi_theta / pi_fp8 =
+ * exp(lp_train - lp_rollout), truncated at clip (C = 2 in the pages; their
+ * clip to [-C, C] is min(w, C) since w > 0).  Precision-alignment page, "how
+ * the gap is measured": the mean over generated tokens of lp_rollout - lp_train.
+ *   d_lp_train, d_lp_rollout  device, fp32 [n] log-probabilities of the sampled tokens
+ *   d_mask          device, uint8 [n] (nonzero: generated token), or null (all tokens)
+ *   d_w             device, fp32 [n] out: min(expf(lp_train - lp_rollout), clip), 0 if masked out
+ *   d_kl            device, double [3] out: mean (0 with no token), sum, token count
+ *   d_workspace     device scratch of fp8rl_tis_workspace_size(n) bytes, owned by the
+ *                   caller, 8-byte aligned; needs no initial contents
+ * Each difference is made exact in fp32 (a TwoSum: rounded difference plus its
+ * error term), accumulated as an fp32 pair and folded into fp64 every 64
+ * tokens; the fp64 partials add up in an order fixed by n: the same bits on
+ * every run.
+ * Errors: INVALID_ARG (negative n, clip <= 0, null pointers, workspace too
+ *         small), ALIGNMENT, CUDA.
+ */
+FP8RL_API size_t fp8rl_tis_workspace_size(int64_t n);
+FP8RL_API fp8rl_status fp8rl_tis_weights(const float* d_lp_train, const float* d_lp_rollout, const uint8_t* d_mask,
+                                         int64_t n, float clip, float* d_w, double* d_kl, void* d_workspace,
+                                         size_t workspace_bytes, void* stream);
+
 /* Static, NUL-terminated name of a status code. */
 FP8RL_API const char* fp8rl_status_string(fp8rl_status s);
 

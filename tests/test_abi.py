@@ -171,3 +171,49 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 8, 7) == 0
     assert _rc("fp8rl_debug_set", 1, 256) == 0
     assert _rc("fp8rl_debug_set", 0, 0) == 0
+
+
+def test_moe_plan_rejects_bad_arguments_on_host(lib):
+    ws = lib.fp8rl_moe_plan_workspace_size(4096, 8, 128)
+    assert ws >= 4 * 128 and ws % 256 == 0
+    assert lib.fp8rl_moe_plan_workspace_size(16, 0, 8) == 0      # topk < 1
+    assert lib.fp8rl_moe_plan_workspace_size(16, 33, 8) == 0     # topk > 32
+    assert lib.fp8rl_moe_plan_workspace_size(16, 8, 8193) == 0   # too many experts
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    assert _rc("fp8rl_moe_plan", fake, 16, 0, 8, fake, fake, fake, fake, ws, None) == 1
+    assert _rc("fp8rl_moe_plan", fake, 16, 8, 0, fake, fake, fake, fake, ws, None) == 1
+    assert _rc("fp8rl_moe_plan", fake, 16, 8, 9000, fake, fake, fake, fake, ws, None) == 2
+    assert _rc("fp8rl_moe_plan", fake, 1 << 28, 8, 8, fake, fake, fake, fake, ws, None) == 2
+    assert _rc("fp8rl_moe_plan", None, 16, 8, 8, fake, fake, fake, fake, ws, None) == 1
+    assert _rc("fp8rl_moe_plan", fake, 16, 8, 8, fake, fake, fake, fake, 0, None) == 1  # workspace too small
+    small = lib.fp8rl_moe_plan_workspace_size(16, 8, 8)
+    assert _rc("fp8rl_moe_plan", fake + 2, 16, 8, 8, fake, fake, fake, fake, small, None) == 3
+
+
+def test_moe_dispatch_and_combine_reject_bad_arguments_on_host(lib):
+    fake = 1 << 20
+    q = "fp8rl_moe_dispatch_quant"
+    assert _rc(q, fake, 16, 256, 256, fake, 8, 128, fake, 256, fake, 2, None) == 1  # bad format
+    assert _rc(q, fake, 16, 256, 100, fake, 8, 128, fake, 256, fake, 0, None) == 1  # ldx < k
+    assert _rc(q, fake, 16, 256, 256, fake, 33, 128, fake, 256, fake, 0, None) == 1  # topk > 32
+    assert _rc(q, fake, 16, 256, 256, None, 8, 128, fake, 256, fake, 0, None) == 1
+    assert _rc(q, fake + 8, 16, 256, 256, fake, 8, 128, fake, 256, fake, 0, None) == 3
+    assert _rc(q, fake, 16, 256, 256, fake, 8, 0, fake, 256, fake, 0, None) == 0  # no rows: no-op
+    c = "fp8rl_moe_combine"
+    assert _rc(c, fake, 256, 256, fake, fake, 16, 0, fake, 256, None) == 1    # topk < 1
+    assert _rc(c, fake, 256, 128, fake, fake, 16, 8, fake, 256, None) == 1    # ldy < n
+    assert _rc(c, None, 256, 256, fake, fake, 16, 8, fake, 256, None) == 1
+    assert _rc(c, fake + 1, 256, 256, fake, fake, 16, 8, fake, 256, None) == 3
+    assert _rc(c, fake, 256, 256, fake, fake, 0, 8, fake, 256, None) == 0     # no tokens: no-op
+
+
+def test_tis_rejects_bad_arguments_on_host(lib):
+    fake = 1 << 20
+    ws = lib.fp8rl_tis_workspace_size(1 << 24)
+    assert ws >= 16 and lib.fp8rl_tis_workspace_size(-1) == 0
+    t = "fp8rl_tis_weights"
+    assert _rc(t, fake, fake, None, -1, 2.0, fake, fake, fake, ws, None) == 1
+    assert _rc(t, fake, fake, None, 1 << 24, 0.0, fake, fake, fake, ws, None) == 1   # clip <= 0
+    assert _rc(t, fake, fake, None, 1 << 24, 2.0, fake, None, fake, ws, None) == 1   # no output
+    assert _rc(t, fake, fake, None, 1 << 24, 2.0, fake, fake, fake, 8, None) == 1    # workspace too small
+    assert _rc(t, fake + 2, fake, None, 1 << 24, 2.0, fake, fake, fake, ws, None) == 3
