@@ -320,17 +320,18 @@ __device__ __forceinline__ void fma_piece(float (&acc)[8], float w, uint4 v) {
   }
 }
 
-// Dispatch with 1x128 quantisation, one warp per token: lane l takes the 16
-// columns [16 l, 16 l + 16) of each 512-column round, so a group of 128
-// columns is 8 consecutive lanes and its amax meets in 3 shuffles.  The whole
-// row (up to 2048 columns per pass) is loaded before any of it is quantised;
-// then each group's codes and scale are written to every row the token's
-// pairs occupy, through row pointers formed once per token: a warp store
-// covers 512 contiguous bytes of a destination row.  The quotient and its
-// rounding are the activation quantiser's (IEEE fp32 x / s, nearest-even
-// E4M3, saturating), so the bytes equal those of quantising gathered rows.
+// Dispatch with 1x128 quantisation.  A warp task is 1024 columns of one
+// token (two 512-column rounds); lane l takes columns [16 l, 16 l + 16) of a
+// round, so a group of 128 columns is 8 consecutive lanes and its amax meets
+// in 3 shuffles.  Each group's codes and scale are written to every row the
+// token's pairs occupy: a warp store covers 512 contiguous bytes of a
+// destination row.  Tasks are taken with a warp-uniform stride, and each
+// warp loads its next task (row chunk and row map) before it quantises and
+// stores the current one.  The quotient and its rounding are the activation
+// quantiser's (IEEE fp32 x / s, nearest-even E4M3, saturating), so the bytes
+// equal those of quantising gathered rows.
 constexpr int kDispatchThreads = 256;
-constexpr int kDispatchRounds = 4;  // 512-column rounds per pass: 2048 columns
+constexpr int kDispatchTaskCols = 1024;
 
 __device__ __forceinline__ uint4 load16_bf16(const uint16_t* src, int64_t c, int64_t k, bool vec) {
   if (vec && c + 8 <= k) return ld_nc_u4(src + c);
@@ -344,86 +345,113 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, uint2 code, int64_t c,
   for (int e = 0; e < 8 && c + e < k; ++e) dst[e] = (uint8_t)(((e < 4 ? code.x : code.y) >> (8 * (e & 3))) & 0xFFu);
 }
 
+struct DispatchTask {
+  uint4 v[2][2];   // this lane's 16 columns of each round
+  int32_t row;     // lane j < topk: the row of the token's pair j
+  int64_t c0;      // first column of the task
+  int64_t token;
+};
+
+__device__ __forceinline__ void dispatch_load(DispatchTask& d, int64_t task, int64_t chunks,
+                                              const uint16_t* __restrict__ x, int64_t k, int64_t ldx,
+                                              const int32_t* __restrict__ row_of_pair, int32_t topk, int64_t rows,
+                                              bool vec, int lane) {
+  d.token = task / chunks;
+  d.c0 = (task - d.token * chunks) * kDispatchTaskCols;
+  d.row = lane < topk ? row_of_pair[d.token * topk + lane] : -1;
+  if (d.row >= rows) d.row = -1;
+  const uint16_t* src = x + d.token * ldx;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int64_t cr = d.c0 + 512 * i;
+    const int64_t c = cr + 16 * lane;
+    if (vec && cr + 512 <= k) {
+      d.v[i][0] = ld_nc_u4(src + c);
+      d.v[i][1] = ld_nc_u4(src + c + 8);
+    } else if (cr < k) {
+      d.v[i][0] = load16_bf16(src, c, k, vec);
+      d.v[i][1] = load16_bf16(src, c + 8, k, vec);
+    }
+  }
+}
+
+template <bool UE8M0>
+__device__ __forceinline__ void dispatch_store(const DispatchTask& d, int64_t k, int32_t topk, int64_t rows,
+                                               uint8_t* __restrict__ q, int64_t ldq, void* __restrict__ scale,
+                                               bool vec, int lane) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int64_t cr = d.c0 + 512 * i;
+    if (cr >= k) break;  // warp-uniform: past the row
+    const bool full = vec && cr + 512 <= k && ldq % 16 == 0;
+    const int64_t c = cr + 16 * lane;
+    uint32_t am = absmax_u4(absmax_u4(0u, d.v[i][0]), d.v[i][1]);
+    am = max(am & 0xFFFFu, am >> 16);
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, s));
+    const float amax = __uint_as_float(am << 16);
+    uint2 c_lo, c_hi;
+    uint32_t sbits;
+    if (UE8M0) {
+      const int e = scale_ue8m0_exponent(amax);
+      const float f = exp2_neg(e);
+      c_lo = quant8_mul(d.v[i][0], f);
+      c_hi = quant8_mul(d.v[i][1], f);
+      sbits = (uint32_t)(e + 127);
+    } else {
+      const float sc = scale_fp32(amax);
+      const float r = __frcp_rn(sc);
+      c_lo = quant8_div(d.v[i][0], sc, r);
+      c_hi = quant8_div(d.v[i][1], sc, r);
+      sbits = __float_as_uint(sc);
+    }
+    const uint4 code = make_uint4(c_lo.x, c_lo.y, c_hi.x, c_hi.y);
+    const bool lead = (lane & 7) == 0 && c < k;  // the group's first lane writes its scale
+    const int64_t sidx = (c / kBlock) * rows;
+    for (int j = 0; j < topk; ++j) {
+      const int32_t row = __shfl_sync(0xffffffffu, d.row, j);
+      if (row < 0) continue;  // warp-uniform
+      uint8_t* dst = q + (int64_t)row * ldq + c;
+      if (full) {
+        *reinterpret_cast<uint4*>(dst) = code;
+      } else if (c < k) {
+        if (vec && c + 16 <= k) {
+          *reinterpret_cast<uint2*>(dst) = c_lo;
+          *reinterpret_cast<uint2*>(dst + 8) = c_hi;
+        } else {
+          store_codes(dst, c_lo, c, k);
+          if (c + 8 < k) store_codes(dst + 8, c_hi, c + 8, k);
+        }
+      }
+      if (lead) {
+        if (UE8M0)
+          static_cast<uint8_t*>(scale)[sidx + row] = (uint8_t)sbits;
+        else
+          static_cast<float*>(scale)[sidx + row] = __uint_as_float(sbits);
+      }
+    }
+  }
+}
+
 template <bool UE8M0>
 __global__ void __launch_bounds__(kDispatchThreads) moe_dispatch_kernel(
     const uint16_t* __restrict__ x, int64_t tokens, int64_t k, int64_t ldx, const int32_t* __restrict__ row_of_pair,
     int32_t topk, int64_t rows, uint8_t* __restrict__ q, int64_t ldq, void* __restrict__ scale, int vec) {
   const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (kDispatchThreads / 32);
-  // full rows: every round whole, and every 16-byte code store aligned (the
-  // common case; vec alone guarantees 8-byte aligned destination rows)
-  const bool fast = vec && k % (32 * 16) == 0 && ldq % 16 == 0;
-  for (int64_t t = (int64_t)blockIdx.x * (kDispatchThreads / 32) + (threadIdx.x >> 5); t < tokens; t += warps) {
-    int32_t my_row = lane < topk ? row_of_pair[t * topk + lane] : -1;
-    if (my_row >= rows) my_row = -1;
-    const uint16_t* src = x + t * ldx;
-    for (int64_t c0 = 0; c0 < k; c0 += 512 * kDispatchRounds) {
-      uint4 v[kDispatchRounds][2];
-#pragma unroll
-      for (int i = 0; i < kDispatchRounds; ++i) {
-        const int64_t c = c0 + 512 * i + 16 * lane;
-        if (fast) {
-          if (c < k) {
-            v[i][0] = ld_nc_u4(src + c);
-            v[i][1] = ld_nc_u4(src + c + 8);
-          }
-        } else {
-          v[i][0] = load16_bf16(src, c, k, vec);
-          v[i][1] = load16_bf16(src, c + 8, k, vec);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kDispatchRounds; ++i) {
-        const int64_t cr = c0 + 512 * i;
-        if (cr >= k) break;  // warp-uniform: past the row
-        const int64_t c = cr + 16 * lane;
-        uint32_t am = absmax_u4(absmax_u4(0u, v[i][0]), v[i][1]);
-        am = max(am & 0xFFFFu, am >> 16);
-#pragma unroll
-        for (int d = 1; d < 8; d <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
-        const float amax = __uint_as_float(am << 16);
-        uint2 c_lo, c_hi;
-        uint32_t sbits;
-        if (UE8M0) {
-          const int e = scale_ue8m0_exponent(amax);
-          const float f = exp2_neg(e);
-          c_lo = quant8_mul(v[i][0], f);
-          c_hi = quant8_mul(v[i][1], f);
-          sbits = (uint32_t)(e + 127);
-        } else {
-          const float s = scale_fp32(amax);
-          const float r = __frcp_rn(s);
-          c_lo = quant8_div(v[i][0], s, r);
-          c_hi = quant8_div(v[i][1], s, r);
-          sbits = __float_as_uint(s);
-        }
-        const uint4 code = make_uint4(c_lo.x, c_lo.y, c_hi.x, c_hi.y);
-        const bool lead = (lane & 7) == 0 && c < k;  // the group's first lane writes its scale
-        const int64_t sidx = (c / kBlock) * rows;
-        for (int j = 0; j < topk; ++j) {
-          const int32_t row = __shfl_sync(0xffffffffu, my_row, j);
-          if (row < 0) continue;  // warp-uniform
-          uint8_t* dst = q + (int64_t)row * ldq + c;
-          if (fast) {
-            *reinterpret_cast<uint4*>(dst) = code;
-          } else if (c < k) {
-            if (vec && c + 16 <= k) {
-              *reinterpret_cast<uint2*>(dst) = c_lo;
-              *reinterpret_cast<uint2*>(dst + 8) = c_hi;
-            } else {
-              store_codes(dst, c_lo, c, k);
-              if (c + 8 < k) store_codes(dst + 8, c_hi, c + 8, k);
-            }
-          }
-          if (lead) {
-            if (UE8M0)
-              static_cast<uint8_t*>(scale)[sidx + row] = (uint8_t)sbits;
-            else
-              static_cast<float*>(scale)[sidx + row] = __uint_as_float(sbits);
-          }
-        }
-      }
-    }
+  const int64_t chunks = (k + kDispatchTaskCols - 1) / kDispatchTaskCols;
+  const int64_t tasks = tokens * chunks;
+  const int64_t wc = (int64_t)gridDim.x * (kDispatchThreads / 32);
+  const int64_t warp = (int64_t)blockIdx.x * (kDispatchThreads / 32) + (threadIdx.x >> 5);
+  if (warp >= tasks) return;
+  DispatchTask da, db;
+  dispatch_load(da, warp, chunks, x, k, ldx, row_of_pair, topk, rows, vec, lane);
+  // two tasks per trip, so that the two register sets keep fixed names
+  for (int64_t t = warp; t < tasks; t += 2 * wc) {
+    const int64_t t1 = t + wc, t2 = t + 2 * wc;
+    if (t1 < tasks) dispatch_load(db, t1, chunks, x, k, ldx, row_of_pair, topk, rows, vec, lane);
+    dispatch_store<UE8M0>(da, k, topk, rows, q, ldq, scale, vec, lane);
+    if (t2 < tasks) dispatch_load(da, t2, chunks, x, k, ldx, row_of_pair, topk, rows, vec, lane);
+    if (t1 < tasks) dispatch_store<UE8M0>(db, k, topk, rows, q, ldq, scale, vec, lane);
   }
 }
 
@@ -556,7 +584,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_moe_dispatch_quant(const void* x_bf16, i
   if (occ[u] == 0)
     occ[u] = u ? ctas_per_sm(moe_dispatch_kernel<true>, kDispatchThreads)
                : ctas_per_sm(moe_dispatch_kernel<false>, kDispatchThreads);
-  const int64_t ctas = (tokens + kDispatchThreads / 32 - 1) / (kDispatchThreads / 32);
+  // one wave of resident CTAs (the SMs share the tasks evenly; a warp's
+  // tasks overlap its neighbours' on the same SM)
+  const int64_t tasks = tokens * ((k + kDispatchTaskCols - 1) / kDispatchTaskCols);
+  const int64_t ctas = (tasks + kDispatchThreads / 32 - 1) / (kDispatchThreads / 32);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)sm_count() * occ[u]));
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);

@@ -11,15 +11,15 @@
 // A token mask marks the generated tokens; others get weight 0 and stay out
 // of the mean.  The weight: the fp32 difference, CUDA's expf, fminf with C.
 // The mean: each difference lp_rollout - lp_train is made exact in fp32 by
-// Knuth's TwoSum (the rounded sum plus its error term), the pairs are summed
-// in an fp32 (hi, lo) accumulator (hi by TwoSum again, lo plainly: its own
-// rounding is 2^-24 of terms already 2^-24 below hi), and every 64 tokens the
-// pair is folded into the thread's fp64 sum.  GB300's fp64 pipe is narrow:
-// fp64 conversions and adds per token made the kernel fp64-bound.  Thread
-// sums then meet in a fixed tree per CTA and the CTA partials in a fixed tree
-// in one CTA -- the same bits on every run of the same size on a given GPU
-// (the grid is one wave of resident CTAs).  HBM-bound: 13
-// bytes per token (two fp32 reads, the mask, the fp32 weight).
+// Knuth's TwoSum (the rounded sum plus its error term) and accumulated in an
+// fp32 (hi, lo) pair -- hi by TwoSum again, lo plainly, whose own rounding is
+// 2^-24 of terms already 2^-24 below hi.  GB300's fp64 pipe is narrow: fp64
+// conversions and adds per token made the kernel fp64-bound.  Each CTA takes
+// fixed 4096-token chunks; its threads' pairs meet in a fixed tree and the
+// CTA's pair is its partial; one CTA adds the partials the same way, in a
+// fixed order, and converts to fp64 once.  The grid depends on n alone, so the result has the same bits on
+// every run and device.  HBM-bound: 13 bytes per token (two fp32 reads, the
+// mask, the fp32 weight).
 #include <algorithm>
 
 #include "common.cuh"
@@ -28,19 +28,24 @@ namespace fp8rl {
 namespace {
 
 constexpr int kTisThreads = 256;
-constexpr int kTisMaxCtas = 4096;       // workspace bound; the grid is one wave of resident CTAs
-constexpr int kTisTokensPerCta = 8192;  // below this many per CTA the grid shrinks
-constexpr int kTisFinalThreads = 1024;
-constexpr int kTrips = 4;  // float4 loads of each input in flight per thread
+constexpr int kTrips = 4;                                     // float4 loads of each input per thread
+constexpr int64_t kTisChunk = (int64_t)kTisThreads * 4 * kTrips;  // 4096 tokens per CTA and chunk
+constexpr int64_t kTisMaxCtas = 65536;                        // more tokens: CTAs take several chunks
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// the grid, and the number of partials, are a function of n alone: the
+// summation order (and so the result's bits) does not depend on the device
+int64_t tis_grid(int64_t n) {
+  return std::max<int64_t>(1, std::min<int64_t>(kTisMaxCtas, (n + kTisChunk - 1) / kTisChunk));
+}
 
 __device__ __forceinline__ float tis_weight(float lt, float lr, float clip) {
   return fminf(expf(lt - lr), clip);
 }
 
-// Knuth's TwoSum: s + e == a + b exactly (round-to-nearest fp32, no
-// reassociation: plain adds, which nvcc does not contract or reorder)
+// Knuth's TwoSum: s + e == a + b exactly (round-to-nearest fp32; explicit
+// _rn adds, which the compiler neither contracts nor reorders)
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
   const float bv = __fsub_rn(s, a);
@@ -48,167 +53,155 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
 }
 
-// lp_rollout - lp_train added exactly (up to the lo word's rounding) to (hi, lo)
-__device__ __forceinline__ void acc_diff(float lr, float lt, float& hi, float& lo) {
-  float d, de, s, se;
-  two_sum(lr, -lt, d, de);
-  two_sum(hi, d, s, se);
+// (hi, lo) += (bhi, blo): hi by TwoSum, the error terms into lo
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float bhi, float blo) {
+  float s, e;
+  two_sum(hi, bhi, s, e);
   hi = s;
-  lo = __fadd_rn(lo, __fadd_rn(se, de));
+  lo = __fadd_rn(lo, __fadd_rn(e, blo));
 }
 
-__global__ void __launch_bounds__(kTisThreads, 3) tis_partial_kernel(const float* __restrict__ lp_train,
+// lp_rollout - lp_train, made exact by TwoSum, added to (hi, lo)
+__device__ __forceinline__ void acc_diff(float lr, float lt, float& hi, float& lo) {
+  float d, de;
+  two_sum(lr, -lt, d, de);
+  pair_add(hi, lo, d, de);
+}
+
+__device__ __forceinline__ void tis_token(float lt, float lr, bool on, float clip, float& w, float& hi, float& lo,
+                                          uint32_t& cnt) {
+  w = on ? tis_weight(lt, lr, clip) : 0.0f;
+  if (on) {
+    acc_diff(lr, lt, hi, lo);
+    ++cnt;
+  }
+}
+
+// One 4096-token chunk per CTA and trip of the outer loop: thread i takes
+// float4 i, i + 256, i + 512, i + 768 of the chunk (coalesced), all loads
+// first.  The per-thread (hi, lo) pairs meet in the CTA by pair additions
+// in a fixed tree; the CTA's partial is the pair's fp64 value.
+__global__ void __launch_bounds__(kTisThreads) tis_partial_kernel(const float* __restrict__ lp_train,
                                                                  const float* __restrict__ lp_rollout,
                                                                  const uint8_t* __restrict__ mask, int64_t n,
                                                                  float clip, float* __restrict__ w,
-                                                                 double* __restrict__ part_sum,
-                                                                 unsigned long long* __restrict__ part_cnt,
-                                                                 int vec) {
-  double sum = 0.0;
-  float hi = 0.0f, lo = 0.0f;  // fp32 pair, folded into sum every 64 tokens
-  uint32_t cnt = 0, trips = 0;
-  const int64_t stride = (int64_t)gridDim.x * kTisThreads;
-  const int64_t tid = (int64_t)blockIdx.x * kTisThreads + threadIdx.x;
-  if (vec) {
-    const int64_t n4 = n / 4;
-    // kTrips float4 trips per loop: all their loads are in flight together
-    for (int64_t i0 = tid; i0 < n4; i0 += kTrips * stride) {
+                                                                 uint4* __restrict__ part, int vec) {
+  float hi = 0.0f, lo = 0.0f;
+  uint32_t cnt = 0;
+  for (int64_t c0 = (int64_t)blockIdx.x * kTisChunk; c0 < n; c0 += (int64_t)gridDim.x * kTisChunk) {
+    if (vec && c0 + kTisChunk <= n) {
+      const int64_t q0 = c0 / 4 + threadIdx.x;
       float4 a[kTrips], b[kTrips];
       uint32_t mk[kTrips];
 #pragma unroll
       for (int u = 0; u < kTrips; ++u) {
-        const int64_t i = i0 + u * stride;
-        const bool in = i < n4;
-        a[u] = in ? __ldcs(reinterpret_cast<const float4*>(lp_train) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        b[u] = in ? __ldcs(reinterpret_cast<const float4*>(lp_rollout) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        mk[u] = !in ? 0u : mask ? __ldcs(reinterpret_cast<const unsigned int*>(mask) + i) : 0x01010101u;
+        a[u] = __ldcs(reinterpret_cast<const float4*>(lp_train) + q0 + u * kTisThreads);
+        b[u] = __ldcs(reinterpret_cast<const float4*>(lp_rollout) + q0 + u * kTisThreads);
+        mk[u] = mask ? __ldcs(reinterpret_cast<const unsigned int*>(mask) + q0 + u * kTisThreads) : 0x01010101u;
       }
 #pragma unroll
       for (int u = 0; u < kTrips; ++u) {
-        const int64_t i = i0 + u * stride;
-        if (i >= n4) break;
-        const float lt[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, lr[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
-        float o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool on = (mk[u] >> (8 * j)) & 0xFFu;
-          o[j] = on ? tis_weight(lt[j], lr[j], clip) : 0.0f;
-          if (on) {
-            acc_diff(lr[j], lt[j], hi, lo);
-            ++cnt;
-          }
-        }
-        __stcs(reinterpret_cast<float4*>(w) + i, make_float4(o[0], o[1], o[2], o[3]));
+        float4 o;
+        tis_token(a[u].x, b[u].x, mk[u] & 0xFFu, clip, o.x, hi, lo, cnt);
+        tis_token(a[u].y, b[u].y, (mk[u] >> 8) & 0xFFu, clip, o.y, hi, lo, cnt);
+        tis_token(a[u].z, b[u].z, (mk[u] >> 16) & 0xFFu, clip, o.z, hi, lo, cnt);
+        tis_token(a[u].w, b[u].w, mk[u] >> 24, clip, o.w, hi, lo, cnt);
+        __stcs(reinterpret_cast<float4*>(w) + q0 + u * kTisThreads, o);
       }
-      if ((++trips & (16 / kTrips - 1)) == 0) {  // every 64 tokens
-        sum += (double)hi + (double)lo;
-        hi = lo = 0.0f;
-      }
-    }
-    for (int64_t i = n4 * 4 + tid; i < n; i += stride) {
-      const bool on = mask ? mask[i] != 0 : true;
-      w[i] = on ? tis_weight(lp_train[i], lp_rollout[i], clip) : 0.0f;
-      if (on) {
-        acc_diff(lp_rollout[i], lp_train[i], hi, lo);
-        ++cnt;
-      }
-    }
-  } else {
-    for (int64_t i = tid; i < n; i += stride) {
-      const bool on = mask ? mask[i] != 0 : true;
-      w[i] = on ? tis_weight(lp_train[i], lp_rollout[i], clip) : 0.0f;
-      if (on) {
-        acc_diff(lp_rollout[i], lp_train[i], hi, lo);
-        ++cnt;
-      }
-      if ((++trips & 63) == 0) {
-        sum += (double)hi + (double)lo;
-        hi = lo = 0.0f;
+    } else {
+      // a ragged last chunk, or unaligned arrays: token by token
+      const int64_t c1 = min(n, c0 + kTisChunk);
+      for (int64_t i = c0 + threadIdx.x; i < c1; i += kTisThreads) {
+        float wi;
+        tis_token(lp_train[i], lp_rollout[i], mask ? mask[i] != 0 : true, clip, wi, hi, lo, cnt);
+        w[i] = wi;
       }
     }
   }
-  sum += (double)hi + (double)lo;
   // fixed-shape tree: lanes, then the CTA's warps in order
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
-    sum += __shfl_xor_sync(0xffffffffu, sum, d);
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, d);
+    const float olo = __shfl_xor_sync(0xffffffffu, lo, d);
+    pair_add(hi, lo, ohi, olo);
     cnt += __shfl_xor_sync(0xffffffffu, cnt, d);
   }
-  __shared__ double ws[kTisThreads / 32];
+  __shared__ float whi[kTisThreads / 32], wlo[kTisThreads / 32];
   __shared__ uint32_t wc[kTisThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
-    ws[warp] = sum;
+    whi[warp] = hi;
+    wlo[warp] = lo;
     wc[warp] = cnt;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    double s = 0.0;
-    unsigned long long c = 0;
-    for (int i = 0; i < kTisThreads / 32; ++i) {
-      s += ws[i];
+    float h = whi[0], l = wlo[0];
+    uint32_t c = wc[0];
+    for (int i = 1; i < kTisThreads / 32; ++i) {
+      pair_add(h, l, whi[i], wlo[i]);
       c += wc[i];
     }
-    part_sum[blockIdx.x] = s;
-    part_cnt[blockIdx.x] = c;
+    part[blockIdx.x] = make_uint4(__float_as_uint(h), __float_as_uint(l), (uint32_t)c, 0u);
   }
 }
 
 // out: [0] mean (0 when no token is selected), [1] sum, [2] token count.
-// Thread i adds partials i, i + 1024, ... in order; then a fixed tree.
-__global__ void __launch_bounds__(kTisFinalThreads) tis_final_kernel(const double* __restrict__ part_sum,
-                                                                    const unsigned long long* __restrict__ part_cnt,
-                                                                    int parts, double* __restrict__ out) {
-  double s = 0.0;
+// Thread i adds the partials i, i + 1024, ... in order (their loads issued
+// together), then the pairs meet in a fixed tree; fp64 only for the result.
+constexpr int kTisFinalThreads = 1024;
+
+__global__ void __launch_bounds__(kTisFinalThreads) tis_final_kernel(const uint4* __restrict__ part, int parts,
+                                                                    double* __restrict__ out) {
+  float hi = 0.0f, lo = 0.0f;
   unsigned long long c = 0;
-  for (int i = threadIdx.x; i < parts; i += kTisFinalThreads) {
-    s += part_sum[i];
-    c += part_cnt[i];
+  for (int i0 = threadIdx.x; i0 < parts; i0 += 4 * kTisFinalThreads) {
+    uint4 p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j * kTisFinalThreads;
+      p[j] = i < parts ? part[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pair_add(hi, lo, __uint_as_float(p[j].x), __uint_as_float(p[j].y));
+      c += p[j].z;
+    }
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
-    s += __shfl_xor_sync(0xffffffffu, s, d);
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, d);
+    const float olo = __shfl_xor_sync(0xffffffffu, lo, d);
+    pair_add(hi, lo, ohi, olo);
     c += __shfl_xor_sync(0xffffffffu, c, d);
   }
-  __shared__ double ws[kTisFinalThreads / 32];
-  __shared__ unsigned long long wc[kTisFinalThreads / 32];
+  __shared__ float whi[32], wlo[32];
+  __shared__ unsigned long long wc[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
-    ws[warp] = s;
+    whi[warp] = hi;
+    wlo[warp] = lo;
     wc[warp] = c;
   }
   __syncthreads();
   if (warp == 0) {
-    s = ws[lane];
+    hi = whi[lane];
+    lo = wlo[lane];
     c = wc[lane];
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
-      s += __shfl_xor_sync(0xffffffffu, s, d);
+      const float ohi = __shfl_xor_sync(0xffffffffu, hi, d);
+      const float olo = __shfl_xor_sync(0xffffffffu, lo, d);
+      pair_add(hi, lo, ohi, olo);
       c += __shfl_xor_sync(0xffffffffu, c, d);
     }
     if (lane == 0) {
-      out[0] = c ? s / (double)c : 0.0;
-      out[1] = s;
+      const double sum = (double)hi + (double)lo;
+      out[0] = c ? sum / (double)c : 0.0;
+      out[1] = sum;
       out[2] = (double)c;
     }
   }
-}
-
-int64_t tis_grid(int64_t n) {
-  static int resident = 0;  // CTAs of the partial kernel resident per SM, asked once
-  static int sms = 0;
-  if (resident == 0) {
-    int dev = 0, r = 0, m = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || m <= 0)
-      m = 152;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, tis_partial_kernel, kTisThreads, 0) != cudaSuccess || r < 1)
-      r = 1;
-    resident = r;
-    sms = m;
-  }
-  const int64_t wave = std::min<int64_t>(kTisMaxCtas, (int64_t)sms * resident);
-  return std::max<int64_t>(1, std::min<int64_t>(wave, (n + kTisTokensPerCta - 1) / kTisTokensPerCta));
 }
 
 }  // namespace
@@ -218,8 +211,7 @@ using namespace fp8rl;
 
 extern "C" FP8RL_API size_t fp8rl_tis_workspace_size(int64_t n) {
   if (n < 0) return 0;
-  return (size_t)std::max<int64_t>(1, std::min<int64_t>(kTisMaxCtas, (n + kTisTokensPerCta - 1) / kTisTokensPerCta)) *
-         16;
+  return (size_t)tis_grid(n) * 16;
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_tis_weights(const float* d_lp_train, const float* d_lp_rollout,
@@ -230,15 +222,14 @@ extern "C" FP8RL_API fp8rl_status fp8rl_tis_weights(const float* d_lp_train, con
   if (n > 0 && (!d_lp_train || !d_lp_rollout || !d_w)) return FP8RL_ERR_INVALID_ARG;
   if (workspace_bytes < fp8rl_tis_workspace_size(n)) return FP8RL_ERR_INVALID_ARG;
   if (!aligned(d_lp_train, 4) || !aligned(d_lp_rollout, 4) || !aligned(d_w, 4) || !aligned(d_kl, 8) ||
-      !aligned(d_workspace, 8))
+      !aligned(d_workspace, 16))
     return FP8RL_ERR_ALIGNMENT;
   const int64_t grid = tis_grid(n);
-  double* part_sum = static_cast<double*>(d_workspace);
-  unsigned long long* part_cnt = reinterpret_cast<unsigned long long*>(part_sum + grid);
+  uint4* part = static_cast<uint4*>(d_workspace);
   const int vec = aligned(d_lp_train, 16) && aligned(d_lp_rollout, 16) && aligned(d_w, 16) && aligned(d_mask, 4);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  tis_partial_kernel<<<(unsigned)grid, kTisThreads, 0, cs>>>(d_lp_train, d_lp_rollout, d_mask, n, clip, d_w,
-                                                              part_sum, part_cnt, vec);
-  tis_final_kernel<<<1, kTisFinalThreads, 0, cs>>>(part_sum, part_cnt, (int)grid, d_kl);
+  tis_partial_kernel<<<(unsigned)grid, kTisThreads, 0, cs>>>(d_lp_train, d_lp_rollout, d_mask, n, clip, d_w, part,
+                                                              vec);
+  tis_final_kernel<<<1, kTisFinalThreads, 0, cs>>>(part, (int)grid, d_kl);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }

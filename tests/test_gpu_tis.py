@@ -6,11 +6,11 @@ fp32 (absolute error <= 2^-24 |d|) and calls expf (within 2 ulp), so
 |w_gpu - w_ref| <= (2^-21 + 2^-23 |d|) w_ref with a factor 2 of margin, plus
 2^-146 for results in the fp32 subnormal range (a few of its ulps); a
 masked-out token's weight is exactly 0.  The KL sum makes each difference
-exact in fp32 (TwoSum) and keeps 64-token chunks in an fp32 (hi, lo) pair,
-whose lo word rounds at 2^-24 of terms already 2^-24 below the chunk sum
-(<= 2^-41 sum |d| per chunk), then adds chunks in fp64 (2^-53 per add along a
-fixed tree), so |sum_gpu - sum_ref| <= 2^-36 sum |d| with margin; the count
-is exact."""
+exact in fp32 (TwoSum) and adds the differences, then the threads' and CTAs'
+sums, as fp32 (hi, lo) pairs: a pair addition rounds only the lo word, by at
+most 2^-48 of the sum it belongs to, so over the 16 tokens of a thread and the
+~20 tree levels above them |sum_gpu - sum_ref| stays below 2^-40 sum |d|; the
+test allows 2^-36 sum |d|; the count is exact."""
 import numpy as np
 import pytest
 import torch
