@@ -727,14 +727,14 @@ def section_tis(torch, synth, fp8rl, dev, seed, peaks):
     flush = l2_flusher(torch, dev)
     lt, lr, m = synth.rollout_logprobs(seed=seed, device=dev)
     n = lt.numel()
-    ws = torch.empty(fp8rl.fp8rl_tis_workspace_size(n), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(fp8rl.fp8rl_tis_workspace_size(n), dtype=torch.uint8, device=dev)
     w = torch.empty(n, dtype=torch.float32, device=dev)
     kl = torch.empty(3, dtype=torch.float64, device=dev)
     fn = lambda: fp8rl.fp8rl_tis_weights(lt, lr, m, n, 2.0, w, kl, ws, ws.numel())
     t = time_loop(torch, fn, 20, 5, flush)
     b = 13 * n
     return {"tokens": n, "ms": t, "bytes": b, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"],
-            "launches": 2, "l2": "flushed before each call"}
+            "launches": 1, "l2": "flushed before each call"}
 
 
 def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt):
@@ -1004,7 +1004,7 @@ def main_case(args):
         lt, lr, msk = synth.rollout_logprobs(int(parts[1]) if len(parts) > 1 else synth.ROLLOUT_RESPONSES,
                                              device=dev)
         n = lt.numel()
-        ws = torch.empty(fp8rl.fp8rl_tis_workspace_size(n), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(fp8rl.fp8rl_tis_workspace_size(n), dtype=torch.uint8, device=dev)
         w = torch.empty(n, dtype=torch.float32, device=dev)
         kl = torch.empty(3, dtype=torch.float64, device=dev)
         fn = lambda: fp8rl.fp8rl_tis_weights(lt, lr, msk, n, 2.0, w, kl, ws, ws.numel())

@@ -517,7 +517,7 @@ def tis_weights(lp_train: torch.Tensor, lp_rollout: torch.Tensor, mask: torch.Te
     dev = lp_train.device
     need = fp8rl_tis_workspace_size(n)
     if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(max(need, 32), dtype=torch.uint8, device=dev)  # header zeroed once
     w, kl = out if out is not None else (torch.empty(n, dtype=torch.float32, device=dev),
                                          torch.empty(3, dtype=torch.float64, device=dev))
     fp8rl_tis_weights(lp_train, lp_rollout, mask, n, clip, w, kl, workspace, workspace.numel(), stream)

@@ -16,8 +16,9 @@
 // 2^-24 of terms already 2^-24 below hi.  GB300's fp64 pipe is narrow: fp64
 // conversions and adds per token made the kernel fp64-bound.  Each CTA takes
 // fixed 4096-token chunks; its threads' pairs meet in a fixed tree and the
-// CTA's pair is its partial; one CTA adds the partials the same way, in a
-// fixed order, and converts to fp64 once.  The grid depends on n alone, so the result has the same bits on
+// CTA's pair is its partial; the last CTA to finish (an atomic ticket in the
+// workspace header, reset by that CTA) adds the partials the same way, in an
+// order fixed by their index, and converts to fp64 once.  The grid depends on n alone, so the result has the same bits on
 // every run and device.  HBM-bound: 13 bytes per token (two fp32 reads, the
 // mask, the fp32 weight).
 #include <algorithm>
@@ -85,7 +86,9 @@ __global__ void __launch_bounds__(kTisThreads) tis_partial_kernel(const float* _
                                                                  const float* __restrict__ lp_rollout,
                                                                  const uint8_t* __restrict__ mask, int64_t n,
                                                                  float clip, float* __restrict__ w,
-                                                                 uint4* __restrict__ part, int vec) {
+                                                                 uint4* __restrict__ part,
+                                                                 uint32_t* __restrict__ ticket,
+                                                                 double* __restrict__ out, int vec) {
   float hi = 0.0f, lo = 0.0f;
   uint32_t cnt = 0;
   for (int64_t c0 = (int64_t)blockIdx.x * kTisChunk; c0 < n; c0 += (int64_t)gridDim.x * kTisChunk) {
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(kTisThreads) tis_partial_kernel(const float* _
   }
   __shared__ float whi[kTisThreads / 32], wlo[kTisThreads / 32];
   __shared__ uint32_t wc[kTisThreads / 32];
+  __shared__ bool last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) {
     whi[warp] = hi;
@@ -142,28 +146,28 @@ __global__ void __launch_bounds__(kTisThreads) tis_partial_kernel(const float* _
       pair_add(h, l, whi[i], wlo[i]);
       c += wc[i];
     }
-    part[blockIdx.x] = make_uint4(__float_as_uint(h), __float_as_uint(l), (uint32_t)c, 0u);
+    part[blockIdx.x] = make_uint4(__float_as_uint(h), __float_as_uint(l), c, 0u);
+    __threadfence();  // the partial is visible before the ticket is taken
+    last = atomicAdd(ticket, 1u) == gridDim.x - 1;
   }
-}
-
-// out: [0] mean (0 when no token is selected), [1] sum, [2] token count.
-// Thread i adds the partials i, i + 1024, ... in order (their loads issued
-// together), then the pairs meet in a fixed tree; fp64 only for the result.
-constexpr int kTisFinalThreads = 1024;
-
-__global__ void __launch_bounds__(kTisFinalThreads) tis_final_kernel(const uint4* __restrict__ part, int parts,
-                                                                    double* __restrict__ out) {
-  float hi = 0.0f, lo = 0.0f;
+  __syncthreads();
+  if (!last) return;
+  // The last CTA to finish adds every partial, in an order fixed by the
+  // partial's index (not by which CTA came last): thread i takes partials
+  // i, i + 256, ... (loads issued in batches of 8), then a fixed tree.
+  __threadfence();
+  hi = lo = 0.0f;
   unsigned long long c = 0;
-  for (int i0 = threadIdx.x; i0 < parts; i0 += 4 * kTisFinalThreads) {
-    uint4 p[4];
+  const int parts = gridDim.x;
+  for (int i0 = threadIdx.x; i0 < parts; i0 += 8 * kTisThreads) {
+    uint4 p[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = i0 + j * kTisFinalThreads;
-      p[j] = i < parts ? part[i] : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * kTisThreads;
+      p[j] = i < parts ? __ldcg(part + i) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       pair_add(hi, lo, __uint_as_float(p[j].x), __uint_as_float(p[j].y));
       c += p[j].z;
     }
@@ -175,32 +179,26 @@ __global__ void __launch_bounds__(kTisFinalThreads) tis_final_kernel(const uint4
     pair_add(hi, lo, ohi, olo);
     c += __shfl_xor_sync(0xffffffffu, c, d);
   }
-  __shared__ float whi[32], wlo[32];
-  __shared__ unsigned long long wc[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ unsigned long long wc64[kTisThreads / 32];
+  __syncthreads();  // the first tree's shared values are no longer read
   if (lane == 0) {
     whi[warp] = hi;
     wlo[warp] = lo;
-    wc[warp] = c;
+    wc64[warp] = c;
   }
   __syncthreads();
-  if (warp == 0) {
-    hi = whi[lane];
-    lo = wlo[lane];
-    c = wc[lane];
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float ohi = __shfl_xor_sync(0xffffffffu, hi, d);
-      const float olo = __shfl_xor_sync(0xffffffffu, lo, d);
-      pair_add(hi, lo, ohi, olo);
-      c += __shfl_xor_sync(0xffffffffu, c, d);
+  if (threadIdx.x == 0) {
+    float h = whi[0], l = wlo[0];
+    unsigned long long cc = wc64[0];
+    for (int i = 1; i < kTisThreads / 32; ++i) {
+      pair_add(h, l, whi[i], wlo[i]);
+      cc += wc64[i];
     }
-    if (lane == 0) {
-      const double sum = (double)hi + (double)lo;
-      out[0] = c ? sum / (double)c : 0.0;
-      out[1] = sum;
-      out[2] = (double)c;
-    }
+    const double sum = (double)h + (double)l;
+    out[0] = cc ? sum / (double)cc : 0.0;
+    out[1] = sum;
+    out[2] = (double)cc;
+    *ticket = 0u;  // ready for the next call on this workspace
   }
 }
 
@@ -209,9 +207,10 @@ __global__ void __launch_bounds__(kTisFinalThreads) tis_final_kernel(const uint4
 
 using namespace fp8rl;
 
+// workspace: a 16-byte header (the CTA ticket), then one 16-byte partial per CTA
 extern "C" FP8RL_API size_t fp8rl_tis_workspace_size(int64_t n) {
   if (n < 0) return 0;
-  return (size_t)tis_grid(n) * 16;
+  return 16 + (size_t)tis_grid(n) * 16;
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_tis_weights(const float* d_lp_train, const float* d_lp_rollout,
@@ -225,11 +224,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_tis_weights(const float* d_lp_train, con
       !aligned(d_workspace, 16))
     return FP8RL_ERR_ALIGNMENT;
   const int64_t grid = tis_grid(n);
-  uint4* part = static_cast<uint4*>(d_workspace);
+  uint32_t* ticket = static_cast<uint32_t*>(d_workspace);
+  uint4* part = static_cast<uint4*>(d_workspace) + 1;
   const int vec = aligned(d_lp_train, 16) && aligned(d_lp_rollout, 16) && aligned(d_w, 16) && aligned(d_mask, 4);
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  tis_partial_kernel<<<(unsigned)grid, kTisThreads, 0, cs>>>(d_lp_train, d_lp_rollout, d_mask, n, clip, d_w, part,
-                                                              vec);
-  tis_final_kernel<<<1, kTisFinalThreads, 0, cs>>>(part, (int)grid, d_kl);
+  tis_partial_kernel<<<(unsigned)grid, kTisThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      d_lp_train, d_lp_rollout, d_mask, n, clip, d_w, part, ticket, d_kl, vec);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }

@@ -433,11 +433,13 @@ FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t n, int64_t 
  *   d_w             device, fp32 [n] out: min(expf(lp_train - lp_rollout), clip), 0 if masked out
  *   d_kl            device, double [3] out: mean (0 with no token), sum, token count
  *   d_workspace     device scratch of fp8rl_tis_workspace_size(n) bytes, owned by the
- *                   caller, 16-byte aligned; needs no initial contents
+ *                   caller, 16-byte aligned; its first 16 bytes must be zero before its
+ *                   first use (zero it once when allocating it); every call leaves them
+ *                   zero.  One call at a time per workspace.
  * Each difference is made exact in fp32 (a TwoSum: rounded difference plus its
  * error term), accumulated as an fp32 pair and folded into fp64 every 64
  * tokens; the fp64 partials add up in an order fixed by n: the same bits on
- * every run.
+ * every run.  One launch.
  * Errors: INVALID_ARG (negative n, clip <= 0, null pointers, workspace too
  *         small), ALIGNMENT, CUDA.
  */

@@ -167,7 +167,7 @@ def test_fused_moe_qwen3_30b_a3b_sampled_rows():
     """128 experts, inter 768, k 2048, T = 4096 top-8 routing (32768 rows)."""
     fmt = fp8rl.SCALE_FP32
     r = synth.moe_routing(4096, synth.MOE_EXPERTS, synth.MOE_TOPK, 0, 0)
-    offsets = r.offsets
+    offsets = oracle.moe_dispatch_plan(r.topk, synth.MOE_EXPERTS)[0]
     rows_total, inter, k = int(offsets[-1]), synth.MOE_INTER, synth.MOE_HIDDEN
     x = synth.normal_bf16((rows_total, k), 1.0, 57, "fused-moe-x")
     xq, sx = oracle.quant_act_group(synth.bf16_bits(x))

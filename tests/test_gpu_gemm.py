@@ -200,25 +200,26 @@ def test_grouped_qwen3_30b_a3b_sampled(which):
     oracle evaluates the first and last row of every non-empty segment plus
     4096 random outputs."""
     r = synth.moe_routing(4096, 128, 8, seed=0, layer=0)
+    offsets = oracle.moe_dispatch_plan(r.topk, synth.MOE_EXPERTS)[0]
     n, k = (1536, 2048) if which == "gate_up" else (2048, 768)
-    rows = int(r.offsets[-1])
+    rows = int(offsets[-1])
     x = synth.normal_bf16((rows, k), 1.0, 0, "moe-x", which)
     xq, sx = oracle.quant_act_group(synth.bf16_bits(x))
     ws = synth.moe_expert_weights(n, k, 128, 0, 0, which)
     wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(ws.reshape(-1, k)))
     wq = wq.reshape(128, n, k)
     sw = sw.reshape(128, n // 128, k // 128)
-    y = run_grouped(r.offsets, xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    y = run_grouped(offsets, xq, sx, wq, sw, fp8rl.SCALE_FP32)
     rng = np.random.default_rng(5)
     edge_rows = []
     for e in range(128):
-        a, b = int(r.offsets[e]), int(r.offsets[e + 1])
+        a, b = int(offsets[e]), int(offsets[e + 1])
         if b > a:
             edge_rows += [a, b - 1]
     er = np.array(edge_rows)
     rr = np.concatenate([er, rng.integers(0, rows, 4096)])
     cc = np.concatenate([rng.integers(0, n, er.size), rng.integers(0, n, 4096)])
-    ref = oracle.grouped_gemm_blockscaled_at(xq, sx, wq, sw, r.offsets, rr, cc)
+    ref = oracle.grouped_gemm_blockscaled_at(xq, sx, wq, sw, offsets, rr, cc)
     within(y[rr, cc], ref)
 
 

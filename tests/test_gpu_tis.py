@@ -89,3 +89,19 @@ def test_tis_full_rollout_batch_and_determinism():
     assert fp8rl.fp8rl_sync_status() == 0
     assert torch.equal(w1, w2) and torch.equal(kl1, kl2)
     check(lt.cpu().numpy(), lr.cpu().numpy(), m.cpu().numpy())
+
+
+def test_tis_reuses_one_workspace_across_sizes():
+    """The workspace's header (the CTA ticket) is zeroed once and every call
+    leaves it zero: calls of different sizes (different grids) on one
+    workspace all match the oracle."""
+    ws = torch.zeros(fp8rl.fp8rl_tis_workspace_size(1 << 20), dtype=torch.uint8, device="cuda")
+    for n in (1 << 20, 5000, 1, 4096 * 3 + 1, 1 << 20):
+        lt, lr, m = synth.rollout_logprobs(1, n, seed=n % 97)
+        w, kl = fp8rl.tis_weights(lt.cuda(), lr.cuda(), m.cuda(), workspace=ws)
+        assert fp8rl.fp8rl_sync_status() == 0
+        mean, total, count = oracle.mismatch_kl(lt.numpy(), lr.numpy(), m.numpy())
+        d = np.abs(lt.numpy().astype(np.float64) - lr.numpy())
+        assert kl.cpu().numpy()[2] == count
+        assert abs(kl.cpu().numpy()[1] - total) <= 2.0 ** -36 * float(d[m.numpy() != 0].sum())
+    assert int(ws[:16].sum().item()) == 0
