@@ -53,13 +53,23 @@ constexpr int kUmmaK = 32;   // K of one E4M3 tcgen05.mma
 
 // EPI 0: bf16 Y.  EPI 1: the fused gate-up epilogue (SiLU(gate) * up kept in
 // fp32, quantised to E4M3 in 1x128 groups); needs 256-wide tiles.
-template <int BN, int AROWS = kBM, int EPI = 0>
+// OUT: finished tiles leave through shared memory and TMA stores (one
+// 32-row x 64-column bf16 box per epilogue warp, in a slot of its own), which
+// takes the operand ring down to what fits beside the slots.
+template <int BN, int AROWS = kBM, int EPI = 0, bool OUT = false>
 struct Cfg {
-  // operand stages: as many as fit in about 200 KB of shared memory
   static constexpr int kStageBytesRaw = AROWS * kBK + BN * kBK;
-  static constexpr int kStages = (200 * 1024) / kStageBytesRaw > 12 ? 12 : (200 * 1024) / kStageBytesRaw;
   static constexpr int kCols = 64;                      // accumulator columns per epilogue thread
   static constexpr int kEpiWarps = 4 * (BN / kCols);    // 4 TMEM lane quadrants x column slices
+  static constexpr int kOutSlotBytes = 32 * kCols * 2;  // one warp's 32 x 64 bf16 box
+  static constexpr int kOutBytes = OUT ? kEpiWarps * kOutSlotBytes : 0;
+  // operand stages: as many as fit in about 200 KB of shared memory, or, with
+  // the output slots, in the 227 KB a CTA may use
+  static constexpr int kStagesFit =
+      OUT ? (227 * 1024 - 3 * 1024 - 1024 - kOutBytes - 16 * (128 + 4) * 4 - (EPI ? 2 * 4 * 128 * 4 : 0)) /
+                kStageBytesRaw
+          : (200 * 1024) / kStageBytesRaw;
+  static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
   static constexpr int kThreads = 128 + kEpiWarps * 32; // warpgroup 0: producer, MMA, two idle warps
   // K chunks handed from the MMA issuer to the epilogue per synchronisation:
   // a 128-wide tile's TMEM buffer holds two chunk partials side by side
@@ -76,8 +86,10 @@ struct Cfg {
   static constexpr int kBookBytes = 1024;  // barriers and small shared state
   // fused epilogue: per-row maxima of the four column slices, two tiles deep
   static constexpr int kRedBytes = EPI ? 2 * 4 * kBM * 4 : 0;
-  static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4 + kRedBytes;
+  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4 + kRedBytes;
+  static constexpr int kOutOffset = (kSharedEnd + 1023) / 1024 * 1024;  // 1024-aligned for the 128-byte swizzle
+  static constexpr int kSmemBytes = 1024 + (OUT ? kOutOffset + kOutBytes : kSharedEnd);
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(EPI == 0 || BN == 256, "the fused epilogue pairs 128 gate with 128 up columns");
   static constexpr int kPartPitch = BN + 4;  // floats per row of a split-K partial tile
   static_assert(kBM * kPartPitch * 4 <= kStages * kStageBytes, "partial tile must fit over the stages");
@@ -303,11 +315,15 @@ __device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
 // stage holds just AROWS activation rows; the M = 128 MMA reads the rest of
 // its A rows from whatever shared memory follows, which only feeds accumulator
 // rows >= AROWS that are never stored.
-template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0>
+// OUT: finished tiles leave through shared memory and TMA stores (data-
+// parallel kernels with 128-row tiles; the host chooses it per launch).
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0, bool OUT = false>
 __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
-                            const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
-  using C = Cfg<BN, AROWS, EPI>;
+                            const __grid_constant__ CUtensorMap tmap_w,
+                            const __grid_constant__ CUtensorMap tmap_y, const GemmArgs a) {
+  static_assert(!OUT || (MODE == kDataParallel && EPI == 0 && AROWS == kBM), "staged output: data-parallel tiles");
+  using C = Cfg<BN, AROWS, EPI, OUT>;
   static_assert(EPI == 0 || MODE == kDataParallel, "the fused epilogue needs whole tiles");
   constexpr bool SPLITK = MODE == kSplitK;
   constexpr bool STREAMK = MODE == kStreamK;
@@ -331,6 +347,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   uint32_t* shared_epoch = reinterpret_cast<uint32_t*>(shared_m_tiles + 1);
   float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
   float* row_max = scale_ring + C::kScaleSlots * C::kScaleSlotFloats;  // fused epilogue only
+  uint8_t* out_slots = base_ptr + C::kOutOffset;                         // OUT only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_kb = a.k / kBK;
@@ -515,7 +532,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
                   tc_fence_after();
                   const uint32_t d = tmem + (buf * C::kGroup + j) * BN;
                   const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
-    #pragma unroll
+                  #pragma unroll
                   for (int k = 0; k < kBK / kUmmaK; ++k)
                     mma_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
                              k > 0 ? 1u : 0u);
@@ -550,11 +567,11 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
               uint32_t v[kLoadBatch][4];
               uint32_t w[kLoadBatch];
               int64_t vi[kLoadBatch][4], wi[kLoadBatch];
-    #pragma unroll
+              #pragma unroll
               for (int b = 0; b < kLoadBatch; ++b) {
                 const int kb = kb_lo + it0 + b;
                 const bool live = it0 + b < nloc;
-    #pragma unroll
+                #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   const int grow = tr.row0 + lane + 32 * j;
                   vi[b][j] = (int64_t)kb * a.rows + grow;
@@ -566,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
                 w[b] = (live && lane < BN / 128) ? __ldg(static_cast<const uint32_t*>(scale_word<UE8M0>(a.sw, wi[b])))
                                                    : 0u;
               }
-    #pragma unroll
+              #pragma unroll
               for (int b = 0; b < kLoadBatch; ++b) {
                 if (it0 + b >= nloc) break;
                 const int q = gs % C::kScaleSlots;
@@ -576,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
                 alive = __all_sync(0xffffffffu, got);
                 if (!alive) break;
                 float* slot = scale_ring + q * C::kScaleSlotFloats;
-    #pragma unroll
+                #pragma unroll
                 for (int j = 0; j < 4; ++j)
                   slot[lane + 32 * j] = tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
                 if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
@@ -970,7 +987,40 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
         }
       }
       if (store_y) {
-        if (ok && row_ok && !*abortv) {
+        bool staged = false;
+        if constexpr (OUT) {
+          // The warp's 32-row x 64-column box goes to its shared slot in the
+          // 128-byte swizzled layout (16-byte chunk c of row r at position
+          // c ^ (r mod 8): 8 lanes cover all banks) and leaves in one TMA
+          // store, so the warp moves on without waiting for global memory.
+          // Dense boxes may run past the last row (the store clips them);
+          // grouped boxes must lie inside the expert's segment, else the rows
+          // go out one by one below.
+          const int box_row0 = tr.row0 + quad * 32;
+          const bool box_ok = a.offsets == nullptr ? box_row0 < a.rows : box_row0 + 32 <= tr.seg_end;
+          if (__all_sync(0xffffffffu, ok && box_ok && !*abortv)) {
+            uint8_t* slot = out_slots + ew * C::kOutSlotBytes;
+            if (lane == 0) bulk_wait_group_read0();  // this slot's previous box has been read
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < C::kCols / 8; ++c) {
+              float x[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) f32x2_unpack(acc[4 * c + q], x[2 * q], x[2 * q + 1]);
+              *reinterpret_cast<uint4*>(slot + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                             pack_bf16x2(x[6], x[7]));
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_y, smem_u32(slot), n0 + slice * C::kCols, box_row0);
+              bulk_commit_group();
+            }
+            staged = true;
+          }
+        }
+        if (!staged && ok && row_ok && !*abortv) {
           // the row segment leaves as full 32-byte sectors (one 256-bit store
           // per 16 columns) when the output allows it
           uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
@@ -1007,6 +1057,12 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           prow[j] = v;
         }
       }
+    }
+    if constexpr (OUT) {
+      // every TMA store of this warp has completed before shared memory is
+      // released and the kernel ends
+      if (lane == 0) bulk_wait_group0();
+      __syncwarp();
     }
   }
   if (SPLITK) {
@@ -1086,6 +1142,7 @@ struct Debug {
   int splits = 0;                 // 0: choose; 1..8: force the split-K cluster size
   int streamk = 0;                // with a workspace: 0 choose, 1 never, 2 always (dense, M > 32)
   int streamk_grid = 0;           // 0: one CTA per SM (at most one per K iteration); else this many
+  int out_stage = 0;              // data-parallel tile stores: 0 choose, 1 through shared memory + TMA, 2 from registers
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -1110,6 +1167,20 @@ EncodeFn encode_fn() {
 }
 
 // row-major E4M3 matrix [outer][inner] (inner contiguous), boxes of box_outer rows x 128 bytes
+// bf16 output [rows][n] for the epilogue's TMA stores: boxes of 32 rows x 64
+// columns (128 bytes), 128-byte swizzle
+bool make_out_map(CUtensorMap* map, void* base, uint64_t n, uint64_t rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {n, rows};
+  cuuint64_t strides[1] = {n * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
@@ -1177,7 +1248,7 @@ struct KernelState {
   int cluster_capacity[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // clusters resident at once
 };
 
-template <int BN, int AROWS, bool UE8M0, int MODE, int EPI>
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI, bool OUT>
 KernelState& kernel_state(int dev) {
   static KernelState st[64];
   return st[dev];
@@ -1197,15 +1268,15 @@ StreamKLayout streamk_layout(int max_ctas) {
   return l;
 }
 
-template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0>
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0, bool OUT = false>
 fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_tiles_bound, int sms,
                     GemmArgs args, int splits, cudaStream_t stream, int streamk_grid = 0) {
-  using C = Cfg<BN, AROWS, EPI>;
+  using C = Cfg<BN, AROWS, EPI, OUT>;
   constexpr bool SPLITK = MODE == kSplitK;
-  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE, EPI>;
+  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE, EPI, OUT>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
-  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE, EPI>(dev);
+  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE, EPI, OUT>(dev);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!ks.ready) {
@@ -1233,9 +1304,14 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
     }
   }
   if (SPLITK && splits == 1) return FP8RL_ERR_UNSUPPORTED;  // the caller launches the plain kernel
-  CUtensorMap mx, mw;
+  CUtensorMap mx, mw, my;
   if (!make_map(&mx, xq, args.k, args.rows, AROWS)) return FP8RL_ERR_CUDA;
   if (!make_map(&mw, wq, args.k, (uint64_t)experts * args.n, BN)) return FP8RL_ERR_CUDA;
+  if (OUT) {
+    if (!make_out_map(&my, args.y, args.n, args.rows)) return FP8RL_ERR_CUDA;
+  } else {
+    my = mx;  // unused by this kernel
+  }
   args.splits = splits;
   // split-K: one CTA per (m-tile, n-tile, split); otherwise persistent CTAs,
   // at most one per SM, striding over the tiles
@@ -1259,12 +1335,12 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, args) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, my, args) != cudaSuccess) {
       cudaGetLastError();
       return FP8RL_ERR_CUDA;
     }
   } else if (!SPLITK) {
-    kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, args);
+    kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(mx, mw, my, args);
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -1278,7 +1354,7 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
     attr[0].val.clusterDim.z = splits;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, args) != cudaSuccess) return FP8RL_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, my, args) != cudaSuccess) return FP8RL_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
@@ -1378,11 +1454,23 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   if (short_a)
     return ue ? launch<128, 32, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
               : launch<128, 32, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+  // Tiles leave through shared memory and TMA stores when the per-tile store
+  // is a large share of a tile's time (few K chunks per tile) or a CTA runs
+  // many tiles; its slots cost the operand ring a stage, which deep-K
+  // kernels with few tiles per CTA feel more (measured on GB300: 8192 x 24576
+  // x 4096 +6%, grouped MoE +5..14%, 1024 x 24576 x 4096 -6% with it).
+  const bool staged = dbg.out_stage == 1 || (dbg.out_stage != 2 && (k <= 2048 || m_tiles * (n / bn) >= 8 * sms64));
   if (bn == 256) {
-    const fp8rl_status st = ue ? launch<256, kBM, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-                               : launch<256, kBM, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+    const fp8rl_status st =
+        staged ? (ue ? launch<256, kBM, true, kDataParallel, 0, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                     : launch<256, kBM, false, kDataParallel, 0, true>(xq, wq, experts, mt_bound, sms, args, 1, cs))
+               : (ue ? launch<256, kBM, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                     : launch<256, kBM, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs));
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
+  if (staged)
+    return ue ? launch<128, kBM, true, kDataParallel, 0, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+              : launch<128, kBM, false, kDataParallel, 0, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
   return ue ? launch<128, kBM, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
             : launch<128, kBM, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
 }
@@ -1550,6 +1638,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 8:
       if (value < 0 || value > 1024) return FP8RL_ERR_INVALID_ARG;
       g_debug.streamk_grid = (int)value;
+      return FP8RL_OK;
+    case 9:
+      if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
+      g_debug.out_stage = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

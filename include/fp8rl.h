@@ -357,6 +357,8 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          (default), 1 never, 2 always (m > 32);
  *   key 8  stream-K CTA count: 0 one per SM (default), else min(value, SMs),
  *          at most one per K iteration (1..1024);
+ *   key 9  how data-parallel GEMM tiles are stored: 0 chooses per shape
+ *          (default), 1 through shared memory and TMA stores, 2 from registers;
  *   key 0  restore all defaults.
  * Errors: INVALID_ARG for an unknown key or value.
  */

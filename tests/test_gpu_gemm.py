@@ -349,3 +349,52 @@ def test_stream_k_short_workspace_is_rejected(workspace):
         fp8rl.fp8rl_gemm_blockscaled_ws(xq, s, xq, s, y, 64, 128, 128, fp8rl.SCALE_FP32, workspace,
                                         workspace.numel() - 1)
     assert e.value.status == 1
+
+
+# --------------------------------------------------------------------------- tile stores
+
+@pytest.fixture
+def out_stage():
+    # small shapes would take split-K clusters: force the data-parallel kernel
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_SPLITS, 1)
+    yield
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, 0)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_SPLITS, 0)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m,n,k", [(300, 512, 512), (129, 384, 256), (1000, 768, 384), (33, 256, 256)])
+def test_tile_stores_through_shared_memory_match_register_stores(m, n, k, fmt, bn, out_stage):
+    """The data-parallel kernel stores finished tiles either from registers
+    or through shared memory and TMA stores (boxes of 32 rows clipped at the
+    last row): the same bits either way, and within tolerance of the oracle.
+    Rows past M keep what the output held."""
+    x = synth.activation_bf16(m, k, m + n, "stage-x")
+    w = synth.weight_bf16(n, k, m + k, "stage-w")
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    outs = []
+    for mode in (1, 2):
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, mode)
+        full = torch.full((m + 40, n), 7.0, dtype=torch.bfloat16, device="cuda")
+        fp8rl.gemm(dx, dsx, dw, dsw, fmt, out=full[:m])
+        assert fp8rl.fp8rl_sync_status() == 0
+        assert bool((full[m:] == 7.0).all())
+        outs.append(full[:m].cpu())
+    assert torch.equal(outs[0], outs[1])
+    within(outs[0].float().numpy(), oracle.gemm_blockscaled(xq, sx, wq, sw, fmt))
+
+
+@pytest.mark.parametrize("counts", [[3, 0, 200, 129], [64, 31, 1, 160], [256, 256], [40, 0, 300]])
+def test_grouped_tile_stores_respect_segment_ends(counts, bn, out_stage):
+    """Grouped: boxes that would cross a segment end are stored row by row;
+    both store paths give the same bits and leave rows outside the offsets
+    untouched."""
+    n, k = 256, 384
+    offsets, xq, sx, wq, sw = grouped_case(counts, n, k, fp8rl.SCALE_FP32, 7 + sum(counts))
+    outs = []
+    for mode in (1, 2):
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, mode)
+        outs.append(run_grouped(offsets, xq, sx, wq, sw, fp8rl.SCALE_FP32, fill=3.0))
+    assert np.array_equal(outs[0], outs[1])
+    within(outs[0], oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, fp8rl.SCALE_FP32))
