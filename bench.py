@@ -44,10 +44,10 @@ STEP_M = 8192          # tokens in the step's forward batch
 # Reported only while the GEMM's sources are those the capture was taken with.
 TRAFFIC = {
     "gemm_gate_up": {
-        "bytes": 142.233856e6 + 374.807552e6,
+        "bytes": 146.484992e6 + 370.831104e6,
         "sources": {
-            "gemm.cu": "853a1b4464eafdd7fa4f70a5755ecc8a2e2f19dab366aa90c6843fe70a561ec1",
-            "ptx.cuh": "cc21b686c76ecef323c84f536a43bd0f7ca9e54117acd193a2f79a8f60e5685e",
+            "gemm.cu": "491a7b595a95a357a0ab76e09507e88af8cf81cd929f5a9e8373f1c66865c9d4",
+            "ptx.cuh": "463915e06bd7baebb37b3b835d1bf73d06ee907eb2d78aaedc6a2c8c07e89cbe",
             "common.cuh": "ce22f13b50d69d05f583fb60eb22375700c10e0326d46e23e9ac29b79ecfa620",
         },
     },
