@@ -87,7 +87,7 @@ def parse():
     ap.add_argument("--case", default=None,
                     help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
                          "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt], kv:TOKENS, "
-                         "moe_plan, moe_dispatch, moe_combine, tis[:RESPONSES]")
+                         "kvcal:TOKENS, moe_plan, moe_dispatch, moe_combine, tis[:RESPONSES]")
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
     ap.add_argument("--wait-mode", type=int, default=0, help="with --case: GEMM wait style (test hook 4)")
     ap.add_argument("--l2-prefetch", type=int, default=-1, help="with --case: GEMM L2 prefetch distance (test hook 5)")
@@ -990,6 +990,13 @@ def main_case(args):
         else:
             fn = lambda: fp8rl.fp8rl_gemm_swiglu_quant(d["xq"], d["sx"], d["wq"], d["sw"], m, inter, k, hq, hs, fmt)
         work = {"flops": 2.0 * m * 2 * inter * k}
+    elif kind == "kvcal":
+        tokens = int(parts[1])
+        k, v, _, _, _ = kv_inputs(torch, synth, dev, 0, tokens, tokens)
+        q = synth.normal_bf16((tokens, Q_DIM), 1.0, 0, "case-kv-q", device=dev)
+        scales = torch.zeros(3, dtype=torch.float32, device=dev)
+        fn = lambda: fp8rl.kv_calibrate(k, v, q, out=scales)
+        work = {"bytes": tokens * (2 * KV_DIM + Q_DIM) * 2}
     elif kind == "kv":
         tokens = int(parts[1])
         k, v, slots, kc, vc = kv_inputs(torch, synth, dev, 0, tokens, max(65536, tokens))
