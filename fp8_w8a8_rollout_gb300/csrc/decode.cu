@@ -1,0 +1,429 @@
+// decode.cu -- the block-scaled W8A8 GEMM for decode-sized M (at most 32
+// tokens), with the operands swapped.
+//
+// Same product as gemm.cu (FP8-RL page, "Method steps": E4M3 operands, one
+// scale per 128x128 weight block and per 1x128 activation group, fp32
+// accumulation, one bf16 rounding): Y[m][n] = bf16(sum over 128-wide K chunks
+// kb of sx[kb][m] * sw[n/128][kb] * P_kb[m][n]).  At decode sizes the weights
+// are the whole cost (HBM-bound), so the tensor-core tile is turned around:
+// the MMA's 128 rows are 128 weight rows and its N is the token count padded
+// to NT = 16 or 32.  A CTA's accumulator is then 128 x NT fp32 (32 or 64 TMEM
+// columns for two buffers), four epilogue warps promote each chunk with NT
+// multiply-adds per thread (instead of a 128 x 128 tile of which 16 or 32 rows
+// are real), and every operand stage carries 16 KB of weights and only NT
+// rows of activations.  (The occupancy query reports one CTA per SM for this
+// kernel on GB300 whatever its registers and shared memory, so the split
+// count is bounded by the clusters that fit at once, as for the 128-row-tile
+// kernel.)  Measured on GB300 at 16 tokens: 24576 x 4096 weights 30 -> 21 us,
+// 6144 / 4096 x 4096 and 4096 x 12288 5-8% faster.
+//
+// Split K: a cluster of `splits` CTAs (grid y) shares one 128-row weight
+// block, each a contiguous K range; their fp32 partials meet through
+// distributed shared memory, summed in rank order.
+//
+// Roles (192 threads): warp 0 lane 0 the TMA producer, warp 1 the TMEM
+// allocator and (lane 0) the MMA issuer, warps 2-5 the epilogue (TMEM lane
+// quadrant = warp mod 4, thread = weight row).  Every wait is bounded, as in
+// gemm.cu: on expiry the CTA raises its abort flag and the device error word,
+// all roles leave their loops, and every thread still reaches the cluster
+// barriers and the common teardown.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8rl {
+namespace {
+
+using namespace ptx;
+
+constexpr int kDecThreads = 192;
+constexpr int kDecStages = 5;
+constexpr int kDecRows = 128;   // weight rows per tile (the MMA's M)
+constexpr int kDecWBytes = kDecRows * 128;  // one 128-wide K chunk of the weight block
+
+struct DecArgs {
+  const void* sx;  // [K/128][rows] fp32 or UE8M0 bytes
+  const void* sw;  // [N/128][K/128]
+  __nv_bfloat16* y;
+  int32_t rows, n, k, splits;
+  uint32_t* err;
+  uint64_t timeout_ns;
+  int32_t fault_skip_kb;  // test hook: the producer never fills this K chunk (-1: off)
+};
+
+template <int NT>
+struct DecCfg {
+  static constexpr int kXBytes = NT * 128;
+  static constexpr int kStageBytes = kDecWBytes + kXBytes;
+  static constexpr int kTmemCols = 2 * NT < 32 ? 32 : 2 * NT;  // two accumulator buffers
+  static constexpr int kSmemBytes = 1024 + kDecStages * kStageBytes + 256;
+  static_assert(kDecRows * NT * 4 <= kDecWBytes, "the split partial fits over one weight stage");
+};
+
+// a scale as fp32: the word holding it (a UE8M0 byte sits in an aligned
+// 32-bit word), decoded as gemm.cu does: byte b -> 2^(b - 127)
+template <bool UE8M0>
+__device__ __forceinline__ float dec_scale(const void* p, int64_t idx) {
+  if (UE8M0) {
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(p) + (idx & ~(int64_t)3)));
+    const uint32_t b = (w >> (8 * (idx & 3))) & 0xFFu;
+    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+  }
+  return __ldg(static_cast<const float*>(p) + idx);
+}
+
+// TMEM allocation with the column count as an immediate operand
+template <uint32_t NCOLS>
+__device__ __forceinline__ void tmem_alloc_n(uint32_t slot_smem) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "n"(NCOLS)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+template <int NT>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[NT]) {
+  if constexpr (NT == 32) {
+    tmem_ld_32x32b_x32(taddr, v);
+  } else {
+    tmem_ld_32x32b_x16(taddr, v);
+  }
+}
+
+template <int NT, bool UE8M0>
+__global__ void __launch_bounds__(kDecThreads, 2)
+    gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                       const DecArgs a) {
+  using C = DecCfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sW = base;                                 // kDecStages x 16 KB
+  const uint32_t sX = base + kDecStages * kDecWBytes;       // kDecStages x NT x 128 B
+  uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + kDecStages * C::kStageBytes);
+  uint64_t* empty = full + kDecStages;
+  uint64_t* tfull = empty + kDecStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* abortv = abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = blockIdx.x;
+  const int splits = a.splits;
+  const int split = splits > 1 ? (int)cluster_ctarank() : 0;
+  const int num_kb = a.k / 128;
+  const int kb_lo = (int)((int64_t)num_kb * split / splits);
+  const int nloc = (int)((int64_t)num_kb * (split + 1) / splits) - kb_lo;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc_n<C::kTmemCols>(smem_u32(tmem_slot));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_w);
+      prefetch_tensormap(&tmap_x);
+      int it = 0;
+      for (; it < nloc; ++it) {
+        const int s = it % kDecStages;
+        const uint32_t ph = (it / kDecStages) & 1;
+        if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns)) break;
+        const int kb = kb_lo + it;
+        if (kb == a.fault_skip_kb) continue;  // the MMA's wait on this stage runs out
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        tma_load_2d(sW + s * kDecWBytes, &tmap_w, kb * 128, nblk * kDecRows, fb);
+        tma_load_2d(sX + s * C::kXBytes, &tmap_x, kb * 128, 0, fb);
+      }
+      if (*abortv) {
+        // let the copies still in flight land before shared memory is released
+        for (int j = it > kDecStages ? it - kDecStages : 0; j < it; ++j)
+          if (kb_lo + j != a.fault_skip_kb)
+            mbar_wait_bounded(smem_u32(&full[j % kDecStages]), (j / kDecStages) & 1, nullptr, nullptr, 10000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kDecRows, NT);
+      for (int it = 0; it < nloc; ++it) {
+        const int buf = it & 1;
+        const uint32_t bph = (it >> 1) & 1;
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns)) break;
+        const int s = it % kDecStages;
+        const uint32_t ph = (it / kDecStages) & 1;
+        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t a0 = sW + s * kDecWBytes, b0 = sX + s * C::kXBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_e4m3(tmem + buf * NT, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
+                   kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&empty[s]));
+        mma_commit(smem_u32(&tfull[buf]));
+      }
+      if (*abortv) {
+        // no MMA may still be writing TMEM when it is released
+        mma_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;  // weight row within the block
+  float acc[NT];
+#pragma unroll
+  for (int m = 0; m < NT; ++m) acc[m] = 0.0f;
+  bool ok = true;
+  if (warp >= 2) {
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    for (int it = 0; it < nloc; ++it) {
+      const int kb = kb_lo + it;
+      // this chunk's scales, loaded before the wait: the weight block's and
+      // one per token (all lanes read the same words)
+      const float swv = dec_scale<UE8M0>(a.sw, (int64_t)nblk * num_kb + kb);
+      float f[NT];
+#pragma unroll
+      for (int m = 0; m < NT; ++m) f[m] = m < a.rows ? dec_scale<UE8M0>(a.sx, (int64_t)kb * a.rows + m) : 0.0f;
+      const int buf = it & 1;
+      const uint32_t bph = (it >> 1) & 1;
+      ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[NT];
+      tmem_ld_cols<NT>(t_lane + buf * NT, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+      // the activation scale times the weight scale, then one fused
+      // multiply-add per token: the 128-row-tile kernel's arithmetic
+#pragma unroll
+      for (int m = 0; m < NT; ++m) acc[m] = fmaf(__uint_as_float(v[m]), f[m] * swv, acc[m]);
+    }
+  }
+  __syncthreads();  // every MMA has been consumed: the operand stages are free
+  const bool write = !*abortv;
+  float* part = reinterpret_cast<float*>(base_ptr);  // [NT][128] fp32 over the first weight stage
+  if (splits == 1) {
+    if (warp >= 2 && write) {
+      __nv_bfloat16* dst = a.y + (int64_t)nblk * kDecRows + row;
+#pragma unroll
+      for (int m = 0; m < NT; ++m)  // a constant bound keeps acc in registers
+        if (m < a.rows) dst[(int64_t)m * a.n] = __float2bfloat16_rn(acc[m]);
+    }
+  } else {
+    if (warp >= 2) {
+#pragma unroll
+      for (int m = 0; m < NT; ++m) part[m * kDecRows + row] = acc[m];
+    }
+    cluster_sync();  // every CTA's partial is in its shared memory
+    if (write) {
+      // this CTA's share of the (token, row) outputs, each the sum of the
+      // cluster's partials in rank order
+      const int total = a.rows * kDecRows;
+      const int i0 = (int)((int64_t)total * split / splits), i1 = (int)((int64_t)total * (split + 1) / splits);
+      const uint32_t pbase = smem_u32(part);
+      for (int i = i0 + (int)threadIdx.x; i < i1; i += kDecThreads) {
+        float sum = 0.0f;
+        for (int r = 0; r < splits; ++r) {
+          float x;
+          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(mapa_shared(pbase + 4u * i, r)) : "memory");
+          sum += x;
+        }
+        const int m = i / kDecRows, nr = i - m * kDecRows;
+        a.y[(int64_t)m * a.n + (int64_t)nblk * kDecRows + nr] = __float2bfloat16_rn(sum);
+      }
+    }
+    cluster_sync();  // no CTA leaves while its partial may still be read
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// E4M3 [outer][inner] row-major, boxes of box_outer rows x 128 bytes, 128-byte
+// swizzle (rows past `outer` read as zeros)
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DecState {
+  bool ready = false, ok = false;
+  int sms = 0;
+  int capacity[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // clusters of each size resident at once
+};
+
+template <int NT, bool UE8M0>
+DecState& dec_state(int dev) {
+  static DecState st[64];
+  return st[dev];
+}
+
+std::mutex g_dec_mu;
+
+template <int NT, bool UE8M0>
+fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0, int force_splits,
+                           cudaStream_t stream) {
+  using C = DecCfg<NT>;
+  auto kernel = gemm_decode_kernel<NT, UE8M0>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
+  DecState& st = dec_state<NT, UE8M0>(dev);
+  DecArgs args = args0;
+  const int nblocks = args.n / kDecRows;
+  const int num_kb = args.k / 128;
+  int splits = 1;
+  {
+    std::lock_guard<std::mutex> lock(g_dec_mu);
+    if (!st.ready) {
+      int sms = 0;
+      st.ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0 &&
+              cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==
+                  cudaSuccess &&
+              cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess &&
+              // the whole unified L1 as shared memory, so that two CTAs fit on an SM
+              cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                   cudaSharedmemCarveoutMaxShared) == cudaSuccess;
+      st.sms = sms;
+      st.ready = true;
+    }
+    if (!st.ok) return FP8RL_ERR_UNSUPPORTED;
+    // K splits so that about two CTAs run on every SM, each with >= 2 chunks
+    if (force_splits > 0) {
+      splits = std::min(std::min(force_splits, 8), num_kb);
+    } else {
+      while (splits < 8 && (int64_t)nblocks * (splits + 1) <= 2 * (int64_t)st.sms && num_kb / (splits + 1) >= 2)
+        ++splits;
+    }
+    // only as many splits as leave every cluster resident at once
+    while (splits > 1) {
+      if (st.capacity[splits] < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nblocks, (unsigned)splits, 1);
+        cfg.blockDim = dim3(kDecThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = splits;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        st.capacity[splits] = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess ? n : 0;
+        cudaGetLastError();
+      }
+      if (st.capacity[splits] >= nblocks) break;
+      --splits;
+    }
+  }
+  args.splits = splits;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, wq, args.k, args.n, kDecRows)) return FP8RL_ERR_CUDA;
+  if (!make_map(&mx, xq, args.k, args.rows, NT)) return FP8RL_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nblocks, (unsigned)splits, 1);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kernel, mw, mx, args) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8RL_ERR_CUDA;
+  }
+  return FP8RL_OK;
+}
+
+}  // namespace
+
+// Called by the GEMM entry points for dense products with rows <= 32 (the
+// arguments already validated); UNSUPPORTED lets the caller fall back to the
+// 128-row-tile kernel.
+fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale, void* y,
+                         int64_t rows, int64_t n, int64_t k, bool ue8m0, uint32_t* err, uint64_t timeout_ns,
+                         int fault_skip_kb, int force_splits, cudaStream_t stream) {
+  if (rows < 1 || rows > 32 || n % kDecRows || k % 128) return FP8RL_ERR_UNSUPPORTED;
+  DecArgs a{};
+  a.sx = x_scale;
+  a.sw = w_scale;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.rows = (int32_t)rows;
+  a.n = (int32_t)n;
+  a.k = (int32_t)k;
+  a.err = err;
+  a.timeout_ns = timeout_ns;
+  a.fault_skip_kb = fault_skip_kb;
+  if (rows <= 16)
+    return ue8m0 ? launch_decode<16, true>(xq, wq, a, force_splits, stream)
+                 : launch_decode<16, false>(xq, wq, a, force_splits, stream);
+  return ue8m0 ? launch_decode<32, true>(xq, wq, a, force_splits, stream)
+               : launch_decode<32, false>(xq, wq, a, force_splits, stream);
+}
+
+}  // namespace fp8rl

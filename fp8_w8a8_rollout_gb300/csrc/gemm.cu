@@ -42,6 +42,10 @@ namespace fp8rl {
 
 uint32_t* device_error_word();  // api.cu
 void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* status);  // static_scratch.cu
+// decode.cu: dense products with at most 32 rows, operands swapped (UNSUPPORTED: use this file's kernel)
+fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale, void* y,
+                         int64_t rows, int64_t n, int64_t k, bool ue8m0, uint32_t* err, uint64_t timeout_ns,
+                         int fault_skip_kb, int force_splits, cudaStream_t stream);
 
 namespace {
 
@@ -1143,6 +1147,7 @@ struct Debug {
   int streamk = 0;                // with a workspace: 0 choose, 1 never, 2 always (dense, M > 32)
   int streamk_grid = 0;           // 0: one CTA per SM (at most one per K iteration); else this many
   int out_stage = 0;              // data-parallel tile stores: 0 choose, 1 through shared memory + TMA, 2 from registers
+  int decode = 0;                 // dense rows <= 32: 0 choose, 1 the swapped-operand decode kernel, 2 the 128-row-tile one
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -1385,6 +1390,17 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   args.fault_skip_kb = dbg.fault_skip_kb;
   args.wait_mode = dbg.wait_mode;
   args.l2_prefetch = dbg.l2_prefetch;
+  // decode sizes (dense): the swapped-operand kernel of decode.cu for at most
+  // 16 rows, or 32 when the weight has a 128-row block per SM (no split
+  // needed); measured on GB300, with 17..32 rows and a K split the 128-row-tile
+  // kernel is as fast or faster.  The test hook forces either.
+  const bool decode_shape = !d_offsets && rows <= 32 && (rows <= 16 || n / 128 >= di.sms || dbg.decode == 1);
+  if (decode_shape && dbg.decode != 2 && dbg.streamk != 2) {
+    const fp8rl_status st = decode_gemm(xq, x_scale, wq, w_scale, y, rows, n, k, fmt == FP8RL_SCALE_UE8M0, err,
+                                        dbg.timeout_ns, dbg.fault_skip_kb, dbg.splits,
+                                        static_cast<cudaStream_t>(stream));
+    if (st != FP8RL_ERR_UNSUPPORTED) return st;
+  }
   const int64_t m_tiles = (rows + kBM - 1) / kBM;
   // Tile width by estimated time: whole waves of tiles x the time of one tile.
   // Measured on GB300 (K = 4096): a 128 x 256 tile takes ~1.35x as long as a
@@ -1642,6 +1658,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 9:
       if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
       g_debug.out_stage = (int)value;
+      return FP8RL_OK;
+    case 10:
+      if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
+      g_debug.decode = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

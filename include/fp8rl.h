@@ -359,6 +359,10 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          at most one per K iteration (1..1024);
  *   key 9  how data-parallel GEMM tiles are stored: 0 chooses per shape
  *          (default), 1 through shared memory and TMA stores, 2 from registers;
+ *   key 10 dense GEMMs with at most 32 rows: 0 chooses (default: the
+ *          swapped-operand decode kernel for <= 16 rows, or <= 32 when the
+ *          weight has a 128-row block per SM), 1 always that kernel, 2 the
+ *          128-row-tile kernel;
  *   key 0  restore all defaults.
  * Errors: INVALID_ARG for an unknown key or value.
  */

@@ -171,6 +171,8 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 8, 7) == 0
     assert _rc("fp8rl_debug_set", 9, 3) == 1
     assert _rc("fp8rl_debug_set", 9, 1) == 0
+    assert _rc("fp8rl_debug_set", 10, 3) == 1
+    assert _rc("fp8rl_debug_set", 10, 2) == 0
     assert _rc("fp8rl_debug_set", 1, 256) == 0
     assert _rc("fp8rl_debug_set", 0, 0) == 0
 

@@ -398,3 +398,46 @@ def test_grouped_tile_stores_respect_segment_ends(counts, bn, out_stage):
         outs.append(run_grouped(offsets, xq, sx, wq, sw, fp8rl.SCALE_FP32, fill=3.0))
     assert np.array_equal(outs[0], outs[1])
     within(outs[0], oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, fp8rl.SCALE_FP32))
+
+
+# --------------------------------------------------------------------------- decode kernel
+
+@pytest.fixture
+def decode_mode():
+    yield
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, 0)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_SPLITS, 0)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("m,n,k,splits", [(16, 6144, 4096, 0), (1, 4096, 4096, 0), (32, 4096, 12288, 0),
+                                          (17, 384, 640, 3), (5, 256, 1280, 8), (31, 128, 256, 2),
+                                          (16, 24576, 4096, 0)])
+def test_decode_kernel_matches_oracle_and_tile_kernel(m, n, k, splits, fmt, decode_mode):
+    """At most 32 rows the dense GEMM runs the swapped-operand decode kernel
+    (weight rows as the MMA's M, tokens as its N, split K over a cluster);
+    within tolerance of the oracle over the whole output, and of the
+    128-row-tile kernel that the test hook selects instead."""
+    x = synth.activation_bf16(m, k, m + 3, "dec-x", n)
+    w = synth.weight_bf16(n, k, k + 5, "dec-w")
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    ref = oracle.gemm_blockscaled(xq, sx, wq, sw, fmt)
+    if splits:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_SPLITS, splits)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, 1)
+    y_dec = run_gemm(xq, sx, wq, sw, fmt)
+    within(y_dec, ref)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, 2)
+    y_tile = run_gemm(xq, sx, wq, sw, fmt)
+    within(y_tile, ref)
+    # both round once from fp32 sums of the same products (orders differ)
+    assert np.max(np.abs(y_dec - y_tile)) <= 2.0 ** -7 * np.max(np.abs(ref)) + 1e-6
+
+
+def test_decode_kernel_is_deterministic(decode_mode):
+    x = synth.activation_bf16(16, 4096, 3, "dec-det")
+    w = synth.weight_bf16(6144, 4096, 4, "dec-det-w")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    a = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    b = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    assert np.array_equal(a, b)
