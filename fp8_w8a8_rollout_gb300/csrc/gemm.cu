@@ -457,7 +457,12 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   volatile int* abortv = abort_flag;
 
   if (warp < 4) {
-    if (C::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(STREAMK ? C::kRoleRegsStreamK : C::kRoleRegs));
+    // the UE8M0 scale loader (byte decode) with staged tile stores runs
+    // better with the stream-K budget (measured on GB300: 8192 x 24576 x 4096
+    // 788 -> 756 us); with register stores the extra registers cost 4-7%
+    if (C::kSplitRegs)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((STREAMK || (UE8M0 && OUT)) ? C::kRoleRegsStreamK
+                                                                                       : C::kRoleRegs));
     if constexpr (!STREAMK) {
       // Data-parallel and split-K: plain loops over whole tiles (or the
       // cluster's one tile).  These loops are latency-critical; measured on
