@@ -1475,12 +1475,11 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   if (short_a)
     return ue ? launch<128, 32, true, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs)
               : launch<128, 32, false, kDataParallel>(xq, wq, experts, mt_bound, sms, args, 1, cs);
-  // Tiles leave through shared memory and TMA stores when the per-tile store
-  // is a large share of a tile's time (few K chunks per tile) or a CTA runs
-  // many tiles; its slots cost the operand ring a stage, which deep-K
-  // kernels with few tiles per CTA feel more (measured on GB300: 8192 x 24576
-  // x 4096 +6%, grouped MoE +5..14%, 1024 x 24576 x 4096 -6% with it).
-  const bool staged = dbg.out_stage == 1 || (dbg.out_stage != 2 && (k <= 2048 || m_tiles * (n / bn) >= 8 * sms64));
+  // Tiles leave through shared memory and TMA stores unless K is deep: the
+  // slots cost the operand ring a stage, which only deep-K tiles feel more
+  // than the store they save (measured on GB300: 8192 x 24576 x 4096 +6%,
+  // 1024 x 6144 x 4096 +5%, grouped MoE +5..14%; 8192 x 4096 x 12288 -3%).
+  const bool staged = dbg.out_stage == 1 || (dbg.out_stage != 2 && k <= 4096);
   if (bn == 256) {
     const fp8rl_status st =
         staged ? (ue ? launch<256, kBM, true, kDataParallel, 0, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
