@@ -691,7 +691,7 @@ def moe_layer_inputs(torch, synth, fp8rl, dev, seed):
                                              d["ws"].numel())
     d["dispatch"] = lambda: fp8rl.fp8rl_moe_dispatch_quant(d["x"], t, h, h, d["rop"], k, rows, d["xq"], h, d["sx"],
                                                            0)
-    d["combine"] = lambda: fp8rl.fp8rl_moe_combine(d["y"], h, h, d["rop"], d["gate"], t, k, d["out"], h)
+    d["combine"] = lambda: fp8rl.fp8rl_moe_combine(d["y"], rows, h, h, d["rop"], d["gate"], t, k, d["out"], h)
     d["plan"]()
     # algorithmic bytes: hidden states read once, codes + scales + row map
     # written; combine: k expert rows read, one row written, plus the map

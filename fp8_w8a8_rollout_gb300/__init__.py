@@ -93,7 +93,7 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_moe_plan_workspace_size": [i64, i64, i64],
             "fp8rl_moe_plan": [vp, i64, i64, i64, vp, vp, vp, vp, ctypes.c_size_t, vp],
             "fp8rl_moe_dispatch_quant": [vp, i64, i64, i64, vp, i64, i64, vp, i64, vp, st, vp],
-            "fp8rl_moe_combine": [vp, i64, i64, vp, vp, i64, i64, vp, i64, vp],
+            "fp8rl_moe_combine": [vp, i64, i64, i64, vp, vp, i64, i64, vp, i64, vp],
             "fp8rl_tis_workspace_size": [i64],
             "fp8rl_tis_weights": [vp, vp, vp, i64, ctypes.c_float, vp, vp, vp, ctypes.c_size_t, vp],
             "fp8rl_debug_set": [i32, i64],
@@ -236,8 +236,9 @@ def fp8rl_moe_dispatch_quant(x_bf16, tokens, k, ldx, d_row_of_pair, topk, rows, 
         "fp8rl_moe_dispatch_quant")
 
 
-def fp8rl_moe_combine(y_bf16, n, ldy, d_row_of_pair, d_gate, tokens, topk, out_bf16, ldo, stream=None) -> None:
-    _ok(load_library().fp8rl_moe_combine(_p(y_bf16), n, ldy, _p(d_row_of_pair), _p(d_gate), tokens, topk,
+def fp8rl_moe_combine(y_bf16, rows, n, ldy, d_row_of_pair, d_gate, tokens, topk, out_bf16, ldo,
+                      stream=None) -> None:
+    _ok(load_library().fp8rl_moe_combine(_p(y_bf16), rows, n, ldy, _p(d_row_of_pair), _p(d_gate), tokens, topk,
                                          _p(out_bf16), ldo, _stream(stream)),
         "fp8rl_moe_combine")
 
@@ -502,7 +503,7 @@ def moe_combine(y: torch.Tensor, row_of_pair: torch.Tensor, gate: torch.Tensor, 
     tokens, k = gate.shape
     n = y.shape[1]
     o = out if out is not None else torch.empty((tokens, n), dtype=torch.bfloat16, device=y.device)
-    fp8rl_moe_combine(y, n, y.stride(0), row_of_pair, gate, tokens, k, o, o.stride(0), stream)
+    fp8rl_moe_combine(y, y.shape[0], n, y.stride(0), row_of_pair, gate, tokens, k, o, o.stride(0), stream)
     return o
 
 

@@ -467,7 +467,7 @@ int ctas_per_sm(K kernel, int threads) {
 // share them); the 8 source loads of a slot group are issued before their
 // multiply-adds.
 __global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
-    const uint16_t* __restrict__ y, int64_t n, int64_t ldy, const int32_t* __restrict__ row_of_pair,
+    const uint16_t* __restrict__ y, int32_t y_rows, int64_t n, int64_t ldy, const int32_t* __restrict__ row_of_pair,
     const float* __restrict__ gate, int32_t tokens, int32_t topk, uint16_t* __restrict__ out, int64_t ldo,
     int32_t pieces, int vec) {
   const int32_t total = tokens * pieces;  // the host keeps this below 2^31
@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         rows[j] = j0 + j < topk ? __ldg(rp + j0 + j) : -1;
+        if (rows[j] >= y_rows) rows[j] = -1;  // a row y does not have adds nothing
         ws[j] = j0 + j < topk ? __ldg(gp + j0 + j) : 0.0f;
       }
 #pragma unroll
@@ -601,22 +602,23 @@ extern "C" FP8RL_API fp8rl_status fp8rl_moe_dispatch_quant(const void* x_bf16, i
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 
-extern "C" FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t n, int64_t ldy,
+extern "C" FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t rows, int64_t n, int64_t ldy,
                                                     const int32_t* d_row_of_pair, const float* d_gate,
                                                     int64_t tokens, int64_t topk, void* out_bf16, int64_t ldo,
                                                     void* stream) {
-  if (n < 0 || tokens < 0 || topk < 1 || topk > kMaxTopk || ldy < n || ldo < n) return FP8RL_ERR_INVALID_ARG;
+  if (rows < 0 || n < 0 || tokens < 0 || topk < 1 || topk > kMaxTopk || ldy < n || ldo < n)
+    return FP8RL_ERR_INVALID_ARG;
   if (tokens == 0 || n == 0) return FP8RL_OK;
-  if (!y_bf16 || !d_row_of_pair || !d_gate || !out_bf16) return FP8RL_ERR_INVALID_ARG;
+  if ((rows > 0 && !y_bf16) || !d_row_of_pair || !d_gate || !out_bf16) return FP8RL_ERR_INVALID_ARG;
   if (!aligned(y_bf16, 2) || !aligned(out_bf16, 2) || !aligned(d_row_of_pair, 4) || !aligned(d_gate, 4))
     return FP8RL_ERR_ALIGNMENT;
   const int64_t pieces = (n + 7) / 8;
-  if (tokens * pieces > (int64_t)INT32_MAX - (1 << 20)) return FP8RL_ERR_SHAPE;
+  if (rows > INT32_MAX || tokens * pieces > (int64_t)INT32_MAX - (1 << 20)) return FP8RL_ERR_SHAPE;
   const int vec = aligned(y_bf16, 16) && aligned(out_bf16, 16) && (ldy * 2) % 16 == 0 && (ldo * 2) % 16 == 0;
   const int64_t ctas = (tokens * pieces + kCombineThreads - 1) / kCombineThreads;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)sm_count() * combine_ctas_per_sm()));
   moe_combine_kernel<<<(unsigned)grid, kCombineThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint16_t*>(y_bf16), n, ldy, d_row_of_pair, d_gate, (int32_t)tokens, (int32_t)topk,
+      static_cast<const uint16_t*>(y_bf16), (int32_t)rows, n, ldy, d_row_of_pair, d_gate, (int32_t)tokens, (int32_t)topk,
       static_cast<uint16_t*>(out_bf16), ldo, (int32_t)pieces, vec);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }

@@ -414,17 +414,21 @@ FP8RL_API fp8rl_status fp8rl_moe_dispatch_quant(const void* x_bf16, int64_t toke
 /*
  * MoE combine: out[t] = sum over j of gate[t][j] * y[row_of_pair[t * topk + j]],
  * fp32 multiply-adds in slot order, rounded once to bf16 (nearest-even);
- * slots with row -1 add nothing.  The gates are an input: the router's
+ * slots with row -1, or a row outside [0, rows), add nothing (a token none
+ * of whose slots has a row gets zeros).  The gates are an input: the router's
  * weights of the recorded experts (replaying indices fixes which experts run,
  * not how their outputs are weighted).
- *   y_bf16          device, bf16 [rows][ldy] (the grouped GEMM's output)
+ *   y_bf16          device, bf16 [rows][ldy] (the grouped GEMM's output);
+ *                   may be null when rows == 0
+ *   rows            y's row count (the plan's offsets[experts] is enough)
  *   d_row_of_pair   device, int32 [tokens * topk] (fp8rl_moe_plan's output)
  *   d_gate          device, fp32 [tokens][topk]
  *   out_bf16        device, bf16 [tokens][ldo]
- * 1 <= topk <= 32.  Errors: INVALID_ARG, SHAPE (tokens * ceil(n/8) >= 2^31 - 2^20),
- *         ALIGNMENT (element alignment), CUDA.
+ * 1 <= topk <= 32.  Errors: INVALID_ARG, SHAPE (rows >= 2^31, or
+ *         tokens * ceil(n/8) >= 2^31 - 2^20), ALIGNMENT (element alignment), CUDA.
  */
-FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t n, int64_t ldy, const int32_t* d_row_of_pair,
+FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t rows, int64_t n, int64_t ldy,
+                                         const int32_t* d_row_of_pair,
                                          const float* d_gate, int64_t tokens, int64_t topk, void* out_bf16,
                                          int64_t ldo, void* stream);
 

@@ -204,11 +204,13 @@ def test_moe_dispatch_and_combine_reject_bad_arguments_on_host(lib):
     assert _rc(q, fake + 8, 16, 256, 256, fake, 8, 128, fake, 256, fake, 0, None) == 3
     assert _rc(q, fake, 16, 256, 256, fake, 8, 0, fake, 256, fake, 0, None) == 0  # no rows: no-op
     c = "fp8rl_moe_combine"
-    assert _rc(c, fake, 256, 256, fake, fake, 16, 0, fake, 256, None) == 1    # topk < 1
-    assert _rc(c, fake, 256, 128, fake, fake, 16, 8, fake, 256, None) == 1    # ldy < n
-    assert _rc(c, None, 256, 256, fake, fake, 16, 8, fake, 256, None) == 1
-    assert _rc(c, fake + 1, 256, 256, fake, fake, 16, 8, fake, 256, None) == 3
-    assert _rc(c, fake, 256, 256, fake, fake, 0, 8, fake, 256, None) == 0     # no tokens: no-op
+    assert _rc(c, fake, 128, 256, 256, fake, fake, 16, 0, fake, 256, None) == 1    # topk < 1
+    assert _rc(c, fake, 128, 256, 128, fake, fake, 16, 8, fake, 256, None) == 1    # ldy < n
+    assert _rc(c, fake, -1, 256, 256, fake, fake, 16, 8, fake, 256, None) == 1     # rows < 0
+    assert _rc(c, None, 128, 256, 256, fake, fake, 16, 8, fake, 256, None) == 1    # rows > 0, no y
+    assert _rc(c, fake, 1 << 31, 256, 256, fake, fake, 16, 8, fake, 256, None) == 2  # rows >= 2^31
+    assert _rc(c, fake + 1, 128, 256, 256, fake, fake, 16, 8, fake, 256, None) == 3
+    assert _rc(c, fake, 128, 256, 256, fake, fake, 0, 8, fake, 256, None) == 0     # no tokens: no-op
 
 
 def test_tis_rejects_bad_arguments_on_host(lib):

@@ -158,6 +158,28 @@ def test_combine_within_tolerance(tokens, n, k, experts, drop, pad):
     assert np.all(got[dead] == 0.0)
 
 
+@pytest.mark.parametrize("keep", [0, 37, 600])
+def test_combine_ignores_rows_past_y(keep):
+    """y holds only its first `keep` rows: slots naming a row at or past it
+    add nothing, as if dropped (keep = 0: y is null, every token zero)."""
+    tokens, n, k, experts = 100, 264, 8, 16
+    idx = random_topk(tokens, k, experts, 0.1, 21 + keep)
+    _, rop, _ = oracle.moe_dispatch_plan(idx, experts)
+    gate = np.random.default_rng(keep).random((tokens, k)).astype(np.float32)
+    y = synth.normal_bf16((tokens * k, n), 1.0, 14, "gpu-combine-past", keep)[:keep]
+    rop_ref = np.where(rop < keep, rop, -1).astype(rop.dtype)
+    yv = y.float().numpy().astype(np.float64)
+    ref = oracle.moe_combine(yv, rop_ref, gate.astype(np.float64))
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -18 * combine_bound(yv, rop_ref, gate.astype(np.float64))
+    yd = y.cuda() if keep else torch.empty((0, n), dtype=torch.bfloat16, device="cuda")
+    out = fp8rl.moe_combine(yd, torch.from_numpy(rop).cuda(), torch.from_numpy(gate).cuda())
+    assert fp8rl.fp8rl_sync_status() == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= bound)
+    if keep == 0:
+        assert np.all(got == 0.0)
+
+
 def test_combine_one_hot_gates_copy_rows_exactly():
     tokens, n, k, experts = 200, 512, 8, 16
     idx = random_topk(tokens, k, experts, 0.0, 5)
