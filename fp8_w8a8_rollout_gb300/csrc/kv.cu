@@ -87,59 +87,6 @@ __global__ void __launch_bounds__(kKvThreads) kv_amax_kernel(KvTensors ts, int64
   }
 }
 
-// amax of up to three contiguous tensors (rows x cols each, cols % 8 == 0)
-// as one flat stream of 16-byte pieces over all of them, so that every CTA
-// gets the same share whatever the tensors' sizes (Q is 4x K and V); eight
-// pieces per thread per trip, loads issued before use; one running maximum
-// per tensor; one wave of resident CTAs.
-constexpr int kFlatTrip = 8;
-__global__ void __launch_bounds__(kKvThreads) kv_amax_flat_kernel(const uint16_t* __restrict__ x0,
-                                                                 const uint16_t* __restrict__ x1,
-                                                                 const uint16_t* __restrict__ x2, int64_t end0,
-                                                                 int64_t end1, int64_t end2, int n,
-                                                                 uint32_t* amax_bits) {
-  // pieces [0, end0) of tensor 0, [end0, end1) of tensor 1, [end1, end2) of tensor 2
-  const int64_t pieces = end2;
-  const int64_t stride = (int64_t)gridDim.x * kKvThreads;
-  uint32_t a0 = 0u, a1 = 0u, a2 = 0u;
-  for (int64_t p0 = (int64_t)blockIdx.x * kKvThreads + threadIdx.x; p0 < pieces; p0 += kFlatTrip * stride) {
-    uint4 v[kFlatTrip];
-    int t[kFlatTrip];
-#pragma unroll
-    for (int j = 0; j < kFlatTrip; ++j) {
-      const int64_t p = p0 + j * stride;
-      t[j] = p < end0 ? 0 : p < end1 ? 1 : 2;
-      const uint16_t* src = t[j] == 0 ? x0 + p * 8 : t[j] == 1 ? x1 + (p - end0) * 8 : x2 + (p - end1) * 8;
-      v[j] = p < pieces ? ld_nc_u4(src) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kFlatTrip; ++j) {
-      const uint32_t m = absmax_u4(0u, v[j]);
-      a0 = t[j] == 0 ? __vmaxu2(a0, m) : a0;
-      a1 = t[j] == 1 ? __vmaxu2(a1, m) : a1;
-      a2 = t[j] == 2 ? __vmaxu2(a2, m) : a2;
-    }
-  }
-  __shared__ uint32_t red[3][kKvThreads / 32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t acc[3] = {a0, a1, a2};
-#pragma unroll
-  for (int i = 0; i < 3; ++i) {
-    uint32_t m = max(acc[i] & 0xFFFFu, acc[i] >> 16) << 16;
-    m = __reduce_max_sync(0xffffffffu, m);
-    if (lane == 0) red[i][warp] = m;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      uint32_t m = threadIdx.x < kKvThreads / 32 ? red[i][threadIdx.x] : 0u;
-      m = __reduce_max_sync(0xffffffffu, m);
-      if (threadIdx.x == 0 && m != 0 && i < n) atomicMax(amax_bits + i, m);
-    }
-  }
-}
-
 // amax bits -> fp32 scale, in place
 __global__ void kv_scale_kernel(float* scales, int n) {
   const int i = threadIdx.x;
@@ -224,29 +171,11 @@ extern "C" FP8RL_API fp8rl_status fp8rl_kv_calibrate(const void* k_bf16, const v
       ts.ld[i] = lds[i];
       ts.vec[i] = aligned(xs[i], 16) && (lds[i] * 2) % 16 == 0;
     }
-    bool flat = true;
-    for (int i = 0; i < n; ++i) flat = flat && ts.vec[i] && ts.ld[i] == ts.cols[i] && ts.cols[i] % 8 == 0;
-    if (flat) {
-      int64_t pieces = 0;
-      for (int i = 0; i < n; ++i) pieces += tokens * ts.cols[i] / 8;
-      static int resident = 0;  // CTAs of the flat kernel per SM, asked once
-      if (resident == 0) {
-        int r = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kv_amax_flat_kernel, kKvThreads, 0) != cudaSuccess || r < 1)
-          r = 1;
-        resident = r;
-      }
-      const int64_t grid = std::max<int64_t>(
-          1, std::min<int64_t>((pieces + kFlatTrip * kKvThreads - 1) / (kFlatTrip * kKvThreads),
-                               (int64_t)sm_count() * resident));
-      const int64_t e0 = tokens * ts.cols[0] / 8, e1 = e0 + tokens * ts.cols[1] / 8;
-      const int64_t e2 = e1 + (n > 2 ? tokens * ts.cols[2] / 8 : 0);
-      kv_amax_flat_kernel<<<(unsigned)grid, kKvThreads, 0, cs>>>(ts.x[0], ts.x[1], n > 2 ? ts.x[2] : ts.x[0], e0, e1,
-                                                                  e2, n, reinterpret_cast<uint32_t*>(d_scales));
-    } else {
-      kv_amax_kernel<<<dim3((unsigned)kv_grid(tokens), (unsigned)n), kKvThreads, 0, cs>>>(
-          ts, tokens, reinterpret_cast<uint32_t*>(d_scales));
-    }
+    // one grid slice per tensor, each warp a row at a time (a flat stream of
+    // 16-byte pieces over all three tensors, one resident wave, measured
+    // 30-50 % slower on GB300 after an L2 flush at 8192 and 32768 tokens)
+    kv_amax_kernel<<<dim3((unsigned)kv_grid(tokens), (unsigned)n), kKvThreads, 0, cs>>>(
+        ts, tokens, reinterpret_cast<uint32_t*>(d_scales));
   }
   kv_scale_kernel<<<1, 32, 0, cs>>>(d_scales, n);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
