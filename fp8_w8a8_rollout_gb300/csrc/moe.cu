@@ -31,6 +31,7 @@
 // piece of an output row, with the k source pieces loaded before any is used.
 // HBM-bound: k rows read, one written per token.
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -514,10 +515,15 @@ __global__ void __launch_bounds__(kCombineThreads) moe_combine_kernel(
   }
 }
 
+// asked once; concurrent first calls store the same value
 int combine_ctas_per_sm() {
-  static int cached = 0;
-  if (cached == 0) cached = ctas_per_sm(moe_combine_kernel, kCombineThreads);
-  return cached;
+  static std::atomic<int> cached{0};
+  int c = cached.load(std::memory_order_relaxed);
+  if (c == 0) {
+    c = ctas_per_sm(moe_combine_kernel, kCombineThreads);
+    cached.store(c, std::memory_order_relaxed);
+  }
+  return c;
 }
 
 }  // namespace
@@ -580,16 +586,19 @@ extern "C" FP8RL_API fp8rl_status fp8rl_moe_dispatch_quant(const void* x_bf16, i
   if (!aligned(x_bf16, 16) || !aligned(q_e4m3, 16) || !aligned(d_row_of_pair, 4)) return FP8RL_ERR_ALIGNMENT;
   if (fmt == FP8RL_SCALE_FP32 && !aligned(x_scale, 4)) return FP8RL_ERR_ALIGNMENT;
   const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
-  static int occ[2] = {0, 0};
+  static std::atomic<int> occ[2];  // asked once per format (zero until then)
   const int u = fmt == FP8RL_SCALE_UE8M0;
-  if (occ[u] == 0)
-    occ[u] = u ? ctas_per_sm(moe_dispatch_kernel<true>, kDispatchThreads)
-               : ctas_per_sm(moe_dispatch_kernel<false>, kDispatchThreads);
+  int resident = occ[u].load(std::memory_order_relaxed);
+  if (resident == 0) {
+    resident = u ? ctas_per_sm(moe_dispatch_kernel<true>, kDispatchThreads)
+                 : ctas_per_sm(moe_dispatch_kernel<false>, kDispatchThreads);
+    occ[u].store(resident, std::memory_order_relaxed);
+  }
   // one wave of resident CTAs (the SMs share the tasks evenly; a warp's
   // tasks overlap its neighbours' on the same SM)
   const int64_t tasks = tokens * ((k + kDispatchTaskCols - 1) / kDispatchTaskCols);
   const int64_t ctas = (tasks + kDispatchThreads / 32 - 1) / (kDispatchThreads / 32);
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)sm_count() * occ[u]));
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctas, (int64_t)sm_count() * resident));
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   uint8_t* q = static_cast<uint8_t*>(q_e4m3);

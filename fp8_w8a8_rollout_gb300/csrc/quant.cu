@@ -13,6 +13,7 @@
 // stores.  Grids are persistent: a multiple of the SM count, striding over the
 // blocks or groups.
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
@@ -317,16 +318,17 @@ int sm_count() {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// resident CTAs per SM of a 256-thread kernel (at least 1), asked once per kernel
+// resident CTAs per SM of a 256-thread kernel (at least 1), asked once per
+// kernel; concurrent first calls store the same value
 template <typename K>
 int ctas_per_sm(K kernel) {
-  static int cached = 0;
-  if (cached == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
-    cached = n;
+  static std::atomic<int> cached{0};
+  int c = cached.load(std::memory_order_relaxed);
+  if (c == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, kernel, 256, 0) != cudaSuccess || c < 1) c = 1;
+    cached.store(c, std::memory_order_relaxed);
   }
-  return cached;
+  return c;
 }
 
 fp8rl_status check_weight(const fp8rl_weight_desc& d, fp8rl_scale_fmt fmt) {
