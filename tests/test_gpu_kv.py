@@ -27,13 +27,28 @@ def kv_inputs(tokens, dim, seed, spread=1.0, ld=None):
     return k, v
 
 
-@pytest.mark.parametrize("tokens,dim,qdim", [(1, 1024, 4096), (300, 1024, 4096), (8192, 1024, 4096),
-                                             (77, 1000, 1000), (5, 8, 0)])
-def test_calibrate_scales_bit_exact(tokens, dim, qdim):
+@pytest.mark.parametrize("tokens,dim,qdim,ld", [(1, 1024, 4096, None), (300, 1024, 4096, None),
+                                                (8192, 1024, 4096, None), (77, 1000, 1000, None), (5, 8, 0, None),
+                                                (300, 1024, 4096, 1088), (64, 1000, 1000, 1003)])
+def test_calibrate_scales_bit_exact(tokens, dim, qdim, ld):
+    """Contiguous and strided rows (ld - dim padding elements after each row,
+    holding 1e30, which must not reach the amax: a padding of 64 keeps 16-byte
+    aligned rows, one of 3 takes the scalar loads)."""
     k, v = kv_inputs(tokens, dim, 1, 3.0)
     q = synth.normal_bf16((tokens, qdim), 0.5, 2, "kv-q") if qdim else None
     ref = oracle.kv_calibrate(synth.bf16_bits(k), synth.bf16_bits(v), synth.bf16_bits(q) if qdim else None)
-    got = fp8rl.kv_calibrate(k.cuda(), v.cuda(), q.cuda() if qdim else None)
+    pad = 0 if ld is None else ld - dim
+
+    def dev(t):  # each row followed by `pad` elements of a huge value
+        if not pad:
+            return t.cuda()
+        full = torch.full((t.shape[0], t.shape[1] + pad), 1e30, dtype=torch.bfloat16)
+        full[:, :t.shape[1]] = t
+        return full.cuda()[:, :t.shape[1]]
+    kd, vd = dev(k), dev(v)
+    qd = dev(q) if qdim else None
+    assert kd.stride(0) == dim + pad and (qd is None or qd.stride(0) == qdim + pad)
+    got = fp8rl.kv_calibrate(kd, vd, qd)
     assert fp8rl.fp8rl_sync_status() == 0
     assert np.array_equal(got.cpu().numpy(), ref)
 
