@@ -48,6 +48,81 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name)
 
 
+def declarations():
+    """{name: (return type, [parameter declarations])} of every FP8RL_API
+    function in include/*.h."""
+    out = {}
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        for ret, name, params in re.findall(r"FP8RL_API\s+([\w\s\*]+?)\b(fp8rl_\w+)\s*\(([^)]*)\)\s*;", text):
+            ps = [re.sub(r"\s+", " ", q).strip() for q in params.split(",") if q.strip()]
+            out[name] = (re.sub(r"\s+", " ", ret).strip(), [] if ps == ["void"] else ps)
+    return out
+
+
+def _c_type(param):
+    """The type of a parameter declaration ('const void* w_bf16' -> 'const void*')."""
+    m = re.match(r"^(.*?[\s\*])(\w+)$", param)
+    assert m, param
+    return m.group(1).strip()
+
+
+def _ctype_matches(c, ct):
+    """Does ctypes type `ct` pass / return C type `c` correctly on this ABI?"""
+    c = c.replace("const ", "").replace(" *", "*").strip()
+    if c.endswith("*"):
+        if c == "char*":
+            return ct is ctypes.c_char_p
+        return ct is ctypes.c_void_p or (isinstance(ct, type) and issubclass(ct, ctypes._Pointer))
+    if c in ("float", "double"):
+        return ct is {"float": ctypes.c_float, "double": ctypes.c_double}[c]
+    width = {"int64_t": 8, "int32_t": 4, "size_t": 8, "fp8rl_scale_fmt": 4, "fp8rl_status": 4}[c]
+    if ct is None or not issubclass(ct, ctypes._SimpleCData):
+        return False
+    if ct in (ctypes.c_float, ctypes.c_double, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_bool):
+        return False
+    unsigned = ct(-1).value > 0
+    return ctypes.sizeof(ct) == width and unsigned == (c == "size_t")
+
+
+def test_binding_signatures_match_the_header(lib):
+    """ctypes checks no argument list against the C one: every entry point's
+    argtypes and restype in the binding must agree with its declaration (count,
+    pointer or value, integer width and signedness, float width)."""
+    decls = declarations()
+    assert len(decls) >= 20
+    for name, (ret, params) in decls.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in the binding"
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), params)
+        for i, (decl, ct) in enumerate(zip(params, fn.argtypes)):
+            assert _ctype_matches(_c_type(decl), ct), (name, i, decl, ct)
+        assert _ctype_matches(ret, fn.restype), (name, ret, fn.restype)
+
+
+def test_weight_descriptor_layout_matches_the_header():
+    """fp8rl_weight_desc and the binding's WeightDesc list the same members
+    in the same order with the same types (so the same layout on this ABI)."""
+    text = open(os.path.join(ROOT, "include", "fp8rl.h")).read()
+    body = re.search(r"typedef struct \{(.*?)\} fp8rl_weight_desc;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    members = []
+    for stmt in body.split(";"):
+        stmt = " ".join(stmt.split())
+        if not stmt:
+            continue
+        m = re.match(r"^(const )?(\w+)(\*?)\s*(.*)$", stmt.replace("* ", "*").replace(" *", "*"))
+        ctype = m.group(2) + m.group(3)
+        for field in m.group(4).split(","):
+            members.append((field.strip().lstrip("*"), ctype))
+    fields = fp8rl.WeightDesc._fields_
+    assert [n for n, _ in fields] == [n for n, _ in members]
+    for (fname, ct), (_, ctype) in zip(fields, members):
+        assert _ctype_matches(ctype, ct), (fname, ctype, ct)
+
+
 def test_library_targets_sm103a_only():
     # the build passes exactly one -gencode, for sm_103a
     assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
