@@ -294,6 +294,22 @@ def _scale_dtype(fmt):
     return torch.float32 if fmt == SCALE_FP32 else torch.uint8
 
 
+def _check_cuda(*tensors):
+    """The kernels dereference device pointers on the current device: every
+    tensor argument of a helper must be a CUDA tensor on it (None and
+    non-tensor arguments are skipped)."""
+    cur = None
+    for t in tensors:
+        if not isinstance(t, torch.Tensor):
+            continue
+        if not t.is_cuda:
+            raise ValueError("fp8rl helpers take CUDA tensors; a host tensor's pointer would reach the kernels")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"a tensor on {t.device} while the current device is cuda:{cur}")
+
+
 def _check_bf16_2d(t: torch.Tensor, name: str):
     if t.dtype != torch.bfloat16 or t.dim() != 2 or t.stride(1) != 1:
         raise ValueError(f"{name} must be a 2-D bf16 tensor with unit column stride")
@@ -301,6 +317,7 @@ def _check_bf16_2d(t: torch.Tensor, name: str):
 
 def quant_weight(w: torch.Tensor, fmt=SCALE_FP32, stream=None):
     """E4M3 codes (uint8 [n,k]) and block scales ([ceil(n/128), ceil(k/128)]) of w."""
+    _check_cuda(w)
     _check_bf16_2d(w, "w")
     n, k = w.shape
     q = torch.empty((n, k), dtype=torch.uint8, device=w.device)
@@ -320,6 +337,8 @@ def weight_descs(items):
 
 def quant_weights_batched(weights, fmt=SCALE_FP32, stream=None, outputs=None):
     """Quantise a list of bf16 matrices in one pass; returns [(q, scale), ...]."""
+    weights = list(weights)
+    _check_cuda(*weights, *(t for pair in (outputs or ()) for t in pair))
     if outputs is None:
         outputs = []
         for w in weights:
@@ -335,6 +354,7 @@ def quant_weights_batched(weights, fmt=SCALE_FP32, stream=None, outputs=None):
 
 def quant_act(x: torch.Tensor, fmt=SCALE_FP32, stream=None):
     """E4M3 codes (uint8 [m,k]) and group scales ([ceil(k/128), m]) of x."""
+    _check_cuda(x)
     _check_bf16_2d(x, "x")
     m, k = x.shape
     q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
@@ -354,6 +374,7 @@ def gemm_workspace(device=None) -> torch.Tensor:
 def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None, workspace=None):
     """bf16 Y [m, n] = block-scaled X W^T.  With a workspace (gemm_workspace),
     shapes that fill the SMs unevenly run the stream-K schedule."""
+    _check_cuda(xq, x_scale, wq, w_scale, out, workspace)
     m, k = xq.shape
     n = wq.shape[0]
     if out is None:
@@ -368,6 +389,7 @@ def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None, worksp
 
 def grouped_gemm(xq, x_scale, wq, w_scale, d_offsets, fmt=SCALE_FP32, out=None, stream=None):
     """bf16 Y [rows, n]: expert e's weights applied to its row segment."""
+    _check_cuda(xq, x_scale, wq, w_scale, d_offsets, out)
     rows, k = xq.shape
     e, n, _ = wq.shape
     if out is None:
@@ -384,6 +406,7 @@ def quant_gate_up_interleaved(gate: torch.Tensor, up: torch.Tensor, fmt=SCALE_FP
     fp8rl_gemm_swiglu_quant consumes: 128-row blocks alternate gate, up.  One
     batched quantiser pass (one descriptor per 128-row block); returns
     (q [..., 2 * inter, k] uint8, scale [..., 2 * inter / 128, k / 128])."""
+    _check_cuda(gate, up, *(out or ()))
     if gate.shape != up.shape or gate.dtype != torch.bfloat16 or up.dtype != torch.bfloat16:
         raise ValueError("gate and up must be bf16 tensors of one shape")
     *lead, inter, k = gate.shape
@@ -413,6 +436,7 @@ def quant_gate_up_interleaved(gate: torch.Tensor, up: torch.Tensor, fmt=SCALE_FP
 
 def gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, fmt=SCALE_FP32, out=None, stream=None):
     """(hq [m, inter] uint8, h_scale [inter/128, m]) of SiLU(gate) * up."""
+    _check_cuda(xq, x_scale, wq_gate_up, w_scale_gate_up, *(out or ()))
     m, k = xq.shape
     inter = wq_gate_up.shape[0] // 2
     if out is None:
@@ -425,6 +449,7 @@ def gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, fmt=SCALE_FP32, 
 def grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, fmt=SCALE_FP32, out=None,
                               stream=None):
     """Grouped (MoE) form of gemm_swiglu_quant."""
+    _check_cuda(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, *(out or ()))
     rows, k = xq.shape
     e, n2, _ = wq_gate_up.shape
     inter = n2 // 2
@@ -438,6 +463,7 @@ def grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offset
 
 def kv_calibrate(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor | None = None, out=None, stream=None):
     """Per-tensor fp32 scales (device float [3]: K, V, Q) of a calibration pass."""
+    _check_cuda(k, v, q, out)
     for name, t in (("k", k), ("v", v)) + ((("q", q),) if q is not None else ()):
         _check_bf16_2d(t, name)
     scales = out if out is not None else torch.zeros(3, dtype=torch.float32, device=k.device)
@@ -450,6 +476,7 @@ def kv_calibrate(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor | None = None
 def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
               v_cache: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
     """Quantise rows of K and V into the E4M3 caches ([num_slots, kv_dim] uint8)."""
+    _check_cuda(k, v, slot_mapping, k_cache, v_cache, scales)
     _check_bf16_2d(k, "k")
     _check_bf16_2d(v, "v")
     tokens, dim = k.shape
@@ -460,6 +487,7 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_ca
 def moe_plan(topk: torch.Tensor, experts: int, workspace: torch.Tensor | None = None, stream=None):
     """Dispatch plan of replayed top-k indices (device int32 [T, k]): returns
     device int32 (offsets [E+1], row_of_pair [T*k], token_of_row [T*k])."""
+    _check_cuda(topk, workspace)
     if topk.dtype != torch.int32 or topk.dim() != 2 or not topk.is_contiguous():
         raise ValueError("topk must be a contiguous int32 [tokens, k] tensor")
     tokens, k = topk.shape
@@ -480,6 +508,7 @@ def moe_dispatch_quant(x: torch.Tensor, row_of_pair: torch.Tensor, topk: int, fm
     """The grouped activation of the dispatch: token t's 1x128 quantisation in
     rows row_of_pair[t * topk + j], (codes uint8 [R, K], scales [K/128, R]
     fp32 or uint8) with R = tokens * topk."""
+    _check_cuda(x, row_of_pair, *(out or ()))
     _check_bf16_2d(x, "x")
     tokens, k = x.shape
     rows = row_of_pair.numel()
@@ -497,6 +526,7 @@ def moe_dispatch_quant(x: torch.Tensor, row_of_pair: torch.Tensor, topk: int, fm
 
 def moe_combine(y: torch.Tensor, row_of_pair: torch.Tensor, gate: torch.Tensor, out=None, stream=None):
     """bf16 [T, N]: each token's expert output rows weighted by its gates."""
+    _check_cuda(y, row_of_pair, gate, out)
     _check_bf16_2d(y, "y")
     if gate.dtype != torch.float32 or gate.dim() != 2 or not gate.is_contiguous():
         raise ValueError("gate must be a contiguous fp32 [tokens, k] tensor")
@@ -510,6 +540,7 @@ def moe_combine(y: torch.Tensor, row_of_pair: torch.Tensor, gate: torch.Tensor, 
 def tis_weights(lp_train: torch.Tensor, lp_rollout: torch.Tensor, mask: torch.Tensor | None = None,
                 clip: float = 2.0, workspace: torch.Tensor | None = None, out=None, stream=None):
     """(w fp32 [n], kl fp64 [3] = mean, sum, count) on the device."""
+    _check_cuda(lp_train, lp_rollout, mask, workspace, *(out or ()))
     for name, t in (("lp_train", lp_train), ("lp_rollout", lp_rollout)):
         if t.dtype != torch.float32 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous fp32 tensor")

@@ -298,3 +298,34 @@ def test_tis_rejects_bad_arguments_on_host(lib):
     assert _rc(t, fake, fake, None, 1 << 24, 2.0, fake, None, fake, ws, None) == 1   # no output
     assert _rc(t, fake, fake, None, 1 << 24, 2.0, fake, fake, fake, 8, None) == 1    # workspace too small
     assert _rc(t, fake + 2, fake, None, 1 << 24, 2.0, fake, fake, fake, ws, None) == 3
+
+
+def test_helpers_reject_host_tensors():
+    """A host tensor's pointer must never reach a kernel: every tensor helper
+    refuses CPU tensors before it loads or calls the library."""
+    import torch
+    w = torch.zeros((128, 128), dtype=torch.bfloat16)
+    u8 = torch.zeros((128, 128), dtype=torch.uint8)
+    f32 = torch.ones((1, 1), dtype=torch.float32)
+    off = torch.tensor([0, 128], dtype=torch.int32)
+    calls = {
+        "quant_weight": lambda: fp8rl.quant_weight(w),
+        "quant_weights_batched": lambda: fp8rl.quant_weights_batched([w]),
+        "quant_act": lambda: fp8rl.quant_act(w),
+        "gemm": lambda: fp8rl.gemm(u8, f32, u8, f32),
+        "grouped_gemm": lambda: fp8rl.grouped_gemm(u8, f32, u8.view(1, 128, 128), f32.view(1, 1, 1), off),
+        "quant_gate_up_interleaved": lambda: fp8rl.quant_gate_up_interleaved(w, w),
+        "gemm_swiglu_quant": lambda: fp8rl.gemm_swiglu_quant(u8, f32, u8, f32),
+        "grouped_gemm_swiglu_quant": lambda: fp8rl.grouped_gemm_swiglu_quant(
+            u8, f32, u8.view(1, 128, 128), f32.view(1, 1, 1), off),
+        "kv_calibrate": lambda: fp8rl.kv_calibrate(w, w),
+        "kv_append": lambda: fp8rl.kv_append(w, w, torch.zeros(128, dtype=torch.int32), u8, u8, f32),
+        "moe_plan": lambda: fp8rl.moe_plan(torch.zeros((64, 2), dtype=torch.int32), 8),
+        "moe_dispatch_quant": lambda: fp8rl.moe_dispatch_quant(w, torch.zeros(256, dtype=torch.int32), 2),
+        "moe_combine": lambda: fp8rl.moe_combine(w, torch.zeros(8, dtype=torch.int32),
+                                                 torch.zeros((4, 2), dtype=torch.float32)),
+        "tis_weights": lambda: fp8rl.tis_weights(torch.zeros(8), torch.zeros(8)),
+    }
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="CUDA tensors"):
+            call()
