@@ -447,9 +447,10 @@ FP8RL_API fp8rl_status fp8rl_moe_combine(const void* y_bf16, int64_t rows, int64
  *                   first use (zero it once when allocating it); every call leaves them
  *                   zero.  One call at a time per workspace.
  * Each difference is made exact in fp32 (a TwoSum: rounded difference plus its
- * error term), accumulated as an fp32 pair and folded into fp64 every 64
- * tokens; the fp64 partials add up in an order fixed by n: the same bits on
- * every run.  One launch.
+ * error term) and added to an fp32 (hi, lo) pair; the threads' pairs meet in a
+ * fixed tree per CTA, the last CTA to finish adds the CTAs' pairs in index
+ * order and converts the total to double once.  The grid, and so the order of
+ * every addition, depends on n alone: the same bits on every run.  One launch.
  * Errors: INVALID_ARG (negative n, clip <= 0, null pointers, workspace too
  *         small), ALIGNMENT, CUDA.
  */
