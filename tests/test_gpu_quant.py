@@ -189,8 +189,9 @@ def test_status_is_ok_after_quantisers():
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_host_weight_sync_pipeline_bit_exact(fmt):
-    """Host-to-host weight sync in small chunks (many more chunks than staging
-    slots, ragged shapes) equals the oracle on every matrix."""
+    """Host-to-host weight sync through HostWeightSync (the C entry point
+    fp8rl_quant_weight_host_batched) in small chunks: many more chunks than
+    staging slots, ragged shapes; equals the oracle on every matrix, twice."""
     shapes = [(384, 256), (200, 300), (1024, 128), (130, 640)]
     ws = [synth.weight_bf16(n, k, 6, "hostsync", n, k) for n, k in shapes]
     host_w = [w.pin_memory() for w in ws]
@@ -198,7 +199,6 @@ def test_host_weight_sync_pipeline_bit_exact(fmt):
     host_q = [torch.empty((n, k), dtype=torch.uint8, pin_memory=True) for n, k in shapes]
     host_s = [torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=sdt, pin_memory=True) for n, k in shapes]
     hs = fp8rl.HostWeightSync(host_w, host_q, host_s, fmt=fmt, chunk_bytes=64 * 1024, slots=2)
-    assert len(hs.items) > 2 * len(hs.slots)
     for _ in range(2):
         hs.run()
     torch.cuda.synchronize()
@@ -206,6 +206,44 @@ def test_host_weight_sync_pipeline_bit_exact(fmt):
         qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(w), fmt)
         assert np.array_equal(q.numpy(), qo)
         assert np.array_equal(s.numpy().view(np.uint8), so.view(np.uint8))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("slots", [2, 3, 8])
+def test_host_sync_c_abi_strided_rows(fmt, pinned, slots):
+    """fp8rl_quant_weight_host_batched on host rows with padded strides (ldw,
+    ldq > k), one chunk per 128-row block row (the staging holds exactly one
+    block row per slot), pinned and pageable host memory; the bytes outside
+    each row's k columns are left as they were."""
+    shapes = [(300, 256), (128, 384), (257, 128), (5, 200)]
+    sdt = torch.float32 if fmt == fp8rl.SCALE_FP32 else torch.uint8
+    ws, host_w, host_q, host_s = [], [], [], []
+    for i, (n, k) in enumerate(shapes):
+        w = synth.weight_bf16(n, k, 70 + i, "hostabi", n, k)
+        big = torch.zeros((n, k + 24), dtype=torch.bfloat16)
+        big[:, :k] = w
+        q = torch.full((n, k + 40), 0xA5, dtype=torch.uint8)
+        s = torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=sdt)
+        if pinned:
+            big, q, s = big.pin_memory(), q.pin_memory(), s.pin_memory()
+        ws.append(w)
+        host_w.append(big)
+        host_q.append(q)
+        host_s.append(s)
+    descs = (fp8rl.WeightDesc * len(shapes))()
+    for i, (n, k) in enumerate(shapes):
+        descs[i] = fp8rl.WeightDesc(host_w[i].data_ptr(), host_q[i].data_ptr(), host_s[i].data_ptr(), n, k,
+                                    k + 24, k + 40)
+    need = max(fp8rl.fp8rl_host_sync_staging_bytes(min(n, 128), k, slots, fmt) for n, k in shapes)
+    staging = torch.empty(need, dtype=torch.uint8, device="cuda")
+    fp8rl.fp8rl_quant_weight_host_batched(descs, len(shapes), fmt, staging, need, slots)
+    assert fp8rl.fp8rl_sync_status() == 0
+    for (n, k), w, q, s in zip(shapes, ws, host_q, host_s):
+        qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(w), fmt)
+        assert np.array_equal(q[:, :k].numpy(), qo)
+        assert np.all(q[:, k:].numpy() == 0xA5)
+        assert np.array_equal(s.numpy().view(np.uint8).reshape(-1), so.view(np.uint8).reshape(-1))
 
 
 def test_host_weight_sync_direct_bit_exact():
@@ -224,43 +262,51 @@ def test_host_weight_sync_direct_bit_exact():
         assert np.array_equal(q.numpy(), qo) and np.array_equal(s.numpy(), so)
 
 
-def _sampled_block_parity(ws, outs, fmt, samples, seed):
-    """Compare randomly chosen 128x128 blocks (and their scales) of device
-    results with the oracle run on just those blocks."""
-    rng = np.random.default_rng(seed)
-    for _ in range(samples):
-        i = int(rng.integers(len(ws)))
-        w = ws[i]
+def _full_parity(ws, outs, fmt):
+    """Every code and every scale of the device results against the oracle,
+    matrix by matrix: each bf16 matrix and its device codes and scales come to
+    the host in turn (host memory stays at one matrix), and the oracle's
+    quantisation of the next matrix runs while the current one is copied."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    def host(i):
         q, s = outs[i]
-        n, k = w.shape
-        nb = int(rng.integers((n + 127) // 128))
-        kb = int(rng.integers((k + 127) // 128))
-        blk = w[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128]
-        qo, so = oracle.quant_weight_blockwise(synth.bf16_bits(blk), fmt)
-        assert np.array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128].cpu().numpy(), qo)
-        assert np.array_equal(s[nb:nb + 1, kb:kb + 1].cpu().numpy().view(np.uint8), so.view(np.uint8))
+        return synth.bf16_bits(ws[i].cpu()), q.cpu().numpy(), s.cpu().numpy()
+
+    with ThreadPoolExecutor(max_workers=1) as pool:
+        bits, q, s = host(0)
+        for i in range(len(ws)):
+            fut = pool.submit(oracle.quant_weight_blockwise, bits, fmt)
+            nxt = host(i + 1) if i + 1 < len(ws) else None
+            qo, so = fut.result()
+            assert np.array_equal(q, qo), f"E4M3 codes of matrix {i} differ"
+            assert np.array_equal(s.view(np.uint8), so.view(np.uint8)), f"scales of matrix {i} differ"
+            if nxt is not None:
+                bits, q, s = nxt
 
 
 @pytest.mark.slow
-def test_full_model_weight_sync_sampled():
+def test_full_model_weight_sync_bit_exact():
     """36 Qwen3-8B-shaped layers (252 matrices, 6.95e9 parameters) in the
-    single batched launch the benchmark times; 256 sampled blocks."""
+    single batched launch the benchmark times; every code and scale."""
     dev = torch.device("cuda")
     ws = []
     for layer in range(synth.QWEN3_8B_LAYERS):
         ws += [w for _, w in synth.qwen3_8b_layer(layer, 1000, device=dev)]
     outs = fp8rl.quant_weights_batched(ws)
     torch.cuda.synchronize()
-    _sampled_block_parity(ws, outs, fp8rl.SCALE_FP32, 256, 1)
+    assert fp8rl.fp8rl_sync_status() == 0
+    _full_parity(ws, outs, fp8rl.SCALE_FP32)
     del ws, outs
     torch.cuda.empty_cache()
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("fmt", FMTS)
-def test_moe_expert_weight_sync_sampled(fmt):
+def test_moe_expert_weight_sync_bit_exact(fmt):
     """48 layers x 128 experts x (gate-up, down) of a Qwen3-30B-A3B-shaped model
-    (2.9e10 parameters, 58 GB of bf16) in one batched launch; 256 sampled blocks."""
+    (2.9e10 parameters, 58 GB of bf16) in one batched launch; every code and
+    scale."""
     dev = torch.device("cuda")
     ws = []
     for layer in range(synth.MOE_LAYERS):
@@ -270,6 +316,7 @@ def test_moe_expert_weight_sync_sampled(fmt):
                                         layer, which, device=dev))
     outs = fp8rl.quant_weights_batched(ws, fmt)
     torch.cuda.synchronize()
-    _sampled_block_parity(ws, outs, fmt, 256, 2)
+    assert fp8rl.fp8rl_sync_status() == 0
+    _full_parity(ws, outs, fmt)
     del ws, outs
     torch.cuda.empty_cache()
