@@ -3,6 +3,8 @@
 // Kernels that wait on mbarriers bound every wait; when one runs out they set
 // a bit in this word and leave through their normal teardown (no trap), so
 // the CUDA context stays usable.  fp8rl_sync_status() reads and clears it.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -13,17 +15,61 @@ namespace fp8rl {
 // allocation is ever made for it)
 static __device__ uint32_t g_error_word;
 
-// device address of the error word on the current device (cached per device)
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+uint64_t current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return 0;
+  if (!ctx) {
+    // no context on this thread yet: cudaSetDevice makes the current device's
+    // primary context current (CUDA 12 and later)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  }
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return static_cast<uint64_t>(id) + 1;
+}
+
+// device address of the error word in the current context (cached per device
+// together with the context it was looked up in)
 uint32_t* device_error_word() {
   static std::mutex mu;
   static uint32_t* cache[64] = {};
+  static uint64_t cache_ctx[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  const uint64_t ctx = current_context_id();
+  if (!ctx) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
+  if (!cache[dev] || cache_ctx[dev] != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
     cache[dev] = static_cast<uint32_t*>(p);
+    cache_ctx[dev] = ctx;
   }
   return cache[dev];
 }

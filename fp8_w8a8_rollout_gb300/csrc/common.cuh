@@ -169,4 +169,12 @@ __device__ __forceinline__ uint32_t absmax_u4(uint32_t acc, uint4 v) {
 // bits recorded in a device error word
 constexpr uint32_t kErrTimeout = 1u;
 
+// A process-unique id of the CUDA context current on this thread, making the
+// runtime's primary context of the current device current first if there is
+// none yet; 0 if it cannot be found.  Per-device host caches of device
+// addresses and function attributes keep the id they were made under and are
+// rebuilt when it changes (a cudaDeviceReset destroys the context: addresses
+// cached from the old one would point nowhere).  api.cu.
+uint64_t current_context_id();
+
 }  // namespace fp8rl

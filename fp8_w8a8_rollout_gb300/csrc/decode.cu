@@ -308,6 +308,7 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 }
 
 struct DecState {
+  uint64_t ctx = 0;  // the context the attributes were set in (redone when it changes)
   bool ready = false, ok = false;
   int sms = 0;
   int capacity[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // clusters of each size resident at once
@@ -333,9 +334,13 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
   const int nblocks = args.n / kDecRows;
   const int num_kb = args.k / 128;
   int splits = 1;
+  const uint64_t ctx = current_context_id();
+  if (!ctx) return FP8RL_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lock(g_dec_mu);
-    if (!st.ready) {
+    if (!st.ready || st.ctx != ctx) {
+      st = DecState{};
+      st.ctx = ctx;
       int sms = 0;
       st.ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0 &&
               cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==

@@ -32,6 +32,8 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -1252,6 +1254,7 @@ int max_active_clusters(K kernel, dim3 grid, int threads, int smem, int splits) 
 // pointers is established once: the shared-memory opt-in, the register check
 // of the setmaxnreg split, and for each split count whether its clusters fit.
 struct KernelState {
+  uint64_t ctx = 0;  // the context the attributes were set in (redone when it changes)
   bool ready = false;
   bool regs_ok = false;
   bool attr_ok = false;
@@ -1287,9 +1290,13 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
   KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE, EPI, OUT>(dev);
+  const uint64_t ctx = current_context_id();
+  if (!ctx) return FP8RL_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!ks.ready) {
+    if (!ks.ready || ks.ctx != ctx) {
+      ks = KernelState{};
+      ks.ctx = ctx;
       cudaFuncAttributes fa;
       ks.regs_ok = cudaFuncGetAttributes(&fa, kernel) == cudaSuccess &&
                    // setmaxnreg.inc waits until the block has the registers it asks
@@ -1626,6 +1633,13 @@ extern "C" FP8RL_API fp8rl_status fp8rl_grouped_gemm_swiglu_quant(
 }
 
 extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
+  // the hooks change every later call of the process: only a process that
+  // asked for them (tests, profiling) may set one; restoring the defaults is
+  // always allowed
+  if (key != 0) {
+    const char* on = std::getenv("FP8RL_TEST_HOOKS");
+    if (!on || std::strcmp(on, "1") != 0) return FP8RL_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   switch (key) {
     case 1:

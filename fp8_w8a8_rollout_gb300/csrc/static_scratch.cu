@@ -7,8 +7,10 @@
 // under memory pressure in a long-running serving loop).  For them,
 // fp8rl_gemm_blockscaled_static uses this array instead: a file-scope device
 // variable, created when this module is loaded, never allocated or freed by a
-// call.  It lives in a translation unit of its own, so processes that never
-// call that entry point do not load it.
+// call.  It lives in a translation unit of its own.  With lazy module loading
+// (CUDA_MODULE_LOADING=LAZY, the CUDA 12 default) a process that never calls
+// that entry point does not load it; with CUDA_MODULE_LOADING=EAGER every
+// device the process uses holds the 24 MiB from the time the library loads.
 #include <mutex>
 
 #include "common.cuh"
@@ -22,14 +24,16 @@ constexpr size_t kStaticScratchBytes = size_t(24) << 20;
 
 static __device__ __align__(256) uint8_t g_gemm_scratch[kStaticScratchBytes];
 
-// Device address of the scratch on the current device, or null (*status says
-// why).  The first call on each device, with that device current, looks the
-// array up and zeroes its first `clear_bytes` (the stream-K header and flags,
-// which must start at zero); later calls return the cached address.
+// Device address of the scratch in the current context, or null (*status
+// says why).  The first call on each device (and again after the device's
+// context was replaced, e.g. by cudaDeviceReset), with that device current,
+// looks the array up and zeroes its first `clear_bytes` (the stream-K header
+// and flags, which must start at zero); later calls return the cached address.
 // need_bytes above the capacity is rejected with FP8RL_ERR_UNSUPPORTED.
 void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* status) {
   static std::mutex mu;
   static void* cache[64] = {};
+  static uint64_t cache_ctx[64] = {};
   *status = FP8RL_OK;
   if (need_bytes > kStaticScratchBytes || clear_bytes > need_bytes) {
     *status = FP8RL_ERR_UNSUPPORTED;
@@ -40,8 +44,14 @@ void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* s
     *status = FP8RL_ERR_CUDA;
     return nullptr;
   }
+  const uint64_t ctx = current_context_id();
+  if (!ctx) {
+    *status = FP8RL_ERR_CUDA;
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
+  if (!cache[dev] || cache_ctx[dev] != ctx) {
+    cache[dev] = nullptr;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_gemm_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
@@ -54,6 +64,7 @@ void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* s
       return nullptr;
     }
     cache[dev] = p;
+    cache_ctx[dev] = ctx;
   }
   return cache[dev];
 }

@@ -252,6 +252,20 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 0, 0) == 0
 
 
+def test_debug_hooks_refused_unless_enabled(lib, monkeypatch):
+    """Without FP8RL_TEST_HOOKS=1 in the environment every hook but the reset
+    is refused (UNSUPPORTED), whatever its value."""
+    monkeypatch.delenv("FP8RL_TEST_HOOKS", raising=False)
+    for key, value in ((1, 256), (2, 3), (3, 1000), (6, 4), (7, 2), (10, 1)):
+        assert _rc("fp8rl_debug_set", key, value) == 4
+    monkeypatch.setenv("FP8RL_TEST_HOOKS", "0")
+    assert _rc("fp8rl_debug_set", 1, 256) == 4
+    assert _rc("fp8rl_debug_set", 0, 0) == 0
+    monkeypatch.setenv("FP8RL_TEST_HOOKS", "1")
+    assert _rc("fp8rl_debug_set", 1, 256) == 0
+    assert _rc("fp8rl_debug_set", 0, 0) == 0
+
+
 def test_moe_plan_rejects_bad_arguments_on_host(lib):
     ws = lib.fp8rl_moe_plan_workspace_size(4096, 8, 128)
     assert ws >= 4 * 128 and ws % 256 == 0
@@ -329,3 +343,32 @@ def test_helpers_reject_host_tensors():
     for name, call in calls.items():
         with pytest.raises(ValueError, match="CUDA tensors"):
             call()
+
+
+def test_host_sync_rejects_bad_arguments_on_host(lib):
+    """fp8rl_quant_weight_host_batched validates everything before it touches
+    the device."""
+    need = lib.fp8rl_host_sync_staging_bytes(128, 256, 2, 0)
+    assert need == 2 * (128 * 256 * 2 + 128 * 256 + 256)
+    assert lib.fp8rl_host_sync_staging_bytes(128, 256, 1, 0) == 0   # slots < 2
+    assert lib.fp8rl_host_sync_staging_bytes(128, 256, 9, 0) == 0   # slots > 8
+    assert lib.fp8rl_host_sync_staging_bytes(0, 256, 2, 0) == 0
+    assert lib.fp8rl_host_sync_staging_bytes(128, 256, 2, 2) == 0   # unknown format
+    buf = (ctypes.c_uint8 * 4096)()
+    d = (fp8rl.WeightDesc * 1)()
+    d[0] = fp8rl.WeightDesc(ctypes.addressof(buf), ctypes.addressof(buf), ctypes.addressof(buf), 256, 256, 256, 256)
+    staging = 1 << 20  # a 256-byte aligned address, never dereferenced by a rejected call
+    f = lib.fp8rl_quant_weight_host_batched
+    assert f(d, 1, 2, staging, need, 2, None) == 1           # unknown format
+    assert f(None, 1, 0, staging, need, 2, None) == 1        # null descriptors
+    assert f(d, -1, 0, staging, need, 2, None) == 1          # negative count
+    assert f(d, 1, 0, None, need, 2, None) == 1              # no staging
+    assert f(d, 1, 0, staging, need, 1, None) == 1           # slots < 2
+    assert f(d, 1, 0, staging, need, 9, None) == 1           # slots > 8
+    assert f(d, 1, 0, staging + 16, need, 2, None) == 3      # staging not 256-byte aligned
+    assert f(d, 1, 0, staging, need - 512, 2, None) == 2     # a slot cannot hold a block row
+    d[0].ldw = 255
+    assert f(d, 1, 0, staging, need, 2, None) == 1           # ldw < k
+    d[0].ldw, d[0].w_bf16 = 256, None
+    assert f(d, 1, 0, staging, need, 2, None) == 1           # null pointer
+    assert f(d, 0, 0, staging, need, 2, None) == 0           # count 0: no-op
