@@ -24,6 +24,7 @@ from . import _build
 __all__ = [
     "Fp8rlError", "SCALE_FP32", "SCALE_UE8M0", "load_library", "library_path",
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
+    "fp8rl_host_sync_staging_bytes", "fp8rl_quant_weight_host_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
     "fp8rl_gemm_workspace_size", "fp8rl_gemm_blockscaled_ws", "gemm_workspace",
     "fp8rl_gemm_blockscaled_static", "fp8rl_gemm_swiglu_quant", "fp8rl_grouped_gemm_swiglu_quant",
@@ -79,6 +80,8 @@ def load_library(build_if_missing: bool = False):
         sig = {
             "fp8rl_quant_weight_blockwise": [vp, i64, i64, i64, vp, i64, vp, st, vp],
             "fp8rl_quant_weight_blockwise_batched": [ctypes.POINTER(WeightDesc), i32, st, vp],
+            "fp8rl_host_sync_staging_bytes": [i64, i64, i32, st],
+            "fp8rl_quant_weight_host_batched": [ctypes.POINTER(WeightDesc), i32, st, vp, ctypes.c_size_t, i32, vp],
             "fp8rl_quant_act_group": [vp, i64, i64, i64, vp, i64, vp, st, vp],
             "fp8rl_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
             "fp8rl_gemm_workspace_size": [ctypes.POINTER(ctypes.c_size_t)],
@@ -107,6 +110,7 @@ def load_library(build_if_missing: bool = False):
             fn.restype = st
         lib.fp8rl_status_string.restype = ctypes.c_char_p
         lib.fp8rl_moe_plan_workspace_size.restype = ctypes.c_size_t
+        lib.fp8rl_host_sync_staging_bytes.restype = ctypes.c_size_t
         lib.fp8rl_tis_workspace_size.restype = ctypes.c_size_t
         lib.fp8rl_version.restype = i32
         _lib = lib
@@ -151,6 +155,16 @@ def fp8rl_quant_weight_blockwise(w_bf16, n, k, ldw, q_e4m3, ldq, w_scale, fmt=SC
 def fp8rl_quant_weight_blockwise_batched(descs, count, fmt=SCALE_FP32, stream=None) -> None:
     _ok(load_library().fp8rl_quant_weight_blockwise_batched(descs, count, fmt, _stream(stream)),
         "fp8rl_quant_weight_blockwise_batched")
+
+
+def fp8rl_host_sync_staging_bytes(rows, k, slots, fmt=SCALE_FP32) -> int:
+    return int(load_library().fp8rl_host_sync_staging_bytes(rows, k, slots, fmt))
+
+
+def fp8rl_quant_weight_host_batched(descs, count, fmt, d_staging, staging_bytes, slots, stream=None) -> None:
+    _ok(load_library().fp8rl_quant_weight_host_batched(descs, count, fmt, _p(d_staging), int(staging_bytes),
+                                                       slots, _stream(stream)),
+        "fp8rl_quant_weight_host_batched")
 
 
 def fp8rl_quant_act_group(x_bf16, m, k, ldx, q_e4m3, ldq, x_scale, fmt=SCALE_FP32,
@@ -559,81 +573,49 @@ def tis_weights(lp_train: torch.Tensor, lp_rollout: torch.Tensor, mask: torch.Te
 
 class HostWeightSync:
     """Weight sync from host memory: bf16 weights in pinned host buffers are
-    copied to the GPU, quantised (128x128 blocks) and the E4M3 codes and scales
-    copied back to pinned host buffers, as a three-stream pipeline (copy in,
-    quantise, copy out) over chunks of whole 128-row block rows, so that both
-    copy directions overlap the kernels and each other.
+    quantised (128x128 blocks) into E4M3 codes and scales in pinned host
+    buffers.
 
-    Each chunk is an independent sub-matrix: its codes and scale rows are
-    exactly those of the whole matrix.  Device staging is allocated once, at
-    construction (`chunk_rows` rows per slot, `slots` slots); `run()` then only
-    enqueues work on the caller's device."""
+    Pipelined (default): one call of ``fp8rl_quant_weight_host_batched``, the
+    library's copy-in / quantise / copy-out pipeline over chunks of whole
+    128-row block rows; the device staging (``slots`` slots of about
+    ``chunk_bytes`` of bf16 each) is allocated once, at construction.
+    Direct: the quantiser itself reads the pinned bf16 weights and writes the
+    codes and scales in host memory over the CPU-GPU link (one batched launch
+    of ``fp8rl_quant_weight_blockwise_batched``, no staging).  ``run()`` only
+    enqueues work on the current stream; the caller synchronises."""
 
     def __init__(self, host_weights, host_codes, host_scales, fmt=SCALE_FP32, chunk_bytes=32 << 20,
                  slots=3, device=None, direct=False):
         device = torch.device(device or "cuda")
         self.fmt = fmt
-        self.items = []
         self.direct = direct
         self.h2d_bytes = sum(w.numel() * 2 for w in host_weights)
         self.d2h_bytes = sum(q.numel() + s.numel() * s.element_size() for q, s in zip(host_codes, host_scales))
+        for t in list(host_weights) + list(host_codes) + list(host_scales):
+            if t.is_cuda:
+                raise ValueError("HostWeightSync takes host tensors")
+            if direct and not t.is_pinned():
+                raise ValueError("direct mode needs pinned host tensors")
+        self._keep = (list(host_weights), list(host_codes), list(host_scales))
+        self.descs = weight_descs(list(zip(host_weights, host_codes, host_scales)))
+        self.count = len(host_weights)
         if direct:
-            # the quantiser reads the pinned bf16 weights and writes the codes and
-            # scales in host memory itself (over the CPU-GPU link): one batched
-            # launch, no staging copies
-            for t in list(host_weights) + list(host_codes) + list(host_scales):
-                if not t.is_pinned():
-                    raise ValueError("direct mode needs pinned host tensors")
-            self.descs = weight_descs(list(zip(host_weights, host_codes, host_scales)))
-            self.count = len(host_weights)
             return
-        for w, q, s in zip(host_weights, host_codes, host_scales):
+        self.slots = slots
+        need = 0
+        for w in host_weights:
             n, k = w.shape
-            rows = max(128, (chunk_bytes // (2 * k)) // 128 * 128)
-            for r0 in range(0, n, rows):
-                r1 = min(n, r0 + rows)
-                self.items.append((w[r0:r1], q[r0:r1], s[r0 // 128:(r1 + 127) // 128], r1 - r0, k))
-        # flat staging, viewed per chunk as contiguous [n][k] / [n/128][k/128]
-        elems = max(it[3] * it[4] for it in self.items)
-        blocks = max(((it[3] + 127) // 128) * ((it[4] + 127) // 128) for it in self.items)
-        self.slots = [(torch.empty(elems, dtype=torch.bfloat16, device=device),
-                       torch.empty(elems, dtype=torch.uint8, device=device),
-                       torch.empty(blocks, dtype=_scale_dtype(fmt), device=device))
-                      for _ in range(slots)]
-        self.s_in = torch.cuda.Stream(device)
-        self.s_q = torch.cuda.Stream(device)
-        self.s_out = torch.cuda.Stream(device)
-        self.ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(slots)]
+            if n == 0 or k == 0:
+                continue
+            rows = min(n, max(128, (chunk_bytes // (2 * k)) // 128 * 128))
+            need = max(need, fp8rl_host_sync_staging_bytes(rows, k, slots, fmt))
+        self.staging = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
 
     def run(self):
         """Enqueue one full weight sync; returns immediately (the caller syncs)."""
         if self.direct:
             fp8rl_quant_weight_blockwise_batched(self.descs, self.count, self.fmt)
             return
-        cur = torch.cuda.current_stream()
-        for st in (self.s_in, self.s_q, self.s_out):
-            st.wait_stream(cur)
-        nslot = len(self.slots)
-        for i, (w, q, s, n, k) in enumerate(self.items):
-            j = i % nslot
-            dw, dq, ds = self.slots[j]
-            e_in, e_q, e_out = self.ev[j]
-            nb, kb = (n + 127) // 128, (k + 127) // 128
-            dw_v = dw[:n * k].view(n, k)
-            dq_v = dq[:n * k].view(n, k)
-            ds_v = ds[:nb * kb].view(nb, kb)
-            if i >= nslot:
-                self.s_in.wait_event(e_out)      # the slot's previous chunk has left the GPU
-            with torch.cuda.stream(self.s_in):
-                dw_v.copy_(w, non_blocking=True)
-                e_in.record(self.s_in)
-            self.s_q.wait_event(e_in)
-            fp8rl_quant_weight_blockwise(dw_v, n, k, k, dq_v, k, ds_v, self.fmt, self.s_q)
-            e_q.record(self.s_q)
-            self.s_out.wait_event(e_q)
-            with torch.cuda.stream(self.s_out):
-                q.copy_(dq_v, non_blocking=True)
-                s.copy_(ds_v, non_blocking=True)
-                e_out.record(self.s_out)
-        for st in (self.s_in, self.s_q, self.s_out):
-            cur.wait_stream(st)
+        fp8rl_quant_weight_host_batched(self.descs, self.count, self.fmt, self.staging, self.staging.numel(),
+                                        self.slots)

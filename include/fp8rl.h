@@ -116,6 +116,42 @@ FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise_batched(const fp8rl_weight_d
                                                             void* stream);
 
 /*
+ * Weight sync from HOST memory to HOST memory ("Method steps", step 2: the
+ * trainer's bf16 weights are quantised to FP8 at every weight sync).  Same
+ * numerics and output layout per matrix as fp8rl_quant_weight_blockwise.
+ *   descs      HOST array of `count` descriptors, read during the call only;
+ *              their w_bf16, q_e4m3 and w_scale are HOST pointers (any
+ *              alignment; row strides ldw, ldq in elements / bytes).  Pinned
+ *              memory (cudaHostAlloc, cudaHostRegister) lets the copies run
+ *              asynchronously and overlap; pageable memory gives the same
+ *              bytes, but then each copy makes the calling thread wait.
+ *   d_staging  DEVICE buffer of staging_bytes, owned by the caller, 256-byte
+ *              aligned, cut into `slots` (2..8) equal slots; its contents are
+ *              overwritten.  fp8rl_host_sync_staging_bytes(rows, k, slots, fmt)
+ *              is the size that holds chunks of `rows` rows of a width-k matrix.
+ * Each matrix is cut into chunks of whole 128-row block rows, as many as fit a
+ * slot (a chunk's codes and scale rows are exactly the whole matrix's); per
+ * chunk, a host-to-device copy into a slot, the quantiser, and the copies of
+ * the codes and scale rows back to the host run on three streams of the
+ * library's own (made once per device and context), chained by events per
+ * slot, so both directions of the host link and the kernels overlap.  The
+ * work starts after everything enqueued on `stream` before the call (and after
+ * the previous call's copies have left the staging slots); work enqueued on
+ * `stream` after the call starts after the last copy back, so the host codes
+ * and scales are valid once `stream` has been synchronised.  The host buffers
+ * must stay alive and untouched until then.  Calls on one device are
+ * serialised by the library.
+ * Errors: INVALID_ARG (count < 0, null pointers, slots outside 2..8, ldw or
+ *         ldq < k, negative sizes), ALIGNMENT (d_staging not 256-byte
+ *         aligned), SHAPE (a slot cannot hold one 128-row block row of some
+ *         matrix), CUDA.  count == 0 is a no-op.
+ */
+FP8RL_API size_t fp8rl_host_sync_staging_bytes(int64_t rows, int64_t k, int32_t slots, fp8rl_scale_fmt fmt);
+FP8RL_API fp8rl_status fp8rl_quant_weight_host_batched(const fp8rl_weight_desc* descs, int32_t count,
+                                                       fp8rl_scale_fmt fmt, void* d_staging,
+                                                       size_t staging_bytes, int32_t slots, void* stream);
+
+/*
  * Dynamic activation quantisation in 1x128 groups along K (one scale per token
  * and per 128 columns; "Method steps", step 1: activations quantised in every
  * forward pass).
@@ -364,7 +400,11 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          weight has a 128-row block per SM), 1 always that kernel, 2 the
  *          128-row-tile kernel;
  *   key 0  restore all defaults.
- * Errors: INVALID_ARG for an unknown key or value.
+ * Every key but 0 is refused (UNSUPPORTED, nothing changes) unless the
+ * process environment holds FP8RL_TEST_HOOKS=1 at the time of the call, so
+ * that no production caller changes the library's behaviour by accident.
+ * Errors: UNSUPPORTED (hooks not enabled), INVALID_ARG for an unknown key or
+ * value.
  */
 FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value);
 
