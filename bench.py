@@ -40,7 +40,7 @@ WORKLOAD = "qwen3-8b-layer"
 STEP_M = 8192          # tokens in the step's forward batch
 
 # DRAM bytes (read + write) per launch of the dominant kernel, taken from one
-# ncu capture of the same launch (profiles/gemm_blockscaled_gate_up_8192x24576x4096.md).
+# ncu capture of the same launch (the 8192 x 24576 x 4096 gate-up GEMM).
 # Reported only while the GEMM's sources are those the capture was taken with.
 TRAFFIC = {
     "gemm_gate_up": {
@@ -117,15 +117,31 @@ def gemm_bytes(m, n, k, scale_bytes=4):
     return n * k + m * k + 2 * m * n + scale_bytes * (m * (k // 128) + (n // 128) * (k // 128))
 
 
+def fp8_peak(peaks):
+    """Dense FP8 tensor roofline: 2 x the measured BURST bf16 GEMM rate (the
+    nominal fp8:bf16 ratio).  The burst figure is the one for kernels timed
+    in isolation or inside a step of a few milliseconds, as every GEMM here
+    is; the sustained figure (a seconds-long loop under the power cap) is
+    reported beside it only as a second, labelled fraction."""
+    return 2.0 * peaks["bf16_tflops"]
+
+
+FP8_PEAK_BASIS = "2 x bf16_tflops (burst), the nominal fp8:bf16 ratio"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
-                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
-                "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
-            "source": "fallback"}
+        peaks = {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                 "source": "measured"}
+    else:
+        peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                 "source": "fallback"}
+    peaks["fp8_tflops"] = fp8_peak(peaks)
+    peaks["fp8_basis"] = FP8_PEAK_BASIS
+    return peaks
 
 
 # --------------------------------------------------------------------------- clocks
@@ -320,7 +336,7 @@ def step_rooflines(inp, timer, peaks):
     """Per-phase achieved rate against its bound (HBM for quantisers and
     weight-streaming GEMMs, FP8 tensor peak for the others)."""
     hbm = peaks["hbm_gbs"]
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # fp8 dense = 2x bf16 (nominal ratio)
+    fp8 = fp8_peak(peaks)
     out = {}
     wbytes = sum(wq_bytes(*w.shape) for w in inp["weights"])
     ms = timer.avg_ms("weight_sync")
@@ -333,7 +349,7 @@ def step_rooflines(inp, timer, peaks):
                                     "unit": "GB/s", "frac": b / ms / 1e6 / hbm, "bytes": b}
         ms = timer.avg_ms(f"gemm_{name}")
         f = gemm_flops(STEP_M, n, k)
-        out[f"gemm_{name}"] = gemm_roof(f, gemm_bytes(STEP_M, n, k), ms, hbm, fp8_peak)
+        out[f"gemm_{name}"] = gemm_roof(f, gemm_bytes(STEP_M, n, k), ms, hbm, fp8)
     if inp["moe"] is not None:
         rows = inp["moe"]["rows"]
         for which, n, k, x, xq, sx, wq, sw, y in inp["moe"]["pairs"]:
@@ -345,7 +361,7 @@ def step_rooflines(inp, timer, peaks):
             ms = timer.avg_ms(f"moe_gemm_{which}")
             e = wq.shape[0]
             bytes_ = e * n * k + rows * k + 2 * rows * n + 4 * (rows * k // 128 + e * (n // 128) * (k // 128))
-            out[f"moe_gemm_{which}"] = gemm_roof(gemm_flops(rows, n, k), bytes_, ms, hbm, fp8_peak)
+            out[f"moe_gemm_{which}"] = gemm_roof(gemm_flops(rows, n, k), bytes_, ms, hbm, fp8)
     return out
 
 
@@ -363,11 +379,13 @@ def gemm_roof(flops, bytes_, ms, hbm_gbs, fp8_tflops):
 
 
 def e2e_weight_sync(torch, fp8rl, inp, stream, steps):
-    """Weight sync through the library from pinned HOST buffers to pinned HOST
-    buffers, every byte crossing the CPU-GPU link inside the timed region.
-    Two ways are timed and the faster is reported: the quantiser reading and
-    writing host memory directly (one launch), and a three-stream
-    copy-in / quantise / copy-out pipeline over 32 MB chunks."""
+    """Weight sync through the library's C ABI from pinned HOST buffers to
+    pinned HOST buffers, every byte crossing the CPU-GPU link inside the timed
+    region.  Two ways are timed and the faster is reported:
+    fp8rl_quant_weight_host_batched (the library's copy-in / quantise /
+    copy-out pipeline over ~32 MB chunks on three streams; "pipelined"), and
+    fp8rl_quant_weight_blockwise_batched given host pointers (the quantiser
+    reading and writing host memory directly, one launch; "direct")."""
     host_w = [w.cpu().pin_memory() for w in inp["weights"]]
     wbytes = sum(wq_bytes(*w.shape) for w in inp["weights"])
     results = {}
@@ -394,6 +412,8 @@ def e2e_weight_sync(torch, fp8rl, inp, stream, steps):
     return {"value": r["value"], "unit": UNIT, "ms_per_step": r["ms_per_step"],
             "h2d_bytes_per_step": r["h2d_bytes_per_step"], "d2h_bytes_per_step": r["d2h_bytes_per_step"],
             "mode": best, "modes": {m: round(v["value"], 1) for m, v in results.items()},
+            "entry_point": {"pipelined": "fp8rl_quant_weight_host_batched",
+                            "direct": "fp8rl_quant_weight_blockwise_batched"}[best],
             "matches_device_result": r["matches_device_result"]}
 
 
@@ -518,7 +538,7 @@ def section_moe_sync(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
 
 def section_sweep(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
     """GEMM sweep at Qwen3-8B shapes; small working sets rotate copies > 4x L2."""
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    fp8 = fp8_peak(peaks)
     res = {}
     sdt = torch.float32 if fmt == 0 else torch.uint8
     for name, n, k in synth.QWEN3_8B_GEMMS:
@@ -543,7 +563,7 @@ def section_sweep(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
             # replayed from a CUDA graph: device time of back-to-back launches
             ms = time_graph(torch, call, max(20, len(sets) * 2))
             r = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k, 4 if fmt == 0 else 1), ms,
-                          peaks["hbm_gbs"], fp8_peak)
+                          peaks["hbm_gbs"], fp8)
             res[f"{name}_m{m}"] = {"m": m, "n": n, "k": k, "ms": ms, "tflops": r["tflops"],
                                    "bound": r["bound"], "frac": r["frac"]}
             del sets
@@ -622,7 +642,7 @@ def section_fused_mlp(torch, synth, fp8rl, dev, seed, peaks, fmt=0):
         res[name] = {"m": m, "inter": inter, "k": k, "fused_ms": t_fused, "unfused_gemm_ms": t_gemm,
                      "unfused_act_quant_ms": t_aq, "saved_ms": t_gemm + t_aq - t_fused,
                      "fused_tflops": flops / t_fused / 1e9,
-                     "fused_frac_fp8": flops / t_fused / 1e9 / (2.0 * peaks["bf16_tflops_sustained"])}
+                     "fused_frac_fp8": flops / t_fused / 1e9 / fp8_peak(peaks)}
         del d, hq, hs, y, q2
         torch.cuda.empty_cache()
     return res
@@ -749,7 +769,7 @@ def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt)
     y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
     ms = time_loop(torch, lambda: fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, m, n, k, fmt), 20, 5)
     r = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k, 1), ms, peaks["hbm_gbs"],
-                  2.0 * peaks["bf16_tflops_sustained"])
+                  fp8_peak(peaks))
     return {"m": m, "n": n, "k": k, "ms": ms, "tflops": r["tflops"], "frac": r["frac"], "bound": r["bound"]}
 
 
@@ -835,7 +855,11 @@ def main_ours(args):
     d = roofs[dominant]
     roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
                 "unit": d["unit"], "frac": d["frac"], "traffic": captured_traffic(dominant),
-                "peak_source": f"{peaks['source']} ({'hbm_gbs' if d['bound'] == 'hbm' else '2 x bf16_tflops_sustained'})"}
+                "peak_source": f"{peaks['source']} ({'hbm_gbs' if d['bound'] == 'hbm' else FP8_PEAK_BASIS})"}
+    if d["bound"] == "tensor":
+        # the same achieved rate against 2 x the sustained bf16 figure, for
+        # comparison only (that figure belongs to seconds-long loops)
+        roofline["frac_vs_2x_bf16_sustained"] = d["achieved"] / (2.0 * peaks["bf16_tflops_sustained"])
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
     wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
@@ -941,6 +965,7 @@ def main_case(args):
     import fp8_w8a8_rollout_gb300 as fp8rl
     from fp8_w8a8_rollout_gb300 import synth
     dev = torch.device("cuda")
+    os.environ["FP8RL_TEST_HOOKS"] = "1"  # --case may force tile widths and schedules
     fp8rl.load_library()
     if args.bn:
         fp8rl.fp8rl_debug_set(fp8rl.DEBUG_GEMM_BN, args.bn)
@@ -951,7 +976,7 @@ def main_case(args):
     parts = args.case.split(":")
     kind = parts[0]
     peaks = load_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    fp8 = fp8_peak(peaks)
     if kind == "gemm":
         m, n, k = (int(v) for v in parts[1:4])
         fmt = int(parts[4]) if len(parts) > 4 else 0
@@ -967,7 +992,7 @@ def main_case(args):
             fn = lambda: fp8rl.fp8rl_gemm_blockscaled_ws(xq, sx, wq, sw, y, m, n, k, fmt, ws, ws.numel())
         else:
             fn = lambda: fp8rl.fp8rl_gemm_blockscaled(xq, sx, wq, sw, y, m, n, k, fmt)
-        work = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k), 1.0, peaks["hbm_gbs"], fp8_peak)
+        work = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k), 1.0, peaks["hbm_gbs"], fp8)
     elif kind == "grouped":
         which = parts[1]
         n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
