@@ -62,41 +62,58 @@ constexpr int kUmmaK = 32;   // K of one E4M3 tcgen05.mma
 // OUT: finished tiles leave through shared memory and TMA stores (one
 // 32-row x 64-column bf16 box per epilogue warp, in a slot of its own), which
 // takes the operand ring down to what fits beside the slots.
-template <int BN, int AROWS = kBM, int EPI = 0, bool OUT = false>
+// MX: UE8M0 scales applied by the tensor cores (tcgen05.mma kind::mxf8f6f4
+// with scale factors in TMEM): one accumulator per tile instead of one per K
+// chunk, so the epilogue reads TMEM once per tile.
+template <int BN, int AROWS = kBM, int EPI = 0, bool OUT = false, bool MX = false>
 struct Cfg {
   static constexpr int kStageBytesRaw = AROWS * kBK + BN * kBK;
   static constexpr int kCols = 64;                      // accumulator columns per epilogue thread
   static constexpr int kEpiWarps = 4 * (BN / kCols);    // 4 TMEM lane quadrants x column slices
   static constexpr int kOutSlotBytes = 32 * kCols * 2;  // one warp's 32 x 64 bf16 box
   static constexpr int kOutBytes = OUT ? kEpiWarps * kOutSlotBytes : 0;
+  // chunk-scale ring filled by the scale-loader warp: per K chunk the tile's
+  // 128 activation scales and its BN/128 weight scales, as fp32; with MX the
+  // scale-factor blocks the tensor cores read instead (one 512-byte block of
+  // 32 rows x 16 bytes for A, one per 128 columns for B: row r's byte at
+  // 16 (r mod 32) + 4 (r / 32) + j for the four 32-wide K blocks j of the
+  // chunk), copied into TMEM by the MMA thread
+  static constexpr int kScaleSlots = MX ? 8 : 16;
+  static constexpr int kScaleSlotFloats = kBM + 4;
+  static constexpr int kMxSfSlotBytes = 512 * (1 + BN / 128);
+  static constexpr int kScaleRingBytes = MX ? kScaleSlots * kMxSfSlotBytes : kScaleSlots * kScaleSlotFloats * 4;
+  // TMEM columns: MX keeps its accumulators in [0, 256) and the scale factors
+  // of each ring slot in 16 columns from 256 on (4 for A, 4 per 128 of B)
+  static constexpr int kMxSfCol0 = 256;
+  static constexpr int kMxSfColsPerSlot = 16;
+  static_assert(!MX || kMxSfCol0 + kScaleSlots * kMxSfColsPerSlot <= 512, "MX scale factors fit in TMEM");
+  static_assert(!MX || 4 + 4 * (BN / 128) <= kMxSfColsPerSlot, "MX scale factors of one chunk");
   // operand stages: as many as fit in about 200 KB of shared memory, or, with
   // the output slots, in the 227 KB a CTA may use
   static constexpr int kStagesFit =
-      OUT ? (227 * 1024 - 3 * 1024 - 1024 - kOutBytes - 16 * (128 + 4) * 4 - (EPI ? 2 * 4 * 128 * 4 : 0)) /
+      OUT ? (227 * 1024 - 3 * 1024 - 1024 - kOutBytes - kScaleRingBytes - (EPI ? 2 * 4 * 128 * 4 : 0)) /
                 kStageBytesRaw
           : (200 * 1024) / kStageBytesRaw;
   static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
   static constexpr int kThreads = 128 + kEpiWarps * 32; // warpgroup 0: producer, MMA, two idle warps
   // K chunks handed from the MMA issuer to the epilogue per synchronisation:
   // a 128-wide tile's TMEM buffer holds two chunk partials side by side
-  static constexpr int kGroup = BN == 128 ? 2 : 1;
-  static constexpr int kAccBufs = 512 / (BN * kGroup);   // TMEM buffers (all 512 columns)
-  static constexpr int kTmemCols = kAccBufs * BN * kGroup;
+  static constexpr int kGroup = (BN == 128 && !MX) ? 2 : 1;
+  // TMEM accumulator buffers (all 512 columns; MX: the 256 below its scale factors)
+  static constexpr int kAccBufs = MX ? 256 / BN : 512 / (BN * kGroup);
+  static constexpr int kTmemCols = 512;
   static constexpr int kABytes = AROWS * kBK;  // activation rows loaded per stage
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  // chunk-scale ring filled by the scale-loader warp: per K chunk the tile's
-  // 128 activation scales and its BN/128 weight scales, as fp32
-  static constexpr int kScaleSlots = 16;
-  static constexpr int kScaleSlotFloats = kBM + 4;
   static constexpr int kBookBytes = 1024;  // barriers and small shared state
   // fused epilogue: per-row maxima of the four column slices, two tiles deep
   static constexpr int kRedBytes = EPI ? 2 * 4 * kBM * 4 : 0;
-  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleSlots * kScaleSlotFloats * 4 + kRedBytes;
+  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleRingBytes + kRedBytes;
   static constexpr int kOutOffset = (kSharedEnd + 1023) / 1024 * 1024;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kSmemBytes = 1024 + (OUT ? kOutOffset + kOutBytes : kSharedEnd);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(EPI == 0 || BN == 256, "the fused epilogue pairs 128 gate with 128 up columns");
+  static_assert(!MX || (EPI == 0 && AROWS == kBM), "MX: plain bf16 epilogue, 128-row activation stages");
   static constexpr int kPartPitch = BN + 4;  // floats per row of a split-K partial tile
   static_assert(kBM * kPartPitch * 4 <= kStages * kStageBytes, "partial tile must fit over the stages");
   static_assert((2 * kStages + 2 * kAccBufs + 2 * kScaleSlots + 2) * 8 + 16 <= kBookBytes, "bookkeeping");
@@ -323,13 +340,15 @@ __device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
 // rows >= AROWS that are never stored.
 // OUT: finished tiles leave through shared memory and TMA stores (data-
 // parallel kernels with 128-row tiles; the host chooses it per launch).
-template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0, bool OUT = false>
+// MX: UE8M0 scales applied by the tensor cores (data-parallel tiles, bf16 out).
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0, bool OUT = false, bool MX = false>
 __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_x,
                             const __grid_constant__ CUtensorMap tmap_w,
                             const __grid_constant__ CUtensorMap tmap_y, const GemmArgs a) {
   static_assert(!OUT || (MODE == kDataParallel && EPI == 0 && AROWS == kBM), "staged output: data-parallel tiles");
-  using C = Cfg<BN, AROWS, EPI, OUT>;
+  static_assert(!MX || (UE8M0 && MODE == kDataParallel), "MX: UE8M0 scales, data-parallel tiles");
+  using C = Cfg<BN, AROWS, EPI, OUT, MX>;
   static_assert(EPI == 0 || MODE == kDataParallel, "the fused epilogue needs whole tiles");
   constexpr bool SPLITK = MODE == kSplitK;
   constexpr bool STREAMK = MODE == kStreamK;
@@ -345,14 +364,16 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   uint64_t* tempty = tfull + C::kAccBufs;
   uint64_t* drain = tempty + C::kAccBufs;
   uint64_t* sfull = drain + 1;                // scale slot filled (1 arrival: the loader)
-  uint64_t* sempty = sfull + C::kScaleSlots;  // scale slot read (one arrival per epilogue warp)
+  uint64_t* sempty = sfull + C::kScaleSlots;  // scale slot read (one arrival per epilogue warp; MX: the MMA
+                                              // thread's commit once the copy into TMEM has read it)
   uint64_t* published = sempty + C::kScaleSlots;  // stream-K partial stored (one arrival per epilogue warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(published + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* shared_m_tiles = abort_flag + 1;
   uint32_t* shared_epoch = reinterpret_cast<uint32_t*>(shared_m_tiles + 1);
   float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
-  float* row_max = scale_ring + C::kScaleSlots * C::kScaleSlotFloats;  // fused epilogue only
+  uint8_t* sf_ring = reinterpret_cast<uint8_t*>(scale_ring);            // MX: the scale-factor blocks
+  float* row_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scale_ring) + C::kScaleRingBytes);  // EPI 1
   uint8_t* out_slots = base_ptr + C::kOutOffset;                         // OUT only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     mbar_init(smem_u32(published), C::kEpiWarps);
     for (int q = 0; q < C::kScaleSlots; ++q) {
       mbar_init(smem_u32(&sfull[q]), 1);
-      mbar_init(smem_u32(&sempty[q]), C::kEpiWarps);
+      mbar_init(smem_u32(&sempty[q]), MX ? 1 : C::kEpiWarps);
     }
     *abort_flag = 0;
     // stream-K flags of this launch carry the value epoch + 1; the epoch in the
@@ -463,8 +484,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     // better with the stream-K budget (measured on GB300: 8192 x 24576 x 4096
     // 788 -> 756 us); with register stores the extra registers cost 4-7%
     if (C::kSplitRegs)
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((STREAMK || (UE8M0 && OUT)) ? C::kRoleRegsStreamK
-                                                                                       : C::kRoleRegs));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((STREAMK || MX || (UE8M0 && OUT)) ? C::kRoleRegsStreamK
+                                                                                             : C::kRoleRegs));
     if constexpr (!STREAMK) {
       // Data-parallel and split-K: plain loops over whole tiles (or the
       // cluster's one tile).  These loops are latency-critical; measured on
@@ -517,7 +538,58 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           __syncwarp();
         } else if (warp == 1) {
           // ---------------------------------------------------------- MMA issuer
-          if (lane == 0) {
+          if (lane == 0 && MX) {
+            // One accumulator per tile: per K chunk, the chunk's scale-factor
+            // blocks are copied from the loader's ring slot into that slot's
+            // TMEM columns, then four block-scaled MMAs (32-wide K blocks j =
+            // 0..3, scale-factor byte j) accumulate into it.  The ring slot is
+            // reused only after the commit that follows its MMAs, so its TMEM
+            // columns are never overwritten while an MMA may still read them.
+            const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
+            uint32_t g = 0;   // chunks consumed (stage ring position)
+            uint32_t gs = 0;  // scale-factor slots consumed
+            bool alive = true;
+            for (int tt = 0; tt < my_tiles && alive; ++tt) {
+              const int buf = tt % C::kAccBufs;
+              const uint32_t bph = (tt / C::kAccBufs) & 1;
+              if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns,
+                                     !(a.wait_mode & 1))) {
+                alive = false;
+                break;
+              }
+              const uint32_t d = tmem + buf * BN;
+              for (int it = 0; it < nloc; ++it, ++g, ++gs) {
+                const int s = g % C::kStages;
+                const int q = gs % C::kScaleSlots;
+                if (!mbar_wait_bounded(smem_u32(&full[s]), (g / C::kStages) & 1, abortv, a.err, a.timeout_ns,
+                                       !(a.wait_mode & 1)) ||
+                    !mbar_wait_bounded(smem_u32(&sfull[q]), (gs / C::kScaleSlots) & 1, abortv, a.err, a.timeout_ns,
+                                       !(a.wait_mode & 1))) {
+                  alive = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint32_t sf_t = tmem + C::kMxSfCol0 + q * C::kMxSfColsPerSlot;
+                const uint32_t sf_s = smem_u32(sf_ring) + q * C::kMxSfSlotBytes;
+                tmem_cp_32x128b_x4(sf_t, rows16_desc(sf_s));
+#pragma unroll
+                for (int h = 0; h < BN / 128; ++h) tmem_cp_32x128b_x4(sf_t + 4 + 4 * h, rows16_desc(sf_s + 512 * (1 + h)));
+                const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k)
+                  mma_mx_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK),
+                              idesc_mx_e4m3_ue8m0(kBM, BN, k, k), sf_t, sf_t + 4, (it > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&empty[s]));
+                mma_commit(smem_u32(&sempty[q]));
+              }
+              if (alive) mma_commit(smem_u32(&tfull[buf]));
+            }
+            if (*abortv) {
+              // no MMA or copy may still be using TMEM when it is released
+              mma_commit(smem_u32(drain));
+              mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+            }
+          } else if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
             const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
             uint32_t g = 0;  // chunks consumed (stage ring position)
@@ -603,11 +675,36 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
                                                    !(a.wait_mode & 1));
                 alive = __all_sync(0xffffffffu, got);
                 if (!alive) break;
-                float* slot = scale_ring + q * C::kScaleSlotFloats;
-                #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  slot[lane + 32 * j] = tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
-                if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
+                if constexpr (MX) {
+                  // the chunk's scale-factor blocks: lane l writes the 16-byte
+                  // row l of each block, its four words the bytes of rows (A) or
+                  // columns (B) l, l+32, l+64, l+96, each byte repeated for the
+                  // chunk's four 32-wide K blocks (rows past the segment: 2^0)
+                  uint8_t* slot = sf_ring + q * C::kMxSfSlotBytes;
+                  uint32_t wa[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const uint32_t byte = tr.row0 + lane + 32 * j < tr.seg_end
+                                              ? (v[b][j] >> (8 * ((uint32_t)vi[b][j] & 3u))) & 0xFFu
+                                              : 127u;
+                    wa[j] = byte * 0x01010101u;
+                  }
+                  *reinterpret_cast<uint4*>(slot + 16 * lane) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+                  const uint32_t wb = ((w[b] >> (8 * ((uint32_t)wi[b] & 3u))) & 0xFFu) * 0x01010101u;
+#pragma unroll
+                  for (int h = 0; h < BN / 128; ++h) {
+                    const uint32_t x = __shfl_sync(0xffffffffu, wb, h);
+                    *reinterpret_cast<uint4*>(slot + 512 * (1 + h) + 16 * lane) = make_uint4(x, x, x, x);
+                  }
+                  fence_proxy_async_shared();  // the tensor cores' copy reads these bytes
+                } else {
+                  float* slot = scale_ring + q * C::kScaleSlotFloats;
+#pragma unroll
+                  for (int j = 0; j < 4; ++j)
+                    slot[lane + 32 * j] =
+                        tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
+                  if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
+                }
                 __syncwarp();  // orders the lanes' stores before lane 0's release
                 if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
                 ++gs;
@@ -811,7 +908,29 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
       const int sw_lane = nb - (n0 >> 7);  // which of the tile's weight scales
-      for (int it = 0; it < nseg; it += C::kGroup, ++g) {
+      if constexpr (MX) {
+        // the whole tile's scaled sum is in one accumulator: read this
+        // thread's 64 columns and hand the buffer back to the MMA thread
+        const int buf = g % C::kAccBufs;
+        const uint32_t bph = (g / C::kAccBufs) & 1;
+        ++g;
+        ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < C::kCols / 32; ++cc) {
+            uint64_t v[16];
+            tmem_ld_32x32b_x32_pairs(t_lane + buf * BN + cc * 32, v);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc[cc * 16 + q] = v[q];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+        }
+      }
+      for (int it = 0; !MX && it < nseg; it += C::kGroup, ++g) {
         const int gsz = min(C::kGroup, nseg - it);
         const int buf = g % C::kAccBufs;
         const uint32_t bph = (g / C::kAccBufs) & 1;
@@ -1155,6 +1274,7 @@ struct Debug {
   int streamk_grid = 0;           // 0: one CTA per SM (at most one per K iteration); else this many
   int out_stage = 0;              // data-parallel tile stores: 0 choose, 1 through shared memory + TMA, 2 from registers
   int decode = 0;                 // dense rows <= 32: 0 choose, 1 the swapped-operand decode kernel, 2 the 128-row-tile one
+  int mx = 0;                     // UE8M0 data-parallel tiles: 0 the block-scaled MMA, 1 the per-chunk promotion
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -1261,7 +1381,7 @@ struct KernelState {
   int cluster_capacity[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // clusters resident at once
 };
 
-template <int BN, int AROWS, bool UE8M0, int MODE, int EPI, bool OUT>
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI, bool OUT, bool MX>
 KernelState& kernel_state(int dev) {
   static KernelState st[64];
   return st[dev];
@@ -1281,15 +1401,15 @@ StreamKLayout streamk_layout(int max_ctas) {
   return l;
 }
 
-template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0, bool OUT = false>
+template <int BN, int AROWS, bool UE8M0, int MODE, int EPI = 0, bool OUT = false, bool MX = false>
 fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_tiles_bound, int sms,
                     GemmArgs args, int splits, cudaStream_t stream, int streamk_grid = 0) {
-  using C = Cfg<BN, AROWS, EPI, OUT>;
+  using C = Cfg<BN, AROWS, EPI, OUT, MX>;
   constexpr bool SPLITK = MODE == kSplitK;
-  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE, EPI, OUT>;
+  auto kernel = gemm_blockscaled_kernel<BN, AROWS, UE8M0, MODE, EPI, OUT, MX>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
-  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE, EPI, OUT>(dev);
+  KernelState& ks = kernel_state<BN, AROWS, UE8M0, MODE, EPI, OUT, MX>(dev);
   const uint64_t ctx = current_context_id();
   if (!ctx) return FP8RL_ERR_CUDA;
   {
@@ -1487,6 +1607,18 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   // than the store they save (measured on GB300: 8192 x 24576 x 4096 +6%,
   // 1024 x 6144 x 4096 +5%, grouped MoE +5..14%; 8192 x 4096 x 12288 -3%).
   const bool staged = dbg.out_stage == 1 || (dbg.out_stage != 2 && k <= 4096);
+  if (ue && dbg.mx != 1) {
+    // UE8M0: the tensor cores apply the power-of-two scales themselves
+    // (block-scaled MMA), one accumulator per tile
+    if (bn == 256) {
+      const fp8rl_status st =
+          staged ? launch<256, kBM, true, kDataParallel, 0, true, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                 : launch<256, kBM, true, kDataParallel, 0, false, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+      if (st != FP8RL_ERR_UNSUPPORTED) return st;
+    }
+    return staged ? launch<128, kBM, true, kDataParallel, 0, true, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
+                  : launch<128, kBM, true, kDataParallel, 0, false, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+  }
   if (bn == 256) {
     const fp8rl_status st =
         staged ? (ue ? launch<256, kBM, true, kDataParallel, 0, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
@@ -1680,6 +1812,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 10:
       if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
       g_debug.decode = (int)value;
+      return FP8RL_OK;
+    case 11:
+      if (value < 0 || value > 1) return FP8RL_ERR_INVALID_ARG;
+      g_debug.mx = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

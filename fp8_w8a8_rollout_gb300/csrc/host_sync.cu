@@ -33,6 +33,15 @@ size_t chunk_bytes(int64_t rows, int64_t k, size_t scale_bytes) {
   return align256((size_t)rows * k * 2) + align256((size_t)rows * k) + align256((size_t)rb * kb * scale_bytes);
 }
 
+// rows x width bytes between pitched buffers: one linear copy when both sides
+// are contiguous (a pitched copy of contiguous rows measured about half the
+// link rate on GB300), else a pitched copy
+cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t rows,
+                      cudaMemcpyKind kind, cudaStream_t s) {
+  if (dpitch == width && spitch == width) return cudaMemcpyAsync(dst, src, width * rows, kind, s);
+  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, s);
+}
+
 // The library's streams and events of one device, made once per context.
 struct SyncState {
   uint64_t ctx = 0;
@@ -132,9 +141,8 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_host_batched(const fp8rl_we
         const size_t scale_len = (size_t)((r + kBlock - 1) / kBlock) * kb * sb;
         // the slot's previous chunk must have left the device before it is overwritten
         if (chunk >= slots && cudaStreamWaitEvent(st.s_in, st.ev_out[j], 0) != cudaSuccess) return FP8RL_ERR_CUDA;
-        if (cudaMemcpy2DAsync(dw, (size_t)d.k * 2, static_cast<const char*>(d.w_bf16) + (size_t)r0 * d.ldw * 2,
-                              (size_t)d.ldw * 2, (size_t)d.k * 2, (size_t)r, cudaMemcpyHostToDevice,
-                              st.s_in) != cudaSuccess ||
+        if (copy_rows(dw, (size_t)d.k * 2, static_cast<const char*>(d.w_bf16) + (size_t)r0 * d.ldw * 2,
+                      (size_t)d.ldw * 2, (size_t)d.k * 2, (size_t)r, cudaMemcpyHostToDevice, st.s_in) != cudaSuccess ||
             cudaEventRecord(st.ev_in[j], st.s_in) != cudaSuccess ||
             cudaStreamWaitEvent(st.s_q, st.ev_in[j], 0) != cudaSuccess)
           return FP8RL_ERR_CUDA;
@@ -142,8 +150,8 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_host_batched(const fp8rl_we
         if (qs != FP8RL_OK) return qs;
         if (cudaEventRecord(st.ev_q[j], st.s_q) != cudaSuccess ||
             cudaStreamWaitEvent(st.s_out, st.ev_q[j], 0) != cudaSuccess ||
-            cudaMemcpy2DAsync(static_cast<char*>(d.q_e4m3) + (size_t)r0 * d.ldq, (size_t)d.ldq, dq, (size_t)d.k,
-                              (size_t)d.k, (size_t)r, cudaMemcpyDeviceToHost, st.s_out) != cudaSuccess ||
+            copy_rows(static_cast<char*>(d.q_e4m3) + (size_t)r0 * d.ldq, (size_t)d.ldq, dq, (size_t)d.k,
+                      (size_t)d.k, (size_t)r, cudaMemcpyDeviceToHost, st.s_out) != cudaSuccess ||
             cudaMemcpyAsync(static_cast<char*>(d.w_scale) + scale_off, ds, scale_len, cudaMemcpyDeviceToHost,
                             st.s_out) != cudaSuccess ||
             cudaEventRecord(st.ev_out[j], st.s_out) != cudaSuccess)

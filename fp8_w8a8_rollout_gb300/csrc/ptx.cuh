@@ -193,6 +193,27 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 (block-scaled): B's
+// scale-factor byte in bits 4-5, A and B E4M3 (bits 7-9, 10-12 = 0), both
+// K-major, N >> 3 in bits 17-22, UE8M0 scale factors (bit 23), M >> 7 in bits
+// 27-28, A's scale-factor byte in bits 29-30; the accumulator is fp32.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3_ue8m0(int m, int n, int sfa_byte, int sfb_byte) {
+  return (static_cast<uint32_t>(sfb_byte) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 7) << 27) | (static_cast<uint32_t>(sfa_byte) << 29);
+}
+
+// Shared-memory descriptor of a 32-row x 16-byte block with rows 16 bytes
+// apart (no swizzle: 8-row core matrices of 128 bytes, stride byte offset
+// 128): the source layout of a tcgen05.cp 32x128b copy.
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
                : "memory");
@@ -220,6 +241,28 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T, one M x N x 32 E4M3 step with
+// UE8M0 scale factors per 32-wide K block read from TMEM (row r of A: lane r,
+// column sfa + r / 32; column n of B: lane n % 32 of every lane quadrant,
+// column sfb + n / 32; the byte the descriptor names), issued by one thread
+__device__ __forceinline__ void mma_mx_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 128 bits from shared memory (descriptor) into TMEM columns
+// taddr .. taddr + 3 of lanes 0..31, replicated into all four lane quadrants;
+// asynchronous, ordered with this thread's tcgen05.mma and tracked by
+// tcgen05.commit
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // arrive once on the mbarrier when every tcgen05 op issued so far by this thread completes

@@ -399,6 +399,9 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          swapped-operand decode kernel for <= 16 rows, or <= 32 when the
  *          weight has a 128-row block per SM), 1 always that kernel, 2 the
  *          128-row-tile kernel;
+ *   key 11 UE8M0 GEMMs on whole tiles (data-parallel): 0 the tensor cores
+ *          apply the power-of-two scales (block-scaled MMA, default), 1 the
+ *          per-chunk fp32 promotion in the epilogue (the fp32-scale path);
  *   key 0  restore all defaults.
  * Every key but 0 is refused (UNSUPPORTED, nothing changes) unless the
  * process environment holds FP8RL_TEST_HOOKS=1 at the time of the call, so

@@ -441,3 +441,107 @@ def test_decode_kernel_is_deterministic(decode_mode):
     a = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
     b = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
     assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------- UE8M0 on the block-scaled MMA
+
+@pytest.fixture(params=[0, 1], ids=["mx", "promote"])
+def mx_mode(request):
+    """UE8M0 tiles on the tensor cores' block-scaled MMA (0, the default) or on
+    the per-chunk fp32 promotion (1)."""
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, request.param)
+    yield request.param
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 0)
+
+
+def exact_operands(m, n, k, seed, experts=1):
+    """Integer-valued E4M3 codes in [-4, 4] and UE8M0 scale bytes in
+    [125, 129] (2^-2 .. 2^2), drawn independently per row, weight block and K
+    chunk: every partial sum of the product is a multiple of 2^-4 below 2^17,
+    so fp32 accumulation in any order is exact and Y is bf16_rne of the exact
+    value."""
+    rng = np.random.default_rng(seed)
+    xq = oracle.e4m3_encode_array(rng.integers(-4, 5, size=(m, k)).astype(np.float32))
+    wq = oracle.e4m3_encode_array(rng.integers(-4, 5, size=(experts * n, k)).astype(np.float32))
+    sx = rng.integers(125, 130, size=(k // 128, m)).astype(np.uint8)
+    sw = rng.integers(125, 130, size=(experts * n // 128, k // 128)).astype(np.uint8)
+    return xq, sx, wq, sw
+
+
+def bf16_bits_of(y):
+    return torch.from_numpy(np.asarray(y, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 512, 512), (128, 256, 256), (1, 128, 384), (257, 384, 512)])
+def test_power_of_two_scales_exact(m, n, k, bn, mx_mode):
+    """With exact partial sums both UE8M0 paths must give bf16_rne of the
+    exact product bit for bit, and so must the fp32-scale path given the same
+    powers of two as fp32 scales: a scale applied to the wrong row, column or
+    K chunk shows as a wrong bit."""
+    xq, sx, wq, sw = exact_operands(m, n, k, m * 7 + n + k)
+    ref_bits = bf16_bits_of(oracle.gemm_blockscaled(xq, sx, wq, sw, fp8rl.SCALE_UE8M0))
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    y = fp8rl.gemm(dx, dsx, dw, dsw, fp8rl.SCALE_UE8M0)
+    assert fp8rl.fp8rl_sync_status() == 0
+    assert np.array_equal(y.view(torch.int16).cpu().numpy(), ref_bits)
+    fx = np.ldexp(1.0, sx.astype(np.int32) - 127).astype(np.float32)
+    fw = np.ldexp(1.0, sw.astype(np.int32) - 127).astype(np.float32)
+    dfx, dfw = to_dev(fx, fw)
+    y32 = fp8rl.gemm(dx, dfx, dw, dfw, fp8rl.SCALE_FP32)
+    assert fp8rl.fp8rl_sync_status() == 0
+    assert np.array_equal(y32.view(torch.int16).cpu().numpy(), ref_bits)
+
+
+@pytest.mark.parametrize("counts", [[3, 0, 200, 129], [128, 128], [0, 0, 5], [300, 0, 0, 1, 0]])
+def test_power_of_two_scales_exact_grouped(counts, bn, mx_mode):
+    """The same exactness over expert segments (segments ending inside tiles,
+    empty experts); rows outside the offsets keep what the output held."""
+    n, k = 256, 384
+    offsets = synth.routing_with_counts(counts)
+    rows, e = int(offsets[-1]), len(counts)
+    xq, sx, wq, sw = exact_operands(rows, n, k, 11 + sum(counts), experts=e)
+    wq = wq.reshape(e, n, k)
+    sw = sw.reshape(e, n // 128, k // 128)
+    ref_bits = bf16_bits_of(oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, fp8rl.SCALE_UE8M0))
+    dx, dsx, dw, dsw, doff = to_dev(xq, sx, wq, sw, offsets)
+    out = torch.full((rows + 16, n), 5.0, dtype=torch.bfloat16, device="cuda")
+    fp8rl.grouped_gemm(dx, dsx, dw, dsw, doff, fp8rl.SCALE_UE8M0, out=out[:rows])
+    assert fp8rl.fp8rl_sync_status() == 0
+    assert np.array_equal(out[:rows].view(torch.int16).cpu().numpy(), ref_bits)
+    assert bool((out[rows:] == 5.0).all())
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 512, 512), (129, 384, 1024), (2000, 768, 384)])
+def test_ue8m0_paths_match_oracle(m, n, k, bn, mx_mode):
+    """Quantised activations with outlier channels and N(0, 0.02) weights:
+    both UE8M0 paths within the stated tolerance of the fp64 oracle."""
+    x = synth.activation_bf16(m, k, m + 3, "mx-x")
+    w = synth.weight_bf16(n, k, n + 5, "mx-w")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_UE8M0)
+    within(run_gemm(xq, sx, wq, sw, fp8rl.SCALE_UE8M0), oracle.gemm_blockscaled(xq, sx, wq, sw, fp8rl.SCALE_UE8M0))
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_grouped_ue8m0_qwen3_30b_a3b_sampled(which):
+    """The Qwen3-30B-A3B-shaped expert layer (128 experts, 32768 routed rows)
+    with UE8M0 scales on the block-scaled MMA: first and last row of every
+    non-empty segment plus 4096 random outputs."""
+    fmt = fp8rl.SCALE_UE8M0
+    n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
+    r = synth.moe_routing(4096, synth.MOE_EXPERTS, synth.MOE_TOPK, 3, 0)
+    offsets = oracle.moe_dispatch_plan(r.topk, synth.MOE_EXPERTS)[0]
+    rows = int(offsets[-1])
+    x = synth.normal_bf16((rows, k), 1.0, 31, "grp-ue-x", which)
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x), fmt)
+    ws = synth.moe_expert_weights(n, k, synth.MOE_EXPERTS, 32, 0, which)
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(ws.reshape(-1, k)), fmt)
+    wq = wq.reshape(synth.MOE_EXPERTS, n, k)
+    sw = sw.reshape(synth.MOE_EXPERTS, n // 128, k // 128)
+    y = run_grouped(offsets, xq, sx, wq, sw, fmt)
+    seg_rows = [int(v) for e in range(synth.MOE_EXPERTS) if offsets[e + 1] > offsets[e]
+                for v in (offsets[e], offsets[e + 1] - 1)]
+    rng = np.random.default_rng(9)
+    rr = np.concatenate([np.repeat(np.array(seg_rows), 4), rng.integers(0, rows, 4096)]).astype(np.int64)
+    cc = np.concatenate([rng.integers(0, n, 4 * len(seg_rows)), rng.integers(0, n, 4096)]).astype(np.int64)
+    ref = oracle.grouped_gemm_blockscaled_at(xq, sx, wq, sw, offsets, rr, cc, fmt)
+    within(y[rr, cc], ref)
