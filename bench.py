@@ -95,6 +95,12 @@ def parse():
     ap.add_argument("--streamk", type=int, default=-1,
                     help="with --case gemm: call the workspace entry point; 0 chooses, 1 never, 2 always stream-K")
     ap.add_argument("--streamk-grid", type=int, default=0, help="with --streamk: stream-K CTA count (0: one per SM)")
+    ap.add_argument("--out-stage", type=int, default=0,
+                    help="with --case: tile stores, 0 chosen, 1 through shared memory + TMA, 2 from registers")
+    ap.add_argument("--pair", type=int, default=0,
+                    help="with --case: dense tiles on tensor-core pairs, 0 chosen, 1 always, 2 never")
+    ap.add_argument("--mx", type=int, default=0,
+                    help="with --case: UE8M0 whole tiles, 0 block-scaled MMA, 1 per-chunk promotion")
     return ap.parse_args()
 
 
@@ -973,6 +979,12 @@ def main_case(args):
         fp8rl.fp8rl_debug_set(4, args.wait_mode)
     if args.l2_prefetch >= 0:
         fp8rl.fp8rl_debug_set(5, args.l2_prefetch)
+    if args.out_stage:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, args.out_stage)
+    if args.mx:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, args.mx)
+    if args.pair:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, args.pair)
     parts = args.case.split(":")
     kind = parts[0]
     peaks = load_peaks()
@@ -1065,7 +1077,7 @@ def main_case(args):
     ms = time_loop(torch, fn, max(1, args.steps), args.warmup)
     assert fp8rl.fp8rl_sync_status() == 0
     out = {"case": args.case, "ms": ms, "bn": args.bn or "auto", "wait_mode": args.wait_mode,
-           "l2_prefetch": args.l2_prefetch, "streamk": args.streamk}
+           "l2_prefetch": args.l2_prefetch, "streamk": args.streamk, "out_stage": args.out_stage, "mx": args.mx, "pair": args.pair}
     if args.graph:
         out["ms_graph"] = time_graph(torch, fn, max(10, args.steps))
     if "flops" in work:

@@ -1246,6 +1246,377 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   streamk_finish();
 }
 
+// ---------------------------------------------------------------- tensor-core pairs
+//
+// UE8M0 products on tensor-core pairs: a cluster of two CTAs on neighbouring
+// SMs computes a 256 x 256 output tile with tcgen05 cta_group::2.  Per K chunk
+// each CTA loads its own 128 activation rows and its half (128 rows) of the
+// tile's 256 weight rows, 32 KB instead of the 48 KB that a 128 x 256 tile of
+// one CTA needs for the same work per SM (measured on GB300, operand delivery
+// is what bounds the one-CTA tile).  The even CTA's MMA thread issues
+// block-scaled M = 256 MMAs that read both CTAs' shared memory and accumulate
+// the whole tile in both CTAs' TMEM (rows 0..127 in the even CTA, 128..255 in
+// the odd one); each CTA's scale loader fills its own scale-factor blocks
+// (its rows' activation scales and the tile's two weight scales), which the
+// MMA thread copies into each CTA's TMEM with one cta_group::2 copy.  Each
+// CTA's epilogue reads and stores its own 128 rows once per tile.
+//   Both producers' copies complete on the even CTA's stage barrier, whose
+// arrival the even producer makes with both CTAs' byte count; both loaders
+// arrive on the even CTA's scale barrier; the MMA thread's commits arrive in
+// both CTAs; both epilogues hand the accumulator back on the even CTA's
+// barrier.  (With fp32 scales the chunk accumulators would have to cross the
+// pair every K chunk: measured at half the one-CTA kernel's speed on GB300,
+// so fp32 keeps one CTA per tile.)
+template <bool OUT>
+struct PairCfg {
+  static constexpr int kBN = 256;                // tile columns
+  static constexpr int kABytes = kBM * kBK;      // this CTA's 128 activation rows
+  static constexpr int kBBytes = 128 * kBK;      // this CTA's 128 of the 256 weight rows
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kCols = 64;               // accumulator columns per epilogue thread
+  static constexpr int kEpiWarps = 16;
+  static constexpr int kThreads = 128 + kEpiWarps * 32;
+  static constexpr int kOutSlotBytes = 32 * kCols * 2;
+  static constexpr int kOutBytes = OUT ? kEpiWarps * kOutSlotBytes : 0;
+  // scale-factor blocks per K chunk: A (this CTA's 128 rows) and B (the
+  // tile's 256 columns), 512 bytes per 128 rows or columns, the layout of the
+  // one-CTA block-scaled kernel
+  static constexpr int kScaleSlots = 8;
+  static constexpr int kSfSlotBytes = 512 * 3;
+  static constexpr int kScaleRingBytes = kScaleSlots * kSfSlotBytes;
+  static constexpr int kSfCol0 = 256;            // TMEM: the accumulator in [0, 256)
+  static constexpr int kSfColsPerSlot = 16;
+  static_assert(kSfCol0 + kScaleSlots * kSfColsPerSlot <= 512, "scale factors fit in TMEM");
+  static constexpr int kBookBytes = 1024;
+  static constexpr int kStagesFit =
+      OUT ? (227 * 1024 - 3 * 1024 - kBookBytes - kOutBytes - kScaleRingBytes) / kStageBytes
+          : (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleRingBytes;
+  static constexpr int kOutOffset = (kSharedEnd + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = 1024 + (OUT ? kOutOffset + kOutBytes : kSharedEnd);
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert((2 * kStages + 2 * kScaleSlots + 4) * 8 + 32 <= kBookBytes, "bookkeeping");
+  // the roles (the MMA thread's copies, cluster waits and descriptors) need
+  // more than the one-CTA kernel's (measured: spills below 80); the epilogue
+  // holds no running sums
+  static constexpr int kRoleRegs = 80;
+  static constexpr int kEpiRegs = 96;
+  static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
+};
+
+template <bool OUT>
+__global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
+    gemm_pair_mx_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ CUtensorMap tmap_y, const GemmArgs a) {
+  using C = PairCfg<OUT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + C::kStages * C::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint64_t* sfull = drain + 1;
+  uint64_t* sempty = sfull + C::kScaleSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::kScaleSlots);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint32_t* issued = reinterpret_cast<uint32_t*>(abort_flag + 1);  // chunks this CTA's producer issued
+  uint8_t* sf_ring = base_ptr + C::kStages * C::kStageBytes + C::kBookBytes;
+  uint8_t* out_slots = base_ptr + C::kOutOffset;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the pair's MMAs
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  const int num_kb = a.k / kBK;
+  const int m_pairs = (a.rows + 2 * kBM - 1) / (2 * kBM);
+  const int n_tiles = a.n / C::kBN;
+  const int total = m_pairs * n_tiles;
+
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);   // the even producer's arrival with both CTAs' bytes
+      mbar_init(smem_u32(&empty[s]), 1);  // the MMA thread's commit
+    }
+    mbar_init(smem_u32(tfull), 1);
+    mbar_init(smem_u32(tempty), 2 * C::kEpiWarps);  // both CTAs' epilogue warps
+    mbar_init(smem_u32(drain), 1);
+    for (int q = 0; q < C::kScaleSlots; ++q) {
+      mbar_init(smem_u32(&sfull[q]), 2);   // both CTAs' scale loaders
+      mbar_init(smem_u32(&sempty[q]), 1);  // the MMA thread's commit after the copies
+    }
+    *abort_flag = 0;
+    *issued = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before any copy or arrival targets them
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abortv = abort_flag;
+  auto coords = [&](int pt, int& mp, int& n_tile) {
+    mp = pt % m_pairs;  // m-pairs fastest: the pairs in flight share a few weight tiles
+    n_tile = pt / m_pairs;
+  };
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRoleRegs));
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      uint32_t g = 0;
+      if (lane == 0) {
+        prefetch_tensormap(&tmap_x);
+        prefetch_tensormap(&tmap_w);
+        const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
+        bool alive = true;
+        for (int pt = pair; pt < total && alive; pt += npairs) {
+          int mp, n_tile;
+          coords(pt, mp, n_tile);
+          const int row0 = mp * 2 * kBM + (int)rank * kBM;
+          const int wrow0 = n_tile * C::kBN + (int)rank * 128;
+          for (int kb = 0; kb < num_kb; ++kb, ++g) {
+            const int s = g % C::kStages;
+            if (!mbar_wait_bounded(smem_u32(&empty[s]), ((g / C::kStages) & 1) ^ 1, abortv, a.err, a.timeout_ns,
+                                   !(a.wait_mode & 1))) {
+              alive = false;
+              break;
+            }
+            if ((int)g == a.fault_skip_kb) continue;
+            if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * C::kStageBytes);
+            const uint32_t fb = full0 + 8u * (uint32_t)s;
+            tma_load_2d_pair(sA + s * C::kABytes, &tmap_x, kb * kBK, row0, fb);
+            tma_load_2d_pair(sB + s * C::kBBytes, &tmap_w, kb * kBK, wrow0, fb);
+          }
+        }
+        *issued = g;
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer (even CTA)
+      if (lane == 0 && rank == 0) {
+        uint32_t g = 0, gs = 0, tt = 0;
+        bool alive = true;
+        for (int pt = pair; pt < total && alive; pt += npairs, ++tt) {
+          if (!mbar_wait_bounded_cluster(smem_u32(tempty), (tt & 1) ^ 1, abortv, a.err, a.timeout_ns)) {
+            alive = false;
+            break;
+          }
+          for (int kb = 0; kb < num_kb; ++kb, ++g, ++gs) {
+            const int s = g % C::kStages;
+            const int q = gs % C::kScaleSlots;
+            if (!mbar_wait_bounded(smem_u32(&full[s]), (g / C::kStages) & 1, abortv, a.err, a.timeout_ns,
+                                   !(a.wait_mode & 1)) ||
+                !mbar_wait_bounded_cluster(smem_u32(&sfull[q]), (gs / C::kScaleSlots) & 1, abortv, a.err,
+                                           a.timeout_ns)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sf_t = tmem + C::kSfCol0 + q * C::kSfColsPerSlot;
+            const uint32_t sf_s = smem_u32(sf_ring) + q * C::kSfSlotBytes;
+#pragma unroll
+            for (int h = 0; h < 3; ++h) tmem_cp_32x128b_x4_pair(sf_t + 4 * h, rows16_desc(sf_s + 512 * h));
+            const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              mma_mx_e4m3_pair(tmem, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK),
+                               idesc_mx_e4m3_ue8m0(2 * kBM, C::kBN, k, k), sf_t, sf_t + 4,
+                               (kb > 0 || k > 0) ? 1u : 0u);
+            mma_commit_pair(smem_u32(&empty[s]));
+            mma_commit_pair(smem_u32(&sempty[q]));
+          }
+          if (alive) mma_commit_pair(smem_u32(tfull));
+        }
+        if (*abortv) {
+          // no MMA or copy may still be using either CTA's TMEM when it is released
+          mma_commit_pair(smem_u32(drain));
+          mbar_wait_bounded(smem_u32(drain), 0, nullptr, nullptr, 10000000ull);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ scale loaders (warps 2, 3; both CTAs)
+      // per K chunk this CTA's scale-factor blocks: lane l writes the 16-byte
+      // row l of each block (the bytes of rows or columns l, l+32, l+64, l+96,
+      // each repeated for the chunk's four 32-wide K blocks; rows past M: 2^0).
+      // Warp 2 takes the even chunks of every tile, warp 3 the odd ones: one
+      // warp's global loads (four chunks at a time) do not keep up with a
+      // pair's MMAs (measured on GB300).
+      const uint32_t sfull0 = mapa_shared(smem_u32(&sfull[0]), 0);
+      const int par = warp & 1;
+      uint32_t tile_gs = 0;  // the chunk count of the tiles before this one
+      bool alive = true;
+      for (int pt = pair; pt < total && alive; pt += npairs, tile_gs += (uint32_t)num_kb) {
+        int mp, n_tile;
+        coords(pt, mp, n_tile);
+        const int row0 = mp * 2 * kBM + (int)rank * kBM;
+        const int64_t wbase = (int64_t)(n_tile * C::kBN >> 7) * num_kb + (int64_t)(lane < 2 ? lane : 0) * num_kb;
+        constexpr int kLoadBatch = 4;
+        for (int it0 = par; it0 < num_kb && alive; it0 += 2 * kLoadBatch) {
+          uint32_t v[kLoadBatch][4];
+          uint32_t w[kLoadBatch];
+#pragma unroll
+          for (int b = 0; b < kLoadBatch; ++b) {
+            const int kb = it0 + 2 * b;
+            const bool live = kb < num_kb;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int grow = row0 + lane + 32 * j;
+              v[b][j] = (live && grow < a.rows)
+                            ? __ldg(static_cast<const uint32_t*>(scale_word<true>(a.sx, (int64_t)kb * a.rows + grow)))
+                            : 0u;
+            }
+            w[b] = (live && lane < 2) ? __ldg(static_cast<const uint32_t*>(scale_word<true>(a.sw, wbase + kb))) : 0u;
+          }
+#pragma unroll
+          for (int b = 0; b < kLoadBatch; ++b) {
+            const uint32_t kb = (uint32_t)(it0 + 2 * b);
+            if ((int)kb >= num_kb) break;
+            const uint32_t gs = tile_gs + kb;
+            const int q = gs % C::kScaleSlots;
+            const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ((gs / C::kScaleSlots) & 1) ^ 1, abortv, a.err,
+                                               a.timeout_ns, !(a.wait_mode & 1));
+            alive = __all_sync(0xffffffffu, got);
+            if (!alive) break;
+            uint8_t* slot = sf_ring + q * C::kSfSlotBytes;
+            uint32_t wa[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int grow = row0 + lane + 32 * j;
+              const uint32_t byte =
+                  grow < a.rows ? (v[b][j] >> (8 * ((kb * (uint32_t)a.rows + (uint32_t)grow) & 3u))) & 0xFFu : 127u;
+              wa[j] = byte * 0x01010101u;
+            }
+            *reinterpret_cast<uint4*>(slot + 16 * lane) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            const uint32_t wb = ((w[b] >> (8 * (((uint32_t)wbase + kb) & 3u))) & 0xFFu) * 0x01010101u;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t x = __shfl_sync(0xffffffffu, wb, h);
+              *reinterpret_cast<uint4*>(slot + 512 * (1 + h) + 16 * lane) = make_uint4(x, x, x, x);
+            }
+            fence_proxy_async_shared();  // the tensor cores' copy reads these bytes
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(sfull0 + 8u * (uint32_t)q);
+          }
+        }
+      }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 4;
+    const int quad = warp & 3;
+    const int slice = ew >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
+    // the accumulator is handed back on the even CTA's barrier (its own
+    // shared::cluster address for the even CTA)
+    const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+    uint32_t tt = 0;
+    bool ok = true;
+    for (int pt = pair; ok && pt < total; pt += npairs, ++tt) {
+      int mp, n_tile;
+      coords(pt, mp, n_tile);
+      const int row0 = mp * 2 * kBM + (int)rank * kBM;
+      const int n0 = n_tile * C::kBN;
+      const int grow = row0 + r;
+      const bool row_ok = grow < a.rows;
+      uint64_t acc[C::kCols / 2];
+      ok = mbar_wait_bounded(smem_u32(tfull), tt & 1, abortv, a.err, a.timeout_ns, !(a.wait_mode & 2));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // straight into the accumulator registers, 32 columns per round trip
+      tmem_ld_32x32b_x32_pairs(t_lane, *reinterpret_cast<uint64_t(*)[16]>(&acc[0]));
+      tmem_ld_32x32b_x32_pairs(t_lane + 32, *reinterpret_cast<uint64_t(*)[16]>(&acc[16]));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader);
+      bool staged = false;
+      if constexpr (OUT) {
+        const int box_row0 = row0 + quad * 32;
+        if (__all_sync(0xffffffffu, box_row0 < a.rows && !*abortv)) {
+          uint8_t* oslot = out_slots + ew * C::kOutSlotBytes;
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < C::kCols / 8; ++c) {
+            float x[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f32x2_unpack(acc[4 * c + j], x[2 * j], x[2 * j + 1]);
+            *reinterpret_cast<uint4*>(oslot + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                           pack_bf16x2(x[6], x[7]));
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_y, smem_u32(oslot), n0 + slice * C::kCols, box_row0);
+            bulk_commit_group();
+          }
+          staged = true;
+        }
+      }
+      if (!staged && row_ok && !*abortv) {
+        uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
+        const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
+#pragma unroll
+        for (int j = 0; j < C::kCols / 16; ++j) {
+          uint4 h[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) f32x2_unpack(acc[8 * j + 4 * e + q], x[2 * q], x[2 * q + 1]);
+            h[e] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                              pack_bf16x2(x[6], x[7]));
+          }
+          if (wide) {
+            st_global_v8(dst + 2 * j, h[0], h[1]);
+          } else {
+            dst[2 * j] = h[0];
+            dst[2 * j + 1] = h[1];
+          }
+        }
+      }
+    }
+    if constexpr (OUT) {
+      if (lane == 0) bulk_wait_group0();
+      __syncwarp();
+    }
+  }
+  // Teardown.  Every copy either CTA issued completes on the even CTA's stage
+  // barriers: after a wait ran out anywhere, the even CTA's producer lets the
+  // last stages' copies of both CTAs land before shared memory is released.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    const uint32_t peer_abort = ld_dsmem_u32(mapa_shared(smem_u32(abort_flag), 1));
+    if (*abortv || peer_abort) {
+      const uint32_t peer_issued = ld_dsmem_u32(mapa_shared(smem_u32(issued), 1));
+      const uint32_t gmax = *issued > peer_issued ? *issued : peer_issued;
+      for (uint32_t j = gmax > (uint32_t)C::kStages ? gmax - C::kStages : 0; j < gmax; ++j) {
+        if ((int)j == a.fault_skip_kb) continue;
+        mbar_wait_bounded(smem_u32(&full[j % C::kStages]), (j / C::kStages) & 1, nullptr, nullptr, 10000000ull);
+      }
+    }
+  }
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -1275,6 +1646,7 @@ struct Debug {
   int out_stage = 0;              // data-parallel tile stores: 0 choose, 1 through shared memory + TMA, 2 from registers
   int decode = 0;                 // dense rows <= 32: 0 choose, 1 the swapped-operand decode kernel, 2 the 128-row-tile one
   int mx = 0;                     // UE8M0 data-parallel tiles: 0 the block-scaled MMA, 1 the per-chunk promotion
+  int pair = 0;                   // dense data-parallel tiles on tensor-core pairs: 0 choose, 1 always, 2 never
   uint64_t timeout_ns = 2000000000ull;
 };
 Debug g_debug;
@@ -1496,6 +1868,81 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 
+// A dense data-parallel UE8M0 product on tensor-core pairs (clusters of two CTAs).
+template <bool OUT>
+fp8rl_status launch_pair(const void* xq, const void* wq, GemmArgs args, cudaStream_t stream) {
+  using C = PairCfg<OUT>;
+  auto kernel = gemm_pair_mx_kernel<OUT>;
+  static KernelState st[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
+  KernelState& ks = st[dev];
+  const uint64_t ctx = current_context_id();
+  if (!ctx) return FP8RL_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!ks.ready || ks.ctx != ctx) {
+      ks = KernelState{};
+      ks.ctx = ctx;
+      cudaFuncAttributes fa;
+      // setmaxnreg.inc waits until the block has the registers it asks for
+      ks.regs_ok = cudaFuncGetAttributes(&fa, kernel) == cudaSuccess && fa.numRegs >= C::kMinLaunchRegs;
+      ks.attr_ok = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==
+                   cudaSuccess;
+      if (ks.attr_ok) {
+        // pairs resident at once (a persistent grid needs no more)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          n = 0;
+        }
+        ks.cluster_capacity[2] = n;
+      }
+      ks.ready = true;
+    }
+    if (!ks.attr_ok) return FP8RL_ERR_CUDA;
+    if (!ks.regs_ok || ks.cluster_capacity[2] < 1) return FP8RL_ERR_UNSUPPORTED;
+  }
+  CUtensorMap mx, mw, my;
+  if (!make_map(&mx, xq, args.k, args.rows, kBM)) return FP8RL_ERR_CUDA;
+  if (!make_map(&mw, wq, args.k, args.n, 128)) return FP8RL_ERR_CUDA;
+  if (OUT) {
+    if (!make_out_map(&my, args.y, args.n, args.rows)) return FP8RL_ERR_CUDA;
+  } else {
+    my = mx;
+  }
+  const int64_t pairs_total = ((int64_t)args.rows + 2 * kBM - 1) / (2 * kBM) * (args.n / C::kBN);
+  const int64_t clusters = std::min<int64_t>(pairs_total, ks.cluster_capacity[2]);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, my, args) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8RL_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
 fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void* w_scale,
                  const int32_t* d_offsets, int64_t experts, int64_t rows, int64_t n, int64_t k, void* y,
                  fp8rl_scale_fmt fmt, void* stream, void* workspace = nullptr) {
@@ -1562,6 +2009,13 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   const int sms = di.sms;
   // decode-sized M: load only 32 activation rows per stage (deeper weight pipeline)
   const bool short_a = !d_offsets && rows <= 32;
+  // dense UE8M0 products with more than one m-tile and 256-wide weight
+  // blocks: tiles of 256 x 256 on tensor-core pairs (clusters of two CTAs)
+  const bool pair_ok = ue && dbg.mx != 1 && !d_offsets && n % 256 == 0 && rows > kBM && !short_a;
+  if (pair_ok && dbg.pair == 1) {
+    const fp8rl_status st = dbg.out_stage == 1 ? launch_pair<true>(xq, wq, args, cs) : launch_pair<false>(xq, wq, args, cs);
+    if (st != FP8RL_ERR_UNSUPPORTED) return st;
+  }
   if (workspace && !d_offsets && !short_a && dbg.streamk != 1) {
     // stream-K when whole tiles would leave the last wave of SMs mostly idle
     // (measured on GB300: it pays when that wave is at most ~30% full, between
@@ -1816,6 +2270,10 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
     case 11:
       if (value < 0 || value > 1) return FP8RL_ERR_INVALID_ARG;
       g_debug.mx = (int)value;
+      return FP8RL_OK;
+    case 12:
+      if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
+      g_debug.pair = (int)value;
       return FP8RL_OK;
     case 0:
       g_debug = Debug{};

@@ -402,6 +402,10 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *   key 11 UE8M0 GEMMs on whole tiles (data-parallel): 0 the tensor cores
  *          apply the power-of-two scales (block-scaled MMA, default), 1 the
  *          per-chunk fp32 promotion in the epilogue (the fp32-scale path);
+ *   key 12 dense data-parallel GEMMs on tensor-core pairs (256 x 256 tiles
+ *          over clusters of two CTAs): 0 chooses per shape (default), 1
+ *          always where the shape allows (n a multiple of 256, m > 128), 2
+ *          never;
  *   key 0  restore all defaults.
  * Every key but 0 is refused (UNSUPPORTED, nothing changes) unless the
  * process environment holds FP8RL_TEST_HOOKS=1 at the time of the call, so

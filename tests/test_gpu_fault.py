@@ -58,6 +58,35 @@ def test_wait_runs_out_and_is_reported(bn):
     assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)
 
 
+@pytest.mark.parametrize("skip", [0, 1, 5])
+def test_pair_wait_runs_out_and_is_reported(skip):
+    """Tensor-core pairs (UE8M0): a chunk that never arrives stops the even CTA's MMA
+    thread and, through the missing commits, the odd CTA's roles; both leave
+    through the teardown (the even CTA lets both CTAs' copies land), TIMEOUT is
+    reported and the next call on the same context is correct."""
+    m, n, k = 512, 512, 1024
+    fmt = fp8rl.SCALE_UE8M0
+    x = synth.activation_bf16(m, k, 4, "fault-x")
+    w = synth.weight_bf16(n, k, 4, "fault-w")
+    xq, sx = oracle.quant_act_group(synth.bf16_bits(x), fmt)
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w), fmt)
+    dx, dsx, dw, dsw = dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 1)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, skip)
+    fp8rl.gemm(dx, dsx, dw, dsw, fmt)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, -1)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 2_000_000_000)
+    assert fp8rl.fp8rl_sync_status() == 0
+    y = fp8rl.gemm(dx, dsx, dw, dsw, fmt)
+    assert fp8rl.fp8rl_sync_status() == 0
+    ref = oracle.gemm_blockscaled(xq, sx, wq, sw, fmt)
+    got = y.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)
+
+
 def test_grouped_wait_runs_out_and_is_reported():
     counts = [100, 0, 300]
     offsets = synth.routing_with_counts(counts)

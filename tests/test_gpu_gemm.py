@@ -545,3 +545,82 @@ def test_grouped_ue8m0_qwen3_30b_a3b_sampled(which):
     cc = np.concatenate([rng.integers(0, n, 4 * len(seg_rows)), rng.integers(0, n, 4096)]).astype(np.int64)
     ref = oracle.grouped_gemm_blockscaled_at(xq, sx, wq, sw, offsets, rr, cc, fmt)
     within(y[rr, cc], ref)
+
+
+# --------------------------------------------------------------------------- tensor-core pairs
+
+@pytest.fixture(params=[1, 2], ids=["pair", "single"])
+def pair_mode(request):
+    """Dense UE8M0 tiles forced onto tensor-core pairs (1) or kept on single
+    CTAs (2), both on the block-scaled MMA."""
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, request.param)
+    yield request.param
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
+
+
+@pytest.fixture(params=[0, 1], ids=["reg-store", "tma-store"])
+def pair_store(request):
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, 1 if request.param else 2)
+    yield request.param
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, 0)
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 512, 512),     # second pair: rows 256..299 in its even CTA only
+                                   (129, 256, 1024),    # one pair, its odd CTA holds a single row
+                                   (256, 256, 256), (1000, 768, 384), (513, 1280, 640)])
+def test_pair_matches_oracle(m, n, k, pair_mode, pair_store):
+    fmt = fp8rl.SCALE_UE8M0
+    x = synth.activation_bf16(m, k, m + 21, "pair-x")
+    w = synth.weight_bf16(n, k, n + 23, "pair-w")
+    xq, sx, wq, sw = oracle_operands(x, w, fmt)
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    full = torch.full((m + 8, n), 9.0, dtype=torch.bfloat16, device="cuda")
+    fp8rl.gemm(dx, dsx, dw, dsw, fmt, out=full[:m])
+    assert fp8rl.fp8rl_sync_status() == 0
+    assert bool((full[m:] == 9.0).all()), "rows past M were written"
+    within(full[:m].float().cpu().numpy(), oracle.gemm_blockscaled(xq, sx, wq, sw, fmt))
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 512, 512), (257, 256, 768), (640, 768, 256), (2048, 512, 1024)])
+def test_pair_power_of_two_scales_exact(m, n, k, pair_mode, pair_store):
+    """Exact partial sums: bf16_rne of the exact product bit for bit, so every
+    row's and column's scale factor of every K chunk reached the right place
+    in both CTAs of a pair."""
+    xq, sx, wq, sw = exact_operands(m, n, k, m + 2 * n + k)
+    ref_bits = bf16_bits_of(oracle.gemm_blockscaled(xq, sx, wq, sw, fp8rl.SCALE_UE8M0))
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    y = fp8rl.gemm(dx, dsx, dw, dsw, fp8rl.SCALE_UE8M0)
+    assert fp8rl.fp8rl_sync_status() == 0
+    assert np.array_equal(y.view(torch.int16).cpu().numpy(), ref_bits)
+
+
+@pytest.mark.parametrize("name,n,k", synth.QWEN3_8B_GEMMS)
+def test_pair_qwen3_8b_m8192_sampled(name, n, k):
+    """The full-size UE8M0 launches on tensor-core pairs (forced): 4 whole
+    rows and 4096 random outputs against the oracle."""
+    m = 8192
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 1)
+    try:
+        x = synth.activation_bf16(m, k, 16, "pair-big", name)
+        w = synth.weight_bf16(n, k, 17, "pair-big", name)
+        xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_UE8M0)
+        y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_UE8M0)
+    finally:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
+    rr, cc = sample_positions(m, n, 4, 4096, n + k)
+    within(y[rr, cc], oracle.gemm_blockscaled_at(xq, sx, wq, sw, rr, cc, fp8rl.SCALE_UE8M0))
+
+
+def test_pair_is_deterministic():
+    m, n, k = 1024, 1024, 1024
+    x = synth.activation_bf16(m, k, 18, "pair-det")
+    w = synth.weight_bf16(n, k, 19, "pair-det")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_UE8M0)
+    dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 1)
+    try:
+        ys = [fp8rl.gemm(dx, dsx, dw, dsw, fp8rl.SCALE_UE8M0) for _ in range(3)]
+        assert fp8rl.fp8rl_sync_status() == 0
+    finally:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
+    assert all(torch.equal(ys[0].view(torch.int16), y.view(torch.int16)) for y in ys[1:])
