@@ -32,6 +32,7 @@ __all__ = [
     "fp8rl_kv_calibrate", "fp8rl_kv_append", "kv_calibrate", "kv_append",
     "fp8rl_e4m3_encode", "fp8rl_debug_set", "fp8rl_sync_status", "fp8rl_status_string", "fp8rl_version",
     "quant_weight", "quant_weights_batched", "quant_act", "gemm", "grouped_gemm", "HostWeightSync",
+    "CanaryError", "canaries_enabled", "check_canaries",
 ]
 
 SCALE_FP32 = 0
@@ -39,7 +40,7 @@ SCALE_UE8M0 = 1
 
 STATUS = {0: "FP8RL_OK", 1: "FP8RL_ERR_INVALID_ARG", 2: "FP8RL_ERR_SHAPE",
           3: "FP8RL_ERR_ALIGNMENT", 4: "FP8RL_ERR_UNSUPPORTED", 5: "FP8RL_ERR_CUDA",
-          6: "FP8RL_ERR_TIMEOUT"}
+          6: "FP8RL_ERR_TIMEOUT", 7: "FP8RL_ERR_DEVICE_CHECK"}
 
 
 class Fp8rlError(RuntimeError):
@@ -60,21 +61,23 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """``libfp8rl.so``, or ``libfp8rl_debug.so`` when FP8RL_DEBUG=1."""
+    return _build.LIB_DEBUG if _build.debug_requested() else _build.LIB
 
 
 def load_library(build_if_missing: bool = False):
-    """Load ``libfp8rl.so`` (raises if it is missing and building is not asked for)."""
+    """Load the library (raises if it is missing and building is not asked for)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
+        path = library_path()
         if build_if_missing:
             _build.build()
-        if not os.path.exists(_build.LIB):
+        if not os.path.exists(path):
             raise FileNotFoundError(
-                f"{_build.LIB} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
-        lib = ctypes.CDLL(_build.LIB)
+                f"{path} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"`")
+        lib = ctypes.CDLL(path)
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
         st = ctypes.c_int
         sig = {
@@ -290,8 +293,13 @@ def fp8rl_debug_set(key, value) -> None:
 
 
 def fp8rl_sync_status(stream=None) -> int:
-    """Synchronise and return the status code (0 = OK, 6 = a device wait ran out)."""
-    return int(load_library().fp8rl_sync_status(_stream(stream)))
+    """Synchronise and return the status code (0 = OK, 6 = a device wait ran
+    out).  With FP8RL_CANARY=1, also checks the guard zones of every output
+    allocated since the last call (raises CanaryError)."""
+    st = int(load_library().fp8rl_sync_status(_stream(stream)))
+    if canaries_enabled():
+        check_canaries()
+    return st
 
 
 def fp8rl_status_string(status: int) -> str:
@@ -306,6 +314,58 @@ def fp8rl_version() -> int:
 
 def _scale_dtype(fmt):
     return torch.float32 if fmt == SCALE_FP32 else torch.uint8
+
+
+# ---------------------------------------------------------------- canary guards
+# With FP8RL_CANARY=1 in the environment (a debugging aid, off by default),
+# every output the helpers below allocate sits between two guard zones filled
+# with a fixed byte; fp8rl_sync_status() checks every guard zone allocated
+# since its last call and raises CanaryError if a kernel wrote outside its
+# output.  The guarded buffers are kept alive until that check.
+CANARY_BYTE = 0xA5
+_CANARY_PRE = 4096           # bytes before the output (keeps its 256-byte alignment)
+_CANARY_POST = 64 * 1024     # bytes after it (a ragged tile overrun lands here)
+_guards = []
+_guards_lock = threading.Lock()
+
+
+class CanaryError(RuntimeError):
+    pass
+
+
+def canaries_enabled() -> bool:
+    return os.environ.get("FP8RL_CANARY") == "1"
+
+
+def _out(shape, dtype, device):
+    """An output tensor: plain torch.empty, or guarded when FP8RL_CANARY=1."""
+    numel = 1
+    for d in shape:
+        numel *= int(d)
+    if not canaries_enabled() or numel == 0:
+        return torch.empty(shape, dtype=dtype, device=device)
+    nbytes = numel * torch.empty((), dtype=dtype).element_size()
+    buf = torch.full((_CANARY_PRE + nbytes + _CANARY_POST,), CANARY_BYTE, dtype=torch.uint8, device=device)
+    with _guards_lock:
+        _guards.append((buf, nbytes))
+    return buf[_CANARY_PRE:_CANARY_PRE + nbytes].view(dtype).view(tuple(shape))
+
+
+def check_canaries() -> int:
+    """Check (and forget) every guarded output allocated so far; returns how
+    many were checked, raises CanaryError naming the first damaged one."""
+    with _guards_lock:
+        guards = list(_guards)
+        _guards.clear()
+    for buf, nbytes in guards:
+        pre = buf[:_CANARY_PRE]
+        post = buf[_CANARY_PRE + nbytes:]
+        if not bool((pre == CANARY_BYTE).all()) or not bool((post == CANARY_BYTE).all()):
+            bad_pre = int((pre != CANARY_BYTE).sum())
+            bad_post = int((post != CANARY_BYTE).sum())
+            raise CanaryError(f"a kernel wrote outside an output of {nbytes} bytes: "
+                              f"{bad_pre} guard bytes before it and {bad_post} after it changed")
+    return len(guards)
 
 
 def _check_cuda(*tensors):
@@ -334,8 +394,8 @@ def quant_weight(w: torch.Tensor, fmt=SCALE_FP32, stream=None):
     _check_cuda(w)
     _check_bf16_2d(w, "w")
     n, k = w.shape
-    q = torch.empty((n, k), dtype=torch.uint8, device=w.device)
-    s = torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=_scale_dtype(fmt), device=w.device)
+    q = _out((n, k), torch.uint8, w.device)
+    s = _out(((n + 127) // 128, (k + 127) // 128), _scale_dtype(fmt), w.device)
     fp8rl_quant_weight_blockwise(w, n, k, w.stride(0), q, k, s, fmt, stream)
     return q, s
 
@@ -358,8 +418,8 @@ def quant_weights_batched(weights, fmt=SCALE_FP32, stream=None, outputs=None):
         for w in weights:
             _check_bf16_2d(w, "w")
             n, k = w.shape
-            outputs.append((torch.empty((n, k), dtype=torch.uint8, device=w.device),
-                            torch.empty(((n + 127) // 128, (k + 127) // 128),
+            outputs.append((_out((n, k), torch.uint8, w.device),
+                            _out(((n + 127) // 128, (k + 127) // 128),
                                         dtype=_scale_dtype(fmt), device=w.device)))
     descs = weight_descs([(w, q, s) for w, (q, s) in zip(weights, outputs)])
     fp8rl_quant_weight_blockwise_batched(descs, len(weights), fmt, stream)
@@ -371,8 +431,8 @@ def quant_act(x: torch.Tensor, fmt=SCALE_FP32, stream=None):
     _check_cuda(x)
     _check_bf16_2d(x, "x")
     m, k = x.shape
-    q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
-    s = torch.empty(((k + 127) // 128, m), dtype=_scale_dtype(fmt), device=x.device)
+    q = _out((m, k), torch.uint8, x.device)
+    s = _out(((k + 127) // 128, m), _scale_dtype(fmt), x.device)
     fp8rl_quant_act_group(x, m, k, x.stride(0), q, k, s, fmt, stream)
     return q, s
 
@@ -392,7 +452,7 @@ def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None, worksp
     m, k = xq.shape
     n = wq.shape[0]
     if out is None:
-        out = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device)
+        out = _out((m, n), torch.bfloat16, xq.device)
     if workspace is None:
         fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, out, m, n, k, fmt, stream)
     else:
@@ -407,7 +467,7 @@ def grouped_gemm(xq, x_scale, wq, w_scale, d_offsets, fmt=SCALE_FP32, out=None, 
     rows, k = xq.shape
     e, n, _ = wq.shape
     if out is None:
-        out = torch.empty((rows, n), dtype=torch.bfloat16, device=xq.device)
+        out = _out((rows, n), torch.bfloat16, xq.device)
     fp8rl_grouped_gemm_blockscaled(xq, x_scale, wq, w_scale, d_offsets, e, rows, n, k, out, fmt,
                                    stream)
     return out
@@ -432,8 +492,8 @@ def quant_gate_up_interleaved(gate: torch.Tensor, up: torch.Tensor, fmt=SCALE_FP
         raise ValueError("weights need unit column stride")
     experts = g2.shape[0]
     if out is None:
-        q = torch.empty((experts, 2 * inter, k), dtype=torch.uint8, device=gate.device)
-        sc = torch.empty((experts, 2 * inter // 128, k // 128), dtype=_scale_dtype(fmt), device=gate.device)
+        q = _out((experts, 2 * inter, k), torch.uint8, gate.device)
+        sc = _out((experts, 2 * inter // 128, k // 128), _scale_dtype(fmt), gate.device)
     else:
         q, sc = (t.view(experts, *t.shape[-2:]) for t in out)
     items = []
@@ -454,8 +514,8 @@ def gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, fmt=SCALE_FP32, 
     m, k = xq.shape
     inter = wq_gate_up.shape[0] // 2
     if out is None:
-        out = (torch.empty((m, inter), dtype=torch.uint8, device=xq.device),
-               torch.empty((inter // 128, m), dtype=_scale_dtype(fmt), device=xq.device))
+        out = (_out((m, inter), torch.uint8, xq.device),
+               _out((inter // 128, m), _scale_dtype(fmt), xq.device))
     fp8rl_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, m, inter, k, out[0], out[1], fmt, stream)
     return out
 
@@ -468,8 +528,8 @@ def grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offset
     e, n2, _ = wq_gate_up.shape
     inter = n2 // 2
     if out is None:
-        out = (torch.empty((rows, inter), dtype=torch.uint8, device=xq.device),
-               torch.empty((inter // 128, rows), dtype=_scale_dtype(fmt), device=xq.device))
+        out = (_out((rows, inter), torch.uint8, xq.device),
+               _out((inter // 128, rows), _scale_dtype(fmt), xq.device))
     fp8rl_grouped_gemm_swiglu_quant(xq, x_scale, wq_gate_up, w_scale_gate_up, d_offsets, e, rows, inter, k,
                                     out[0], out[1], fmt, stream)
     return out
@@ -480,7 +540,7 @@ def kv_calibrate(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor | None = None
     _check_cuda(k, v, q, out)
     for name, t in (("k", k), ("v", v)) + ((("q", q),) if q is not None else ()):
         _check_bf16_2d(t, name)
-    scales = out if out is not None else torch.zeros(3, dtype=torch.float32, device=k.device)
+    scales = out if out is not None else _out((3,), torch.float32, k.device).zero_()
     tokens, dim = k.shape
     fp8rl_kv_calibrate(k, v, q, tokens, dim, k.stride(0), v.stride(0), 0 if q is None else q.shape[1],
                        0 if q is None else q.stride(0), scales, stream)
@@ -509,9 +569,9 @@ def moe_plan(topk: torch.Tensor, experts: int, workspace: torch.Tensor | None = 
     need = fp8rl_moe_plan_workspace_size(tokens, k, experts)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    offsets = torch.empty(experts + 1, dtype=torch.int32, device=dev)
-    row_of_pair = torch.empty(tokens * k, dtype=torch.int32, device=dev)
-    token_of_row = torch.empty(tokens * k, dtype=torch.int32, device=dev)
+    offsets = _out((experts + 1,), torch.int32, dev)
+    row_of_pair = _out((tokens * k,), torch.int32, dev)
+    token_of_row = _out((tokens * k,), torch.int32, dev)
     fp8rl_moe_plan(topk, tokens, k, experts, offsets, row_of_pair, token_of_row, workspace, workspace.numel(),
                    stream)
     return offsets, row_of_pair, token_of_row
@@ -529,9 +589,9 @@ def moe_dispatch_quant(x: torch.Tensor, row_of_pair: torch.Tensor, topk: int, fm
     if rows != tokens * topk:
         raise ValueError("row_of_pair must have tokens * topk entries")
     if out is None:
-        q = torch.empty((rows, k), dtype=torch.uint8, device=x.device)
+        q = _out((rows, k), torch.uint8, x.device)
         sdt = torch.float32 if fmt == SCALE_FP32 else torch.uint8
-        s = torch.empty(((k + 127) // 128, rows), dtype=sdt, device=x.device)
+        s = _out(((k + 127) // 128, rows), sdt, x.device)
     else:
         q, s = out
     fp8rl_moe_dispatch_quant(x, tokens, k, x.stride(0), row_of_pair, topk, rows, q, q.stride(0), s, fmt, stream)
@@ -546,7 +606,7 @@ def moe_combine(y: torch.Tensor, row_of_pair: torch.Tensor, gate: torch.Tensor, 
         raise ValueError("gate must be a contiguous fp32 [tokens, k] tensor")
     tokens, k = gate.shape
     n = y.shape[1]
-    o = out if out is not None else torch.empty((tokens, n), dtype=torch.bfloat16, device=y.device)
+    o = out if out is not None else _out((tokens, n), torch.bfloat16, y.device)
     fp8rl_moe_combine(y, y.shape[0], n, y.stride(0), row_of_pair, gate, tokens, k, o, o.stride(0), stream)
     return o
 
@@ -565,8 +625,8 @@ def tis_weights(lp_train: torch.Tensor, lp_rollout: torch.Tensor, mask: torch.Te
     need = fp8rl_tis_workspace_size(n)
     if workspace is None:
         workspace = torch.zeros(max(need, 32), dtype=torch.uint8, device=dev)  # header zeroed once
-    w, kl = out if out is not None else (torch.empty(n, dtype=torch.float32, device=dev),
-                                         torch.empty(3, dtype=torch.float64, device=dev))
+    w, kl = out if out is not None else (_out((n,), torch.float32, dev),
+                                         _out((3,), torch.float64, dev))
     fp8rl_tis_weights(lp_train, lp_rollout, mask, n, clip, w, kl, workspace, workspace.numel(), stream)
     return w, kl
 

@@ -18,7 +18,20 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8rl.so")
+# debug flavour (FP8RL_DEBUG=1): device-side checks of every store index,
+# failures reported as FP8RL_ERR_DEVICE_CHECK instead of a store
+LIB_DEBUG = os.path.join(PKG, "libfp8rl_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
+
+
+def debug_requested() -> bool:
+    return os.environ.get("FP8RL_DEBUG") == "1"
+
+
+def lib_path(debug: bool | None = None) -> str:
+    """The library of the requested flavour (default: FP8RL_DEBUG=1 selects
+    the debug build)."""
+    return LIB_DEBUG if (debug_requested() if debug is None else debug) else LIB
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -44,26 +57,31 @@ def _deps():
         [os.path.join(INCLUDE, "fp8rl.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(debug: bool = False) -> bool:
+    lib = lib_path(debug)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of ``libfp8rl.so``."""
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, debug: bool | None = None) -> str:
+    """Compile (if stale) and return the path of ``libfp8rl.so`` (or, for the
+    debug flavour, ``libfp8rl_debug.so``)."""
+    debug = debug_requested() if debug is None else debug
+    lib = lib_path(debug)
+    if not force and up_to_date(debug):
+        return lib
     home = cuda_home()
     nvcc = os.path.join(home, "bin", "nvcc")
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(build_dir, exist_ok=True)
     procs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *(["-DFP8RL_DEBUG"] if debug else []), "-I", INCLUDE, "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -78,15 +96,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         msg = "\n".join(f"== {s}\n{t}" for s, t in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
             f"-L{home}/lib64", "-Xlinker", f"-rpath,{home}/lib64"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug=True if "--debug" in sys.argv else None))

@@ -91,6 +91,7 @@ extern "C" FP8RL_API fp8rl_status fp8rl_sync_status(void* stream) {
   if (cudaMemcpyToSymbolAsync(g_error_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, cs) != cudaSuccess)
     return FP8RL_ERR_CUDA;
   if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8RL_ERR_CUDA;
+  if (v & kErrDeviceCheck) return FP8RL_ERR_DEVICE_CHECK;
   if (v & kErrTimeout) return FP8RL_ERR_TIMEOUT;
   return FP8RL_OK;
 }
@@ -104,6 +105,7 @@ extern "C" FP8RL_API const char* fp8rl_status_string(fp8rl_status s) {
     case FP8RL_ERR_UNSUPPORTED: return "FP8RL_ERR_UNSUPPORTED";
     case FP8RL_ERR_CUDA: return "FP8RL_ERR_CUDA";
     case FP8RL_ERR_TIMEOUT: return "FP8RL_ERR_TIMEOUT";
+    case FP8RL_ERR_DEVICE_CHECK: return "FP8RL_ERR_DEVICE_CHECK";
   }
   return "FP8RL_ERR_UNKNOWN";
 }

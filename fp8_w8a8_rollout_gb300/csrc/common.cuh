@@ -168,6 +168,24 @@ __device__ __forceinline__ uint32_t absmax_u4(uint32_t acc, uint4 v) {
 
 // bits recorded in a device error word
 constexpr uint32_t kErrTimeout = 1u;
+constexpr uint32_t kErrDeviceCheck = 2u;
+
+// Debug builds (compiled with FP8RL_DEBUG): the kernels check the index of
+// each global store against its buffer before storing; a failed check sets
+// kErrDeviceCheck in the device error word and the store is skipped (no
+// trap).  Release builds compile the checks away.
+__device__ __forceinline__ bool dcheck(bool ok, uint32_t* err) {
+#ifdef FP8RL_DEBUG
+  if (!ok && err) atomicOr(err, kErrDeviceCheck);
+  return ok;
+#else
+  (void)err;
+  return true;
+#endif
+}
+
+// the device error word of the current device and context (api.cu)
+uint32_t* device_error_word();
 
 // A process-unique id of the CUDA context current on this thread, making the
 // runtime's primary context of the current device current first if there is

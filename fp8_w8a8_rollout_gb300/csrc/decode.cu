@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       __nv_bfloat16* dst = a.y + (int64_t)nblk * kDecRows + row;
 #pragma unroll
       for (int m = 0; m < NT; ++m)  // a constant bound keeps acc in registers
-        if (m < a.rows) dst[(int64_t)m * a.n] = __float2bfloat16_rn(acc[m]);
+        if (m < a.rows && dcheck(nblk * kDecRows + row < a.n, a.err)) dst[(int64_t)m * a.n] = __float2bfloat16_rn(acc[m]);
     }
   } else {
     if (warp >= 2) {
@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           sum += x;
         }
         const int m = i / kDecRows, nr = i - m * kDecRows;
-        a.y[(int64_t)m * a.n + (int64_t)nblk * kDecRows + nr] = __float2bfloat16_rn(sum);
+        if (dcheck(m < a.rows && nblk * kDecRows + nr < a.n, a.err))
+          a.y[(int64_t)m * a.n + (int64_t)nblk * kDecRows + nr] = __float2bfloat16_rn(sum);
       }
     }
     cluster_sync();  // no CTA leaves while its partial may still be read

@@ -42,7 +42,6 @@
 
 namespace fp8rl {
 
-uint32_t* device_error_word();  // api.cu
 void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* status);  // static_scratch.cu
 // decode.cu: dense products with at most 32 rows, operands swapped (UNSUPPORTED: use this file's kernel)
 fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale, void* y,
@@ -1002,7 +1001,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
         // once any wait has run out
         if (*abortv) break;
         const float amax = fmaxf(fmaxf(red[r], red[kBM + r]), fmaxf(red[2 * kBM + r], red[3 * kBM + r]));
-        if (ok && row_ok) {
+        if (ok && row_ok &&
+            dcheck(grow < a.rows && n_tile * 128 + slice * 32 + 32 <= a.n / 2 && n_tile < a.n / 256, a.err)) {
           uint32_t w[8];
           if (UE8M0) {
             const int e = scale_ue8m0_exponent(amax);
@@ -1096,7 +1096,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
               streamk_fold(srow, a.ws_part + (int64_t)(ew * (C::kCols / 4) * 32 + lane) * 4, (int64_t)kBM * BN, a.ws_flag,
                            *shared_epoch, (uint32_t)((t - sch.dp_tiles + 1) * num_kb), (uint32_t)sk_iters,
                            C::kCols / 4, ok && row_ok, abortv, a.err, a.timeout_ns);
-          if (folded && ok && row_ok && !*abortv) {
+          if (folded && ok && row_ok && !*abortv &&
+              dcheck(grow < a.rows && n0 + slice * C::kCols + C::kCols <= a.n, a.err)) {
             uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
             const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
 #pragma unroll 1
@@ -1128,7 +1129,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           // go out one by one below.
           const int box_row0 = tr.row0 + quad * 32;
           const bool box_ok = a.offsets == nullptr ? box_row0 < a.rows : box_row0 + 32 <= tr.seg_end;
-          if (__all_sync(0xffffffffu, ok && box_ok && !*abortv)) {
+          if (__all_sync(0xffffffffu, ok && box_ok && !*abortv &&
+                                     dcheck(box_row0 < a.rows && n0 + slice * C::kCols + C::kCols <= a.n, a.err))) {
             uint8_t* slot = out_slots + ew * C::kOutSlotBytes;
             if (lane == 0) bulk_wait_group_read0();  // this slot's previous box has been read
             __syncwarp();
@@ -1150,7 +1152,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
             staged = true;
           }
         }
-        if (!staged && ok && row_ok && !*abortv) {
+        if (!staged && ok && row_ok && !*abortv &&
+            dcheck(grow < a.rows && n0 + slice * C::kCols + C::kCols <= a.n, a.err)) {
           // the row segment leaves as full 32-byte sectors (one 256-bit store
           // per 16 columns) when the output allows it
           uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
@@ -1229,6 +1232,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
               x[0] += u[q].x; x[1] += u[q].y; x[2] += u[q].z; x[3] += u[q].w;
               x[4] += w[q].x; x[5] += w[q].y; x[6] += w[q].z; x[7] += w[q].w;
             }
+          if (dcheck(tr.row0 + r < a.rows && n0 + ch * 8 + 8 <= a.n, a.err))
           *reinterpret_cast<uint4*>(a.y + (int64_t)(tr.row0 + r) * a.n + n0 + ch * 8) =
               make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                          pack_bf16x2(x[6], x[7]));
@@ -1543,7 +1547,8 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
       bool staged = false;
       if constexpr (OUT) {
         const int box_row0 = row0 + quad * 32;
-        if (__all_sync(0xffffffffu, box_row0 < a.rows && !*abortv)) {
+        if (__all_sync(0xffffffffu, box_row0 < a.rows && !*abortv &&
+                                   dcheck(n0 + slice * C::kCols + C::kCols <= a.n, a.err))) {
           uint8_t* oslot = out_slots + ew * C::kOutSlotBytes;
           if (lane == 0) bulk_wait_group_read0();
           __syncwarp();
@@ -1565,7 +1570,7 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
           staged = true;
         }
       }
-      if (!staged && row_ok && !*abortv) {
+      if (!staged && row_ok && !*abortv && dcheck(grow < a.rows && n0 + slice * C::kCols + C::kCols <= a.n, a.err)) {
         uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
         const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
 #pragma unroll

@@ -40,6 +40,7 @@ struct WBatch {
   int32_t count;
   int32_t pad;
   int64_t total_blocks;
+  uint32_t* err;  // device error word (debug builds' store checks)
   WDesc d[MAXD];
 };
 
@@ -107,23 +108,26 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
 #pragma unroll
       for (int w = 1; w < 8; ++w) m8 = max(m8, red[parity][w]);
       const float amax = __uint_as_float(m8 << 16);
+      const bool scale_in = dcheck(local < (D.n + kBlock - 1) / kBlock * D.kbs, batch.err);
       if (UE8M0) {
         const int e = scale_ue8m0_exponent(amax);
         const float f = exp2_neg(e);
-        if (t == 0) static_cast<uint8_t*>(D.scale)[local] = (uint8_t)(e + 127);
+        if (t == 0 && scale_in) static_cast<uint8_t*>(D.scale)[local] = (uint8_t)(e + 127);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint2 a = quant8_mul(v[i][0], f), b = quant8_mul(v[i][1], f);
-          st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
+          if (dcheck(r0 + rs + 32 * i < D.n && c0 + cc + 16 <= D.k, batch.err))
+            st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
         }
       } else {
         const float s = scale_fp32(amax);
         const float rcp = __frcp_rn(s);
-        if (t == 0) static_cast<float*>(D.scale)[local] = s;
+        if (t == 0 && scale_in) static_cast<float*>(D.scale)[local] = s;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint2 a = quant8_div(v[i][0], s, rcp), b = quant8_div(v[i][1], s, rcp);
-          st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
+          if (dcheck(r0 + rs + 32 * i < D.n && c0 + cc + 16 <= D.k, batch.err))
+            st_stream(D.q + (r0 + rs + 32 * i) * D.ldq + c0 + cc, make_uint4(a.x, a.y, b.x, b.y));
         }
       }
     } else {
@@ -142,17 +146,18 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const __grid_constant
       const float amax = __uint_as_float(m8 << 16);
       int e = 0;
       float s = 1.0f, f = 1.0f;
+      const bool scale_in = dcheck(local < (D.n + kBlock - 1) / kBlock * D.kbs, batch.err);
       if (UE8M0) {
         e = scale_ue8m0_exponent(amax);
         f = exp2_neg(e);
-        if (t == 0) static_cast<uint8_t*>(D.scale)[local] = (uint8_t)(e + 127);
+        if (t == 0 && scale_in) static_cast<uint8_t*>(D.scale)[local] = (uint8_t)(e + 127);
       } else {
         s = scale_fp32(amax);
-        if (t == 0) static_cast<float*>(D.scale)[local] = s;
+        if (t == 0 && scale_in) static_cast<float*>(D.scale)[local] = s;
       }
       for (int idx = t; idx < kBlock * kBlock; idx += 256) {
         const int r = idx >> 7, c = idx & 127;
-        if (r < rows && c < cols) {
+        if (r < rows && c < cols && dcheck(r0 + r < D.n && c0 + c < D.k, batch.err)) {
           const float x = __uint_as_float((uint32_t)D.w[(r0 + r) * D.ldw + c0 + c] << 16);
           const float y = UE8M0 ? x * f : __fdiv_rn(x, s);
           D.q[(r0 + r) * D.ldq + c0 + c] = (uint8_t)(e4m3x2(y, 0.0f) & 0xFFu);
@@ -217,7 +222,7 @@ __device__ __forceinline__ void act_load(const uint16_t* __restrict__ x, int64_t
 template <bool UE8M0>
 __device__ __forceinline__ void act_quant_store(const uint4 (&v)[4], const ActTask& a, int32_t m, int64_t k,
                                                 uint8_t* __restrict__ q, int64_t ldq, void* __restrict__ scale,
-                                                int part) {
+                                                int part, uint32_t* err) {
   uint32_t acc = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc = absmax_u4(acc, v[j]);
@@ -225,6 +230,7 @@ __device__ __forceinline__ void act_quant_store(const uint4 (&v)[4], const ActTa
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
   am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
   if (!a.live) return;
+  if (!dcheck(a.row < m && a.c0 < k, err)) return;
   const float amax = __uint_as_float(am << 16);
   const int64_t sidx = (a.c0 / kBlock) * m + a.row;
   uint2 codes[4];
@@ -246,8 +252,9 @@ __device__ __forceinline__ void act_quant_store(const uint4 (&v)[4], const ActTa
   for (int j = 0; j < 4; ++j) {
     const int piece = part + 4 * j;
     if (a.full) {
-      asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst + piece * 8), "r"(codes[j].x), "r"(codes[j].y)
-                   : "memory");
+      if (dcheck(a.c0 + piece * 8 + 8 <= k, err))
+        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst + piece * 8), "r"(codes[j].x), "r"(codes[j].y)
+                     : "memory");
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e)
@@ -261,7 +268,7 @@ template <bool UE8M0>
 __global__ void __launch_bounds__(256, 3) quant_act_kernel(const uint16_t* __restrict__ x, int32_t m,
                                                         int64_t k, int64_t ldx, uint8_t* __restrict__ q,
                                                         int64_t ldq, void* __restrict__ scale,
-                                                        int32_t groups, int vec) {
+                                                        int32_t groups, int vec, uint32_t* err) {
   const int lane = threadIdx.x & 31, sub = lane >> 2, part = lane & 3;
   const int32_t warp = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int32_t warp_count = gridDim.x * 8;
@@ -279,12 +286,12 @@ __global__ void __launch_bounds__(256, 3) quant_act_kernel(const uint16_t* __res
       tb = act_task(t1, rblocks, m, k, vec, sub);
       act_load(x, ldx, k, tb, part, vb);
     }
-    act_quant_store<UE8M0>(va, ta, m, k, q, ldq, scale, part);
+    act_quant_store<UE8M0>(va, ta, m, k, q, ldq, scale, part, err);
     if (t2 < tasks) {
       ta = act_task(t2, rblocks, m, k, vec, sub);
       act_load(x, ldx, k, ta, part, va);
     }
-    if (t1 < tasks) act_quant_store<UE8M0>(vb, tb, m, k, q, ldq, scale, part);
+    if (t1 < tasks) act_quant_store<UE8M0>(vb, tb, m, k, q, ldq, scale, part, err);
   }
 }
 
@@ -386,6 +393,8 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise(const void* w_bf1
   fp8rl_status st = check_weight(s, fmt);
   if (st != FP8RL_OK || n == 0 || k == 0) return st;
   WBatch<1> b{};
+  b.err = device_error_word();
+  if (!b.err) return FP8RL_ERR_CUDA;
   b.count = 1;
   b.d[0] = make_desc(s, 0);
   b.total_blocks = ((n + kBlock - 1) / kBlock) * b.d[0].kbs;
@@ -405,6 +414,7 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise_batched(const fp8
   // heap-allocated host staging: the parameter block is ~18 KB
   std::vector<WBatch<kMaxBatch>> staged(1);
   WBatch<kMaxBatch>& b = staged[0];
+  b.err = nullptr;  // looked up before the first launch (a batch of empty matrices touches no device)
   int32_t i = 0;
   while (i < count) {
     b.count = 0;
@@ -417,6 +427,7 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_weight_blockwise_batched(const fp8
       ++b.count;
     }
     if (b.count == 0) continue;
+    if (!b.err && !(b.err = device_error_word())) return FP8RL_ERR_CUDA;
     fp8rl_status st = launch_weight(b, fmt, static_cast<cudaStream_t>(stream));
     if (st != FP8RL_OK) return st;
   }
@@ -443,15 +454,17 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int6
   const int64_t per_warp = (warp_tasks + resident_warps - 1) / resident_warps;
   const int64_t grid = std::max<int64_t>(1, (warp_tasks + 8 * per_warp - 1) / (8 * per_warp));
   const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
+  uint32_t* err = device_error_word();
+  if (!err) return FP8RL_ERR_CUDA;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (fmt == FP8RL_SCALE_UE8M0)
     quant_act_kernel<true><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), (int32_t)m,
                                                            k, ldx, static_cast<uint8_t*>(q_e4m3), ldq,
-                                                           x_scale, (int32_t)groups, vec);
+                                                           x_scale, (int32_t)groups, vec, err);
   else
     quant_act_kernel<false><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), (int32_t)m,
                                                             k, ldx, static_cast<uint8_t*>(q_e4m3), ldq,
-                                                            x_scale, (int32_t)groups, vec);
+                                                            x_scale, (int32_t)groups, vec, err);
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 

@@ -65,7 +65,9 @@ typedef enum {
     FP8RL_ERR_ALIGNMENT = 3,   /* pointer or leading dimension misaligned    */
     FP8RL_ERR_UNSUPPORTED = 4, /* device is not sm_103 / feature unavailable */
     FP8RL_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed       */
-    FP8RL_ERR_TIMEOUT = 6      /* a device-side bounded wait ran out         */
+    FP8RL_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out         */
+    FP8RL_ERR_DEVICE_CHECK = 7 /* a device-side bounds check failed (builds
+                                  with FP8RL_DEBUG only; the store was skipped) */
 } fp8rl_status;
 
 typedef enum {

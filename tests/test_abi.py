@@ -376,3 +376,18 @@ def test_host_sync_rejects_bad_arguments_on_host(lib):
     d[0].ldw, d[0].w_bf16 = 256, None
     assert f(d, 1, 0, staging, need, 2, None) == 1           # null pointer
     assert f(d, 0, 0, staging, need, 2, None) == 0           # count 0: no-op
+
+
+def test_debug_flavour_builds_with_the_same_entry_points(lib):
+    """The FP8RL_DEBUG build (device-side store checks) compiles and exports
+    every declared entry point, like the release library."""
+    path = _build.build(debug=True)
+    assert path == _build.LIB_DEBUG and os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(fp8rl_\w+)", out))
+    assert set(declared_entry_points()) <= exported
+
+
+def test_device_check_status_is_named(lib):
+    assert lib.fp8rl_status_string(7) == b"FP8RL_ERR_DEVICE_CHECK"
+    assert fp8rl.STATUS[7] == "FP8RL_ERR_DEVICE_CHECK"
