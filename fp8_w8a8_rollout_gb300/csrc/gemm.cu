@@ -72,17 +72,19 @@ struct Cfg {
   static constexpr int kOutSlotBytes = 32 * kCols * 2;  // one warp's 32 x 64 bf16 box
   static constexpr int kOutBytes = OUT ? kEpiWarps * kOutSlotBytes : 0;
   // chunk-scale ring filled by the scale-loader warp: per K chunk the tile's
-  // 128 activation scales and its BN/128 weight scales, as fp32; with MX the
-  // scale-factor blocks the tensor cores read instead (one 512-byte block of
-  // 32 rows x 16 bytes for A, one per 128 columns for B: row r's byte at
-  // 16 (r mod 32) + 4 (r / 32) + j for the four 32-wide K blocks j of the
-  // chunk), copied into TMEM by the MMA thread
-  static constexpr int kScaleSlots = MX ? 8 : 16;
+  // 128 activation scales and its BN/128 weight scales, as fp32.  MX needs no
+  // ring in shared memory: the epilogue warps write the scale factors of each
+  // group of four consecutive K chunks into one of kScaleSlots TMEM slots
+  static constexpr int kScaleSlots = 16;
   static constexpr int kScaleSlotFloats = kBM + 4;
-  static constexpr int kMxSfSlotBytes = 512 * (1 + BN / 128);
-  static constexpr int kScaleRingBytes = MX ? kScaleSlots * kMxSfSlotBytes : kScaleSlots * kScaleSlotFloats * 4;
+  static constexpr int kScaleRingBytes = MX ? 0 : kScaleSlots * kScaleSlotFloats * 4;
   // TMEM columns: MX keeps its accumulators in [0, 256) and the scale factors
-  // of each ring slot in 16 columns from 256 on (4 for A, 4 per 128 of B)
+  // of each slot in 16 columns from 256 on: row r of A's factor in lane r,
+  // column r / 32; column n of B's in lane n mod 32 of every lane quadrant,
+  // column 4 + n / 32.  The MMA picks a byte of each 32-bit cell (one per
+  // 32-wide K block); our scales are per 128-wide chunk, so all four K blocks
+  // of a chunk use the same byte and the cell's four bytes hold four
+  // consecutive chunks: chunk c reads byte c mod 4 of slot (c / 4) mod slots
   static constexpr int kMxSfCol0 = 256;
   static constexpr int kMxSfColsPerSlot = 16;
   static_assert(!MX || kMxSfCol0 + kScaleSlots * kMxSfColsPerSlot <= 512, "MX scale factors fit in TMEM");
@@ -124,6 +126,11 @@ struct Cfg {
   static constexpr int kRoleRegs = 56;
   static constexpr int kRoleRegsStreamK = 64;  // its schedule state needs a little more
   static constexpr int kEpiRegs = 104;
+  // MX: the epilogue keeps no running sums; the role warps get more
+  // (measured: below 80 they spill a little, 72 with 96 epilogue registers
+  // still fits the launch's allocation)
+  static constexpr int kRoleRegsMx = 80;
+  static constexpr int kEpiRegsMx = 96;
   static constexpr int kMinLaunchRegs =
       (128 * (kRoleRegsStreamK > kRoleRegs ? kRoleRegsStreamK : kRoleRegs) + kEpiWarps * 32 * kEpiRegs + kThreads - 1) /
       kThreads;
@@ -371,7 +378,6 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   int* shared_m_tiles = abort_flag + 1;
   uint32_t* shared_epoch = reinterpret_cast<uint32_t*>(shared_m_tiles + 1);
   float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
-  uint8_t* sf_ring = reinterpret_cast<uint8_t*>(scale_ring);            // MX: the scale-factor blocks
   float* row_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scale_ring) + C::kScaleRingBytes);  // EPI 1
   uint8_t* out_slots = base_ptr + C::kOutOffset;                         // OUT only
 
@@ -403,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     mbar_init(smem_u32(published), C::kEpiWarps);
     for (int q = 0; q < C::kScaleSlots; ++q) {
-      mbar_init(smem_u32(&sfull[q]), 1);
+      mbar_init(smem_u32(&sfull[q]), MX ? 4 : 1);  // MX: one epilogue warp per lane quadrant
       mbar_init(smem_u32(&sempty[q]), MX ? 1 : C::kEpiWarps);
     }
     *abort_flag = 0;
@@ -483,8 +489,9 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     // better with the stream-K budget (measured on GB300: 8192 x 24576 x 4096
     // 788 -> 756 us); with register stores the extra registers cost 4-7%
     if (C::kSplitRegs)
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((STREAMK || MX || (UE8M0 && OUT)) ? C::kRoleRegsStreamK
-                                                                                             : C::kRoleRegs));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(MX ? C::kRoleRegsMx
+                                                             : (STREAMK || (UE8M0 && OUT)) ? C::kRoleRegsStreamK
+                                                                                           : C::kRoleRegs));
     if constexpr (!STREAMK) {
       // Data-parallel and split-K: plain loops over whole tiles (or the
       // cluster's one tile).  These loops are latency-critical; measured on
@@ -538,15 +545,16 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
         } else if (warp == 1) {
           // ---------------------------------------------------------- MMA issuer
           if (lane == 0 && MX) {
-            // One accumulator per tile: per K chunk, the chunk's scale-factor
-            // blocks are copied from the loader's ring slot into that slot's
-            // TMEM columns, then four block-scaled MMAs (32-wide K blocks j =
-            // 0..3, scale-factor byte j) accumulate into it.  The ring slot is
-            // reused only after the commit that follows its MMAs, so its TMEM
-            // columns are never overwritten while an MMA may still read them.
+            // One accumulator per tile: per K chunk, four block-scaled MMAs
+            // (32-wide K blocks) accumulate into it, all reading the chunk's
+            // scale-factor byte c mod 4 of its group's TMEM slot.  The MMA
+            // thread waits for a slot once per group of four chunks (once the
+            // epilogue warps have written it) and releases it after the
+            // group's last chunk; a slot is rewritten only after that commit.
             const int my_tiles = (total_tiles - first_tile + tile_stride - 1) / tile_stride;
+            const uint32_t total_chunks = (uint32_t)my_tiles * (uint32_t)nloc;
             uint32_t g = 0;   // chunks consumed (stage ring position)
-            uint32_t gs = 0;  // scale-factor slots consumed
+            uint32_t gs = 0;  // chunks consumed (scale-factor position)
             bool alive = true;
             for (int tt = 0; tt < my_tiles && alive; ++tt) {
               const int buf = tt % C::kAccBufs;
@@ -559,27 +567,25 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
               const uint32_t d = tmem + buf * BN;
               for (int it = 0; it < nloc; ++it, ++g, ++gs) {
                 const int s = g % C::kStages;
-                const int q = gs % C::kScaleSlots;
+                const uint32_t grp = gs >> 2, j = gs & 3u;
+                const int q = grp % C::kScaleSlots;
                 if (!mbar_wait_bounded(smem_u32(&full[s]), (g / C::kStages) & 1, abortv, a.err, a.timeout_ns,
                                        !(a.wait_mode & 1)) ||
-                    !mbar_wait_bounded(smem_u32(&sfull[q]), (gs / C::kScaleSlots) & 1, abortv, a.err, a.timeout_ns,
-                                       !(a.wait_mode & 1))) {
+                    (j == 0 && !mbar_wait_bounded(smem_u32(&sfull[q]), (grp / C::kScaleSlots) & 1, abortv, a.err,
+                                                  a.timeout_ns, !(a.wait_mode & 1)))) {
                   alive = false;
                   break;
                 }
                 tc_fence_after();
                 const uint32_t sf_t = tmem + C::kMxSfCol0 + q * C::kMxSfColsPerSlot;
-                const uint32_t sf_s = smem_u32(sf_ring) + q * C::kMxSfSlotBytes;
-                tmem_cp_32x128b_x4(sf_t, rows16_desc(sf_s));
-#pragma unroll
-                for (int h = 0; h < BN / 128; ++h) tmem_cp_32x128b_x4(sf_t + 4 + 4 * h, rows16_desc(sf_s + 512 * (1 + h)));
                 const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+                const uint32_t idesc = idesc_mx_e4m3_ue8m0(kBM, BN, 0, 0) | (j << 4) | (j << 29);
 #pragma unroll
                 for (int k = 0; k < kBK / kUmmaK; ++k)
-                  mma_mx_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK),
-                              idesc_mx_e4m3_ue8m0(kBM, BN, k, k), sf_t, sf_t + 4, (it > 0 || k > 0) ? 1u : 0u);
+                  mma_mx_e4m3(d, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                              sf_t, sf_t + 4, (it > 0 || k > 0) ? 1u : 0u);
                 mma_commit(smem_u32(&empty[s]));
-                mma_commit(smem_u32(&sempty[q]));
+                if (j == 3 || gs + 1 == total_chunks) mma_commit(smem_u32(&sempty[q]));
               }
               if (alive) mma_commit(smem_u32(&tfull[buf]));
             }
@@ -630,7 +636,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
             }
           }
           __syncwarp();
-        } else if (warp == 2) {
+        } else if (warp == 2 && !MX) {
           // ---------------------------------------------------------- scale loader
           // Runs up to kScaleSlots K chunks ahead of the epilogue, so the latency
           // of these small loads never paces the pipeline.  Lane l loads the
@@ -674,36 +680,11 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
                                                    !(a.wait_mode & 1));
                 alive = __all_sync(0xffffffffu, got);
                 if (!alive) break;
-                if constexpr (MX) {
-                  // the chunk's scale-factor blocks: lane l writes the 16-byte
-                  // row l of each block, its four words the bytes of rows (A) or
-                  // columns (B) l, l+32, l+64, l+96, each byte repeated for the
-                  // chunk's four 32-wide K blocks (rows past the segment: 2^0)
-                  uint8_t* slot = sf_ring + q * C::kMxSfSlotBytes;
-                  uint32_t wa[4];
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const uint32_t byte = tr.row0 + lane + 32 * j < tr.seg_end
-                                              ? (v[b][j] >> (8 * ((uint32_t)vi[b][j] & 3u))) & 0xFFu
-                                              : 127u;
-                    wa[j] = byte * 0x01010101u;
-                  }
-                  *reinterpret_cast<uint4*>(slot + 16 * lane) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-                  const uint32_t wb = ((w[b] >> (8 * ((uint32_t)wi[b] & 3u))) & 0xFFu) * 0x01010101u;
-#pragma unroll
-                  for (int h = 0; h < BN / 128; ++h) {
-                    const uint32_t x = __shfl_sync(0xffffffffu, wb, h);
-                    *reinterpret_cast<uint4*>(slot + 512 * (1 + h) + 16 * lane) = make_uint4(x, x, x, x);
-                  }
-                  fence_proxy_async_shared();  // the tensor cores' copy reads these bytes
-                } else {
-                  float* slot = scale_ring + q * C::kScaleSlotFloats;
-#pragma unroll
-                  for (int j = 0; j < 4; ++j)
-                    slot[lane + 32 * j] =
-                        tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
-                  if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
-                }
+                float* slot = scale_ring + q * C::kScaleSlotFloats;
+                #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  slot[lane + 32 * j] = tr.row0 + lane + 32 * j < tr.seg_end ? scale_value<UE8M0>(v[b][j], vi[b][j]) : 0.0f;
+                if (lane < BN / 128) slot[kBM + lane] = scale_value<UE8M0>(w[b], wi[b]);
                 __syncwarp();  // orders the lanes' stores before lane 0's release
                 if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
                 ++gs;
@@ -876,7 +857,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
       }
     }
   } else {
-    if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
+    if (C::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(MX ? C::kEpiRegsMx : C::kEpiRegs));
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 4;
     const int quad = warp & 3;   // TMEM lanes this warp may read: 32*quad .. +31
@@ -889,6 +870,70 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     uint32_t g = 0;   // chunk groups folded so far (TMEM ring position)
     uint32_t gs = 0;  // chunks whose scales were taken (scale ring position)
     bool ok = true;
+    // MX: the epilogue warps write the scale factors of this CTA's K chunks
+    // (numbered across its tiles) into TMEM, four consecutive chunks per slot
+    // (one per byte of each cell); group G is written by the four warps of
+    // slice G mod (kEpiWarps / 4), one per lane quadrant, up to kMxLead
+    // chunks ahead of the tile being accumulated.  A warp writes every
+    // kEpiWarps / 4-th group, so its scale loads have that many groups of
+    // MMAs to arrive in.
+    constexpr int kMxStep = C::kEpiWarps / 4;
+    constexpr uint32_t kMxLead = 4 * (C::kScaleSlots / 2);  // chunks of lead into the next tile
+    const uint32_t mx_total = MX ? (uint32_t)((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) *
+                                       (uint32_t)num_kb
+                                 : 0u;
+    uint32_t mx_next = (uint32_t)slice;  // this warp's next group to write
+    uint32_t mx_tile = 0;                // tiles of this CTA drained so far
+    // write group mx_next's scale factors into its TMEM slot once the MMAs
+    // that last read the slot have completed; false when a wait ran out
+    auto mx_write = [&]() -> bool {
+      const uint32_t grp = mx_next;
+      mx_next += kMxStep;
+      uint32_t xw = 0u, b0 = 0u, b1 = 0u;  // cell bytes: byte j for chunk 4 grp + j
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t c = 4u * grp + (uint32_t)j;
+        uint32_t xb = 127u, wb0 = 127u, wb1 = 127u;
+        if (c < mx_total) {
+          const int tseq = (int)(c / (uint32_t)num_kb), kbc = (int)(c - (uint32_t)tseq * (uint32_t)num_kb);
+          int mi, nt;
+          tile_coords((int)blockIdx.x + tseq * (int)gridDim.x, mi, nt);
+          const TileRows st = tile_rows(a, mi, lane);  // warp-collective
+          const int srow = st.row0 + quad * 32 + lane;
+          if (srow < st.seg_end) {
+            const int64_t xi = (int64_t)kbc * a.rows + srow;
+            xb = (__ldg(static_cast<const uint32_t*>(scale_word<true>(a.sx, xi))) >> (8 * ((uint32_t)xi & 3u))) &
+                 0xFFu;
+          }
+          const int64_t wi = ((int64_t)st.expert * (a.n / 128) + (nt * BN >> 7)) * num_kb + kbc;
+          wb0 = (__ldg(static_cast<const uint32_t*>(scale_word<true>(a.sw, wi))) >> (8 * ((uint32_t)wi & 3u))) &
+                0xFFu;
+          wb1 = wb0;
+          if (BN == 256)
+            wb1 = (__ldg(static_cast<const uint32_t*>(scale_word<true>(a.sw, wi + num_kb))) >>
+                   (8 * ((uint32_t)(wi + num_kb) & 3u))) &
+                  0xFFu;
+        }
+        xw |= xb << (8 * j);
+        b0 |= wb0 << (8 * j);
+        b1 |= wb1 << (8 * j);
+      }
+      const int q = grp % C::kScaleSlots;
+      bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ((grp / C::kScaleSlots) & 1) ^ 1, abortv, a.err,
+                                   a.timeout_ns, !(a.wait_mode & 2));
+      got = __all_sync(0xffffffffu, got);
+      if (!got) return false;
+      tc_fence_after();
+      const uint32_t sf = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kMxSfCol0 + q * C::kMxSfColsPerSlot;
+      tmem_st_32x32b_x1(sf + quad, xw);
+      const uint32_t bw[8] = {b0, b0, b0, b0, b1, b1, b1, b1};
+      tmem_st_32x32b_x8(sf + 4, bw);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sfull[q]));
+      return true;
+    };
     Schedule<MODE> sch = sched0;
     int t, lo, hi;
     while (ok && sch.next(t, lo, hi)) {
@@ -908,6 +953,11 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
       for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
       const int sw_lane = nb - (n0 >> 7);  // which of the tile's weight scales
       if constexpr (MX) {
+        // scale factors up to kScaleSlots chunks into the next tile, so the
+        // MMA thread can start it while this tile drains and stores
+        const uint32_t lim = min(mx_total, (mx_tile + 1) * (uint32_t)num_kb + kMxLead);
+        while (ok && 4u * mx_next < lim) ok = mx_write();
+        ++mx_tile;
         // the whole tile's scaled sum is in one accumulator: read this
         // thread's 64 columns and hand the buffer back to the MMA thread
         const int buf = g % C::kAccBufs;
@@ -1260,15 +1310,15 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
 // is what bounds the one-CTA tile).  The even CTA's MMA thread issues
 // block-scaled M = 256 MMAs that read both CTAs' shared memory and accumulate
 // the whole tile in both CTAs' TMEM (rows 0..127 in the even CTA, 128..255 in
-// the odd one); each CTA's scale loader fills its own scale-factor blocks
-// (its rows' activation scales and the tile's two weight scales), which the
-// MMA thread copies into each CTA's TMEM with one cta_group::2 copy.  Each
-// CTA's epilogue reads and stores its own 128 rows once per tile.
+// the odd one); each CTA's epilogue warps write that CTA's scale factors (its
+// rows' activation scales and the tile's two weight scales) into its own
+// TMEM a few chunks ahead, as in the one-CTA block-scaled kernel, and read
+// and store its own 128 rows once per tile.
 //   Both producers' copies complete on the even CTA's stage barrier, whose
-// arrival the even producer makes with both CTAs' byte count; both loaders
-// arrive on the even CTA's scale barrier; the MMA thread's commits arrive in
-// both CTAs; both epilogues hand the accumulator back on the even CTA's
-// barrier.  (With fp32 scales the chunk accumulators would have to cross the
+// arrival the even producer makes with both CTAs' byte count; both CTAs'
+// scale-factor writers arrive on the even CTA's scale barrier; the MMA
+// thread's commits arrive in both CTAs; both epilogues hand the accumulator
+// back on the even CTA's barrier.  (With fp32 scales the chunk accumulators would have to cross the
 // pair every K chunk: measured at half the one-CTA kernel's speed on GB300,
 // so fp32 keeps one CTA per tile.)
 template <bool OUT>
@@ -1282,12 +1332,10 @@ struct PairCfg {
   static constexpr int kThreads = 128 + kEpiWarps * 32;
   static constexpr int kOutSlotBytes = 32 * kCols * 2;
   static constexpr int kOutBytes = OUT ? kEpiWarps * kOutSlotBytes : 0;
-  // scale-factor blocks per K chunk: A (this CTA's 128 rows) and B (the
-  // tile's 256 columns), 512 bytes per 128 rows or columns, the layout of the
-  // one-CTA block-scaled kernel
-  static constexpr int kScaleSlots = 8;
-  static constexpr int kSfSlotBytes = 512 * 3;
-  static constexpr int kScaleRingBytes = kScaleSlots * kSfSlotBytes;
+  // scale-factor slots in TMEM, four K chunks each (the one-CTA block-scaled
+  // kernel's layout); no ring in shared memory
+  static constexpr int kScaleSlots = 16;
+  static constexpr int kScaleRingBytes = 0;
   static constexpr int kSfCol0 = 256;            // TMEM: the accumulator in [0, 256)
   static constexpr int kSfColsPerSlot = 16;
   static_assert(kSfCol0 + kScaleSlots * kSfColsPerSlot <= 512, "scale factors fit in TMEM");
@@ -1331,7 +1379,6 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::kScaleSlots);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint32_t* issued = reinterpret_cast<uint32_t*>(abort_flag + 1);  // chunks this CTA's producer issued
-  uint8_t* sf_ring = base_ptr + C::kStages * C::kStageBytes + C::kBookBytes;
   uint8_t* out_slots = base_ptr + C::kOutOffset;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1351,8 +1398,8 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
     mbar_init(smem_u32(tempty), 2 * C::kEpiWarps);  // both CTAs' epilogue warps
     mbar_init(smem_u32(drain), 1);
     for (int q = 0; q < C::kScaleSlots; ++q) {
-      mbar_init(smem_u32(&sfull[q]), 2);   // both CTAs' scale loaders
-      mbar_init(smem_u32(&sempty[q]), 1);  // the MMA thread's commit after the copies
+      mbar_init(smem_u32(&sfull[q]), 8);   // both CTAs' writers, one warp per lane quadrant
+      mbar_init(smem_u32(&sempty[q]), 1);  // the MMA thread's commit after the chunk's MMAs
     }
     *abort_flag = 0;
     *issued = 0;
@@ -1406,6 +1453,7 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer (even CTA)
       if (lane == 0 && rank == 0) {
+        const uint32_t total_chunks = (uint32_t)((total - pair + npairs - 1) / npairs) * (uint32_t)num_kb;
         uint32_t g = 0, gs = 0, tt = 0;
         bool alive = true;
         for (int pt = pair; pt < total && alive; pt += npairs, ++tt) {
@@ -1415,27 +1463,25 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
           }
           for (int kb = 0; kb < num_kb; ++kb, ++g, ++gs) {
             const int s = g % C::kStages;
-            const int q = gs % C::kScaleSlots;
+            const uint32_t grp = gs >> 2, j = gs & 3u;
+            const int q = grp % C::kScaleSlots;
             if (!mbar_wait_bounded(smem_u32(&full[s]), (g / C::kStages) & 1, abortv, a.err, a.timeout_ns,
                                    !(a.wait_mode & 1)) ||
-                !mbar_wait_bounded_cluster(smem_u32(&sfull[q]), (gs / C::kScaleSlots) & 1, abortv, a.err,
-                                           a.timeout_ns)) {
+                (j == 0 && !mbar_wait_bounded_cluster(smem_u32(&sfull[q]), (grp / C::kScaleSlots) & 1, abortv,
+                                                      a.err, a.timeout_ns))) {
               alive = false;
               break;
             }
             tc_fence_after();
             const uint32_t sf_t = tmem + C::kSfCol0 + q * C::kSfColsPerSlot;
-            const uint32_t sf_s = smem_u32(sf_ring) + q * C::kSfSlotBytes;
-#pragma unroll
-            for (int h = 0; h < 3; ++h) tmem_cp_32x128b_x4_pair(sf_t + 4 * h, rows16_desc(sf_s + 512 * h));
             const uint32_t a0 = sA + s * C::kABytes, b0 = sB + s * C::kBBytes;
+            const uint32_t idesc = idesc_mx_e4m3_ue8m0(2 * kBM, C::kBN, 0, 0) | (j << 4) | (j << 29);
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
-              mma_mx_e4m3_pair(tmem, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK),
-                               idesc_mx_e4m3_ue8m0(2 * kBM, C::kBN, k, k), sf_t, sf_t + 4,
-                               (kb > 0 || k > 0) ? 1u : 0u);
+              mma_mx_e4m3_pair(tmem, sw128_kmajor_desc(a0 + k * kUmmaK), sw128_kmajor_desc(b0 + k * kUmmaK), idesc,
+                               sf_t, sf_t + 4, (kb > 0 || k > 0) ? 1u : 0u);
             mma_commit_pair(smem_u32(&empty[s]));
-            mma_commit_pair(smem_u32(&sempty[q]));
+            if (j == 3 || gs + 1 == total_chunks) mma_commit_pair(smem_u32(&sempty[q]));
           }
           if (alive) mma_commit_pair(smem_u32(tfull));
         }
@@ -1446,72 +1492,6 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
         }
       }
       __syncwarp();
-    } else {
-      // ------------------------------------------------------------ scale loaders (warps 2, 3; both CTAs)
-      // per K chunk this CTA's scale-factor blocks: lane l writes the 16-byte
-      // row l of each block (the bytes of rows or columns l, l+32, l+64, l+96,
-      // each repeated for the chunk's four 32-wide K blocks; rows past M: 2^0).
-      // Warp 2 takes the even chunks of every tile, warp 3 the odd ones: one
-      // warp's global loads (four chunks at a time) do not keep up with a
-      // pair's MMAs (measured on GB300).
-      const uint32_t sfull0 = mapa_shared(smem_u32(&sfull[0]), 0);
-      const int par = warp & 1;
-      uint32_t tile_gs = 0;  // the chunk count of the tiles before this one
-      bool alive = true;
-      for (int pt = pair; pt < total && alive; pt += npairs, tile_gs += (uint32_t)num_kb) {
-        int mp, n_tile;
-        coords(pt, mp, n_tile);
-        const int row0 = mp * 2 * kBM + (int)rank * kBM;
-        const int64_t wbase = (int64_t)(n_tile * C::kBN >> 7) * num_kb + (int64_t)(lane < 2 ? lane : 0) * num_kb;
-        constexpr int kLoadBatch = 4;
-        for (int it0 = par; it0 < num_kb && alive; it0 += 2 * kLoadBatch) {
-          uint32_t v[kLoadBatch][4];
-          uint32_t w[kLoadBatch];
-#pragma unroll
-          for (int b = 0; b < kLoadBatch; ++b) {
-            const int kb = it0 + 2 * b;
-            const bool live = kb < num_kb;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int grow = row0 + lane + 32 * j;
-              v[b][j] = (live && grow < a.rows)
-                            ? __ldg(static_cast<const uint32_t*>(scale_word<true>(a.sx, (int64_t)kb * a.rows + grow)))
-                            : 0u;
-            }
-            w[b] = (live && lane < 2) ? __ldg(static_cast<const uint32_t*>(scale_word<true>(a.sw, wbase + kb))) : 0u;
-          }
-#pragma unroll
-          for (int b = 0; b < kLoadBatch; ++b) {
-            const uint32_t kb = (uint32_t)(it0 + 2 * b);
-            if ((int)kb >= num_kb) break;
-            const uint32_t gs = tile_gs + kb;
-            const int q = gs % C::kScaleSlots;
-            const bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ((gs / C::kScaleSlots) & 1) ^ 1, abortv, a.err,
-                                               a.timeout_ns, !(a.wait_mode & 1));
-            alive = __all_sync(0xffffffffu, got);
-            if (!alive) break;
-            uint8_t* slot = sf_ring + q * C::kSfSlotBytes;
-            uint32_t wa[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int grow = row0 + lane + 32 * j;
-              const uint32_t byte =
-                  grow < a.rows ? (v[b][j] >> (8 * ((kb * (uint32_t)a.rows + (uint32_t)grow) & 3u))) & 0xFFu : 127u;
-              wa[j] = byte * 0x01010101u;
-            }
-            *reinterpret_cast<uint4*>(slot + 16 * lane) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-            const uint32_t wb = ((w[b] >> (8 * (((uint32_t)wbase + kb) & 3u))) & 0xFFu) * 0x01010101u;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t x = __shfl_sync(0xffffffffu, wb, h);
-              *reinterpret_cast<uint4*>(slot + 512 * (1 + h) + 16 * lane) = make_uint4(x, x, x, x);
-            }
-            fence_proxy_async_shared();  // the tensor cores' copy reads these bytes
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(sfull0 + 8u * (uint32_t)q);
-          }
-        }
-      }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kEpiRegs));
@@ -1521,12 +1501,67 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
     const int slice = ew >> 2;
     const int r = quad * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + slice * C::kCols;
-    // the accumulator is handed back on the even CTA's barrier (its own
-    // shared::cluster address for the even CTA)
+    // the accumulator is handed back, and the scale factors announced, on the
+    // even CTA's barriers (its own shared::cluster addresses for the even CTA)
     const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+    const uint32_t sfull_leader = mapa_shared(smem_u32(&sfull[0]), 0);
+    // Scale factors of the pair's K chunks (numbered across its tiles), four
+    // consecutive chunks per TMEM slot (one per byte of each cell): group G
+    // is written into this CTA's TMEM by the four warps of slice G mod 4, one
+    // per lane quadrant, up to 32 chunks ahead of the tile being accumulated.
+    const uint32_t sf_total = (uint32_t)((total - pair + npairs - 1) / npairs) * (uint32_t)num_kb;
+    uint32_t sf_next = (uint32_t)slice;  // this warp's next group
+    auto sf_write = [&]() -> bool {
+      const uint32_t grp = sf_next;
+      sf_next += 4;
+      uint32_t xw = 0u, b0 = 0u, b1 = 0u;  // cell bytes: byte j for chunk 4 grp + j
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t c = 4u * grp + (uint32_t)j;
+        uint32_t xb = 127u, wb0 = 127u, wb1 = 127u;
+        if (c < sf_total) {
+          const int tseq = (int)(c / (uint32_t)num_kb), kbc = (int)(c - (uint32_t)tseq * (uint32_t)num_kb);
+          int mp, nt;
+          coords(pair + tseq * npairs, mp, nt);
+          const int srow = mp * 2 * kBM + (int)rank * kBM + quad * 32 + lane;
+          if (srow < a.rows) {
+            const int64_t xi = (int64_t)kbc * a.rows + srow;
+            xb = (__ldg(static_cast<const uint32_t*>(scale_word<true>(a.sx, xi))) >> (8 * ((uint32_t)xi & 3u))) &
+                 0xFFu;
+          }
+          const int64_t wi = (int64_t)(nt * C::kBN >> 7) * num_kb + kbc;
+          wb0 = (__ldg(static_cast<const uint32_t*>(scale_word<true>(a.sw, wi))) >> (8 * ((uint32_t)wi & 3u))) &
+                0xFFu;
+          wb1 = (__ldg(static_cast<const uint32_t*>(scale_word<true>(a.sw, wi + num_kb))) >>
+                 (8 * ((uint32_t)(wi + num_kb) & 3u))) &
+                0xFFu;
+        }
+        xw |= xb << (8 * j);
+        b0 |= wb0 << (8 * j);
+        b1 |= wb1 << (8 * j);
+      }
+      const int q = grp % C::kScaleSlots;
+      bool got = mbar_wait_bounded(smem_u32(&sempty[q]), ((grp / C::kScaleSlots) & 1) ^ 1, abortv, a.err,
+                                   a.timeout_ns, !(a.wait_mode & 2));
+      got = __all_sync(0xffffffffu, got);
+      if (!got) return false;
+      tc_fence_after();
+      const uint32_t sf = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kSfCol0 + q * C::kSfColsPerSlot;
+      tmem_st_32x32b_x1(sf + quad, xw);
+      const uint32_t bw[8] = {b0, b0, b0, b0, b1, b1, b1, b1};
+      tmem_st_32x32b_x8(sf + 4, bw);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(sfull_leader + 8u * (uint32_t)q);
+      return true;
+    };
     uint32_t tt = 0;
     bool ok = true;
     for (int pt = pair; ok && pt < total; pt += npairs, ++tt) {
+      const uint32_t lim = min(sf_total, (tt + 1) * (uint32_t)num_kb + 4u * (C::kScaleSlots / 2));
+      while (ok && 4u * sf_next < lim) ok = sf_write();
+      if (!ok) break;
       int mp, n_tile;
       coords(pt, mp, n_tile);
       const int row0 = mp * 2 * kBM + (int)rank * kBM;
@@ -2018,7 +2053,7 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   // blocks: tiles of 256 x 256 on tensor-core pairs (clusters of two CTAs)
   const bool pair_ok = ue && dbg.mx != 1 && !d_offsets && n % 256 == 0 && rows > kBM && !short_a;
   if (pair_ok && dbg.pair == 1) {
-    const fp8rl_status st = dbg.out_stage == 1 ? launch_pair<true>(xq, wq, args, cs) : launch_pair<false>(xq, wq, args, cs);
+    const fp8rl_status st = launch_pair<false>(xq, wq, args, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
   if (workspace && !d_offsets && !short_a && dbg.streamk != 1) {
@@ -2068,15 +2103,16 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   const bool staged = dbg.out_stage == 1 || (dbg.out_stage != 2 && k <= 4096);
   if (ue && dbg.mx != 1) {
     // UE8M0: the tensor cores apply the power-of-two scales themselves
-    // (block-scaled MMA), one accumulator per tile
+    // (block-scaled MMA), one accumulator per tile; the tile stores stay in
+    // the epilogue's registers (measured on GB300: 8192 x 24576 x 4096 0.559
+    // vs 0.604 ms through shared memory, every shape faster), since the
+    // store does not hold up the next tile's MMAs
     if (bn == 256) {
       const fp8rl_status st =
-          staged ? launch<256, kBM, true, kDataParallel, 0, true, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-                 : launch<256, kBM, true, kDataParallel, 0, false, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+          launch<256, kBM, true, kDataParallel, 0, false, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
       if (st != FP8RL_ERR_UNSUPPORTED) return st;
     }
-    return staged ? launch<128, kBM, true, kDataParallel, 0, true, true>(xq, wq, experts, mt_bound, sms, args, 1, cs)
-                  : launch<128, kBM, true, kDataParallel, 0, false, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
+    return launch<128, kBM, true, kDataParallel, 0, false, true>(xq, wq, experts, mt_bound, sms, args, 1, cs);
   }
   if (bn == 256) {
     const fp8rl_status st =
