@@ -558,17 +558,10 @@ def pair_mode(request):
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
 
 
-@pytest.fixture(params=[0, 1], ids=["reg-store", "tma-store"])
-def pair_store(request):
-    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, 1 if request.param else 2)
-    yield request.param
-    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_OUT_STAGE, 0)
-
-
 @pytest.mark.parametrize("m,n,k", [(300, 512, 512),     # second pair: rows 256..299 in its even CTA only
                                    (129, 256, 1024),    # one pair, its odd CTA holds a single row
                                    (256, 256, 256), (1000, 768, 384), (513, 1280, 640)])
-def test_pair_matches_oracle(m, n, k, pair_mode, pair_store):
+def test_pair_matches_oracle(m, n, k, pair_mode):
     fmt = fp8rl.SCALE_UE8M0
     x = synth.activation_bf16(m, k, m + 21, "pair-x")
     w = synth.weight_bf16(n, k, n + 23, "pair-w")
@@ -582,7 +575,7 @@ def test_pair_matches_oracle(m, n, k, pair_mode, pair_store):
 
 
 @pytest.mark.parametrize("m,n,k", [(300, 512, 512), (257, 256, 768), (640, 768, 256), (2048, 512, 1024)])
-def test_pair_power_of_two_scales_exact(m, n, k, pair_mode, pair_store):
+def test_pair_power_of_two_scales_exact(m, n, k, pair_mode):
     """Exact partial sums: bf16_rne of the exact product bit for bit, so every
     row's and column's scale factor of every K chunk reached the right place
     in both CTAs of a pair."""
