@@ -80,7 +80,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="all",
-                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused,kv,moe_layer,tis "
+                    help="comma list of extra sections: model,moe_sync,sweep,ue8m0,fused,kv,moe_layer,tis,decode "
                          "(or all/none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -101,6 +101,8 @@ def parse():
                     help="with --case: dense tiles on tensor-core pairs, 0 chosen, 1 always, 2 never")
     ap.add_argument("--mx", type=int, default=0,
                     help="with --case: UE8M0 whole tiles, 0 block-scaled MMA, 1 per-chunk promotion")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="with --case: launch the activation quantiser and decode GEMM without overlap")
     return ap.parse_args()
 
 
@@ -767,6 +769,61 @@ def section_tis(torch, synth, fp8rl, dev, seed, peaks):
             "launches": 1, "l2": "flushed before each call"}
 
 
+def section_decode_layer(torch, synth, fp8rl, dev, seed, peaks, m=16, layers=8):
+    """The linear path of a rollout decode step at m tokens: per layer the four
+    Qwen3-8B projections (qkv, o_proj, gate-up, down), each behind the 1x128
+    quantisation of its input (the attention and SwiGLU outputs that feed
+    o_proj and down are synthetic stand-ins of their shapes), over `layers`
+    layers' weights (1.5 GB of codes, far beyond L2), captured once in a CUDA
+    graph and replayed.  Timed with overlapped launches (the default: each
+    kernel starts while the one before it finishes) and without them."""
+    gemms = synth.QWEN3_8B_GEMMS
+    W = []
+    for l in range(layers):
+        per = []
+        for name, n, k in gemms:
+            w = synth.weight_bf16(n, k, seed, "decode", l, name, device=dev)
+            wq, sw = fp8rl.quant_weight(w)
+            del w
+            per.append((n, k, wq, sw))
+        W.append(per)
+    ks = sorted({k for _, _, k in gemms})
+    ns = sorted({n for _, n, _ in gemms})
+    xs = {k: synth.activation_bf16(m, k, seed, "decode-x", k, device=dev) for k in ks}
+    qs = {k: torch.empty((m, k), dtype=torch.uint8, device=dev) for k in ks}
+    ss = {k: torch.empty((k // 128, m), dtype=torch.float32, device=dev) for k in ks}
+    ys = {n: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for n in ns}
+
+    def run():
+        for per in W:
+            for n, k, wq, sw in per:
+                fp8rl.fp8rl_quant_act_group(xs[k], m, k, k, qs[k], k, ss[k], 0)
+                fp8rl.fp8rl_gemm_blockscaled(qs[k], ss[k], wq, sw, ys[n], m, n, k, 0)
+
+    per_layer = sum(gemm_bytes(m, n, k) + aq_bytes(m, k) for _, n, k in gemms)
+    launches = 2 * len(gemms)
+    res = {"m": m, "layers": layers, "bytes_per_layer": per_layer, "launches_per_layer": launches,
+           "l2": "weights of all layers (%.2f GB) far larger than L2" % (layers * per_layer / 1e9)}
+    hooks = os.environ.get("FP8RL_TEST_HOOKS")
+    for label, off in (("overlapped", 0), ("serialised", 1)):
+        if off:
+            os.environ["FP8RL_TEST_HOOKS"] = "1"
+            fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 1)
+        try:
+            ms = time_graph(torch, run, 1) / layers
+        finally:
+            if off:
+                fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 0)
+                if hooks is None:
+                    os.environ.pop("FP8RL_TEST_HOOKS", None)
+                else:
+                    os.environ["FP8RL_TEST_HOOKS"] = hooks
+        gbs = per_layer / ms / 1e6
+        res[label] = {"us_per_layer": ms * 1e3, "us_per_launch": ms * 1e3 / launches, "gbs": gbs,
+                      "frac_hbm": gbs / peaks["hbm_gbs"]}
+    return res
+
+
 def section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, name, n, k, m, fmt):
     w = synth.weight_bf16(n, k, seed, "ue8m0", name, device=dev)
     wq, sw = fp8rl.quant_weight(w, fmt)
@@ -869,7 +926,7 @@ def main_ours(args):
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
     wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
-        {"model", "moe_sync", "sweep", "ue8m0", "fused", "kv", "moe_layer", "tis"} if args.sections == "all"
+        {"model", "moe_sync", "sweep", "ue8m0", "fused", "kv", "moe_layer", "tis", "decode"} if args.sections == "all"
         else set())
     del inp
     torch.cuda.empty_cache()
@@ -889,6 +946,8 @@ def main_ours(args):
         sections["moe_dispatch_combine_qwen3_30b_a3b"] = section_moe_layer(torch, synth, fp8rl, dev, seed, peaks)
     if "tis" in wanted:
         sections["tis_rollout_512x16384"] = section_tis(torch, synth, fp8rl, dev, seed, peaks)
+    if "decode" in wanted and have_gemm:
+        sections["decode_layer_qwen3_8b_m16"] = section_decode_layer(torch, synth, fp8rl, dev, seed, peaks)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_sample(synth)
@@ -985,6 +1044,8 @@ def main_case(args):
         fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, args.mx)
     if args.pair:
         fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, args.pair)
+    if args.no_overlap:
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 1)
     parts = args.case.split(":")
     kind = parts[0]
     peaks = load_peaks()
@@ -1077,7 +1138,8 @@ def main_case(args):
     ms = time_loop(torch, fn, max(1, args.steps), args.warmup)
     assert fp8rl.fp8rl_sync_status() == 0
     out = {"case": args.case, "ms": ms, "bn": args.bn or "auto", "wait_mode": args.wait_mode,
-           "l2_prefetch": args.l2_prefetch, "streamk": args.streamk, "out_stage": args.out_stage, "mx": args.mx, "pair": args.pair}
+           "l2_prefetch": args.l2_prefetch, "streamk": args.streamk, "out_stage": args.out_stage, "mx": args.mx, "pair": args.pair,
+           "overlap": not args.no_overlap}
     if args.graph:
         out["ms_graph"] = time_graph(torch, fn, max(10, args.steps))
     if "flops" in work:

@@ -285,7 +285,7 @@ def fp8rl_e4m3_encode(d_in, n, d_out, stream=None) -> None:
 
 DEBUG_RESET, DEBUG_GEMM_BN, DEBUG_FAULT_SKIP_KB, DEBUG_TIMEOUT_NS = 0, 1, 2, 3
 DEBUG_WAIT_MODE, DEBUG_L2_PREFETCH, DEBUG_SPLITS, DEBUG_STREAMK, DEBUG_STREAMK_GRID = 4, 5, 6, 7, 8
-DEBUG_OUT_STAGE, DEBUG_DECODE, DEBUG_MX, DEBUG_PAIR = 9, 10, 11, 12
+DEBUG_OUT_STAGE, DEBUG_DECODE, DEBUG_MX, DEBUG_PAIR, DEBUG_PDL = 9, 10, 11, 12, 13
 
 
 def fp8rl_debug_set(key, value) -> None:

@@ -195,4 +195,9 @@ uint32_t* device_error_word();
 // cached from the old one would point nowhere).  api.cu.
 uint64_t current_context_id();
 
+// Whether the activation quantiser and the decode GEMM are launched with
+// programmatic stream serialisation (on unless test hook 13 turns it off;
+// gemm.cu)
+bool pdl_enabled();
+
 }  // namespace fp8rl

@@ -140,13 +140,32 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The next kernel of the stream may start now (when launched with
+  // programmatic stream serialisation: it waits for this grid's completion
+  // before it reads anything this grid writes).
+  grid_dep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&tmap_w);
       prefetch_tensormap(&tmap_x);
-      int it = 0;
+      // No kernel of this library that lets a dependent start early writes
+      // weights (the weight quantiser does not), so the first stages' weight
+      // tiles are requested before the wait for the earlier kernels of the
+      // stream; the activations, their outputs, are loaded after it.
+      const int pre = nloc < kDecStages ? nloc : kDecStages;
+      for (int j = 0; j < pre; ++j) {
+        if (kb_lo + j == a.fault_skip_kb) continue;
+        const uint32_t fb = smem_u32(&full[j]);
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        tma_load_2d(sW + j * kDecWBytes, &tmap_w, (kb_lo + j) * 128, nblk * kDecRows, fb);
+      }
+      grid_dep_wait();
+      for (int j = 0; j < pre; ++j)
+        if (kb_lo + j != a.fault_skip_kb)
+          tma_load_2d(sX + j * C::kXBytes, &tmap_x, (kb_lo + j) * 128, 0, smem_u32(&full[j]));
+      int it = pre;
       for (; it < nloc; ++it) {
         const int s = it % kDecStages;
         const uint32_t ph = (it / kDecStages) & 1;
@@ -164,10 +183,13 @@ __global__ void __launch_bounds__(kDecThreads, 2)
           if (kb_lo + j != a.fault_skip_kb)
             mbar_wait_bounded(smem_u32(&full[j % kDecStages]), (j / kDecStages) & 1, nullptr, nullptr, 10000000ull);
       }
+    } else {
+      grid_dep_wait();
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    grid_dep_wait();
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kDecRows, NT);
       for (int it = 0; it < nloc; ++it) {
@@ -203,6 +225,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   for (int m = 0; m < NT; ++m) acc[m] = 0.0f;
   bool ok = true;
   if (warp >= 2) {
+    grid_dep_wait();  // the activation scales come from earlier kernels
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     for (int it = 0; it < nloc; ++it) {
       const int kb = kb_lo + it;
@@ -392,13 +415,25 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = splits;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (splits > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = splits;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl_enabled()) {
+    // start while the previous kernel of the stream finishes: the prologue
+    // and the first weight stages overlap its tail (the kernel waits for it
+    // before loading activations or writing Y)
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = splits > 1 ? 1 : 0;
+  cfg.numAttrs = na;
   if (cudaLaunchKernelEx(&cfg, kernel, mw, mx, args) != cudaSuccess) {
     cudaGetLastError();
     return FP8RL_ERR_CUDA;

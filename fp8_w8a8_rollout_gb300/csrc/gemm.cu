@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -953,7 +954,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
       for (int j = 0; j < C::kCols / 2; ++j) acc[j] = 0ull;
       const int sw_lane = nb - (n0 >> 7);  // which of the tile's weight scales
       if constexpr (MX) {
-        // scale factors up to kScaleSlots chunks into the next tile, so the
+        // scale factors up to kMxLead chunks into the next tile, so the
         // MMA thread can start it while this tile drains and stores
         const uint32_t lim = min(mx_total, (mx_tile + 1) * (uint32_t)num_kb + kMxLead);
         while (ok && 4u * mx_next < lim) ok = mx_write();
@@ -1321,7 +1322,6 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
 // back on the even CTA's barrier.  (With fp32 scales the chunk accumulators would have to cross the
 // pair every K chunk: measured at half the one-CTA kernel's speed on GB300,
 // so fp32 keeps one CTA per tile.)
-template <bool OUT>
 struct PairCfg {
   static constexpr int kBN = 256;                // tile columns
   static constexpr int kABytes = kBM * kBK;      // this CTA's 128 activation rows
@@ -1330,8 +1330,6 @@ struct PairCfg {
   static constexpr int kCols = 64;               // accumulator columns per epilogue thread
   static constexpr int kEpiWarps = 16;
   static constexpr int kThreads = 128 + kEpiWarps * 32;
-  static constexpr int kOutSlotBytes = 32 * kCols * 2;
-  static constexpr int kOutBytes = OUT ? kEpiWarps * kOutSlotBytes : 0;
   // scale-factor slots in TMEM, four K chunks each (the one-CTA block-scaled
   // kernel's layout); no ring in shared memory
   static constexpr int kScaleSlots = 16;
@@ -1340,14 +1338,10 @@ struct PairCfg {
   static constexpr int kSfColsPerSlot = 16;
   static_assert(kSfCol0 + kScaleSlots * kSfColsPerSlot <= 512, "scale factors fit in TMEM");
   static constexpr int kBookBytes = 1024;
-  static constexpr int kStagesFit =
-      OUT ? (227 * 1024 - 3 * 1024 - kBookBytes - kOutBytes - kScaleRingBytes) / kStageBytes
-          : (200 * 1024) / kStageBytes;
+  static constexpr int kStagesFit = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kTmemCols = 512;
-  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleRingBytes;
-  static constexpr int kOutOffset = (kSharedEnd + 1023) / 1024 * 1024;
-  static constexpr int kSmemBytes = 1024 + (OUT ? kOutOffset + kOutBytes : kSharedEnd);
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBookBytes + kScaleRingBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert((2 * kStages + 2 * kScaleSlots + 4) * 8 + 32 <= kBookBytes, "bookkeeping");
   // the roles (the MMA thread's copies, cluster waits and descriptors) need
@@ -1358,11 +1352,10 @@ struct PairCfg {
   static constexpr int kMinLaunchRegs = (128 * kRoleRegs + kEpiWarps * 32 * kEpiRegs + kThreads - 1) / kThreads;
 };
 
-template <bool OUT>
-__global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
+__global__ void __launch_bounds__(PairCfg::kThreads, 1)
     gemm_pair_mx_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_y, const GemmArgs a) {
-  using C = PairCfg<OUT>;
+                        const GemmArgs a) {
+  using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1379,7 +1372,6 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sempty + C::kScaleSlots);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint32_t* issued = reinterpret_cast<uint32_t*>(abort_flag + 1);  // chunks this CTA's producer issued
-  uint8_t* out_slots = base_ptr + C::kOutOffset;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the pair's MMAs
@@ -1579,33 +1571,7 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader);
-      bool staged = false;
-      if constexpr (OUT) {
-        const int box_row0 = row0 + quad * 32;
-        if (__all_sync(0xffffffffu, box_row0 < a.rows && !*abortv &&
-                                   dcheck(n0 + slice * C::kCols + C::kCols <= a.n, a.err))) {
-          uint8_t* oslot = out_slots + ew * C::kOutSlotBytes;
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-#pragma unroll
-          for (int c = 0; c < C::kCols / 8; ++c) {
-            float x[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) f32x2_unpack(acc[4 * c + j], x[2 * j], x[2 * j + 1]);
-            *reinterpret_cast<uint4*>(oslot + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                           pack_bf16x2(x[6], x[7]));
-          }
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmap_y, smem_u32(oslot), n0 + slice * C::kCols, box_row0);
-            bulk_commit_group();
-          }
-          staged = true;
-        }
-      }
-      if (!staged && row_ok && !*abortv && dcheck(grow < a.rows && n0 + slice * C::kCols + C::kCols <= a.n, a.err)) {
+      if (row_ok && !*abortv && dcheck(grow < a.rows && n0 + slice * C::kCols + C::kCols <= a.n, a.err)) {
         uint4* dst = reinterpret_cast<uint4*>(a.y + (int64_t)grow * a.n + n0 + slice * C::kCols);
         const bool wide = (reinterpret_cast<uintptr_t>(a.y) & 31) == 0;
 #pragma unroll
@@ -1627,10 +1593,6 @@ __global__ void __launch_bounds__(PairCfg<false>::kThreads, 1)
           }
         }
       }
-    }
-    if constexpr (OUT) {
-      if (lane == 0) bulk_wait_group0();
-      __syncwarp();
     }
   }
   // Teardown.  Every copy either CTA issued completes on the even CTA's stage
@@ -1691,6 +1653,7 @@ struct Debug {
 };
 Debug g_debug;
 std::mutex g_mu;
+std::atomic<int> g_pdl_off{0};    // test hook 13: launch without programmatic stream serialisation
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1909,10 +1872,9 @@ fp8rl_status launch(const void* xq, const void* wq, int64_t experts, int64_t m_t
 }
 
 // A dense data-parallel UE8M0 product on tensor-core pairs (clusters of two CTAs).
-template <bool OUT>
 fp8rl_status launch_pair(const void* xq, const void* wq, GemmArgs args, cudaStream_t stream) {
-  using C = PairCfg<OUT>;
-  auto kernel = gemm_pair_mx_kernel<OUT>;
+  using C = PairCfg;
+  auto kernel = gemm_pair_mx_kernel;
   static KernelState st[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8RL_ERR_CUDA;
@@ -1954,14 +1916,9 @@ fp8rl_status launch_pair(const void* xq, const void* wq, GemmArgs args, cudaStre
     if (!ks.attr_ok) return FP8RL_ERR_CUDA;
     if (!ks.regs_ok || ks.cluster_capacity[2] < 1) return FP8RL_ERR_UNSUPPORTED;
   }
-  CUtensorMap mx, mw, my;
+  CUtensorMap mx, mw;
   if (!make_map(&mx, xq, args.k, args.rows, kBM)) return FP8RL_ERR_CUDA;
   if (!make_map(&mw, wq, args.k, args.n, 128)) return FP8RL_ERR_CUDA;
-  if (OUT) {
-    if (!make_out_map(&my, args.y, args.n, args.rows)) return FP8RL_ERR_CUDA;
-  } else {
-    my = mx;
-  }
   const int64_t pairs_total = ((int64_t)args.rows + 2 * kBM - 1) / (2 * kBM) * (args.n / C::kBN);
   const int64_t clusters = std::min<int64_t>(pairs_total, ks.cluster_capacity[2]);
   cudaLaunchConfig_t cfg = {};
@@ -1976,7 +1933,7 @@ fp8rl_status launch_pair(const void* xq, const void* wq, GemmArgs args, cudaStre
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, my, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kernel, mx, mw, args) != cudaSuccess) {
     cudaGetLastError();
     return FP8RL_ERR_CUDA;
   }
@@ -2053,7 +2010,7 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   // blocks: tiles of 256 x 256 on tensor-core pairs (clusters of two CTAs)
   const bool pair_ok = ue && dbg.mx != 1 && !d_offsets && n % 256 == 0 && rows > kBM && !short_a;
   if (pair_ok && dbg.pair == 1) {
-    const fp8rl_status st = launch_pair<false>(xq, wq, args, cs);
+    const fp8rl_status st = launch_pair(xq, wq, args, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
   }
   if (workspace && !d_offsets && !short_a && dbg.streamk != 1) {
@@ -2167,6 +2124,9 @@ fp8rl_status run_swiglu(const void* xq, const void* x_scale, const void* wq, con
 }
 
 }  // namespace
+
+bool pdl_enabled() { return g_pdl_off.load() == 0; }
+
 }  // namespace fp8rl
 
 using namespace fp8rl;
@@ -2316,8 +2276,13 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
       if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
       g_debug.pair = (int)value;
       return FP8RL_OK;
+    case 13:
+      if (value < 0 || value > 1) return FP8RL_ERR_INVALID_ARG;
+      g_pdl_off.store((int)value);
+      return FP8RL_OK;
     case 0:
       g_debug = Debug{};
+      g_pdl_off.store(0);
       return FP8RL_OK;
   }
   return FP8RL_ERR_INVALID_ARG;

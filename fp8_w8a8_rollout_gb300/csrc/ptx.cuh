@@ -201,6 +201,20 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Let the next kernel of the stream, when it was launched with programmatic
+// stream serialisation, start before this grid completes (it still waits in
+// grid_dep_wait for this grid's completion before reading what it wrote)
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until every grid this one depends on programmatically has completed
+// and its memory operations are visible; returns at once for a grid launched
+// without programmatic stream serialisation
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ cp.async (LDGSTS)
 
 // 4-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros and
@@ -248,18 +262,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
 __host__ __device__ constexpr uint32_t idesc_mx_e4m3_ue8m0(int m, int n, int sfa_byte, int sfb_byte) {
   return (static_cast<uint32_t>(sfb_byte) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(m >> 7) << 27) | (static_cast<uint32_t>(sfa_byte) << 29);
-}
-
-// Shared-memory descriptor of a 32-row x 16-byte block with rows 16 bytes
-// apart (no swizzle: 8-row core matrices of 128 bytes, stride byte offset
-// 128): the source layout of a tcgen05.cp 32x128b copy.
-__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(128u >> 4) << 16;
-  d |= static_cast<uint64_t>(128u >> 4) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  return d;
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
@@ -317,14 +319,6 @@ __device__ __forceinline__ void mma_mx_e4m3(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
-// Copy 32 rows x 128 bits from shared memory (descriptor) into TMEM columns
-// taddr .. taddr + 3 of lanes 0..31, replicated into all four lane quadrants;
-// asynchronous, ordered with this thread's tcgen05.mma and tracked by
-// tcgen05.commit
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
-}
-
 // The block-scaled pair form: scale factors read from each CTA's TMEM at the
 // same addresses (its rows' A factors, the tile's B factors), laid out as in
 // mma_mx_e4m3
@@ -336,12 +330,6 @@ __device__ __forceinline__ void mma_mx_e4m3_pair(uint32_t d_tmem, uint64_t a_des
       "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
-}
-
-// tmem_cp_32x128b_x4 for a pair: each CTA's block at this shared-memory
-// offset goes to its own TMEM
-__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t s_desc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // arrive once on the mbarrier at this offset in each CTA of the pair when every

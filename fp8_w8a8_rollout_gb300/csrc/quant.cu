@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace fp8rl {
 
@@ -274,6 +275,10 @@ __global__ void __launch_bounds__(256, 3) quant_act_kernel(const uint16_t* __res
   const int32_t warp_count = gridDim.x * 8;
   const int32_t rblocks = (m + kActRows - 1) / kActRows;
   const int32_t tasks = rblocks * groups;  // the host keeps m * groups below 2^31
+  // the next kernel of the stream may start (it waits for this grid before
+  // reading the codes); this grid's input comes from the earlier ones
+  ptx::grid_dep_launch_dependents();
+  ptx::grid_dep_wait();
   if (warp >= tasks) return;
   uint4 va[4], vb[4];
   ActTask ta = act_task(warp, rblocks, m, k, vec, sub);
@@ -456,15 +461,28 @@ extern "C" FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int6
   const int vec = (ldx * 2) % 16 == 0 && ldq % 8 == 0;
   uint32_t* err = device_error_word();
   if (!err) return FP8RL_ERR_CUDA;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (fmt == FP8RL_SCALE_UE8M0)
-    quant_act_kernel<true><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), (int32_t)m,
-                                                           k, ldx, static_cast<uint8_t*>(q_e4m3), ldq,
-                                                           x_scale, (int32_t)groups, vec, err);
-  else
-    quant_act_kernel<false><<<(unsigned)grid, 256, 0, cs>>>(static_cast<const uint16_t*>(x_bf16), (int32_t)m,
-                                                            k, ldx, static_cast<uint8_t*>(q_e4m3), ldq,
-                                                            x_scale, (int32_t)groups, vec, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  // start while the previous kernel of the stream finishes (the kernel waits
+  // for it before reading X): at decode sizes the launch is most of the cost
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  const uint16_t* xp = static_cast<const uint16_t*>(x_bf16);
+  uint8_t* qp = static_cast<uint8_t*>(q_e4m3);
+  const int32_t m32 = (int32_t)m, g32 = (int32_t)groups;
+  const cudaError_t e =
+      fmt == FP8RL_SCALE_UE8M0
+          ? cudaLaunchKernelEx(&cfg, quant_act_kernel<true>, xp, m32, k, ldx, qp, ldq, x_scale, g32, vec, err)
+          : cudaLaunchKernelEx(&cfg, quant_act_kernel<false>, xp, m32, k, ldx, qp, ldq, x_scale, g32, vec, err);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FP8RL_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 

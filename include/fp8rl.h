@@ -36,6 +36,17 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream).  Results are ready once the stream
  *     is synchronised.
+ *   - Overlapped launches: fp8rl_quant_act_group and the GEMMs at decode
+ *     sizes (dense, m <= 32) are launched with programmatic stream
+ *     serialisation, and let the next kernel of the stream start before they
+ *     complete.  Such a kernel may begin while the kernel before it on the
+ *     stream is still running; it waits for that kernel's completion before
+ *     it reads any activation or scale of X and before it writes anything,
+ *     but the decode GEMM reads its first weight tiles (wq) before that wait.
+ *     No kernel of this library that lets a dependent start early writes
+ *     weights; a caller whose own kernel writes wq and triggers its
+ *     dependents early (griddepcontrol.launch_dependents) must not enqueue a
+ *     decode-size GEMM on that weight right behind it.
  *   - Arguments are validated on the host before any launch; a call that
  *     returns an error launched nothing.
  *   - Matrices are row-major with an explicit leading dimension in elements.
@@ -408,6 +419,8 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          over clusters of two CTAs): 0 chooses per shape (default), 1
  *          always where the shape allows (n a multiple of 256, m > 128), 2
  *          never;
+ *   key 13 overlapped launches of the activation quantiser and the decode
+ *          GEMM (see the conventions above): 0 on (default), 1 off;
  *   key 0  restore all defaults.
  * Every key but 0 is refused (UNSUPPORTED, nothing changes) unless the
  * process environment holds FP8RL_TEST_HOOKS=1 at the time of the call, so

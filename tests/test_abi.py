@@ -252,6 +252,8 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 11, 1) == 0
     assert _rc("fp8rl_debug_set", 12, 3) == 1
     assert _rc("fp8rl_debug_set", 12, 1) == 0
+    assert _rc("fp8rl_debug_set", 13, 2) == 1
+    assert _rc("fp8rl_debug_set", 13, 1) == 0
     assert _rc("fp8rl_debug_set", 1, 256) == 0
     assert _rc("fp8rl_debug_set", 0, 0) == 0
 

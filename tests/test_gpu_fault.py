@@ -178,3 +178,34 @@ def test_fused_epilogue_wait_runs_out_and_is_reported():
     assert fp8rl.fp8rl_sync_status() == 0
     h_ref, hq_ref, hs_ref = oracle.gemm_swiglu_quant(xq, sx, wq, sw)
     assert np.all(np.abs(hs.cpu().numpy() - hs_ref) <= 1e-4 * hs_ref)
+
+
+@pytest.mark.parametrize("skip", [0, 7])
+def test_decode_wait_runs_out_and_is_reported(skip):
+    """The decode-size GEMM launched behind the activation quantiser with
+    overlapped launches: a chunk among the weight stages fetched before the
+    wait for the quantiser (0) or one of the later ones (7) never arrives; the
+    MMA's wait runs out, TIMEOUT is reported, and the next call is correct."""
+    m, n, k = 16, 256, 4096
+    x = synth.activation_bf16(m, k, 8, "fault-dx", device="cuda")
+    w = synth.weight_bf16(n, k, 8, "fault-dw")
+    wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w))
+    dw, dsw = dev(wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_SPLITS, 1)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, skip)
+    xq, sx = fp8rl.quant_act(x)
+    fp8rl.gemm(xq, sx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == TIMEOUT
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, -1)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 2_000_000_000)
+    assert fp8rl.fp8rl_sync_status() == 0
+    xq, sx = fp8rl.quant_act(x)
+    y = fp8rl.gemm(xq, sx, dw, dsw)
+    assert fp8rl.fp8rl_sync_status() == 0
+    rxq, rsx = oracle.quant_act_group(synth.bf16_bits(x.cpu()))
+    assert np.array_equal(xq.cpu().numpy(), rxq)
+    ref = oracle.gemm_blockscaled(rxq, rsx, wq, sw)
+    got = y.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 1e-3 * rms)
