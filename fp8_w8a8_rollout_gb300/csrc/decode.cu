@@ -7,19 +7,28 @@
 // kb of sx[kb][m] * sw[n/128][kb] * P_kb[m][n]).  At decode sizes the weights
 // are the whole cost (HBM-bound), so the tensor-core tile is turned around:
 // the MMA's 128 rows are 128 weight rows and its N is the token count padded
-// to NT = 16 or 32.  A CTA's accumulator is then 128 x NT fp32 (32 or 64 TMEM
-// columns for two buffers), four epilogue warps promote each chunk with NT
-// multiply-adds per thread (instead of a 128 x 128 tile of which 16 or 32 rows
-// are real), and every operand stage carries 16 KB of weights and only NT
-// rows of activations.  (The occupancy query reports one CTA per SM for this
-// kernel on GB300 whatever its registers and shared memory, so the split
-// count is bounded by the clusters that fit at once, as for the 128-row-tile
-// kernel.)  Measured on GB300 at 16 tokens: 24576 x 4096 weights 30 -> 21 us,
-// 6144 / 4096 x 4096 and 4096 x 12288 5-8% faster.
+// to NT = 16 or 32.  A CTA's accumulator is then 128 x NT fp32 (four buffers,
+// so the MMA runs up to four chunks ahead of the epilogue), four epilogue
+// warps promote each chunk with NT multiply-adds per thread (instead of a
+// 128 x 128 tile of which 16 or 32 rows are real), and every operand stage
+// carries 16 KB of weights and only NT rows of activations.  The chunk scales
+// reach the epilogue 32 chunks at a time (one lane per chunk, shared by
+// shuffles), not one memory round trip per chunk.
 //
 // Split K: a cluster of `splits` CTAs (grid y) shares one 128-row weight
 // block, each a contiguous K range; their fp32 partials meet through
-// distributed shared memory, summed in rank order.
+// distributed shared memory, summed in rank order, every rank's 16-byte
+// pieces requested before the first is added.
+//
+// Launch (measured on GB300, 16 tokens, weights streamed from HBM): a power
+// of two of splits that keeps about two CTAs per SM, as many stages as let
+// two CTAs share an SM; the first stages' weight tiles are requested by the
+// thread that initialises the barriers, before the block's setup completes.
+// With overlapped launches (programmatic stream serialisation) the kernel
+// lets the next one start at once and waits for the previous one only
+// before it loads activations and scales of X or writes Y.  Qwen3-8B
+// projections at 16 tokens, back to back: 6144 x 4096 11.0 -> 7.8 us,
+// 4096 x 4096 7.4 -> 6.7, 4096 x 12288 14.4 -> 11.7, 24576 x 4096 20.8 -> 19.5.
 //
 // Roles (192 threads): warp 0 lane 0 the TMA producer, warp 1 the TMEM
 // allocator and (lane 0) the MMA issuer, warps 2-5 the epilogue (TMEM lane
@@ -42,7 +51,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kDecThreads = 192;
-constexpr int kDecStages = 5;
+constexpr int kDecMaxStages = 12; // operand stages at most (one CTA per SM)
+constexpr int kDecAccBufs = 4;    // accumulator buffers: the MMA runs up to 4 chunks ahead of the epilogue
+constexpr int kDecMaxSplits = 8;  // K splits per weight block (cluster size)
 constexpr int kDecRows = 128;   // weight rows per tile (the MMA's M)
 constexpr int kDecWBytes = kDecRows * 128;  // one 128-wide K chunk of the weight block
 
@@ -51,6 +62,7 @@ struct DecArgs {
   const void* sw;  // [N/128][K/128]
   __nv_bfloat16* y;
   int32_t rows, n, k, splits;
+  int32_t stages;  // operand stages in shared memory (at most kDecMaxStages)
   uint32_t* err;
   uint64_t timeout_ns;
   int32_t fault_skip_kb;  // test hook: the producer never fills this K chunk (-1: off)
@@ -60,9 +72,18 @@ template <int NT>
 struct DecCfg {
   static constexpr int kXBytes = NT * 128;
   static constexpr int kStageBytes = kDecWBytes + kXBytes;
-  static constexpr int kTmemCols = 2 * NT < 32 ? 32 : 2 * NT;  // two accumulator buffers
-  static constexpr int kSmemBytes = 1024 + kDecStages * kStageBytes + 256;
+  static constexpr int kTmemCols = kDecAccBufs * NT < 32 ? 32 : kDecAccBufs * NT;  // a power of two
+  static constexpr int kBookBytes = 512;
+  static constexpr int smem_bytes(int stages) { return 1024 + stages * kStageBytes + kBookBytes; }
+  // the most stages one CTA can hold (227 KB of shared memory per block)
+  static constexpr int kStagesFit = (227 * 1024 - 1024 - kBookBytes) / kStageBytes;
+  static constexpr int kMaxStages = kStagesFit < kDecMaxStages ? kStagesFit : kDecMaxStages;
+  // the most stages that let two CTAs share an SM (228 KB of shared memory,
+  // 1 KB of it reserved per CTA)
+  static constexpr int kPairStages = (114 * 1024 - 1024 - 1024 - kBookBytes) / kStageBytes;
+  static_assert(kPairStages >= 2 && kPairStages <= kMaxStages, "stages");
   static_assert(kDecRows * NT * 4 <= kDecWBytes, "the split partial fits over one weight stage");
+  static_assert((2 * kDecMaxStages + 2 * kDecAccBufs + 1) * 8 + 8 <= kBookBytes, "bookkeeping");
 };
 
 // a scale as fp32: the word holding it (a UE8M0 byte sits in an aligned
@@ -75,6 +96,23 @@ __device__ __forceinline__ float dec_scale(const void* p, int64_t idx) {
     return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
   }
   return __ldg(static_cast<const float*>(p) + idx);
+}
+
+// 16 bytes of another CTA's shared memory (a cluster address from mapa);
+// volatile keeps it after the cluster barrier that makes the data valid
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// two fp32 values rounded to nearest-even bf16, the first in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // TMEM allocation with the column count as an immediate operand
@@ -103,13 +141,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t sW = base;                                 // kDecStages x 16 KB
-  const uint32_t sX = base + kDecStages * kDecWBytes;       // kDecStages x NT x 128 B
-  uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + kDecStages * C::kStageBytes);
-  uint64_t* empty = full + kDecStages;
-  uint64_t* tfull = empty + kDecStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  const int stages = a.stages;
+  const uint32_t sW = base;                                 // stages x 16 KB
+  const uint32_t sX = base + stages * kDecWBytes;           // stages x NT x 128 B
+  uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + stages * C::kStageBytes);
+  uint64_t* empty = full + kDecMaxStages;
+  uint64_t* tfull = empty + kDecMaxStages;
+  uint64_t* tempty = tfull + kDecAccBufs;
+  uint64_t* drain = tempty + kDecAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* abortv = abort_flag;
@@ -121,19 +160,33 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int num_kb = a.k / 128;
   const int kb_lo = (int)((int64_t)num_kb * split / splits);
   const int nloc = (int)((int64_t)num_kb * (split + 1) / splits) - kb_lo;
+  const int pre = nloc < stages ? nloc : stages;  // stages filled before the loop
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kDecAccBufs; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
       mbar_init(smem_u32(&tempty[b]), 4);  // one arrival per epilogue warp
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    fence_proxy_async_shared();  // the barriers are seen by this thread's copies below
+    // No kernel of this library that lets a dependent start early writes
+    // weights (the weight quantiser does not), so the first stages' weight
+    // tiles are requested at once, before the block's setup completes and
+    // before the wait for the earlier kernels of the stream; the
+    // activations, their outputs, are loaded after that wait.
+    prefetch_tensormap(&tmap_w);
+    for (int j = 0; j < pre; ++j) {
+      if (kb_lo + j == a.fault_skip_kb) continue;
+      const uint32_t fb = smem_u32(&full[j]);
+      mbar_arrive_expect_tx(fb, C::kStageBytes);
+      tma_load_2d(sW + j * kDecWBytes, &tmap_w, (kb_lo + j) * 128, nblk * kDecRows, fb);
+    }
   }
   if (warp == 1) tmem_alloc_n<C::kTmemCols>(smem_u32(tmem_slot));
   tc_fence_before();
@@ -148,27 +201,15 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&tmap_w);
       prefetch_tensormap(&tmap_x);
-      // No kernel of this library that lets a dependent start early writes
-      // weights (the weight quantiser does not), so the first stages' weight
-      // tiles are requested before the wait for the earlier kernels of the
-      // stream; the activations, their outputs, are loaded after it.
-      const int pre = nloc < kDecStages ? nloc : kDecStages;
-      for (int j = 0; j < pre; ++j) {
-        if (kb_lo + j == a.fault_skip_kb) continue;
-        const uint32_t fb = smem_u32(&full[j]);
-        mbar_arrive_expect_tx(fb, C::kStageBytes);
-        tma_load_2d(sW + j * kDecWBytes, &tmap_w, (kb_lo + j) * 128, nblk * kDecRows, fb);
-      }
       grid_dep_wait();
       for (int j = 0; j < pre; ++j)
         if (kb_lo + j != a.fault_skip_kb)
           tma_load_2d(sX + j * C::kXBytes, &tmap_x, (kb_lo + j) * 128, 0, smem_u32(&full[j]));
       int it = pre;
       for (; it < nloc; ++it) {
-        const int s = it % kDecStages;
-        const uint32_t ph = (it / kDecStages) & 1;
+        const int s = it % stages;
+        const uint32_t ph = (it / stages) & 1;
         if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1, abortv, a.err, a.timeout_ns)) break;
         const int kb = kb_lo + it;
         if (kb == a.fault_skip_kb) continue;  // the MMA's wait on this stage runs out
@@ -179,9 +220,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       if (*abortv) {
         // let the copies still in flight land before shared memory is released
-        for (int j = it > kDecStages ? it - kDecStages : 0; j < it; ++j)
+        for (int j = it > stages ? it - stages : 0; j < it; ++j)
           if (kb_lo + j != a.fault_skip_kb)
-            mbar_wait_bounded(smem_u32(&full[j % kDecStages]), (j / kDecStages) & 1, nullptr, nullptr, 10000000ull);
+            mbar_wait_bounded(smem_u32(&full[j % stages]), (j / stages) & 1, nullptr, nullptr, 10000000ull);
       }
     } else {
       grid_dep_wait();
@@ -193,11 +234,11 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kDecRows, NT);
       for (int it = 0; it < nloc; ++it) {
-        const int buf = it & 1;
-        const uint32_t bph = (it >> 1) & 1;
+        const int buf = it % kDecAccBufs;
+        const uint32_t bph = (it / kDecAccBufs) & 1;
         if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns)) break;
-        const int s = it % kDecStages;
-        const uint32_t ph = (it / kDecStages) & 1;
+        const int s = it % stages;
+        const uint32_t ph = (it / stages) & 1;
         if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns)) break;
         tc_fence_after();
         const uint32_t a0 = sW + s * kDecWBytes, b0 = sX + s * C::kXBytes;
@@ -227,16 +268,22 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   if (warp >= 2) {
     grid_dep_wait();  // the activation scales come from earlier kernels
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    // The chunks' scales, 32 chunks at a time: lane j loads chunk w0 + j's
+    // weight scale and its NT activation scales (one round trip to memory
+    // per 32 chunks instead of one per chunk), and each chunk's values reach
+    // the whole warp by shuffles.
+    float wsw = 0.0f, wsx[NT];
     for (int it = 0; it < nloc; ++it) {
-      const int kb = kb_lo + it;
-      // this chunk's scales, loaded before the wait: the weight block's and
-      // one per token (all lanes read the same words)
-      const float swv = dec_scale<UE8M0>(a.sw, (int64_t)nblk * num_kb + kb);
-      float f[NT];
+      const int j = it & 31;
+      if (j == 0) {
+        const int c = it + lane;
+        const int kb = kb_lo + (c < nloc ? c : it);
+        wsw = dec_scale<UE8M0>(a.sw, (int64_t)nblk * num_kb + kb);
 #pragma unroll
-      for (int m = 0; m < NT; ++m) f[m] = m < a.rows ? dec_scale<UE8M0>(a.sx, (int64_t)kb * a.rows + m) : 0.0f;
-      const int buf = it & 1;
-      const uint32_t bph = (it >> 1) & 1;
+        for (int m = 0; m < NT; ++m) wsx[m] = m < a.rows ? dec_scale<UE8M0>(a.sx, (int64_t)kb * a.rows + m) : 0.0f;
+      }
+      const int buf = it % kDecAccBufs;
+      const uint32_t bph = (it / kDecAccBufs) & 1;
       ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -249,8 +296,10 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
       // the activation scale times the weight scale, then one fused
       // multiply-add per token: the 128-row-tile kernel's arithmetic
+      const float swv = __shfl_sync(0xffffffffu, wsw, j);
 #pragma unroll
-      for (int m = 0; m < NT; ++m) acc[m] = fmaf(__uint_as_float(v[m]), f[m] * swv, acc[m]);
+      for (int m = 0; m < NT; ++m)
+        acc[m] = fmaf(__uint_as_float(v[m]), __shfl_sync(0xffffffffu, wsx[m], j) * swv, acc[m]);
     }
   }
   __syncthreads();  // every MMA has been consumed: the operand stages are free
@@ -270,24 +319,40 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
     cluster_sync();  // every CTA's partial is in its shared memory
     if (write) {
-      // this CTA's share of the (token, row) outputs, each the sum of the
-      // cluster's partials in rank order
-      const int total = a.rows * kDecRows;
-      const int i0 = (int)((int64_t)total * split / splits), i1 = (int)((int64_t)total * (split + 1) / splits);
+      // This CTA's share of the outputs, four weight rows of one token at a
+      // time, each the sum of the cluster's partials in rank order: all
+      // ranks' 16-byte pieces are requested before the first is added.
+      const int quads = a.rows * (kDecRows / 4);
+      const int q0 = (int)((int64_t)quads * split / splits), q1 = (int)((int64_t)quads * (split + 1) / splits);
       const uint32_t pbase = smem_u32(part);
-      for (int i = i0 + (int)threadIdx.x; i < i1; i += kDecThreads) {
-        float sum = 0.0f;
-        for (int r = 0; r < splits; ++r) {
-          float x;
-          asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(x) : "r"(mapa_shared(pbase + 4u * i, r)) : "memory");
-          sum += x;
+      for (int q = q0 + (int)threadIdx.x; q < q1; q += kDecThreads) {
+        float4 p[kDecMaxSplits];
+#pragma unroll
+        for (int r = 0; r < kDecMaxSplits; ++r)
+          if (r < splits) p[r] = ld_dsmem_f32x4(mapa_shared(pbase + 16u * (uint32_t)q, r));
+        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kDecMaxSplits; ++r)
+          if (r < splits) {
+            s0 += p[r].x;
+            s1 += p[r].y;
+            s2 += p[r].z;
+            s3 += p[r].w;
+          }
+        const int m = q / (kDecRows / 4), nr = (q - m * (kDecRows / 4)) * 4;
+        if (dcheck(m < a.rows && nblk * kDecRows + nr + 4 <= a.n, a.err)) {
+          const uint32_t lo = pack_bf16x2_rn(s0, s1), hi = pack_bf16x2_rn(s2, s3);
+          asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.y + (int64_t)m * a.n + (int64_t)nblk * kDecRows + nr),
+                       "r"(lo), "r"(hi)
+                       : "memory");
         }
-        const int m = i / kDecRows, nr = i - m * kDecRows;
-        if (dcheck(m < a.rows && nblk * kDecRows + nr < a.n, a.err))
-          a.y[(int64_t)m * a.n + (int64_t)nblk * kDecRows + nr] = __float2bfloat16_rn(sum);
       }
     }
-    cluster_sync();  // no CTA leaves while its partial may still be read
+    // No CTA leaves while its partial may still be read.  The values this
+    // CTA loaded were consumed before the arrival, and nothing written here
+    // is read through the cluster afterwards, so the arrival need not
+    // release (a release would also wait for the Y stores to complete).
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -335,7 +400,6 @@ struct DecState {
   uint64_t ctx = 0;  // the context the attributes were set in (redone when it changes)
   bool ready = false, ok = false;
   int sms = 0;
-  int capacity[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // clusters of each size resident at once
 };
 
 template <int NT, bool UE8M0>
@@ -357,9 +421,9 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
   DecArgs args = args0;
   const int nblocks = args.n / kDecRows;
   const int num_kb = args.k / 128;
-  int splits = 1;
   const uint64_t ctx = current_context_id();
   if (!ctx) return FP8RL_ERR_CUDA;
+  int splits = 1, stages = C::kPairStages;
   {
     std::lock_guard<std::mutex> lock(g_dec_mu);
     if (!st.ready || st.ctx != ctx) {
@@ -367,8 +431,8 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
       st.ctx = ctx;
       int sms = 0;
       st.ok = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0 &&
-              cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) ==
-                  cudaSuccess &&
+              cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::smem_bytes(C::kMaxStages)) == cudaSuccess &&
               cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) == cudaSuccess &&
               // the whole unified L1 as shared memory, so that two CTAs fit on an SM
               cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -377,43 +441,32 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
       st.ready = true;
     }
     if (!st.ok) return FP8RL_ERR_UNSUPPORTED;
-    // K splits so that about two CTAs run on every SM, each with >= 2 chunks
+    // K splits (measured on GB300 at 16 tokens, weights streamed from HBM):
+    // about two CTAs per SM with few stages each beat one deep CTA per SM
+    // (more CTAs keep more weight rows in flight at once), and a split count
+    // that divides the K chunks evenly (a power of two) beats an uneven one.
+    // Clusters that cannot all be resident at once simply run later; the
+    // occupancy query reports one CTA per SM for clustered launches of this
+    // kernel, but two run (measured: 6144 x 4096 weights in 4 splits, 192
+    // CTAs, 7.9 us against 9.4 us for the 2 splits that query allows).
     if (force_splits > 0) {
-      splits = std::min(std::min(force_splits, 8), num_kb);
+      splits = std::min(std::min(force_splits, kDecMaxSplits), num_kb);
     } else {
-      while (splits < 8 && (int64_t)nblocks * (splits + 1) <= 2 * (int64_t)st.sms && num_kb / (splits + 1) >= 2)
-        ++splits;
+      while (splits * 2 <= kDecMaxSplits && (int64_t)nblocks * splits * 2 <= 2 * (int64_t)st.sms &&
+             num_kb / (splits * 2) >= 2)
+        splits *= 2;
     }
-    // only as many splits as leave every cluster resident at once
-    while (splits > 1) {
-      if (st.capacity[splits] < 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)nblocks, (unsigned)splits, 1);
-        cfg.blockDim = dim3(kDecThreads);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 1;
-        attr[0].val.clusterDim.y = splits;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        st.capacity[splits] = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess ? n : 0;
-        cudaGetLastError();
-      }
-      if (st.capacity[splits] >= nblocks) break;
-      --splits;
-    }
+    stages = C::kPairStages;
   }
   args.splits = splits;
+  args.stages = stages;
   CUtensorMap mw, mx;
   if (!make_map(&mw, wq, args.k, args.n, kDecRows)) return FP8RL_ERR_CUDA;
   if (!make_map(&mx, xq, args.k, args.rows, NT)) return FP8RL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nblocks, (unsigned)splits, 1);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = C::smem_bytes(stages);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int na = 0;

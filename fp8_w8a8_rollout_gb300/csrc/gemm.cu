@@ -880,9 +880,9 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
     // MMAs to arrive in.
     constexpr int kMxStep = C::kEpiWarps / 4;
     constexpr uint32_t kMxLead = 4 * (C::kScaleSlots / 2);  // chunks of lead into the next tile
-    const uint32_t mx_total = MX ? (uint32_t)((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) *
-                                       (uint32_t)num_kb
-                                 : 0u;
+    // (the count for every kernel: the block-scaled ones alone use it)
+    const uint32_t mx_total =
+        (uint32_t)((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) * (uint32_t)num_kb;
     uint32_t mx_next = (uint32_t)slice;  // this warp's next group to write
     uint32_t mx_tile = 0;                // tiles of this CTA drained so far
     // write group mx_next's scale factors into its TMEM slot once the MMAs
@@ -1966,11 +1966,10 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   args.fault_skip_kb = dbg.fault_skip_kb;
   args.wait_mode = dbg.wait_mode;
   args.l2_prefetch = dbg.l2_prefetch;
-  // decode sizes (dense): the swapped-operand kernel of decode.cu for at most
-  // 16 rows, or 32 when the weight has a 128-row block per SM (no split
-  // needed); measured on GB300, with 17..32 rows and a K split the 128-row-tile
-  // kernel is as fast or faster.  The test hook forces either.
-  const bool decode_shape = !d_offsets && rows <= 32 && (rows <= 16 || n / 128 >= di.sms || dbg.decode == 1);
+  // decode sizes (dense, at most 32 rows): the swapped-operand kernel of
+  // decode.cu (measured on GB300 at 17 and 32 rows, Qwen3-8B projections:
+  // 30-50% faster than the 128-row-tile kernel).  The test hook forces either.
+  const bool decode_shape = !d_offsets && rows <= 32;
   if (decode_shape && dbg.decode != 2 && dbg.streamk != 2) {
     const fp8rl_status st = decode_gemm(xq, x_scale, wq, w_scale, y, rows, n, k, fmt == FP8RL_SCALE_UE8M0, err,
                                         dbg.timeout_ns, dbg.fault_skip_kb, dbg.splits,
