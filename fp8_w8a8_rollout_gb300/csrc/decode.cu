@@ -1,5 +1,6 @@
-// decode.cu -- the block-scaled W8A8 GEMM for decode-sized M (at most 32
-// tokens), with the operands swapped.
+// decode.cu -- the block-scaled W8A8 GEMM for decode-sized M (up to 128
+// tokens; by default the GEMMs route at most 64 here), with the operands
+// swapped.
 //
 // Same product as gemm.cu (FP8-RL page, "Method steps": E4M3 operands, one
 // scale per 128x128 weight block and per 1x128 activation group, fp32
@@ -7,13 +8,15 @@
 // kb of sx[kb][m] * sw[n/128][kb] * P_kb[m][n]).  At decode sizes the weights
 // are the whole cost (HBM-bound), so the tensor-core tile is turned around:
 // the MMA's 128 rows are 128 weight rows and its N is the token count padded
-// to NT = 16 or 32.  A CTA's accumulator is then 128 x NT fp32 (four buffers,
-// so the MMA runs up to four chunks ahead of the epilogue), four epilogue
-// warps promote each chunk with NT multiply-adds per thread (instead of a
-// 128 x 128 tile of which 16 or 32 rows are real), and every operand stage
-// carries 16 KB of weights and only NT rows of activations.  The chunk scales
-// reach the epilogue 32 chunks at a time (one lane per chunk, shared by
-// shuffles), not one memory round trip per chunk.
+// to NT = 16, 32, 64 or 128.  A CTA's accumulator is then 128 x NT fp32 (four
+// buffers, two at 128 columns, so the MMA runs ahead of the epilogue), four
+// epilogue warps per 32 token columns promote each chunk with up to 32
+// multiply-adds per thread (instead of a 128 x 128 tile of which only the
+// first rows are real), and every operand stage carries 16 KB of weights and
+// only NT rows of activations.  Up to 32 columns the chunk scales reach the
+// epilogue 32 chunks at a time (one lane per chunk, shared by shuffles); with
+// more columns (more warps, fewer registers each) every warp keeps a ring of
+// eight chunks' scales in shared memory, filled ahead by asynchronous copies.
 //
 // Split K: a cluster of `splits` CTAs (grid y) shares one 128-row weight
 // block, each a contiguous K range; their fp32 partials meet through
@@ -50,10 +53,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kDecThreads = 192;
 constexpr int kDecMaxStages = 12; // operand stages at most (one CTA per SM)
-constexpr int kDecAccBufs = 4;    // accumulator buffers: the MMA runs up to 4 chunks ahead of the epilogue
+constexpr int kDecMaxAccBufs = 4; // accumulator buffers at most
 constexpr int kDecMaxSplits = 8;  // K splits per weight block (cluster size)
+constexpr int kDecRing = 8;       // chunks of scales in flight per epilogue warp (64 tokens and more)
+constexpr int kDecRingSlot = 40;  // words per ring slot: 32 token scales, the weight scale, padding
 constexpr int kDecRows = 128;   // weight rows per tile (the MMA's M)
 constexpr int kDecWBytes = kDecRows * 128;  // one 128-wide K chunk of the weight block
 
@@ -68,22 +72,34 @@ struct DecArgs {
   int32_t fault_skip_kb;  // test hook: the producer never fills this K chunk (-1: off)
 };
 
+// NT token columns (16, 32, 64 or 128): up to 32 per epilogue thread, so 4
+// epilogue warps (one per TMEM lane quadrant) for every 32 columns.
 template <int NT>
 struct DecCfg {
+  static constexpr int kSlice = NT < 32 ? NT : 32;   // token columns per epilogue thread
+  static constexpr int kEpiWarps = 4 * (NT / kSlice);
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kAccBufs = NT <= 64 ? 4 : 2;   // 256 TMEM columns at most, two CTAs per SM
+  static constexpr int kTmemCols = kAccBufs * NT < 32 ? 32 : kAccBufs * NT;  // a power of two
   static constexpr int kXBytes = NT * 128;
   static constexpr int kStageBytes = kDecWBytes + kXBytes;
-  static constexpr int kTmemCols = kDecAccBufs * NT < 32 ? 32 : kDecAccBufs * NT;  // a power of two
   static constexpr int kBookBytes = 512;
-  static constexpr int smem_bytes(int stages) { return 1024 + stages * kStageBytes + kBookBytes; }
+  // the epilogue warps' scale rings (64 token columns and more)
+  static constexpr int kRingBytes = NT > 32 ? kEpiWarps * kDecRing * kDecRingSlot * 4 : 0;
+  static constexpr int smem_bytes(int stages) { return 1024 + stages * kStageBytes + kBookBytes + kRingBytes; }
   // the most stages one CTA can hold (227 KB of shared memory per block)
-  static constexpr int kStagesFit = (227 * 1024 - 1024 - kBookBytes) / kStageBytes;
+  static constexpr int kStagesFit = (227 * 1024 - 1024 - kBookBytes - kRingBytes) / kStageBytes;
   static constexpr int kMaxStages = kStagesFit < kDecMaxStages ? kStagesFit : kDecMaxStages;
   // the most stages that let two CTAs share an SM (228 KB of shared memory,
-  // 1 KB of it reserved per CTA)
-  static constexpr int kPairStages = (114 * 1024 - 1024 - 1024 - kBookBytes) / kStageBytes;
-  static_assert(kPairStages >= 2 && kPairStages <= kMaxStages, "stages");
-  static_assert(kDecRows * NT * 4 <= kDecWBytes, "the split partial fits over one weight stage");
-  static_assert((2 * kDecMaxStages + 2 * kDecAccBufs + 1) * 8 + 8 <= kBookBytes, "bookkeeping");
+  // 1 KB of it reserved per CTA); below three, one CTA per SM with more
+  static constexpr int kPairStages = (114 * 1024 - 1024 - 1024 - kBookBytes - kRingBytes) / kStageBytes;
+  static constexpr bool kPairs = kPairStages >= 3;
+  static constexpr int kStages = kPairs ? kPairStages : kMaxStages;
+  static constexpr int kMinBlocks = kPairs ? 2 : 1;
+  static_assert(kStages >= 2 && kStages <= kDecMaxStages, "stages");
+  static_assert(kDecRows * NT * 4 <= kStages * kStageBytes, "the split partial fits over the operand stages");
+  static_assert(kAccBufs <= kDecMaxAccBufs, "accumulators");
+  static_assert((2 * kDecMaxStages + 2 * kDecMaxAccBufs + 1) * 8 + 8 <= kBookBytes, "bookkeeping");
 };
 
 // a scale as fp32: the word holding it (a UE8M0 byte sits in an aligned
@@ -115,6 +131,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// the scale 2^(b - 127) of UE8M0 byte `which` of a 32-bit word (byte 0: 2^-127)
+__device__ __forceinline__ float ue8m0_word_to_f32(uint32_t word, uint32_t which) {
+  const uint32_t b = (word >> (8u * which)) & 0xFFu;
+  return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
 // TMEM allocation with the column count as an immediate operand
 template <uint32_t NCOLS>
 __device__ __forceinline__ void tmem_alloc_n(uint32_t slot_smem) {
@@ -123,9 +145,9 @@ __device__ __forceinline__ void tmem_alloc_n(uint32_t slot_smem) {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
-template <int NT>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[NT]) {
-  if constexpr (NT == 32) {
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[W]) {
+  if constexpr (W == 32) {
     tmem_ld_32x32b_x32(taddr, v);
   } else {
     tmem_ld_32x32b_x16(taddr, v);
@@ -133,7 +155,7 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[NT]) 
 }
 
 template <int NT, bool UE8M0>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__global__ void __launch_bounds__(DecCfg<NT>::kThreads, DecCfg<NT>::kMinBlocks)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
                        const DecArgs a) {
   using C = DecCfg<NT>;
@@ -147,11 +169,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(base_ptr + stages * C::kStageBytes);
   uint64_t* empty = full + kDecMaxStages;
   uint64_t* tfull = empty + kDecMaxStages;
-  uint64_t* tempty = tfull + kDecAccBufs;
-  uint64_t* drain = tempty + kDecAccBufs;
+  uint64_t* tempty = tfull + kDecMaxAccBufs;
+  uint64_t* drain = tempty + kDecMaxAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* abortv = abort_flag;
+  const uint32_t ring = smem_u32(base_ptr + stages * C::kStageBytes + C::kBookBytes);  // epilogue scale rings
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = blockIdx.x;
@@ -167,9 +190,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int b = 0; b < kDecAccBufs; ++b) {
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 4);  // one arrival per epilogue warp
+      mbar_init(smem_u32(&tempty[b]), C::kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -234,8 +257,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kDecRows, NT);
       for (int it = 0; it < nloc; ++it) {
-        const int buf = it % kDecAccBufs;
-        const uint32_t bph = (it / kDecAccBufs) & 1;
+        const int buf = it % C::kAccBufs;
+        const uint32_t bph = (it / C::kAccBufs) & 1;
         if (!mbar_wait_bounded(smem_u32(&tempty[buf]), bph ^ 1, abortv, a.err, a.timeout_ns)) break;
         const int s = it % stages;
         const uint32_t ph = (it / stages) & 1;
@@ -259,47 +282,110 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   }
 
   // ---------------------------------------------------------------- epilogue
+  // thread = one weight row (TMEM lane) x kSlice token columns
   const int quad = warp & 3;
   const int row = quad * 32 + lane;  // weight row within the block
-  float acc[NT];
+  const int slice = warp >= 2 ? (warp - 2) >> 2 : 0;
+  const int tok0 = slice * C::kSlice;  // this thread's first token column
+  constexpr int S = C::kSlice;
+  float acc[S];
 #pragma unroll
-  for (int m = 0; m < NT; ++m) acc[m] = 0.0f;
+  for (int m = 0; m < S; ++m) acc[m] = 0.0f;
   bool ok = true;
   if (warp >= 2) {
     grid_dep_wait();  // the activation scales come from earlier kernels
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    // The chunks' scales, 32 chunks at a time: lane j loads chunk w0 + j's
-    // weight scale and its NT activation scales (one round trip to memory
-    // per 32 chunks instead of one per chunk), and each chunk's values reach
-    // the whole warp by shuffles.
-    float wsw = 0.0f, wsx[NT];
-    for (int it = 0; it < nloc; ++it) {
-      const int j = it & 31;
-      if (j == 0) {
-        const int c = it + lane;
-        const int kb = kb_lo + (c < nloc ? c : it);
-        wsw = dec_scale<UE8M0>(a.sw, (int64_t)nblk * num_kb + kb);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16) + tok0;
+    if constexpr (NT <= 32) {
+      // The chunks' scales, 32 chunks at a time: lane j loads chunk w0 + j's
+      // weight scale and its NT activation scales (one round trip to memory
+      // per 32 chunks instead of one per chunk), and each chunk's values
+      // reach the whole warp by shuffles.
+      float wsw = 0.0f, wsx[S];
+      for (int it = 0; it < nloc; ++it) {
+        const int j = it & 31;
+        if (j == 0) {
+          const int c = it + lane;
+          const int kb = kb_lo + (c < nloc ? c : it);
+          wsw = dec_scale<UE8M0>(a.sw, (int64_t)nblk * num_kb + kb);
 #pragma unroll
-        for (int m = 0; m < NT; ++m) wsx[m] = m < a.rows ? dec_scale<UE8M0>(a.sx, (int64_t)kb * a.rows + m) : 0.0f;
+          for (int m = 0; m < S; ++m) wsx[m] = m < a.rows ? dec_scale<UE8M0>(a.sx, (int64_t)kb * a.rows + m) : 0.0f;
+        }
+        const int buf = it % C::kAccBufs;
+        const uint32_t bph = (it / C::kAccBufs) & 1;
+        ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[S];
+        tmem_ld_cols<S>(t_lane + buf * NT, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+        // the activation scale times the weight scale, then one fused
+        // multiply-add per token: the 128-row-tile kernel's arithmetic
+        const float swv = __shfl_sync(0xffffffffu, wsw, j);
+#pragma unroll
+        for (int m = 0; m < S; ++m)
+          acc[m] = fmaf(__uint_as_float(v[m]), __shfl_sync(0xffffffffu, wsx[m], j) * swv, acc[m]);
       }
-      const int buf = it % kDecAccBufs;
-      const uint32_t bph = (it / kDecAccBufs) & 1;
-      ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t v[NT];
-      tmem_ld_cols<NT>(t_lane + buf * NT, v);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
-      // the activation scale times the weight scale, then one fused
-      // multiply-add per token: the 128-row-tile kernel's arithmetic
-      const float swv = __shfl_sync(0xffffffffu, wsw, j);
+    } else {
+      // The chunks' scales through a ring of kDecRing slots per warp, filled
+      // kDecRing chunks ahead by asynchronous 4-byte copies: lane t copies
+      // the word holding token tok0 + t's scale (zeros past the last token),
+      // lane 0 also the weight scale's word; every lane then reads the whole
+      // slot (broadcast).  One round trip per chunk, kDecRing chunks ahead.
+      const uint32_t my_ring = ring + (uint32_t)((warp - 2) * kDecRing * kDecRingSlot * 4);
+      const int tok = tok0 + lane;
+      auto issue = [&](int c) {  // chunk c of this CTA's range into its slot
+        const uint32_t slot = my_ring + (uint32_t)((c % kDecRing) * kDecRingSlot * 4);
+        if (c < nloc) {
+          const int64_t kb = kb_lo + c;
+          const int64_t xi = kb * a.rows + (tok < a.rows ? tok : 0);
+          const int64_t wi = (int64_t)nblk * num_kb + kb;
+          const uint8_t* xs = static_cast<const uint8_t*>(a.sx);
+          const uint8_t* ws = static_cast<const uint8_t*>(a.sw);
+          cp_async_4(slot + 4u * (uint32_t)lane, UE8M0 ? xs + (xi & ~(int64_t)3) : xs + 4 * xi, tok < a.rows ? 4u : 0u);
+          if (lane == 0) cp_async_4(slot + 4u * 32u, UE8M0 ? ws + (wi & ~(int64_t)3) : ws + 4 * wi, 4u);
+        }
+        cp_async_commit();  // empty past the range: the group count stays uniform
+      };
+      for (int c = 0; c < kDecRing; ++c) issue(c);
+      for (int it = 0; it < nloc; ++it) {
+        const int buf = it % C::kAccBufs;
+        const uint32_t bph = (it / C::kAccBufs) & 1;
+        ok = mbar_wait_bounded(smem_u32(&tfull[buf]), bph, abortv, a.err, a.timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[S];
+        tmem_ld_cols<S>(t_lane + buf * NT, v);
+        cp_async_wait<kDecRing - 1>();  // this chunk's scales have landed (this lane's copies)
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();  // ... and every lane's
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+        const int64_t kb = kb_lo + it;
+        const uint32_t slot = my_ring + (uint32_t)((it % kDecRing) * kDecRingSlot * 4);
+        const uint32_t* sp = reinterpret_cast<const uint32_t*>(base_ptr) + (slot - base) / 4;
+        uint32_t wword = sp[32];
+        const int64_t wi = (int64_t)nblk * num_kb + kb;
+        const float swv = UE8M0 ? ue8m0_word_to_f32(wword, (uint32_t)(wi & 3)) : __uint_as_float(wword);
 #pragma unroll
-      for (int m = 0; m < NT; ++m)
-        acc[m] = fmaf(__uint_as_float(v[m]), __shfl_sync(0xffffffffu, wsx[m], j) * swv, acc[m]);
+        for (int m4 = 0; m4 < S; m4 += 4) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(sp + m4);
+          const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int m = m4 + q;
+            const float f = UE8M0 ? ue8m0_word_to_f32(ww[q], (uint32_t)((kb * a.rows + tok0 + m) & 3)) : __uint_as_float(ww[q]);
+            acc[m] = fmaf(__uint_as_float(v[m]), f * swv, acc[m]);
+          }
+        }
+        __syncwarp();  // every lane has read the slot before it is refilled
+        issue(it + kDecRing);
+      }
+      cp_async_wait<0>();  // no copy into the ring outlives the loop
     }
   }
   __syncthreads();  // every MMA has been consumed: the operand stages are free
@@ -307,15 +393,16 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   float* part = reinterpret_cast<float*>(base_ptr);  // [NT][128] fp32 over the first weight stage
   if (splits == 1) {
     if (warp >= 2 && write) {
-      __nv_bfloat16* dst = a.y + (int64_t)nblk * kDecRows + row;
+      __nv_bfloat16* dst = a.y + (int64_t)tok0 * a.n + (int64_t)nblk * kDecRows + row;
 #pragma unroll
-      for (int m = 0; m < NT; ++m)  // a constant bound keeps acc in registers
-        if (m < a.rows && dcheck(nblk * kDecRows + row < a.n, a.err)) dst[(int64_t)m * a.n] = __float2bfloat16_rn(acc[m]);
+      for (int m = 0; m < S; ++m)  // a constant bound keeps acc in registers
+        if (tok0 + m < a.rows && dcheck(nblk * kDecRows + row < a.n, a.err))
+          dst[(int64_t)m * a.n] = __float2bfloat16_rn(acc[m]);
     }
   } else {
     if (warp >= 2) {
 #pragma unroll
-      for (int m = 0; m < NT; ++m) part[m * kDecRows + row] = acc[m];
+      for (int m = 0; m < S; ++m) part[(tok0 + m) * kDecRows + row] = acc[m];
     }
     cluster_sync();  // every CTA's partial is in its shared memory
     if (write) {
@@ -325,7 +412,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       const int quads = a.rows * (kDecRows / 4);
       const int q0 = (int)((int64_t)quads * split / splits), q1 = (int)((int64_t)quads * (split + 1) / splits);
       const uint32_t pbase = smem_u32(part);
-      for (int q = q0 + (int)threadIdx.x; q < q1; q += kDecThreads) {
+      for (int q = q0 + (int)threadIdx.x; q < q1; q += C::kThreads) {
         float4 p[kDecMaxSplits];
 #pragma unroll
         for (int r = 0; r < kDecMaxSplits; ++r)
@@ -423,7 +510,8 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
   const int num_kb = args.k / 128;
   const uint64_t ctx = current_context_id();
   if (!ctx) return FP8RL_ERR_CUDA;
-  int splits = 1, stages = C::kPairStages;
+  int splits = 1;
+  const int stages = C::kStages;
   {
     std::lock_guard<std::mutex> lock(g_dec_mu);
     if (!st.ready || st.ctx != ctx) {
@@ -449,14 +537,14 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
     // occupancy query reports one CTA per SM for clustered launches of this
     // kernel, but two run (measured: 6144 x 4096 weights in 4 splits, 192
     // CTAs, 7.9 us against 9.4 us for the 2 splits that query allows).
+    // (64 and 128 token columns: C::kMinBlocks CTAs per SM, by shared memory.)
     if (force_splits > 0) {
       splits = std::min(std::min(force_splits, kDecMaxSplits), num_kb);
     } else {
-      while (splits * 2 <= kDecMaxSplits && (int64_t)nblocks * splits * 2 <= 2 * (int64_t)st.sms &&
-             num_kb / (splits * 2) >= 2)
+      const int64_t slots = (int64_t)C::kMinBlocks * st.sms;
+      while (splits * 2 <= kDecMaxSplits && (int64_t)nblocks * splits * 2 <= slots && num_kb / (splits * 2) >= 2)
         splits *= 2;
     }
-    stages = C::kPairStages;
   }
   args.splits = splits;
   args.stages = stages;
@@ -465,7 +553,7 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
   if (!make_map(&mx, xq, args.k, args.rows, NT)) return FP8RL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nblocks, (unsigned)splits, 1);
-  cfg.blockDim = dim3(kDecThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::smem_bytes(stages);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -496,13 +584,13 @@ fp8rl_status launch_decode(const void* xq, const void* wq, const DecArgs& args0,
 
 }  // namespace
 
-// Called by the GEMM entry points for dense products with rows <= 32 (the
+// Called by the GEMM entry points for dense products with rows <= 128 (the
 // arguments already validated); UNSUPPORTED lets the caller fall back to the
 // 128-row-tile kernel.
 fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale, void* y,
                          int64_t rows, int64_t n, int64_t k, bool ue8m0, uint32_t* err, uint64_t timeout_ns,
                          int fault_skip_kb, int force_splits, cudaStream_t stream) {
-  if (rows < 1 || rows > 32 || n % kDecRows || k % 128) return FP8RL_ERR_UNSUPPORTED;
+  if (rows < 1 || rows > 128 || n % kDecRows || k % 128) return FP8RL_ERR_UNSUPPORTED;
   DecArgs a{};
   a.sx = x_scale;
   a.sw = w_scale;
@@ -516,8 +604,14 @@ fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, co
   if (rows <= 16)
     return ue8m0 ? launch_decode<16, true>(xq, wq, a, force_splits, stream)
                  : launch_decode<16, false>(xq, wq, a, force_splits, stream);
-  return ue8m0 ? launch_decode<32, true>(xq, wq, a, force_splits, stream)
-               : launch_decode<32, false>(xq, wq, a, force_splits, stream);
+  if (rows <= 32)
+    return ue8m0 ? launch_decode<32, true>(xq, wq, a, force_splits, stream)
+                 : launch_decode<32, false>(xq, wq, a, force_splits, stream);
+  if (rows <= 64)
+    return ue8m0 ? launch_decode<64, true>(xq, wq, a, force_splits, stream)
+                 : launch_decode<64, false>(xq, wq, a, force_splits, stream);
+  return ue8m0 ? launch_decode<128, true>(xq, wq, a, force_splits, stream)
+               : launch_decode<128, false>(xq, wq, a, force_splits, stream);
 }
 
 }  // namespace fp8rl

@@ -44,7 +44,7 @@
 namespace fp8rl {
 
 void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* status);  // static_scratch.cu
-// decode.cu: dense products with at most 32 rows, operands swapped (UNSUPPORTED: use this file's kernel)
+// decode.cu: dense products with at most 128 rows, operands swapped (UNSUPPORTED: use this file's kernel)
 fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale, void* y,
                          int64_t rows, int64_t n, int64_t k, bool ue8m0, uint32_t* err, uint64_t timeout_ns,
                          int fault_skip_kb, int force_splits, cudaStream_t stream);
@@ -1646,7 +1646,7 @@ struct Debug {
   int streamk = 0;                // with a workspace: 0 choose, 1 never, 2 always (dense, M > 32)
   int streamk_grid = 0;           // 0: one CTA per SM (at most one per K iteration); else this many
   int out_stage = 0;              // data-parallel tile stores: 0 choose, 1 through shared memory + TMA, 2 from registers
-  int decode = 0;                 // dense rows <= 32: 0 choose, 1 the swapped-operand decode kernel, 2 the 128-row-tile one
+  int decode = 0;                 // dense rows <= 128: 0 choose, 1 the swapped-operand decode kernel, 2 the 128-row-tile one
   int mx = 0;                     // UE8M0 data-parallel tiles: 0 the block-scaled MMA, 1 the per-chunk promotion
   int pair = 0;                   // dense data-parallel tiles on tensor-core pairs: 0 choose, 1 always, 2 never
   uint64_t timeout_ns = 2000000000ull;
@@ -1966,10 +1966,14 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   args.fault_skip_kb = dbg.fault_skip_kb;
   args.wait_mode = dbg.wait_mode;
   args.l2_prefetch = dbg.l2_prefetch;
-  // decode sizes (dense, at most 32 rows): the swapped-operand kernel of
-  // decode.cu (measured on GB300 at 17 and 32 rows, Qwen3-8B projections:
-  // 30-50% faster than the 128-row-tile kernel).  The test hook forces either.
-  const bool decode_shape = !d_offsets && rows <= 32;
+  // decode sizes (dense, at most 64 rows): the swapped-operand kernel of
+  // decode.cu (measured on GB300, Qwen3-8B projections with weights from
+  // HBM: 30-50% faster than the 128-row-tile kernel at 17 and 32 rows, 5-30%
+  // at 64).  Its 128-column form (one CTA per SM) is only as fast as the
+  // tile kernel at 128 rows and slower for wide weights, so 65..128 rows run
+  // there unless the test hook forces it; the hook also forces the tile
+  // kernel.
+  const bool decode_shape = !d_offsets && (rows <= 64 || (rows <= 128 && dbg.decode == 1));
   if (decode_shape && dbg.decode != 2 && dbg.streamk != 2) {
     const fp8rl_status st = decode_gemm(xq, x_scale, wq, w_scale, y, rows, n, k, fmt == FP8RL_SCALE_UE8M0, err,
                                         dbg.timeout_ns, dbg.fault_skip_kb, dbg.splits,

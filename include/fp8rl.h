@@ -408,9 +408,9 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          at most one per K iteration (1..1024);
  *   key 9  how data-parallel GEMM tiles are stored: 0 chooses per shape
  *          (default), 1 through shared memory and TMA stores, 2 from registers;
- *   key 10 dense GEMMs with at most 32 rows: 0 chooses (default: the
- *          swapped-operand decode kernel for <= 16 rows, or <= 32 when the
- *          weight has a 128-row block per SM), 1 always that kernel, 2 the
+ *   key 10 dense GEMMs with at most 128 rows: 0 chooses (default: the
+ *          swapped-operand decode kernel up to 64 rows, the 128-row-tile
+ *          kernel above), 1 the decode kernel up to 128 rows, 2 the
  *          128-row-tile kernel;
  *   key 11 UE8M0 GEMMs on whole tiles (data-parallel): 0 the tensor cores
  *          apply the power-of-two scales (block-scaled MMA, default), 1 the

@@ -180,14 +180,15 @@ def test_fused_epilogue_wait_runs_out_and_is_reported():
     assert np.all(np.abs(hs.cpu().numpy() - hs_ref) <= 1e-4 * hs_ref)
 
 
-@pytest.mark.parametrize("skip", [0, 7])
-def test_decode_wait_runs_out_and_is_reported(skip):
+@pytest.mark.parametrize("skip,m", [(0, 16), (7, 16), (3, 96)])
+def test_decode_wait_runs_out_and_is_reported(skip, m):
     """The decode-size GEMM launched behind the activation quantiser with
     overlapped launches: a chunk among the weight stages fetched before the
     wait for the quantiser (0) or one of the later ones (7) never arrives; the
     MMA's wait runs out, TIMEOUT is reported, and the next call is correct."""
-    m, n, k = 16, 256, 4096
+    n, k = 256, 4096
     x = synth.activation_bf16(m, k, 8, "fault-dx", device="cuda")
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, 1)
     w = synth.weight_bf16(n, k, 8, "fault-dw")
     wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w))
     dw, dsw = dev(wq, sw)

@@ -412,12 +412,17 @@ def decode_mode():
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("m,n,k,splits", [(16, 6144, 4096, 0), (1, 4096, 4096, 0), (32, 4096, 12288, 0),
                                           (17, 384, 640, 3), (5, 256, 1280, 8), (31, 128, 256, 2),
-                                          (16, 24576, 4096, 0)])
+                                          (16, 24576, 4096, 0),
+                                          # 64 and 128 token columns (forced: 33..128 rows)
+                                          (33, 384, 640, 3), (64, 4096, 4096, 0), (50, 256, 2048, 8),
+                                          (65, 6144, 4096, 0), (128, 4096, 12288, 0), (100, 128, 384, 2),
+                                          (128, 24576, 4096, 0)])
 def test_decode_kernel_matches_oracle_and_tile_kernel(m, n, k, splits, fmt, decode_mode):
     """At most 32 rows the dense GEMM runs the swapped-operand decode kernel
-    (weight rows as the MMA's M, tokens as its N, split K over a cluster);
-    within tolerance of the oracle over the whole output, and of the
-    128-row-tile kernel that the test hook selects instead."""
+    (weight rows as the MMA's M, tokens as its N, split K over a cluster),
+    and up to 128 when the test hook asks for it; within tolerance of the
+    oracle over the whole output, and of the 128-row-tile kernel that the
+    hook selects instead."""
     x = synth.activation_bf16(m, k, m + 3, "dec-x", n)
     w = synth.weight_bf16(n, k, k + 5, "dec-w")
     xq, sx, wq, sw = oracle_operands(x, w, fmt)

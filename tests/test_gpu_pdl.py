@@ -37,6 +37,7 @@ def _lib():
 def pdl_off():
     yield lambda off: fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 1 if off else 0)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 0)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, 0)
 
 
 def within(got, ref):
@@ -89,10 +90,12 @@ def host(bufs):
     return [(q.cpu().numpy(), s.cpu().numpy(), y.view(torch.int16).cpu().numpy()) for q, s, y in bufs]
 
 
-@pytest.mark.parametrize("m", [16, 1, 7])
+@pytest.mark.parametrize("m", [16, 1, 7, 40, 128])
 def test_chain_matches_oracle_on_its_own_intermediates(m, weights, pdl_off):
     fmt, layers = weights
     pdl_off(False)
+    if m > 32:  # the decode kernel's 64- and 128-column forms (test hook)
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, 1)
     x0 = synth.activation_bf16(m, CHAIN[0][1], 50 + m, "pdl-x", device="cuda")
     bufs = make_buffers(m, fmt, layers)
     poison(bufs)
