@@ -85,7 +85,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], grouped:gate_up|down, "
+                    help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], aqg:M:N:K[:fmt], grouped:gate_up|down, "
                          "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt], kv:TOKENS, "
                          "kvcal:TOKENS, moe_plan, moe_dispatch, moe_combine, tis[:RESPONSES]")
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
@@ -775,8 +775,11 @@ def section_decode_layer(torch, synth, fp8rl, dev, seed, peaks, m=16, layers=8):
     quantisation of its input (the attention and SwiGLU outputs that feed
     o_proj and down are synthetic stand-ins of their shapes), over `layers`
     layers' weights (1.5 GB of codes, far beyond L2), captured once in a CUDA
-    graph and replayed.  Timed with overlapped launches (the default: each
-    kernel starts while the one before it finishes) and without them."""
+    graph and replayed.  Timed as one fused call per projection
+    (fp8rl_gemm_act_quant), and as two calls (quantiser, GEMM) with
+    overlapped launches (the default: each kernel starts while the one before
+    it finishes) and without them.  The same algorithmic bytes for all three
+    (the fused form also writes the codes and scales out)."""
     gemms = synth.QWEN3_8B_GEMMS
     W = []
     for l in range(layers):
@@ -800,17 +803,24 @@ def section_decode_layer(torch, synth, fp8rl, dev, seed, peaks, m=16, layers=8):
                 fp8rl.fp8rl_quant_act_group(xs[k], m, k, k, qs[k], k, ss[k], 0)
                 fp8rl.fp8rl_gemm_blockscaled(qs[k], ss[k], wq, sw, ys[n], m, n, k, 0)
 
+    def run_fused():
+        for per in W:
+            for n, k, wq, sw in per:
+                fp8rl.fp8rl_gemm_act_quant(xs[k], k, wq, sw, ys[n], m, n, k, 0, qs[k], ss[k])
+
     per_layer = sum(gemm_bytes(m, n, k) + aq_bytes(m, k) for _, n, k in gemms)
-    launches = 2 * len(gemms)
-    res = {"m": m, "layers": layers, "bytes_per_layer": per_layer, "launches_per_layer": launches,
+    res = {"m": m, "layers": layers, "bytes_per_layer": per_layer,
            "l2": "weights of all layers (%.2f GB) far larger than L2" % (layers * per_layer / 1e9)}
     hooks = os.environ.get("FP8RL_TEST_HOOKS")
-    for label, off in (("overlapped", 0), ("serialised", 1)):
+    # two calls per projection (quantiser, GEMM) with and without overlapped
+    # launches, and the one-call fused form (overlapped)
+    for label, fn, off, launches in (("fused", run_fused, 0, len(gemms)), ("overlapped", run, 0, 2 * len(gemms)),
+                                     ("serialised", run, 1, 2 * len(gemms))):
         if off:
             os.environ["FP8RL_TEST_HOOKS"] = "1"
             fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 1)
         try:
-            ms = time_graph(torch, run, 1) / layers
+            ms = time_graph(torch, fn, 1) / layers
         finally:
             if off:
                 fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 0)
@@ -819,7 +829,7 @@ def section_decode_layer(torch, synth, fp8rl, dev, seed, peaks, m=16, layers=8):
                 else:
                     os.environ["FP8RL_TEST_HOOKS"] = hooks
         gbs = per_layer / ms / 1e6
-        res[label] = {"us_per_layer": ms * 1e3, "us_per_launch": ms * 1e3 / launches, "gbs": gbs,
+        res[label] = {"us_per_layer": ms * 1e3, "launches_per_layer": launches, "gbs": gbs,
                       "frac_hbm": gbs / peaks["hbm_gbs"]}
     return res
 
@@ -1133,6 +1143,19 @@ def main_case(args):
         sc = torch.empty(((k + 127) // 128, m), dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev)
         fn = lambda: fp8rl.fp8rl_quant_act_group(x, m, k, k, q, k, sc, fmt)
         work = {"bytes": aq_bytes(m, k, 4 if fmt == 0 else 1)}
+    elif kind == "aqg":
+        # the activation quantisation and the GEMM in one call (fp8rl_gemm_act_quant)
+        m, n, k = (int(v) for v in parts[1:4])
+        fmt = int(parts[4]) if len(parts) > 4 else 0
+        w = synth.weight_bf16(n, k, 0, "case-w", device=dev)
+        wq, sw = fp8rl.quant_weight(w, fmt)
+        del w
+        x = synth.activation_bf16(m, k, 0, "case-x", device=dev)
+        q = torch.empty((m, k), dtype=torch.uint8, device=dev)
+        sc = torch.empty((k // 128, m), dtype=torch.float32 if fmt == 0 else torch.uint8, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        fn = lambda: fp8rl.fp8rl_gemm_act_quant(x, k, wq, sw, y, m, n, k, fmt, q, sc)
+        work = {"bytes": gemm_bytes(m, n, k, 4 if fmt == 0 else 1) + aq_bytes(m, k, 4 if fmt == 0 else 1)}
     else:
         raise SystemExit(f"unknown case {args.case}")
     ms = time_loop(torch, fn, max(1, args.steps), args.warmup)

@@ -26,6 +26,7 @@ __all__ = [
     "fp8rl_quant_weight_blockwise", "fp8rl_quant_weight_blockwise_batched",
     "fp8rl_host_sync_staging_bytes", "fp8rl_quant_weight_host_batched",
     "fp8rl_quant_act_group", "fp8rl_gemm_blockscaled", "fp8rl_grouped_gemm_blockscaled",
+    "fp8rl_gemm_act_quant", "gemm_act_quant",
     "fp8rl_gemm_workspace_size", "fp8rl_gemm_blockscaled_ws", "gemm_workspace",
     "fp8rl_gemm_blockscaled_static", "fp8rl_gemm_swiglu_quant", "fp8rl_grouped_gemm_swiglu_quant",
     "gemm_swiglu_quant", "grouped_gemm_swiglu_quant", "quant_gate_up_interleaved",
@@ -87,6 +88,7 @@ def load_library(build_if_missing: bool = False):
             "fp8rl_quant_weight_host_batched": [ctypes.POINTER(WeightDesc), i32, st, vp, ctypes.c_size_t, i32, vp],
             "fp8rl_quant_act_group": [vp, i64, i64, i64, vp, i64, vp, st, vp],
             "fp8rl_gemm_blockscaled": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
+            "fp8rl_gemm_act_quant": [vp, i64, vp, vp, vp, i64, i64, i64, st, vp, vp, vp],
             "fp8rl_gemm_workspace_size": [ctypes.POINTER(ctypes.c_size_t)],
             "fp8rl_gemm_blockscaled_ws": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp, ctypes.c_size_t, vp],
             "fp8rl_gemm_blockscaled_static": [vp, vp, vp, vp, vp, i64, i64, i64, st, vp],
@@ -182,6 +184,13 @@ def fp8rl_gemm_blockscaled(xq, x_scale, wq, w_scale, y_bf16, m, n, k, fmt=SCALE_
     _ok(load_library().fp8rl_gemm_blockscaled(_p(xq), _p(x_scale), _p(wq), _p(w_scale),
                                               _p(y_bf16), m, n, k, fmt, _stream(stream)),
         "fp8rl_gemm_blockscaled")
+
+
+def fp8rl_gemm_act_quant(x_bf16, ldx, wq, w_scale, y_bf16, m, n, k, fmt, xq, x_scale,
+                         stream=None) -> None:
+    _ok(load_library().fp8rl_gemm_act_quant(_p(x_bf16), ldx, _p(wq), _p(w_scale), _p(y_bf16), m, n, k,
+                                            fmt, _p(xq), _p(x_scale), _stream(stream)),
+        "fp8rl_gemm_act_quant")
 
 
 def fp8rl_gemm_workspace_size() -> int:
@@ -459,6 +468,21 @@ def gemm(xq, x_scale, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None, worksp
         fp8rl_gemm_blockscaled_ws(xq, x_scale, wq, w_scale, out, m, n, k, fmt, workspace,
                                   workspace.numel() * workspace.element_size(), stream)
     return out
+
+
+def gemm_act_quant(x, wq, w_scale, fmt=SCALE_FP32, out=None, stream=None):
+    """bf16 Y [m, n] = X W^T with X (bf16 [m, k]) quantised 1x128 on the way,
+    plus the codes and scales (the results of quant_act(x) then gemm)."""
+    _check_cuda(x, wq, w_scale, out)
+    _check_bf16_2d(x, "x")
+    m, k = x.shape
+    n = wq.shape[0]
+    if out is None:
+        out = _out((m, n), torch.bfloat16, x.device)
+    xq = _out((m, k), torch.uint8, x.device)
+    sx = _out(((k + 127) // 128, m), _scale_dtype(fmt), x.device)
+    fp8rl_gemm_act_quant(x, x.stride(0), wq, w_scale, out, m, n, k, fmt, xq, sx, stream)
+    return out, xq, sx
 
 
 def grouped_gemm(xq, x_scale, wq, w_scale, d_offsets, fmt=SCALE_FP32, out=None, stream=None):

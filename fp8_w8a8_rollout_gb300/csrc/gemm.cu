@@ -48,6 +48,11 @@ void* static_gemm_scratch(size_t need_bytes, size_t clear_bytes, fp8rl_status* s
 fp8rl_status decode_gemm(const void* xq, const void* x_scale, const void* wq, const void* w_scale, void* y,
                          int64_t rows, int64_t n, int64_t k, bool ue8m0, uint32_t* err, uint64_t timeout_ns,
                          int fault_skip_kb, int force_splits, cudaStream_t stream);
+// decode.cu: the same with the 1x128 activation quantisation inside (at most 16 rows)
+fp8rl_status decode_gemm_qx(const void* x_bf16, int64_t ldx, const void* wq, const void* w_scale, void* y,
+                            int64_t rows, int64_t n, int64_t k, bool ue8m0, void* xq_out, void* sx_out,
+                            uint32_t* err, uint64_t timeout_ns, int fault_skip_kb, int force_splits,
+                            cudaStream_t stream);
 
 namespace {
 
@@ -2130,6 +2135,28 @@ fp8rl_status run_swiglu(const void* xq, const void* x_scale, const void* wq, con
 
 bool pdl_enabled() { return g_pdl_off.load() == 0; }
 
+namespace {
+
+// fp8rl_gemm_act_quant at decode sizes: one kernel that quantises X and
+// multiplies; UNSUPPORTED when the shape or layout needs the two-call path
+fp8rl_status run_act_quant_fused(const void* x_bf16, int64_t ldx, const void* wq, const void* w_scale, void* y,
+                                 int64_t m, int64_t n, int64_t k, fp8rl_scale_fmt fmt, void* xq, void* x_scale,
+                                 void* stream) {
+  const DeviceInfo di = device_info();
+  if (!di.ok) return FP8RL_ERR_UNSUPPORTED;
+  Debug dbg;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    dbg = g_debug;
+  }
+  if (m > 16 || dbg.decode == 2 || dbg.streamk == 2) return FP8RL_ERR_UNSUPPORTED;
+  uint32_t* err = device_error_word();
+  if (!err) return FP8RL_ERR_CUDA;
+  return decode_gemm_qx(x_bf16, ldx, wq, w_scale, y, m, n, k, fmt == FP8RL_SCALE_UE8M0, xq, x_scale, err,
+                        dbg.timeout_ns, dbg.fault_skip_kb, dbg.splits, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
 }  // namespace fp8rl
 
 using namespace fp8rl;
@@ -2140,6 +2167,23 @@ extern "C" FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const v
                                                          fp8rl_scale_fmt fmt, void* stream) {
   fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, m, n, k, fmt);
   if (st != FP8RL_OK || m == 0 || n == 0) return st;
+  return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream);
+}
+
+extern "C" FP8RL_API fp8rl_status fp8rl_gemm_act_quant(const void* x_bf16, int64_t ldx, const void* wq,
+                                                       const void* w_scale, void* y, int64_t m, int64_t n,
+                                                       int64_t k, fp8rl_scale_fmt fmt, void* xq, void* x_scale,
+                                                       void* stream) {
+  fp8rl_status st = check_gemm(xq, x_scale, wq, w_scale, y, m, n, k, fmt);
+  if (st != FP8RL_OK || m == 0) return st;
+  if (!x_bf16 || ldx < k) return FP8RL_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 2)) return FP8RL_ERR_ALIGNMENT;
+  if (n > 0) {
+    st = run_act_quant_fused(x_bf16, ldx, wq, w_scale, y, m, n, k, fmt, xq, x_scale, stream);
+    if (st != FP8RL_ERR_UNSUPPORTED) return st;
+  }
+  st = fp8rl_quant_act_group(x_bf16, m, k, ldx, xq, k, x_scale, fmt, stream);
+  if (st != FP8RL_OK || n == 0) return st;
   return run(xq, x_scale, wq, w_scale, nullptr, 1, m, n, k, y, fmt, stream);
 }
 

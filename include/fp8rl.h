@@ -37,9 +37,9 @@
  *     NULL is the legacy default stream).  Results are ready once the stream
  *     is synchronised.
  *   - Overlapped launches: fp8rl_quant_act_group and the GEMMs at decode
- *     sizes (dense, m <= 32) are launched with programmatic stream
- *     serialisation, and let the next kernel of the stream start before they
- *     complete.  Such a kernel may begin while the kernel before it on the
+ *     sizes (dense, m <= 64; fp8rl_gemm_act_quant at m <= 16) are launched
+ *     with programmatic stream serialisation, and let the next kernel of the
+ *     stream start before they complete.  Such a kernel may begin while the kernel before it on the
  *     stream is still running; it waits for that kernel's completion before
  *     it reads any activation or scale of X and before it writes anything,
  *     but the decode GEMM reads its first weight tiles (wq) before that wait.
@@ -236,6 +236,33 @@ FP8RL_API fp8rl_status fp8rl_gemm_blockscaled(const void* xq, const void* x_scal
                                               const void* w_scale, void* y_bf16, int64_t m,
                                               int64_t n, int64_t k, fp8rl_scale_fmt fmt,
                                               void* stream);
+
+/*
+ * The activation quantisation and the block-scaled GEMM in one call: X (bf16)
+ * is quantised in 1x128 groups exactly as fp8rl_quant_act_group quantises it
+ * (its codes and scales are written to xq and x_scale), and Y = X W^T is
+ * computed from them exactly as fp8rl_gemm_blockscaled computes it, so the
+ * results are bit for bit those of the two calls ("Method steps", step 1:
+ * activations quantised dynamically in every forward pass, then the W8A8
+ * linear).  At decode sizes (m <= 16, ldx a multiple of 8, X 16-byte
+ * aligned) one kernel does both: it quantises each 128-wide chunk of X as it
+ * streams the weights (one launch instead of two; measured on GB300 as fast
+ * as the two overlapped launches over a Qwen3-8B decode layer, faster for
+ * the smaller projections, slower for the wide gate-up); otherwise the call
+ * runs the two kernels.
+ *   x_bf16   device, bf16 [m][k], row stride ldx elements (ldx >= k)
+ *   wq, w_scale, y_bf16, m, n, k, fmt   as fp8rl_gemm_blockscaled
+ *   xq       device, E4M3 [m][k] row-major (row stride k), 16-byte aligned:
+ *            receives the activation codes
+ *   x_scale  device, [k/128][m], fp32 or uint8 (fmt): receives the scales
+ * Errors: as fp8rl_gemm_blockscaled (xq and x_scale are checked as its X
+ * operands), INVALID_ARG for a null x_bf16 or ldx < k.  n == 0 quantises X
+ * only; m == 0 is a no-op.
+ */
+FP8RL_API fp8rl_status fp8rl_gemm_act_quant(const void* x_bf16, int64_t ldx, const void* wq,
+                                            const void* w_scale, void* y_bf16, int64_t m, int64_t n,
+                                            int64_t k, fp8rl_scale_fmt fmt, void* xq, void* x_scale,
+                                            void* stream);
 
 /*
  * Fused gate-up projection of a gated MLP: the block-scaled GEMM against the

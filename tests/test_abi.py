@@ -185,6 +185,22 @@ def test_gemm_rejects_bad_shapes_and_alignment_on_host(lib):
     assert _rc(g, a16, a16, a16, a16, a16, 0, 256, 256, 0, None) == 0  # m == 0: no-op
 
 
+def test_act_quant_gemm_rejects_bad_arguments_on_host(lib):
+    """fp8rl_gemm_act_quant(x, ldx, wq, w_scale, y, m, n, k, fmt, xq, x_scale,
+    stream): the GEMM's checks on its X operands (xq, x_scale), plus x and
+    ldx; nothing is launched."""
+    a16 = 1 << 20
+    g = "fp8rl_gemm_act_quant"
+    assert _rc(g, None, 256, a16, a16, a16, 16, 256, 256, 0, a16, a16, None) == 1  # x null
+    assert _rc(g, a16, 200, a16, a16, a16, 16, 256, 256, 0, a16, a16, None) == 1  # ldx < k
+    assert _rc(g, a16 + 1, 256, a16, a16, a16, 16, 256, 256, 0, a16, a16, None) == 3  # x not 2-byte aligned
+    assert _rc(g, a16, 256, a16, a16, a16, 16, 256, 256, 0, None, a16, None) == 1  # xq null
+    assert _rc(g, a16, 256, a16, a16, a16, 16, 256, 256, 0, a16 + 8, a16, None) == 3  # xq alignment
+    assert _rc(g, a16, 256, a16, a16, a16, 16, 200, 256, 0, a16, a16, None) == 2  # n % 128
+    assert _rc(g, a16, 256, a16, a16, a16, 16, 256, 256, 7, a16, a16, None) == 1  # fmt
+    assert _rc(g, a16, 256, a16, a16, a16, 0, 256, 256, 0, a16, a16, None) == 0  # m == 0: no-op
+
+
 def test_workspace_gemm_rejects_bad_arguments_on_host(lib):
     a16 = 1 << 20
     g = "fp8rl_gemm_blockscaled_ws"
