@@ -44,11 +44,11 @@ STEP_M = 8192          # tokens in the step's forward batch
 # Reported only while the GEMM's sources are those the capture was taken with.
 TRAFFIC = {
     "gemm_gate_up": {
-        "bytes": 146.822656e6 + 372.616448e6,
+        "bytes": 147.116032e6 + 372.525056e6,
         "sources": {
-            "gemm.cu": "14272a7d089d2260ff2dd5cf534137002600e1065342d118dfa950517a143383",
-            "ptx.cuh": "463915e06bd7baebb37b3b835d1bf73d06ee907eb2d78aaedc6a2c8c07e89cbe",
-            "common.cuh": "ce22f13b50d69d05f583fb60eb22375700c10e0326d46e23e9ac29b79ecfa620",
+            "gemm.cu": "4b00e02870e48c1d6f51bdd7211e56cc0fc99c2668a99dde5f393fa386493f7a",
+            "ptx.cuh": "7611be7f4488dec541b5332e198986f65689abe958fd940e526f41325f47e1be",
+            "common.cuh": "6401f31a7a6a92810a87d55c9eae24512fe80ad094dc69922897bb43c8e0894d",
         },
     },
 }
