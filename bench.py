@@ -85,7 +85,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], aqg:M:N:K[:fmt], grouped:gate_up|down, "
+                    help="time one kernel alone (for profiling): gemm:M:N:K[:fmt], aqg:M:N:K[:fmt], grouped:gate_up|down[:fmt], "
                          "wq:layer[:fmt], aq:M:K[:fmt], fused:M[:fmt], fused_moe[:fmt], kv:TOKENS, "
                          "kvcal:TOKENS, moe_plan, moe_dispatch, moe_combine, tis[:RESPONSES]")
     ap.add_argument("--bn", type=int, default=0, help="with --case: force the GEMM tile width (128 or 256)")
@@ -100,7 +100,7 @@ def parse():
     ap.add_argument("--pair", type=int, default=0,
                     help="with --case: dense tiles on tensor-core pairs, 0 chosen, 1 always, 2 never")
     ap.add_argument("--mx", type=int, default=0,
-                    help="with --case: UE8M0 whole tiles, 0 block-scaled MMA, 1 per-chunk promotion")
+                    help="with --case: UE8M0 whole tiles, 0 chosen by K, 1 per-chunk promotion, 2 block-scaled MMA")
     ap.add_argument("--no-overlap", action="store_true",
                     help="with --case: launch the activation quantiser and decode GEMM without overlap")
     return ap.parse_args()
@@ -593,6 +593,29 @@ def section_ue8m0(torch, synth, fp8rl, dev, seed, peaks, have_gemm):
     if have_gemm:
         res["gemm"] = section_sweep_one(torch, synth, fp8rl, dev, seed, peaks, "gate_up", 24576, 4096,
                                         STEP_M, 1)
+        # the MoE expert pair (T = 4096, top-8) with UE8M0 scales, against the
+        # same pair with fp32 scales
+        _, offsets, _, _, rows = moe_plan_for(torch, synth, fp8rl, dev, seed)
+        for which in ("gate_up", "down"):
+            n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
+            wb = synth.moe_expert_weights(n, k, synth.MOE_EXPERTS, seed, 0, which, device=dev)
+            x = synth.normal_bf16((rows, k), 1.0, seed, "ue8m0-moe-x", which, device=dev)
+            y = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
+            entry = {"rows": rows, "n": n, "k": k}
+            for fmt, label in ((1, "ue8m0"), (0, "fp32")):
+                wq, sw = fp8rl.quant_weight(wb.view(-1, k), fmt)
+                xq, sx = fp8rl.quant_act(x, fmt)
+                fn = lambda: fp8rl.fp8rl_grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, synth.MOE_EXPERTS, rows,
+                                                                  n, k, y, fmt)
+                ms = time_loop(torch, fn, 20, 5)
+                sb = 4 if fmt == 0 else 1
+                b = synth.MOE_EXPERTS * (n * k + sb * (n // 128) * (k // 128)) + rows * k + 2 * rows * n + \
+                    sb * rows * (k // 128)
+                entry[label] = {"ms": ms, "gbs": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"],
+                                "tflops": gemm_flops(rows, n, k) / ms / 1e9}
+                del wq, sw, xq, sx
+            res[f"moe_{which}_t{MOE_T}"] = entry
+            del wb, x, y
     return res
 
 
@@ -1078,17 +1101,22 @@ def main_case(args):
         work = gemm_roof(gemm_flops(m, n, k), gemm_bytes(m, n, k), 1.0, peaks["hbm_gbs"], fp8)
     elif kind == "grouped":
         which = parts[1]
+        fmt = int(parts[2]) if len(parts) > 2 else 0
         n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
         _, offsets, _, _, rows = moe_plan_for(torch, synth, fp8rl, dev, 0)
         wb = synth.moe_expert_weights(n, k, synth.MOE_EXPERTS, 0, 0, which, device=dev)
-        wq, sw = fp8rl.quant_weight(wb.view(-1, k))
+        wq, sw = fp8rl.quant_weight(wb.view(-1, k), fmt)
         wq = wq.view(synth.MOE_EXPERTS, n, k)
         sw = sw.view(synth.MOE_EXPERTS, n // 128, k // 128)
         x = synth.normal_bf16((rows, k), 1.0, 0, "case-x", device=dev)
-        xq, sx = fp8rl.quant_act(x)
+        xq, sx = fp8rl.quant_act(x, fmt)
         y = torch.empty((rows, n), dtype=torch.bfloat16, device=dev)
-        fn = lambda: fp8rl.fp8rl_grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, synth.MOE_EXPERTS, rows, n, k, y)
-        work = {"flops": gemm_flops(rows, n, k)}
+        fn = lambda: fp8rl.fp8rl_grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, synth.MOE_EXPERTS, rows, n, k, y,
+                                                          fmt)
+        sb = 4 if fmt == 0 else 1
+        work = {"flops": gemm_flops(rows, n, k),
+                "bytes": synth.MOE_EXPERTS * (n * k + sb * (n // 128) * (k // 128)) + rows * k + 2 * rows * n
+                + sb * rows * (k // 128)}
     elif kind in ("fused", "fused_moe"):
         fmt = int(parts[-1]) if (kind == "fused" and len(parts) > 2) or (kind == "fused_moe" and len(parts) > 1) else 0
         d = fused_mlp_inputs(torch, synth, fp8rl, dev, 0, int(parts[1]) if kind == "fused" else 0, fmt,

@@ -1652,7 +1652,7 @@ struct Debug {
   int streamk_grid = 0;           // 0: one CTA per SM (at most one per K iteration); else this many
   int out_stage = 0;              // data-parallel tile stores: 0 choose, 1 through shared memory + TMA, 2 from registers
   int decode = 0;                 // dense rows <= 128: 0 choose, 1 the swapped-operand decode kernel, 2 the 128-row-tile one
-  int mx = 0;                     // UE8M0 data-parallel tiles: 0 the block-scaled MMA, 1 the per-chunk promotion
+  int mx = 0;                     // UE8M0 data-parallel tiles: 0 choose, 1 the per-chunk promotion, 2 the block-scaled MMA
   int pair = 0;                   // dense data-parallel tiles on tensor-core pairs: 0 choose, 1 always, 2 never
   uint64_t timeout_ns = 2000000000ull;
 };
@@ -2016,7 +2016,12 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   const bool short_a = !d_offsets && rows <= 32;
   // dense UE8M0 products with more than one m-tile and 256-wide weight
   // blocks: tiles of 256 x 256 on tensor-core pairs (clusters of two CTAs)
-  const bool pair_ok = ue && dbg.mx != 1 && !d_offsets && n % 256 == 0 && rows > kBM && !short_a;
+  // UE8M0 on the block-scaled MMA (one accumulator per tile) unless K is
+  // short: measured on GB300, the MoE expert pair (T = 4096) gate-up at
+  // K = 2048 126 vs 142 us, but down at K = 768 112 vs 94 us (six chunks a
+  // tile leave the scale-factor writes and the register stores exposed)
+  const bool mx = ue && (dbg.mx == 2 || (dbg.mx == 0 && num_kb >= 16));
+  const bool pair_ok = mx && !d_offsets && n % 256 == 0 && rows > kBM && !short_a;
   if (pair_ok && dbg.pair == 1) {
     const fp8rl_status st = launch_pair(xq, wq, args, cs);
     if (st != FP8RL_ERR_UNSUPPORTED) return st;
@@ -2066,7 +2071,7 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   // than the store they save (measured on GB300: 8192 x 24576 x 4096 +6%,
   // 1024 x 6144 x 4096 +5%, grouped MoE +5..14%; 8192 x 4096 x 12288 -3%).
   const bool staged = dbg.out_stage == 1 || (dbg.out_stage != 2 && k <= 4096);
-  if (ue && dbg.mx != 1) {
+  if (mx) {
     // UE8M0: the tensor cores apply the power-of-two scales themselves
     // (block-scaled MMA), one accumulator per tile; the tile stores stay in
     // the epilogue's registers (measured on GB300: 8192 x 24576 x 4096 0.559
@@ -2316,7 +2321,7 @@ extern "C" FP8RL_API fp8rl_status fp8rl_debug_set(int32_t key, int64_t value) {
       g_debug.decode = (int)value;
       return FP8RL_OK;
     case 11:
-      if (value < 0 || value > 1) return FP8RL_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return FP8RL_ERR_INVALID_ARG;
       g_debug.mx = (int)value;
       return FP8RL_OK;
     case 12:

@@ -439,9 +439,10 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          swapped-operand decode kernel up to 64 rows, the 128-row-tile
  *          kernel above), 1 the decode kernel up to 128 rows, 2 the
  *          128-row-tile kernel;
- *   key 11 UE8M0 GEMMs on whole tiles (data-parallel): 0 the tensor cores
- *          apply the power-of-two scales (block-scaled MMA, default), 1 the
- *          per-chunk fp32 promotion in the epilogue (the fp32-scale path);
+ *   key 11 UE8M0 GEMMs on whole tiles (data-parallel): 0 chooses (default:
+ *          the tensor cores apply the power-of-two scales, block-scaled MMA,
+ *          when K >= 2048; below, the per-chunk fp32 promotion), 1 always the
+ *          promotion (the fp32-scale path), 2 always the block-scaled MMA;
  *   key 12 dense data-parallel GEMMs on tensor-core pairs (256 x 256 tiles
  *          over clusters of two CTAs): 0 chooses per shape (default), 1
  *          always where the shape allows (n a multiple of 256, m > 128), 2

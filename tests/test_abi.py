@@ -264,7 +264,8 @@ def test_debug_hook_validates_on_host(lib):
     assert _rc("fp8rl_debug_set", 9, 1) == 0
     assert _rc("fp8rl_debug_set", 10, 3) == 1
     assert _rc("fp8rl_debug_set", 10, 2) == 0
-    assert _rc("fp8rl_debug_set", 11, 2) == 1
+    assert _rc("fp8rl_debug_set", 11, 3) == 1
+    assert _rc("fp8rl_debug_set", 11, 2) == 0
     assert _rc("fp8rl_debug_set", 11, 1) == 0
     assert _rc("fp8rl_debug_set", 12, 3) == 1
     assert _rc("fp8rl_debug_set", 12, 1) == 0

@@ -71,6 +71,7 @@ def test_pair_wait_runs_out_and_is_reported(skip):
     xq, sx = oracle.quant_act_group(synth.bf16_bits(x), fmt)
     wq, sw = oracle.quant_weight_blockwise(synth.bf16_bits(w), fmt)
     dx, dsx, dw, dsw = dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 2)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 1)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_TIMEOUT_NS, 50_000_000)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_FAULT_SKIP_KB, skip)

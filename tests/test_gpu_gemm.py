@@ -450,10 +450,10 @@ def test_decode_kernel_is_deterministic(decode_mode):
 
 # --------------------------------------------------------------------------- UE8M0 on the block-scaled MMA
 
-@pytest.fixture(params=[0, 1], ids=["mx", "promote"])
+@pytest.fixture(params=[2, 1], ids=["mx", "promote"])
 def mx_mode(request):
-    """UE8M0 tiles on the tensor cores' block-scaled MMA (0, the default) or on
-    the per-chunk fp32 promotion (1)."""
+    """UE8M0 tiles on the tensor cores' block-scaled MMA (2; the default for
+    K >= 2048) or on the per-chunk fp32 promotion (1)."""
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, request.param)
     yield request.param
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 0)
@@ -527,10 +527,10 @@ def test_ue8m0_paths_match_oracle(m, n, k, bn, mx_mode):
 
 
 @pytest.mark.parametrize("which", ["gate_up", "down"])
-def test_grouped_ue8m0_qwen3_30b_a3b_sampled(which):
+def test_grouped_ue8m0_qwen3_30b_a3b_sampled(which, mx_mode):
     """The Qwen3-30B-A3B-shaped expert layer (128 experts, 32768 routed rows)
-    with UE8M0 scales on the block-scaled MMA: first and last row of every
-    non-empty segment plus 4096 random outputs."""
+    with UE8M0 scales, on the block-scaled MMA and on the per-chunk promotion:
+    first and last row of every non-empty segment plus 4096 random outputs."""
     fmt = fp8rl.SCALE_UE8M0
     n, k = (2 * synth.MOE_INTER, synth.MOE_HIDDEN) if which == "gate_up" else (synth.MOE_HIDDEN, synth.MOE_INTER)
     r = synth.moe_routing(4096, synth.MOE_EXPERTS, synth.MOE_TOPK, 3, 0)
@@ -557,10 +557,13 @@ def test_grouped_ue8m0_qwen3_30b_a3b_sampled(which):
 @pytest.fixture(params=[1, 2], ids=["pair", "single"])
 def pair_mode(request):
     """Dense UE8M0 tiles forced onto tensor-core pairs (1) or kept on single
-    CTAs (2), both on the block-scaled MMA."""
+    CTAs (2), both on the block-scaled MMA (forced: short K chooses the
+    per-chunk promotion)."""
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 2)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, request.param)
     yield request.param
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 0)
 
 
 @pytest.mark.parametrize("m,n,k", [(300, 512, 512),     # second pair: rows 256..299 in its even CTA only
@@ -597,6 +600,7 @@ def test_pair_qwen3_8b_m8192_sampled(name, n, k):
     """The full-size UE8M0 launches on tensor-core pairs (forced): 4 whole
     rows and 4096 random outputs against the oracle."""
     m = 8192
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 2)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 1)
     try:
         x = synth.activation_bf16(m, k, 16, "pair-big", name)
@@ -605,6 +609,7 @@ def test_pair_qwen3_8b_m8192_sampled(name, n, k):
         y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_UE8M0)
     finally:
         fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 0)
     rr, cc = sample_positions(m, n, 4, 4096, n + k)
     within(y[rr, cc], oracle.gemm_blockscaled_at(xq, sx, wq, sw, rr, cc, fp8rl.SCALE_UE8M0))
 
@@ -615,10 +620,12 @@ def test_pair_is_deterministic():
     w = synth.weight_bf16(n, k, 19, "pair-det")
     xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_UE8M0)
     dx, dsx, dw, dsw = to_dev(xq, sx, wq, sw)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 2)
     fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 1)
     try:
         ys = [fp8rl.gemm(dx, dsx, dw, dsw, fp8rl.SCALE_UE8M0) for _ in range(3)]
         assert fp8rl.fp8rl_sync_status() == 0
     finally:
         fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PAIR, 0)
+        fp8rl.fp8rl_debug_set(fp8rl.DEBUG_MX, 0)
     assert all(torch.equal(ys[0].view(torch.int16), y.view(torch.int16)) for y in ys[1:])
