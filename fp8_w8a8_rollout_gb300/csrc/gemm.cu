@@ -98,7 +98,8 @@ struct Cfg {
   // operand stages: as many as fit in about 200 KB of shared memory, or, with
   // the output slots, in the 227 KB a CTA may use
   static constexpr int kStagesFit =
-      OUT ? (227 * 1024 - 3 * 1024 - 1024 - kOutBytes - kScaleRingBytes - (EPI ? 2 * 4 * 128 * 4 : 0)) /
+      OUT ? (227 * 1024 - 3 * 1024 - 1024 - kOutBytes - kScaleRingBytes - (EPI ? 2 * 4 * 128 * 4 : 0) -
+             3 * 256 * 4) /
                 kStageBytesRaw
           : (200 * 1024) / kStageBytesRaw;
   static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
@@ -115,7 +116,8 @@ struct Cfg {
   static constexpr int kBookBytes = 1024;  // barriers and small shared state
   // fused epilogue: per-row maxima of the four column slices, two tiles deep
   static constexpr int kRedBytes = EPI ? 2 * 4 * kBM * 4 : 0;
-  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleRingBytes + kRedBytes;
+  static constexpr int kTileCacheBytes = 3 * 256 * 4;  // grouped: the experts' segments (TileMap)
+  static constexpr int kSharedEnd = kStages * kStageBytes + kBookBytes + kScaleRingBytes + kRedBytes + kTileCacheBytes;
   static constexpr int kOutOffset = (kSharedEnd + 1023) / 1024 * 1024;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kSmemBytes = 1024 + (OUT ? kOutOffset + kOutBytes : kSharedEnd);
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -346,6 +348,74 @@ __device__ __forceinline__ int count_m_tiles(const GemmArgs& a, int lane) {
   return total;
 }
 
+// Grouped products with at most kTileCacheExperts experts keep each expert's
+// segment (start, end) and the running count of m-tiles in shared memory,
+// built once per CTA, so that every role finds a tile's rows with a binary
+// search there instead of a scan over the offsets in global memory per tile
+// (measured on GB300: the scan's round trips stalled the producer at every
+// tile boundary of the MoE expert GEMMs).
+constexpr int kTileCacheExperts = 256;
+struct TileMap {
+  // shared-memory address of [0, E) segment starts (clamped as in
+  // tile_rows), [E, 2E) segment ends, [2E, 3E) m-tiles of experts 0..e,
+  // E = kTileCacheExperts
+  uint32_t t;
+  bool cached;
+  __device__ __forceinline__ int get(int i) const {
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(t + 4u * (uint32_t)i));
+    return v;
+  }
+  __device__ __forceinline__ void put(int i, int v) const {
+    asm volatile("st.shared.s32 [%0], %1;" ::"r"(t + 4u * (uint32_t)i), "r"(v) : "memory");
+  }
+  __device__ __forceinline__ int start(int e) const { return get(e); }
+  __device__ __forceinline__ int end(int e) const { return get(kTileCacheExperts + e); }
+  __device__ __forceinline__ int incl(int e) const { return get(2 * kTileCacheExperts + e); }
+};
+
+// fills the map (warp-collective; one warp) and returns the m-tile count
+__device__ __forceinline__ int build_tile_map(const GemmArgs& a, const TileMap& tm, int lane) {
+  int carry = 0;
+  for (int e0 = 0; e0 < a.experts; e0 += 32) {
+    const int ex = e0 + lane;
+    int start = 0, end = 0;
+    if (ex < a.experts) {
+      start = min(max(a.offsets[ex], 0), a.rows);
+      end = min(max(a.offsets[ex + 1], 0), a.rows);
+      end = max(end, start);
+    }
+    const int tiles = (end - start + kBM - 1) / kBM;
+    int incl = tiles;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (ex < a.experts) {
+      tm.put(ex, start);
+      tm.put(kTileCacheExperts + ex, end);
+      tm.put(2 * kTileCacheExperts + ex, carry + incl);
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return carry;
+}
+
+// tile_rows from the map: the expert is the first whose running tile count
+// exceeds m_idx (experts without tiles never are); not warp-collective
+__device__ __forceinline__ TileRows tile_rows_cached(const GemmArgs& a, const TileMap& tm, int m_idx) {
+  int lo = 0, hi = a.experts - 1;
+  if (hi < 0 || tm.incl(hi) <= m_idx) return TileRows{-1, 0, 0};
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (tm.incl(mid) > m_idx) hi = mid; else lo = mid + 1;
+  }
+  const int start = tm.start(lo), end = tm.end(lo);
+  const int tiles = (end - start + kBM - 1) / kBM;
+  return TileRows{lo, start + (m_idx - (tm.incl(lo) - tiles)) * kBM, end};
+}
+
 // AROWS < 128 (decode-sized M, at most AROWS rows in the only m-tile): each
 // stage holds just AROWS activation rows; the M = 128 MMA reads the rest of
 // its A rows from whatever shared memory follows, which only feeds accumulator
@@ -385,6 +455,13 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   uint32_t* shared_epoch = reinterpret_cast<uint32_t*>(shared_m_tiles + 1);
   float* scale_ring = reinterpret_cast<float*>(base_ptr + C::kStages * C::kStageBytes + C::kBookBytes);
   float* row_max = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scale_ring) + C::kScaleRingBytes);  // EPI 1
+  // (the map is rebuilt from base_ptr and the parameters at each use, so it
+  // holds no registers across the role loops)
+#define FP8RL_TMAP                                                                                    \
+  TileMap {                                                                                           \
+    base + (uint32_t)(C::kStages * C::kStageBytes + C::kBookBytes + C::kScaleRingBytes + C::kRedBytes), \
+        a.offsets != nullptr && a.experts <= kTileCacheExperts                                        \
+  }
   uint8_t* out_slots = base_ptr + C::kOutOffset;                         // OUT only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -400,7 +477,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   const int nloc = (int)((int64_t)num_kb * (split + 1) / splits) - kb_lo;
 
   if (warp == 0) {
-    const int mt = SPLITK ? 0 : count_m_tiles(a, lane);
+    const int mt = SPLITK ? 0 : (FP8RL_TMAP.cached ? build_tile_map(a, FP8RL_TMAP, lane) : count_m_tiles(a, lane));
     if (lane == 0) *shared_m_tiles = mt;
   }
   if (threadIdx.x == 32) {
@@ -516,7 +593,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
             int m_idx, n_tile;
             tile_coords(t, m_idx, n_tile);
-            const TileRows tr = tile_rows(a, m_idx, lane);
+            const TileRows tr = (FP8RL_TMAP.cached ? tile_rows_cached(a, FP8RL_TMAP, m_idx) : tile_rows(a, m_idx, lane));
             if (lane == 0) {
               const int wrow0 = tr.expert * a.n + n_tile * BN;
               for (int it = 0; it < nloc; ++it, ++g) {
@@ -652,6 +729,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           for (int t = first_tile; t < total_tiles && alive; t += tile_stride) {
             int m_idx, n_tile;
             tile_coords(t, m_idx, n_tile);
+            // (the scan: the map's lookup would not fit the role warps'
+            // registers here, and this warp runs kScaleSlots chunks ahead)
             const TileRows tr = tile_rows(a, m_idx, lane);
             const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
             // batches of kLoadBatch chunks: all their loads first, then the stores
@@ -711,7 +790,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
         for_each_segment<MODE>(sched0, total_tiles, [&](int t, int lo, int nseg) {
           int m_idx, n_tile;
           tile_coords(t, m_idx, n_tile);
-          const TileRows tr = tile_rows(a, m_idx, lane);
+          const TileRows tr = (FP8RL_TMAP.cached ? tile_rows_cached(a, FP8RL_TMAP, m_idx) : tile_rows(a, m_idx, lane));
           if (lane == 0) {
             const int wrow0 = tr.expert * a.n + n_tile * BN;
             for (int it = 0; it < nseg; ++it, ++g) {
@@ -798,7 +877,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
         for_each_segment<MODE>(sched0, total_tiles, [&](int t, int lo, int nseg) {
           int m_idx, n_tile;
           tile_coords(t, m_idx, n_tile);
-          const TileRows tr = tile_rows(a, m_idx, lane);
+          const TileRows tr = (FP8RL_TMAP.cached ? tile_rows_cached(a, FP8RL_TMAP, m_idx) : tile_rows(a, m_idx, lane));
           const int64_t sw_row = ((int64_t)tr.expert * (a.n / 128) + (n_tile * BN >> 7)) * num_kb;
           // batches of kLoadBatch chunks: all their loads first, then the stores
           constexpr int kLoadBatch = 4;
@@ -904,7 +983,7 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
           const int tseq = (int)(c / (uint32_t)num_kb), kbc = (int)(c - (uint32_t)tseq * (uint32_t)num_kb);
           int mi, nt;
           tile_coords((int)blockIdx.x + tseq * (int)gridDim.x, mi, nt);
-          const TileRows st = tile_rows(a, mi, lane);  // warp-collective
+          const TileRows st = (FP8RL_TMAP.cached ? tile_rows_cached(a, FP8RL_TMAP, mi) : tile_rows(a, mi, lane));  // warp-collective
           const int srow = st.row0 + quad * 32 + lane;
           if (srow < st.seg_end) {
             const int64_t xi = (int64_t)kbc * a.rows + srow;
@@ -946,7 +1025,10 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
       const int nseg = hi - lo;
       int m_idx, n_tile;
       tile_coords(t, m_idx, n_tile);
-      const TileRows tr = tile_rows(a, m_idx, lane);
+      // (the fused epilogue keeps the scan: the map's lookup would not leave
+      // it the registers it holds)
+      const TileRows tr =
+          (EPI == 0 && FP8RL_TMAP.cached) ? tile_rows_cached(a, FP8RL_TMAP, m_idx) : tile_rows(a, m_idx, lane);
       const int n0 = n_tile * BN;
       const int grow = tr.row0 + r;
       const bool row_ok = grow < tr.seg_end;
@@ -1305,6 +1387,8 @@ __global__ void __launch_bounds__(Cfg<BN, AROWS, EPI>::kThreads, 1)
   }
   streamk_finish();
 }
+
+#undef FP8RL_TMAP
 
 // ---------------------------------------------------------------- tensor-core pairs
 //
