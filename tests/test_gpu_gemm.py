@@ -194,6 +194,20 @@ def test_grouped_small_full(counts, fmt, bn):
     within(y, oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, fmt))
 
 
+@pytest.mark.parametrize("experts", [256, 257, 300])
+def test_grouped_many_experts(experts):
+    """Expert counts at and past the shared-memory map of segments (256): the
+    map's lookup and the scan over the offsets in global memory give the
+    oracle's results; many experts are empty, a few hold ragged segments."""
+    rng = np.random.default_rng(experts)
+    counts = [int(c) if rng.random() < 0.3 else 0 for c in rng.integers(1, 300, experts)]
+    counts[-1] = 131  # the last expert holds rows
+    n, k = 256, 256
+    offsets, xq, sx, wq, sw = grouped_case(counts, n, k, fp8rl.SCALE_FP32, experts)
+    y = run_grouped(offsets, xq, sx, wq, sw, fp8rl.SCALE_FP32, fill=7.0)
+    within(y, oracle.grouped_gemm_blockscaled(xq, sx, wq, sw, offsets, fp8rl.SCALE_FP32))
+
+
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 def test_grouped_qwen3_30b_a3b_sampled(which):
     """128 experts, T = 4096 tokens routed top-8 by replayed indices; the
