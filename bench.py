@@ -38,6 +38,7 @@ METRIC = "weight-sync quant GB/s; W8A8 block-scaled GEMM TFLOPS; % of roofline, 
 UNIT = "GB/s"
 WORKLOAD = "qwen3-8b-layer"
 STEP_M = 8192          # tokens in the step's forward batch
+NOMINAL_FP8_DENSE_TFLOPS = 4500.0  # GB300 dense FP8 tensor rate as published (context only)
 
 # DRAM bytes (read + write) per launch of the dominant kernel, taken from one
 # ncu capture of the same launch (the 8192 x 24576 x 4096 gate-up GEMM).
@@ -956,6 +957,9 @@ def main_ours(args):
         # the same achieved rate against 2 x the sustained bf16 figure, for
         # comparison only (that figure belongs to seconds-long loops)
         roofline["frac_vs_2x_bf16_sustained"] = d["achieved"] / (2.0 * peaks["bf16_tflops_sustained"])
+        # and against the nominal dense FP8 rate of the part (4.5 PFLOP/s),
+        # the most conservative basis
+        roofline["frac_vs_nominal_fp8_dense"] = d["achieved"] / NOMINAL_FP8_DENSE_TFLOPS
     e2e = e2e_weight_sync(torch, fp8rl, inp, stream, max(3, min(args.steps, 10)))
     sections = {}
     wanted = set(args.sections.split(",")) if args.sections not in ("all", "none") else (
