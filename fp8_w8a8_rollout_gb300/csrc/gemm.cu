@@ -2058,11 +2058,14 @@ fp8rl_status run(const void* xq, const void* x_scale, const void* wq, const void
   // decode sizes (dense, at most 64 rows): the swapped-operand kernel of
   // decode.cu (measured on GB300, Qwen3-8B projections with weights from
   // HBM: 30-50% faster than the 128-row-tile kernel at 17 and 32 rows, 5-30%
-  // at 64).  Its 128-column form (one CTA per SM) is only as fast as the
-  // tile kernel at 128 rows and slower for wide weights, so 65..128 rows run
-  // there unless the test hook forces it; the hook also forces the tile
-  // kernel.
-  const bool decode_shape = !d_offsets && (rows <= 64 || (rows <= 128 && dbg.decode == 1));
+  // at 64).  Its 128-column form (one CTA per SM) beats the tile kernel at
+  // 65..128 rows only where the weight's 128-row blocks leave room for four
+  // K splits in one wave (fp32 scales, 128 rows: 4096 x 4096 10.6 against
+  // 14.0 us, 4096 x 12288 even; 6144 x 4096 even with two splits, 24576 x
+  // 4096 1.8x slower), so only those shapes take it.  The test hook forces
+  // either kernel.
+  const bool narrow = fmt == FP8RL_SCALE_FP32 && n / 128 * 4 <= di.sms && k >= 4096;
+  const bool decode_shape = !d_offsets && (rows <= 64 || (rows <= 128 && (dbg.decode == 1 || narrow)));
   if (decode_shape && dbg.decode != 2 && dbg.streamk != 2) {
     const fp8rl_status st = decode_gemm(xq, x_scale, wq, w_scale, y, rows, n, k, fmt == FP8RL_SCALE_UE8M0, err,
                                         dbg.timeout_ns, dbg.fault_skip_kb, dbg.splits,

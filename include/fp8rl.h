@@ -37,7 +37,8 @@
  *     NULL is the legacy default stream).  Results are ready once the stream
  *     is synchronised.
  *   - Overlapped launches: fp8rl_quant_act_group and the GEMMs at decode
- *     sizes (dense, m <= 64; fp8rl_gemm_act_quant at m <= 16) are launched
+ *     sizes (dense, m <= 64, and up to 128 for the narrow shapes that debug
+ *     key 10 lists; fp8rl_gemm_act_quant at m <= 16) are launched
  *     with programmatic stream serialisation, and let the next kernel of the
  *     stream start before they complete.  Such a kernel may begin while the kernel before it on the
  *     stream is still running; it waits for that kernel's completion before
@@ -436,9 +437,10 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *   key 9  how data-parallel GEMM tiles are stored: 0 chooses per shape
  *          (default), 1 through shared memory and TMA stores, 2 from registers;
  *   key 10 dense GEMMs with at most 128 rows: 0 chooses (default: the
- *          swapped-operand decode kernel up to 64 rows, the 128-row-tile
- *          kernel above), 1 the decode kernel up to 128 rows, 2 the
- *          128-row-tile kernel;
+ *          swapped-operand decode kernel up to 64 rows, and up to 128 rows
+ *          for fp32 scales, K >= 4096 and at most SMs / 4 blocks of 128
+ *          weight rows; the 128-row-tile kernel otherwise), 1 the decode
+ *          kernel up to 128 rows, 2 the 128-row-tile kernel;
  *   key 11 UE8M0 GEMMs on whole tiles (data-parallel): 0 chooses (default:
  *          the tensor cores apply the power-of-two scales, block-scaled MMA,
  *          when K >= 2048; below, the per-chunk fp32 promotion), 1 always the

@@ -432,11 +432,12 @@ def decode_mode():
                                           (65, 6144, 4096, 0), (128, 4096, 12288, 0), (100, 128, 384, 2),
                                           (128, 24576, 4096, 0)])
 def test_decode_kernel_matches_oracle_and_tile_kernel(m, n, k, splits, fmt, decode_mode):
-    """At most 32 rows the dense GEMM runs the swapped-operand decode kernel
-    (weight rows as the MMA's M, tokens as its N, split K over a cluster),
-    and up to 128 when the test hook asks for it; within tolerance of the
-    oracle over the whole output, and of the 128-row-tile kernel that the
-    hook selects instead."""
+    """At most 64 rows (up to 128 for narrow weights with fp32 scales) the
+    dense GEMM runs the swapped-operand decode kernel (weight rows as the
+    MMA's M, tokens as its N, split K over a cluster), and up to 128 for any
+    shape when the test hook asks for it; within tolerance of the oracle over
+    the whole output, and of the 128-row-tile kernel that the hook selects
+    instead."""
     x = synth.activation_bf16(m, k, m + 3, "dec-x", n)
     w = synth.weight_bf16(n, k, k + 5, "dec-w")
     xq, sx, wq, sw = oracle_operands(x, w, fmt)
@@ -451,6 +452,23 @@ def test_decode_kernel_matches_oracle_and_tile_kernel(m, n, k, splits, fmt, deco
     within(y_tile, ref)
     # both round once from fp32 sums of the same products (orders differ)
     assert np.max(np.abs(y_dec - y_tile)) <= 2.0 ** -7 * np.max(np.abs(ref)) + 1e-6
+
+
+@pytest.mark.parametrize("m,n,k,kernel", [(128, 4096, 4096, 1), (100, 4096, 12288, 1), (128, 6144, 4096, 2),
+                                          (128, 24576, 4096, 2), (128, 4096, 2048, 2)])
+def test_default_kernel_between_65_and_128_rows(m, n, k, kernel, decode_mode):
+    """The default choice at 65..128 rows (fp32 scales): the decode kernel
+    for weights of at most SMs / 4 blocks of 128 rows with K >= 4096, the
+    128-row-tile kernel otherwise; the default's output is bit for bit that
+    of the kernel the test hook forces, and within tolerance of the oracle."""
+    x = synth.activation_bf16(m, k, m + 7, "dec-default-x", n)
+    w = synth.weight_bf16(n, k, k + 9, "dec-default-w")
+    xq, sx, wq, sw = oracle_operands(x, w, fp8rl.SCALE_FP32)
+    y = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_DECODE, kernel)
+    y_forced = run_gemm(xq, sx, wq, sw, fp8rl.SCALE_FP32)
+    assert np.array_equal(y.view(np.uint32), y_forced.view(np.uint32))
+    within(y, oracle.gemm_blockscaled(xq, sx, wq, sw))
 
 
 def test_decode_kernel_is_deterministic(decode_mode):
