@@ -45,9 +45,9 @@ NOMINAL_FP8_DENSE_TFLOPS = 4500.0  # GB300 dense FP8 tensor rate as published (c
 # Reported only while the GEMM's sources are those the capture was taken with.
 TRAFFIC = {
     "gemm_gate_up": {
-        "bytes": 147.8144e6 + 372.342016e6,
+        "bytes": 151.327488e6 + 372.452096e6,
         "sources": {
-            "gemm.cu": "f513e5af9ce40aad7e6bb594aadb0de1156e7fcf74e98e174bfba7c36ec51e52",
+            "gemm.cu": "6fd895098b82807637e85bb8c33aefeedb0dfbfe92cfe5310cceb6a471775fcd",
             "ptx.cuh": "7611be7f4488dec541b5332e198986f65689abe958fd940e526f41325f47e1be",
             "common.cuh": "6401f31a7a6a92810a87d55c9eae24512fe80ad094dc69922897bb43c8e0894d",
         },
