@@ -16,6 +16,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace fp8rl {
 namespace {
@@ -37,11 +38,23 @@ struct KvTensors {
   int32_t vec[3];
 };
 
+// The amax words start at zero (an empty tensor keeps 0: scale 1.0).  This
+// kernel is launched in stream order (it begins once everything before it on
+// the stream has completed) and lets the amax kernel start at once.
+__global__ void kv_zero_kernel(uint32_t* amax_bits, int n) {
+  ptx::grid_dep_launch_dependents();
+  if ((int)threadIdx.x < n) amax_bits[threadIdx.x] = 0u;
+}
+
 // amax of tensor blockIdx.y (rows x cols bf16) into amax_bits[blockIdx.y]:
 // the fp32 bit pattern of the magnitude (non-negative floats order like
 // unsigned integers, so atomicMax is exact and the result is independent of
-// the order of the updates)
+// the order of the updates).  Launched behind kv_zero_kernel with
+// programmatic stream serialisation: that kernel began only after every
+// earlier kernel of the stream had completed, so K, V and Q are read at once;
+// the wait for its completion (the zeroed words) comes before the atomicMax.
 __global__ void __launch_bounds__(kKvThreads) kv_amax_kernel(KvTensors ts, int64_t rows, uint32_t* amax_bits) {
+  ptx::grid_dep_launch_dependents();
   const int ti = blockIdx.y;
   // selected, not indexed: an indexed parameter struct is copied to local memory
   const uint16_t* x = ti == 0 ? ts.x[0] : ti == 1 ? ts.x[1] : ts.x[2];
@@ -83,12 +96,16 @@ __global__ void __launch_bounds__(kKvThreads) kv_amax_kernel(KvTensors ts, int64
   if (threadIdx.x < 32) {
     m = threadIdx.x < kKvThreads / 32 ? red[threadIdx.x] : 0u;
     m = __reduce_max_sync(0xffffffffu, m);
-    if (threadIdx.x == 0 && m != 0) atomicMax(amax_bits + ti, m);
+    if (threadIdx.x == 0) {
+      ptx::grid_dep_wait();
+      if (m != 0) atomicMax(amax_bits + ti, m);
+    }
   }
 }
 
-// amax bits -> fp32 scale, in place
+// amax bits -> fp32 scale, in place (after the amax kernel has completed)
 __global__ void kv_scale_kernel(float* scales, int n) {
+  ptx::grid_dep_wait();
   const int i = threadIdx.x;
   if (i < n) scales[i] = scale_fp32(scales[i]);  // the word holds the amax's bits
 }
@@ -159,8 +176,17 @@ extern "C" FP8RL_API fp8rl_status fp8rl_kv_calibrate(const void* k_bf16, const v
     return FP8RL_ERR_ALIGNMENT;
   const int n = q_bf16 ? 3 : 2;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  // amax words start at zero (an empty tensor keeps 0: scale 1.0)
-  if (cudaMemsetAsync(d_scales, 0, n * sizeof(float), cs) != cudaSuccess) return FP8RL_ERR_CUDA;
+  uint32_t* words = reinterpret_cast<uint32_t*>(d_scales);
+  // zero the amax words, reduce, convert: each kernel after the first starts
+  // while the one before it runs, and waits for it before it touches d_scales
+  kv_zero_kernel<<<1, 32, 0, cs>>>(words, n);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = cs;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
   if (tokens > 0) {
     KvTensors ts{};
     const void* xs[3] = {k_bf16, v_bf16, q_bf16};
@@ -174,10 +200,19 @@ extern "C" FP8RL_API fp8rl_status fp8rl_kv_calibrate(const void* k_bf16, const v
     // one grid slice per tensor, each warp a row at a time (a flat stream of
     // 16-byte pieces over all three tensors, one resident wave, measured
     // 30-50 % slower on GB300 after an L2 flush at 8192 and 32768 tokens)
-    kv_amax_kernel<<<dim3((unsigned)kv_grid(tokens), (unsigned)n), kKvThreads, 0, cs>>>(
-        ts, tokens, reinterpret_cast<uint32_t*>(d_scales));
+    cfg.gridDim = dim3((unsigned)kv_grid(tokens), (unsigned)n);
+    cfg.blockDim = dim3(kKvThreads);
+    if (cudaLaunchKernelEx(&cfg, kv_amax_kernel, ts, tokens, words) != cudaSuccess) {
+      cudaGetLastError();
+      return FP8RL_ERR_CUDA;
+    }
   }
-  kv_scale_kernel<<<1, 32, 0, cs>>>(d_scales, n);
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  if (cudaLaunchKernelEx(&cfg, kv_scale_kernel, d_scales, n) != cudaSuccess) {
+    cudaGetLastError();
+    return FP8RL_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 

@@ -191,6 +191,11 @@ FP8RL_API fp8rl_status fp8rl_quant_act_group(const void* x_bf16, int64_t m, int6
  *   q_bf16          device, bf16 [tokens][q_dim] (row stride ldq), or null
  *   d_scales        device, float [3] (q given) or [2]: K, V (, Q) scales;
  *                   written on the stream, never read back on the host
+ * Three kernels (zero the words, reduce, convert): the first starts once
+ * everything before it on the stream has completed, each later one starts
+ * while the one before it runs (overlapped launches, debug key 13) and
+ * waits for it before it writes d_scales; work enqueued after the call sees
+ * the finished scales.
  * Errors: INVALID_ARG (negative sizes, short strides, null pointers),
  *         ALIGNMENT (element alignment), CUDA.
  */
@@ -450,7 +455,8 @@ FP8RL_API fp8rl_status fp8rl_sync_status(void* stream);
  *          always where the shape allows (n a multiple of 256, m > 128), 2
  *          never;
  *   key 13 overlapped launches of the activation quantiser and the decode
- *          GEMM (see the conventions above): 0 on (default), 1 off;
+ *          GEMM (see the conventions above) and within fp8rl_kv_calibrate:
+ *          0 on (default), 1 off;
  *   key 0  restore all defaults.
  * Every key but 0 is refused (UNSUPPORTED, nothing changes) unless the
  * process environment holds FP8RL_TEST_HOOKS=1 at the time of the call, so

@@ -123,3 +123,58 @@ def test_append_rejects_bad_arguments():
     with pytest.raises(fp8rl.Fp8rlError):
         fp8rl.fp8rl_kv_append(x, x, 4, 128, 128, 128, None, c, c, 128, 4, s)
     fp8rl.fp8rl_kv_append(x, x, 0, 128, 128, 128, None, None, None, 128, 0, None)  # empty: no-op
+
+
+@pytest.fixture
+def overlap():
+    yield lambda off: fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 1 if off else 0)
+    fp8rl.fp8rl_debug_set(fp8rl.DEBUG_PDL, 0)
+
+
+@pytest.mark.parametrize("tokens", [8192, 0, 3])
+def test_calibrate_chain_from_poisoned_scales(tokens, overlap):
+    """The calibration's three kernels (zero, reduce, convert; each later one
+    started while the one before it runs): d_scales starts out holding values
+    larger than any amax, K is written by a kernel enqueued right before the
+    call, and the result is the oracle's with the overlap on and off and when
+    replayed from a CUDA graph."""
+    dim, qdim = 1024, 4096
+    k, v = kv_inputs(max(tokens, 1), dim, 5, 2.0)
+    q = synth.normal_bf16((max(tokens, 1), qdim), 0.5, 6, "kv-q-chain")
+    ref = oracle.kv_calibrate(synth.bf16_bits(k[:tokens]), synth.bf16_bits(v[:tokens]),
+                              synth.bf16_bits(q[:tokens]))
+    # row slices of device tensors: no pointer is null even at 0 tokens
+    kd0, vd, qd = k.cuda()[:tokens], v.cuda()[:tokens], q.cuda()[:tokens]
+    kd = torch.empty((max(tokens, 1), dim), dtype=torch.bfloat16, device="cuda")[:tokens]
+    scales = torch.empty(3, dtype=torch.float32, device="cuda")
+
+    def run():
+        kd.copy_(kd0)  # the producer of K, right before the call
+        fp8rl.fp8rl_kv_calibrate(kd, vd, qd, tokens, dim, dim, dim, qdim, qdim, scales)
+
+    results = []
+    for off in (False, True):
+        overlap(off)
+        kd.fill_(float("inf"))
+        scales.fill_(3.0e38)
+        run()
+        assert fp8rl.fp8rl_sync_status() == 0
+        results.append(scales.cpu().numpy().copy())
+    overlap(False)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(2):
+        kd.fill_(float("inf"))
+        scales.fill_(3.0e38)
+        g.replay()
+        torch.cuda.synchronize()
+        results.append(scales.cpu().numpy().copy())
+    for got in results:
+        assert np.array_equal(got.view(np.uint32), np.asarray(ref, np.float32).view(np.uint32))
