@@ -137,14 +137,18 @@ def test_calibrate_chain_from_poisoned_scales(tokens, overlap):
     started while the one before it runs): d_scales starts out holding values
     larger than any amax, K is written by a kernel enqueued right before the
     call, and the result is the oracle's with the overlap on and off and when
-    replayed from a CUDA graph."""
-    dim, qdim = 1024, 4096
+    replayed from a CUDA graph.  At 0 tokens (no Q: torch gives an empty
+    tensor a null pointer) only the K and V words are written."""
+    dim = 1024
+    qdim = 4096 if tokens else 0
     k, v = kv_inputs(max(tokens, 1), dim, 5, 2.0)
-    q = synth.normal_bf16((max(tokens, 1), qdim), 0.5, 6, "kv-q-chain")
+    q = synth.normal_bf16((max(tokens, 1), 4096), 0.5, 6, "kv-q-chain")
     ref = oracle.kv_calibrate(synth.bf16_bits(k[:tokens]), synth.bf16_bits(v[:tokens]),
-                              synth.bf16_bits(q[:tokens]))
-    # row slices of device tensors: no pointer is null even at 0 tokens
-    kd0, vd, qd = k.cuda()[:tokens], v.cuda()[:tokens], q.cuda()[:tokens]
+                              synth.bf16_bits(q[:tokens]) if qdim else None)
+    written = 3 if qdim else 2
+    poison = np.float32(3.0e38)
+    kd0, vd = k.cuda()[:tokens], v.cuda()[:tokens]
+    qd = q.cuda()[:tokens] if qdim else None
     kd = torch.empty((max(tokens, 1), dim), dtype=torch.bfloat16, device="cuda")[:tokens]
     scales = torch.empty(3, dtype=torch.float32, device="cuda")
 
@@ -156,7 +160,7 @@ def test_calibrate_chain_from_poisoned_scales(tokens, overlap):
     for off in (False, True):
         overlap(off)
         kd.fill_(float("inf"))
-        scales.fill_(3.0e38)
+        scales.fill_(float(poison))
         run()
         assert fp8rl.fp8rl_sync_status() == 0
         results.append(scales.cpu().numpy().copy())
@@ -172,9 +176,11 @@ def test_calibrate_chain_from_poisoned_scales(tokens, overlap):
         run()
     for _ in range(2):
         kd.fill_(float("inf"))
-        scales.fill_(3.0e38)
+        scales.fill_(float(poison))
         g.replay()
         torch.cuda.synchronize()
         results.append(scales.cpu().numpy().copy())
+    expect = np.asarray(ref, np.float32).copy()
+    expect[written:] = poison
     for got in results:
-        assert np.array_equal(got.view(np.uint32), np.asarray(ref, np.float32).view(np.uint32))
+        assert np.array_equal(got.view(np.uint32), expect.view(np.uint32))
