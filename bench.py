@@ -1067,6 +1067,7 @@ def main_case(args):
     import fp8_w8a8_rollout_gb300 as fp8rl
     from fp8_w8a8_rollout_gb300 import synth
     dev = torch.device("cuda")
+    flush = None  # set by the cases whose inputs L2 could hold between calls
     os.environ["FP8RL_TEST_HOOKS"] = "1"  # --case may force tile widths and schedules
     fp8rl.load_library()
     if args.bn:
@@ -1141,6 +1142,8 @@ def main_case(args):
         scales = torch.zeros(3, dtype=torch.float32, device=dev)
         fn = lambda: fp8rl.kv_calibrate(k, v, q, out=scales)
         work = {"bytes": tokens * (2 * KV_DIM + Q_DIM) * 2}
+        if tokens * (2 * KV_DIM + Q_DIM) * 2 < 2 * L2_BYTES:
+            flush = l2_flusher(torch, dev)  # inputs L2 could hold: flush before every call
     elif kind == "kv":
         tokens = int(parts[1])
         k, v, slots, kc, vc = kv_inputs(torch, synth, dev, 0, tokens, max(65536, tokens))
@@ -1190,7 +1193,7 @@ def main_case(args):
         work = {"bytes": gemm_bytes(m, n, k, 4 if fmt == 0 else 1) + aq_bytes(m, k, 4 if fmt == 0 else 1)}
     else:
         raise SystemExit(f"unknown case {args.case}")
-    ms = time_loop(torch, fn, max(1, args.steps), args.warmup)
+    ms = time_loop(torch, fn, max(1, args.steps), args.warmup, flush)
     assert fp8rl.fp8rl_sync_status() == 0
     out = {"case": args.case, "ms": ms, "bn": args.bn or "auto", "wait_mode": args.wait_mode,
            "l2_prefetch": args.l2_prefetch, "streamk": args.streamk, "out_stage": args.out_stage, "mx": args.mx, "pair": args.pair,
