@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import threading
 import sys
 import time
 
@@ -156,43 +157,80 @@ def load_peaks():
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi clock and throttle samples around the timed region: the
+    sampler runs before the region starts (the first sample has arrived), a
+    reader thread stamps each sample with the host clock, and the summary
+    keeps the samples taken between mark_start() and mark_end()."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
-    def __init__(self, index: str, enabled: bool = True):
+    def __init__(self, index: str, enabled: bool = True, command=None):
         self.index = index
         self.proc = None
         self.enabled = enabled
+        self.command = command  # a stand-in for nvidia-smi (tests)
+        self.samples = []       # (host time, csv line)
+        self.t0 = self.t1 = None
+        self.thread = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.samples.append((time.monotonic(), ln.strip()))
 
     def __enter__(self):
         if self.enabled:
+            cmd = self.command or ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                   "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)]
             try:
-                self.proc = subprocess.Popen(
-                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits", "-lms", "50"],
-                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
+            if self.proc is not None:
+                self.thread = threading.Thread(target=self._read, daemon=True)
+                self.thread.start()
+                deadline = time.monotonic() + 5.0
+                while not self.samples and time.monotonic() < deadline and self.proc.poll() is None:
+                    time.sleep(0.005)
         return self
 
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
+        # a region shorter than the sampling interval still gets the sample
+        # that was being taken while it ran
+        if self.proc is not None:
+            time.sleep(self.INTERVAL_MS / 1000.0 * 1.5)
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def window(self):
+        """The samples stamped inside the region (a sample's line is printed
+        up to one interval after it was taken, so the window ends one
+        interval late)."""
+        if self.t0 is None or self.t1 is None:
+            return [ln for _, ln in self.samples]
+        late = self.INTERVAL_MS / 1000.0
+        return [ln for t, ln in self.samples if self.t0 <= t <= self.t1 + late]
 
     def summary(self):
-        if not getattr(self, "lines", None):
-            return None
+        lines = self.window()
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -207,7 +245,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "interval_ms": self.INTERVAL_MS}
 
 
 def gpu_smi_id(torch, local: int) -> str:
@@ -927,11 +965,13 @@ def main_ours(args):
         barrier()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
+        clocks.mark_start()
         start.record()
         for _ in range(args.steps):
             launches += run_step(fp8rl, inp, timer, stream)
         end.record()
         barrier()
+        clocks.mark_end()
     total_ms = start.elapsed_time(end)
     timer.collect()
     status = fp8rl.fp8rl_sync_status()
