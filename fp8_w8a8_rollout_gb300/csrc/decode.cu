@@ -97,6 +97,7 @@ struct DecCfg {
   // kXRing slots (the chunk's codes, then their bf16 source), so that their
   // quantisation runs ahead of the MMA without holding a weight stage.
   static constexpr int kXRing = QX ? 4 : 0;
+  static constexpr int kXRingDiv = QX ? kXRing : 1;  // the ring as a divisor (reached only when QX)
   static constexpr int kXRawBytes = NT * 256;
   static constexpr int kXSlotBytes = kXBytes + kXRawBytes;
   static constexpr int kStageBytes = kDecWBytes + (QX ? 0 : kXBytes);  // a weight stage (+ the codes unfused)
@@ -269,9 +270,9 @@ __global__ void __launch_bounds__(DecCfg<NT, QX>::kThreads, DecCfg<NT, QX>::kMin
       // MMAs of chunk c - kXRing have completed; false when a wait ran out
       int xissued = 0;
       auto issue_x = [&](int c) {
-        const int xs = c % C::kXRing;
+        const int xs = c % C::kXRingDiv;
         if (c >= C::kXRing &&
-            !mbar_wait_bounded(smem_u32(&xempty[xs]), ((c / C::kXRing) - 1) & 1, abortv, a.err, a.timeout_ns))
+            !mbar_wait_bounded(smem_u32(&xempty[xs]), ((c / C::kXRingDiv) - 1) & 1, abortv, a.err, a.timeout_ns))
           return false;
         mbar_arrive_expect_tx(smem_u32(&xfull[xs]), C::kXRawBytes);
         tma_load_2d(xring + xs * C::kXSlotBytes + C::kXBytes, &tmap_x, (kb_lo + c) * 128, 0, smem_u32(&xfull[xs]));
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(DecCfg<NT, QX>::kThreads, DecCfg<NT, QX>::kMin
           if (kb_lo + j != a.fault_skip_kb)
             mbar_wait_bounded(smem_u32(&full[j % stages]), (j / stages) & 1, nullptr, nullptr, 10000000ull);
         for (int c = xissued > C::kXRing ? xissued - C::kXRing : 0; c < xissued; ++c)
-          mbar_wait_bounded(smem_u32(&xfull[c % C::kXRing]), (c / C::kXRing) & 1, nullptr, nullptr, 10000000ull);
+          mbar_wait_bounded(smem_u32(&xfull[c % C::kXRingDiv]), (c / C::kXRingDiv) & 1, nullptr, nullptr, 10000000ull);
       }
     } else {
       grid_dep_wait();
@@ -335,8 +336,8 @@ __global__ void __launch_bounds__(DecCfg<NT, QX>::kThreads, DecCfg<NT, QX>::kMin
         const int s = it % stages;
         const uint32_t ph = (it / stages) & 1;
         if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abortv, a.err, a.timeout_ns)) break;
-        const int xs = QX ? it % C::kXRing : 0;
-        if (QX && !mbar_wait_bounded(smem_u32(&xready[xs]), (it / C::kXRing) & 1, abortv, a.err, a.timeout_ns)) break;
+        const int xs = QX ? it % C::kXRingDiv : 0;
+        if (QX && !mbar_wait_bounded(smem_u32(&xready[xs]), (it / C::kXRingDiv) & 1, abortv, a.err, a.timeout_ns)) break;
         tc_fence_after();
         const uint32_t a0 = sW + s * kDecWBytes;
         const uint32_t b0 = QX ? xring + xs * C::kXSlotBytes : sX + s * C::kXBytes;
@@ -372,8 +373,8 @@ __global__ void __launch_bounds__(DecCfg<NT, QX>::kThreads, DecCfg<NT, QX>::kMin
     const int part = lane & 7;
     const bool out = a.xq_out != nullptr && nblk == 0;
     for (int it = 0; it < nloc; ++it) {
-      const int xs = it % C::kXRing;
-      bool got = mbar_wait_bounded(smem_u32(&xfull[xs]), (it / C::kXRing) & 1, abortv, a.err, a.timeout_ns);
+      const int xs = it % C::kXRingDiv;
+      bool got = mbar_wait_bounded(smem_u32(&xfull[xs]), (it / C::kXRingDiv) & 1, abortv, a.err, a.timeout_ns);
       got = __all_sync(0xffffffffu, got);
       if (!got) break;
       const int kb = kb_lo + it;
