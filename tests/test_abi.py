@@ -337,6 +337,26 @@ def test_tis_rejects_bad_arguments_on_host(lib):
     assert _rc(t, fake + 2, fake, None, 1 << 24, 2.0, fake, fake, fake, ws, None) == 3
 
 
+def test_kv_rejects_bad_arguments_on_host(lib):
+    fake = 1 << 20  # never dereferenced: every call below fails validation first (or has no work)
+    c = "fp8rl_kv_calibrate"
+    assert _rc(c, fake, fake, fake, -1, 1024, 1024, 1024, 4096, 4096, fake, None) == 1    # tokens < 0
+    assert _rc(c, fake, fake, fake, 16, 1024, 1000, 1024, 4096, 4096, fake, None) == 1    # ldk < kv_dim
+    assert _rc(c, fake, fake, fake, 16, 1024, 1024, 1024, 4096, 4000, fake, None) == 1    # ldq < q_dim
+    assert _rc(c, fake, fake, None, 16, 1024, 1024, 1024, 0, 0, None, None) == 1          # no d_scales
+    assert _rc(c, None, fake, None, 16, 1024, 1024, 1024, 0, 0, fake, None) == 1          # tokens, no K
+    assert _rc(c, fake, fake, None, 16, 1024, 1024, 1024, 0, 0, fake + 2, None) == 3      # scales misaligned
+    assert _rc(c, fake + 1, fake, None, 16, 1024, 1024, 1024, 0, 0, fake, None) == 3      # odd bf16 address
+    a = "fp8rl_kv_append"
+    assert _rc(a, fake, fake, -1, 1024, 1024, 1024, fake, fake, fake, 1024, 64, fake, None) == 1  # tokens < 0
+    assert _rc(a, fake, fake, 16, 1024, 1024, 1024, fake, fake, fake, 1000, 64, fake, None) == 1  # ld_cache < kv_dim
+    assert _rc(a, fake, fake, 16, 1024, 1024, 1024, fake, fake, fake, 1024, -1, fake, None) == 1  # num_slots < 0
+    assert _rc(a, fake, fake, 16, 1024, 1024, 1024, None, fake, fake, 1024, 64, fake, None) == 1  # no slot map
+    assert _rc(a, fake, fake, 16, 1024, 1024, 1024, fake, fake, fake, 1024, 64, None, None) == 1  # no scales
+    assert _rc(a, fake, fake, 16, 1024, 1024, 1024, fake + 2, fake, fake, 1024, 64, fake, None) == 3
+    assert _rc(a, None, None, 0, 1024, 1024, 1024, None, None, None, 1024, 64, None, None) == 0   # no tokens: no-op
+
+
 def test_helpers_reject_host_tensors():
     """A host tensor's pointer must never reach a kernel: every tensor helper
     refuses CPU tensors before it loads or calls the library."""
