@@ -127,6 +127,12 @@ def gemm_bytes(m, n, k, scale_bytes=4):
     return n * k + m * k + 2 * m * n + scale_bytes * (m * (k // 128) + (n // 128) * (k // 128))
 
 
+def grouped_gemm_bytes(experts, rows, n, k, scale_bytes=4):
+    """Every expert's weights once, the routed rows' codes in, bf16 out, scales."""
+    return (experts * n * k + rows * k + 2 * rows * n +
+            scale_bytes * (rows * (k // 128) + experts * (n // 128) * (k // 128)))
+
+
 def fp8_peak(peaks):
     """Dense FP8 tensor roofline: 2 x the measured BURST bf16 GEMM rate (the
     nominal fp8:bf16 ratio).  The burst figure is the one for kernels timed
@@ -407,7 +413,7 @@ def step_rooflines(inp, timer, peaks):
                                              "frac": b / ms / 1e6 / hbm, "bytes": b}
             ms = timer.avg_ms(f"moe_gemm_{which}")
             e = wq.shape[0]
-            bytes_ = e * n * k + rows * k + 2 * rows * n + 4 * (rows * k // 128 + e * (n // 128) * (k // 128))
+            bytes_ = grouped_gemm_bytes(e, rows, n, k)
             out[f"moe_gemm_{which}"] = gemm_roof(gemm_flops(rows, n, k), bytes_, ms, hbm, fp8)
     return out
 
