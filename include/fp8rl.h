@@ -49,7 +49,8 @@
  *     dependents early (griddepcontrol.launch_dependents) must not enqueue a
  *     decode-size GEMM on that weight right behind it.
  *   - Arguments are validated on the host before any launch; a call that
- *     returns an error launched nothing.
+ *     returns a validation error (INVALID_ARG, SHAPE, ALIGNMENT) launched
+ *     nothing.
  *   - Matrices are row-major with an explicit leading dimension in elements.
  *   - No call throws; every call returns an fp8rl_status.
  *   - Non-finite inputs give unspecified codes.
